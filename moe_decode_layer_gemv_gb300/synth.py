@@ -1,0 +1,113 @@
+"""Seeded synthetic inputs for the MoE decode layer.
+
+This module only draws random numbers: it holds none of the layer's
+arithmetic, so the CUDA path and the CPU oracle can both be fed from it.
+
+Recipe (every tensor has its own generator stream, seeded from
+``(seed, tensor_id, expert)``):
+
+* x:            N(0, 1), fp32 (bf16 for the prefill-sized workload);
+                tensor_id 1000 + step.
+* W_router[l]:  N(0, sigma_r) rounded to bf16 (round-to-nearest-even);
+                tensor_id 10 + 3l.  sigma_r = 0.02, or 1/sqrt(H) for the
+                uniform/skewed routing workloads, so that the logits are
+                ~N(0, 1) given x.
+* gate_up[l]:   [E, 2I, H], N(0, 0.02) -> bf16; tensor_id 11 + 3l; one
+                stream per expert, so an expert can be regenerated alone.
+* down[l]:      [E, H, I], N(0, 0.02) -> bf16; tensor_id 12 + 3l.
+* bias (skewed routing only): b_e = 2 * log(1 / rank_e ** 1.1) with rank a
+                seeded random permutation of 1..E (tensor_id 1).
+
+Small cases are generated on the CPU and copied to the device; the
+full-size workloads are generated directly on the GPU by torch's own
+generator (the values then depend on the device, so each case records
+which device drew it).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    I: int
+    E: int
+    top_k: int
+    layers: int = 1
+    sigma_router: float = 0.02
+    sigma_expert: float = 0.02
+    x_bf16: bool = False
+    zipf_bias: bool = False
+    residual: bool = False
+    batches: tuple = field(default_factory=tuple)
+
+    def with_batch(self, B: int) -> "Workload":
+        return Workload(self.name, B, self.H, self.I, self.E, self.top_k, self.layers,
+                        self.sigma_router, self.sigma_expert, self.x_bf16, self.zipf_bias,
+                        self.residual, self.batches)
+
+
+# The five workloads the layer is measured and checked on.
+TINY = Workload("tiny_b4_h64_i32_e8_k2", B=4, H=64, I=32, E=8, top_k=2)
+STACK = Workload("stack30_b1_h2048_i768_e128_k2", B=1, H=2048, I=768, E=128, top_k=2,
+                 layers=30, residual=True)
+UNIFORM = Workload("uniform_e256_k8_h2048_i768", B=64, H=2048, I=768, E=256, top_k=8,
+                   sigma_router=2048 ** -0.5, batches=(1, 4, 8, 16, 32, 64))
+SKEWED = Workload("skewed_zipf_e256_k6_h2048_i768", B=128, H=2048, I=768, E=256, top_k=6,
+                  sigma_router=2048 ** -0.5, zipf_bias=True, batches=(1, 16, 64, 128))
+PREFILL = Workload("prefill_b512_e256_k8_h4096_i1536", B=512, H=4096, I=1536, E=256, top_k=8,
+                   x_bf16=True)
+
+WORKLOADS = {w.name: w for w in (TINY, STACK, UNIFORM, SKEWED, PREFILL)}
+
+
+def _gen(seed: int, tensor_id: int, sub: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    # a fixed mixing of the three integers into one 63-bit seed
+    s = (seed * 0x9E3779B1 + tensor_id * 0x85EBCA77 + sub * 0xC2B2AE3D + 0x27D4EB2F) % (2 ** 63 - 1)
+    g.manual_seed(s)
+    return g
+
+
+def normal_bf16(shape, sigma, seed, tensor_id, sub, device) -> torch.Tensor:
+    g = _gen(seed, tensor_id, sub, device)
+    t = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+    return (t * sigma).to(torch.bfloat16)
+
+
+def make_layer(w: Workload, layer: int = 0, seed: int = 0, device="cpu"):
+    """Weights of one layer as torch tensors on ``device``."""
+    E, H, I = w.E, w.H, w.I
+    wr = normal_bf16((E, H), w.sigma_router, seed, 10 + 3 * layer, 0, device)
+    gate_up = torch.empty((E, 2 * I, H), dtype=torch.bfloat16, device=device)
+    down = torch.empty((E, H, I), dtype=torch.bfloat16, device=device)
+    for e in range(E):
+        gate_up[e] = normal_bf16((2 * I, H), w.sigma_expert, seed, 11 + 3 * layer, e, device)
+        down[e] = normal_bf16((H, I), w.sigma_expert, seed, 12 + 3 * layer, e, device)
+    bias = zipf_bias(E, seed).to(device) if w.zipf_bias else None
+    return {"w_router": wr, "gate_up": gate_up, "down": down, "bias": bias}
+
+
+def zipf_bias(E: int, seed: int = 0) -> torch.Tensor:
+    """b_e = 2*log(1/rank_e^1.1), rank a seeded permutation of 1..E (fp32)."""
+    g = _gen(seed, 1, 0, "cpu")
+    rank = torch.randperm(E, generator=g).to(torch.float64) + 1.0
+    return (2.0 * torch.log(1.0 / rank ** 1.1)).to(torch.float32)
+
+
+def make_x(w: Workload, step: int = 0, seed: int = 0, device="cpu", B: int | None = None):
+    B = w.B if B is None else B
+    g = _gen(seed, 1000 + step, 0, device)
+    x = torch.randn((B, w.H), generator=g, device=device, dtype=torch.float32)
+    return x.to(torch.bfloat16) if w.x_bf16 else x
+
+
+def bf16_bits(t: torch.Tensor):
+    """bf16 tensor -> numpy uint16 array of its bit patterns (CPU copy)."""
+    import numpy as np
+    return t.detach().to("cpu").contiguous().view(torch.int16).numpy().view(np.uint16)
