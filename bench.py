@@ -1,0 +1,411 @@
+"""Benchmark: the 30-layer MoE decode stack (B=1, H=2048, I=768, E=128, top-2)
+on one GB300, through the C ABI of libmoe.so.
+
+Prints ONE JSON line (rank 0).  A step is one decode token through all 30
+layers (router GEMV, softmax/top-k, grouping, grouped gate_up/SiLU*up, down
+and combine, with the residual add), one fused persistent kernel launch.
+
+  value     tokens/s of the whole job (sum over ranks / max-over-ranks time),
+            inputs resident in HBM, L2 flushed (256 MiB memset) before every
+            timed step, timed with CUDA events on the launching stream;
+  e2e       the same metric through the public Python API with pinned HOST
+            buffers: x copied in, the stack run, x copied out, each step;
+  roofline  algorithmic bytes per launch (each layer's bf16 router plus each
+            unique selected expert once) / mean launch time, against the
+            measured HBM copy bandwidth;
+  cpu_baseline  the CPU oracle on a bounded sample of the same workload.
+
+--impl reference times the CPU oracle itself on this workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/s and achieved HBM GB/s (unique-expert bytes) vs roofline"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--mode", default="fused", choices=["fused", "unfused"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="bound on the oracle's CPU sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            for key in ("hbm_gbs", "hbm_copy_gbs"):
+                if key in d:
+                    return float(d[key]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "moe_decode_layer_gemv_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "moe.h"), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        rec = d.get(f"{kernel}@{workload}")
+        if rec and rec.get("source_hash") == kernel_source_hash():
+            return rec.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        time.sleep(0.2)
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle
+def oracle_stack_sample(layers_cpu_fn, x0_list, k, seconds):
+    """Run the CPU oracle on whole tokens through the stack until `seconds`
+    of oracle time accumulate (at least one token).  layers_cpu_fn(l, ids)
+    returns the layer's weights as the oracle takes them (host arrays),
+    fetching only the experts in ids.  Returns (tokens, oracle_seconds)."""
+    import numpy as np
+    import oracle
+    done, spent = 0, 0.0
+    for x0 in x0_list:
+        x = np.array(x0, dtype=np.float32, copy=True)
+        for l in range(30):
+            wr, bias = layers_cpu_fn(l, None)
+            t0 = time.perf_counter()
+            lo = oracle.router(x, wr, bias)
+            ids, w = oracle.topk(lo, k)
+            spent += time.perf_counter() - t0
+            gu, dn = layers_cpu_fn(l, ids)
+            t0 = time.perf_counter()
+            x = oracle.experts(x, gu, dn, ids, w, wr.shape[0], residual=x)
+            spent += time.perf_counter() - t0
+        done += 1
+        if spent >= seconds:
+            break
+    return done, spent
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    os.environ.setdefault("OMP_NUM_THREADS", str(cpu_threads()))
+    import numpy as np
+    import torch
+    from moe_decode_layer_gemv_gb300 import accounting, synth
+    w = synth.STACK
+    cache = {}
+
+    def layer_cpu(l, ids):
+        key = ("r", l)
+        if key not in cache:
+            cache[key] = (synth.bf16_bits(synth.normal_bf16((w.E, w.H), w.sigma_router, args.seed,
+                                                             10 + 3 * l, 0, "cpu")), None)
+        if ids is None:
+            return cache[key]
+        gu, dn = {}, {}
+        for e in np.unique(ids):
+            e = int(e)
+            kg = ("g", l, e)
+            if kg not in cache:
+                cache[kg] = (synth.bf16_bits(synth.normal_bf16((2 * w.I, w.H), w.sigma_expert, args.seed,
+                                                                11 + 3 * l, e, "cpu")),
+                             synth.bf16_bits(synth.normal_bf16((w.H, w.I), w.sigma_expert, args.seed,
+                                                                12 + 3 * l, e, "cpu")))
+            gu[e], dn[e] = cache[kg]
+        return gu, dn
+
+    xs = [synth.make_x(w, s, seed=args.seed, device="cpu").numpy() for s in range(args.warmup + args.steps)]
+    per_step = max(1.0, args.cpu_seconds / max(args.steps, 1))
+    for s in range(args.warmup):
+        oracle_stack_sample(layer_cpu, [xs[s]], w.top_k, 0.0)
+    total_tok, total_t = 0, 0.0
+    for s in range(args.steps):
+        n, t = oracle_stack_sample(layer_cpu, [xs[args.warmup + s]], w.top_k, per_step)
+        total_tok += n
+        total_t += t
+    value = total_tok * w.B / total_t
+    cores = int(os.environ.get("OMP_NUM_THREADS", cpu_threads()))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * total_t / max(total_tok, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": {"workload": w.name, "layers": w.layers, "B": w.B, "H": w.H,
+                                         "I": w.I, "E": w.E, "top_k": w.top_k},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{total_tok} whole tokens through all 30 layers (CPU-drawn weights)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------------- ours
+def run_ours(args):
+    rank, world, local = dist_env()
+    import numpy as np
+    import torch
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        pg = dist
+    from moe_decode_layer_gemv_gb300 import accounting, build, synth
+    build.build()
+    from moe_decode_layer_gemv_gb300 import api
+    w = synth.STACK
+    flags = api.MOE_F_UNFUSED if args.mode == "unfused" else 0
+    layers = [synth.make_layer(w, l, seed=args.seed + 7919 * rank, device=dev) for l in range(w.layers)]
+    sw = api.StackWeights(layers)
+    nsteps = args.warmup + args.steps
+    xs = [synth.make_x(w, s, seed=args.seed + 7919 * rank, device=dev) for s in range(nsteps)]
+    xbuf = torch.empty_like(xs[0])
+    ids = torch.empty((w.layers, w.B, w.top_k), dtype=torch.int32, device=dev)
+    ws = api.new_workspace(w.B, w.H, w.I, w.E, w.top_k, dev)
+    status = api.new_status(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        xbuf.copy_(xs[i])
+        api.stack_forward_(xbuf, sw, w.top_k, flags=flags, ids_out=ids, workspace=ws, status=status,
+                           stream=stream)
+
+    for i in range(args.warmup):
+        flush.zero_()
+        step(i)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    uniq = []
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        for s in range(args.steps):
+            i = args.warmup + s
+            flush.zero_()
+            xbuf.copy_(xs[i])
+            ev[s][0].record(stream)
+            api.stack_forward_(xbuf, sw, w.top_k, flags=flags, ids_out=ids, workspace=ws, status=status,
+                               stream=stream)
+            ev[s][1].record(stream)
+            uniq.append(ids.clone())
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+    times_ms = [a.elapsed_time(b) for a, b in ev]
+    st = int(status.item())
+    if st != 0:
+        raise SystemExit(f"device status {st}: {api.status_string(st)}")
+    total_ms = sum(times_ms)
+    if pg:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    tokens = w.B * args.steps * world
+    value = tokens / (total_ms / 1000.0)
+    # algorithmic bytes: per layer the router + each unique selected expert once
+    bytes_steps = []
+    for u in uniq:
+        un = u.cpu().numpy()
+        bytes_steps.append(sum(accounting.layer_bytes(w.H, w.I, w.E, len(np.unique(un[l])))
+                               for l in range(w.layers)))
+    bytes_per_launch = statistics.mean(bytes_steps)
+    mean_ms = statistics.mean(times_ms)
+    achieved = bytes_per_launch / (mean_ms / 1000.0) / 1e9
+    peak, peak_src = hbm_peak()
+    clocks = clk.summary()
+
+    # ---- e2e: public API, pinned host buffers, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        xh = [xs[args.warmup + s].cpu().pin_memory() for s in range(args.steps)]
+        out_h = torch.empty_like(xh[0]).pin_memory()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for s in range(args.steps):
+            flush.zero_()
+            xbuf.copy_(xh[s], non_blocking=True)
+            api.stack_forward_(xbuf, sw, w.top_k, flags=flags, ids_out=ids, workspace=ws, status=status,
+                               stream=stream)
+            out_h.copy_(xbuf, non_blocking=True)
+            stream.synchronize()
+        e2e_s = time.perf_counter() - t0
+        # the L2 flush is not part of the user's call: subtract its device time
+        fe = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        fe[0].record(stream)
+        for _ in range(args.steps):
+            flush.zero_()
+        fe[1].record(stream)
+        torch.cuda.synchronize()
+        e2e_s -= fe[0].elapsed_time(fe[1]) / 1000.0
+        nbytes = xh[0].numel() * 4
+        e2e = {"value": w.B * args.steps * world / e2e_s, "unit": "tokens/s",
+               "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes}
+
+    launches_per_step = 1 if args.mode == "fused" else 6 * w.layers
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "weights_dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "layers": w.layers, "B": w.B, "H": w.H, "I": w.I, "E": w.E,
+                   "top_k": w.top_k, "mode": args.mode,
+                   "l2": "flushed before every timed step (256 MiB memset, outside the events)"},
+        "hbm_gbs": achieved,
+        "us_per_layer": 1000.0 * mean_ms / w.layers,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_src,
+                     "traffic": recorded_traffic("moe_stack_fused", w.name),
+                     "kernel": "fused_kernel (one launch = 30 layers)",
+                     "bytes_per_launch": bytes_per_launch},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        os.environ.setdefault("OMP_NUM_THREADS", str(cpu_threads()))
+        cache = {}
+
+        def layer_cpu(l, ids_np):
+            lw = layers[l]
+            if ("r", l) not in cache:
+                cache[("r", l)] = (synth.bf16_bits(lw["w_router"]), None)
+            if ids_np is None:
+                return cache[("r", l)]
+            gu, dn = {}, {}
+            for e in np.unique(ids_np):
+                e = int(e)
+                if ("g", l, e) not in cache:
+                    cache[("g", l, e)] = (synth.bf16_bits(lw["gate_up"][e]), synth.bf16_bits(lw["down"][e]))
+                gu[e], dn[e] = cache[("g", l, e)]
+            return gu, dn
+
+        x_np = [xs[args.warmup + s].cpu().numpy() for s in range(args.steps)]
+        n, t = oracle_stack_sample(layer_cpu, x_np, w.top_k, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": n * w.B / t, "unit": "tokens/s",
+                                "cores": int(os.environ["OMP_NUM_THREADS"]), "kind": "oracle",
+                                "sample": f"{n} whole tokens through all 30 layers (same weights, "
+                                          f"{t:.1f} s of oracle time)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

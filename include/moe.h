@@ -1,0 +1,185 @@
+/*
+ * moe.h -- C ABI of libmoe.so, a GB300 (sm_103a) Mixture-of-Experts decode
+ * layer: router GEMV, fp32 softmax + top-k, stable grouping of the routes by
+ * expert, grouped gate_up projection with SiLU(gate)*up, grouped down
+ * projection and the routing-weighted combine -- all on the device, with no
+ * host read-back of router scores and no synchronisation inside a layer or
+ * between layers.
+ *
+ * Common conventions
+ *  - Every tensor argument is a DEVICE pointer unless stated otherwise.
+ *    The caller owns all memory; no entry point allocates or frees device
+ *    memory.  Scratch space is the caller's `workspace`, sized by
+ *    moe_workspace_bytes().
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every entry point only enqueues work on it and returns; none
+ *    synchronises the stream or copies device -> host, so every call can be
+ *    captured in a CUDA graph.
+ *  - Layouts are row-major and contiguous:
+ *      x        [B, H]       fp32 or bf16 (x_dtype)
+ *      w_router [E, H]       bf16
+ *      gate_up  [E, 2I, H]   bf16; rows [0, I) of an expert are the gate
+ *                            projection, rows [I, 2I) the up projection
+ *      down     [E, H, I]    bf16
+ *      y        [B, H]       fp32
+ *    bf16 is passed as raw 16-bit patterns (uint16_t).
+ *  - Requirements: 1 <= E <= MOE_MAX_E, 1 <= top_k <= min(E, MOE_MAX_TOPK),
+ *    0 <= B <= MOE_MAX_B, H and I multiples of 8 in [8, MOE_MAX_DIM], every
+ *    pointer 16-byte aligned.  Violations return MOE_ERR_INVALID_ARG before
+ *    anything is enqueued.
+ *  - Return value: MOE_OK, or a negative moe_status.  Launch failures
+ *    return MOE_ERR_CUDA.  Faults found on the device (a bad expert id, a
+ *    barrier that timed out, a non-finite logit) are OR-ed as MOE_DEV_* bits
+ *    into *dev_status (a device int32 the caller zeroes and reads after its
+ *    own synchronisation); dev_status may be NULL to ignore them.
+ *
+ * The operation is the MoE layer of the pages "MoE Performance Optimization
+ * Analysis" (Root Cause / GPU Router Design: router, selection and the
+ * combination on the GPU with no CPU read) and "perf(cpu-moe): dedup experts
+ * across the batch in pass 1 - #46" (commit message: routes grouped by
+ * expert with a counting sort; pass 1 = gate_up [2I, H], pass 2 = down
+ * [H, I]).
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* host return codes */
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = -1,
+    MOE_ERR_UNSUPPORTED = -2,
+    MOE_ERR_CUDA = -3,
+    MOE_ERR_WORKSPACE = -4
+} moe_status;
+
+/* device status bits (written asynchronously into *dev_status) */
+#define MOE_DEV_TIMEOUT 1        /* a grid barrier gave up waiting           */
+#define MOE_DEV_BAD_EXPERT_ID 2  /* an expert id outside [0, E)              */
+#define MOE_DEV_DUP_EXPERT 4     /* one token lists the same expert twice    */
+#define MOE_DEV_NONFINITE 8      /* a router logit was NaN or infinite       */
+
+/* activation dtypes */
+typedef enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 } moe_dtype;
+
+/* limits */
+#define MOE_MAX_E 256
+#define MOE_MAX_TOPK 8
+#define MOE_MAX_B 1024
+#define MOE_MAX_DIM 16384
+#define MOE_MAX_LAYERS 64
+
+/* flags for moe_expert_forward / moe_layer_forward / moe_stack_forward */
+#define MOE_F_NO_DEDUP 1u   /* evaluate every route on its own (each route re-reads
+                               its expert's weights): the A/B baseline of the
+                               dedup page; results are identical */
+#define MOE_F_UNFUSED 2u    /* layer/stack: run the phases as separate kernels
+                               instead of the persistent fused kernel */
+
+/*
+ * moe_workspace_bytes -- size of the scratch buffer the forward entry points
+ * need for a problem of this shape.  Host-only; *bytes receives the size.
+ * Returns MOE_ERR_INVALID_ARG for unsupported shapes.
+ */
+int moe_workspace_bytes(int B, int H, int I, int E, int top_k, size_t* bytes);
+
+/*
+ * moe_route -- router GEMV + fp32 softmax + top-k + renormalisation.
+ * ("MoE Performance Optimization Analysis", GPU Router Design: router
+ * kernel = compute + selection; Batch Router Design: [B, H] -> [B, E].)
+ *   logits[t,e] = sum_h x[t,h] * w_router[e,h] + (logit_bias ? logit_bias[e] : 0)
+ *   p = softmax(logits[t,:]) in fp32
+ *   expert_ids[t, 0..k) = the k largest logits, descending, ties to the lower id
+ *   route_w[t,j] = p[id_j] / sum_j' p[id_j']
+ * In:  x [B,H] (x_dtype), w_router [E,H] bf16, logit_bias [E] fp32 or NULL.
+ * Out: expert_ids [B,k] int32, route_w [B,k] fp32, logits_out [B,E] fp32
+ *      (may be NULL; then the workspace holds the logits and must be given).
+ */
+int moe_route(const void* x, int x_dtype, const uint16_t* w_router, const float* logit_bias,
+              int B, int H, int E, int top_k, int32_t* expert_ids, float* route_w,
+              float* logits_out, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+              void* stream);
+
+/*
+ * moe_group_by_expert -- stable counting sort of the R = B*top_k routes
+ * r = t*top_k + j by expert id ("perf(cpu-moe): dedup experts across the
+ * batch in pass 1 - #46", commit message: group the routes by expert with a
+ * counting sort over the ids, so each expert's weights are read once).
+ * In:  expert_ids [B, top_k] int32; the ids of one token must be distinct.
+ * Out: offsets [E+1]        exclusive prefix sum of the per-expert counts
+ *      route_idx [R]        routes grouped by expert, increasing r in a group
+ *      unique_experts [E]   experts with a nonzero count, ascending (first
+ *                           *num_unique entries valid)
+ *      num_unique [1]       U
+ * Bad ids set MOE_DEV_BAD_EXPERT_ID / MOE_DEV_DUP_EXPERT and are skipped
+ * (the outputs are then not a valid grouping).
+ */
+int moe_group_by_expert(const int32_t* expert_ids, int B, int top_k, int E, int32_t* offsets,
+                        int32_t* route_idx, int32_t* unique_experts, int32_t* num_unique,
+                        int32_t* dev_status, void* stream);
+
+/*
+ * moe_expert_forward -- the grouped experts and the combine for a given
+ * routing ("perf(cpu-moe) ... #46": pass 1 = gate_up, pass 2 = down;
+ * "MoE Performance Optimization Analysis": combination on the GPU).
+ *   h_r = SiLU(gate_e x_t) * (up_e x_t),  o_r = down_e h_r   for each route
+ *   y[t] = sum_j route_w[t,j] * o_(t,j)  (+ residual[t])
+ * Each expert's weights are streamed once per call however many routes
+ * chose it (unless MOE_F_NO_DEDUP).
+ * In:  x [B,H], gate_up [E,2I,H], down [E,H,I], expert_ids/route_w [B,k],
+ *      the grouping from moe_group_by_expert (offsets, route_idx,
+ *      unique_experts, num_unique), residual [B,H] fp32 or NULL.
+ * Out: y [B,H] fp32.  y may alias residual (in-place residual add).
+ */
+int moe_expert_forward(const void* x, int x_dtype, const uint16_t* gate_up, const uint16_t* down,
+                       const int32_t* expert_ids, const float* route_w, const int32_t* offsets,
+                       const int32_t* route_idx, const int32_t* unique_experts,
+                       const int32_t* num_unique, int B, int H, int I, int E, int top_k,
+                       const float* residual, float* y, uint32_t flags, void* workspace,
+                       size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * moe_layer_forward -- the whole layer: moe_route, moe_group_by_expert and
+ * moe_expert_forward in one enqueue.  Unless MOE_F_UNFUSED, the phases run in
+ * one persistent cooperative kernel (one CTA per SM, device-wide barriers
+ * with a bounded wait).
+ * Out: y [B,H] fp32 (may alias residual); expert_ids_out / route_w_out
+ *      [B,k] (may be NULL).
+ */
+int moe_layer_forward(const void* x, int x_dtype, const uint16_t* w_router,
+                      const float* logit_bias, const uint16_t* gate_up, const uint16_t* down,
+                      int B, int H, int I, int E, int top_k, const float* residual, float* y,
+                      int32_t* expert_ids_out, float* route_w_out, uint32_t flags,
+                      void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                      void* stream);
+
+/*
+ * moe_stack_forward -- L MoE layers with the residual add between them,
+ *   x <- x + layer_l(x),  l = 0..L-1,
+ * entirely on the device ("TEXT Generation Optimization Report", optimized
+ * forward flow: the layer loop runs with no wait; "MoE Performance
+ * Optimization Analysis": GPU routing removes the per-layer router wait).
+ * w_router, logit_bias, gate_up and down are HOST arrays of L device
+ * pointers (logit_bias itself, or any of its entries, may be NULL).
+ * x_inout [B,H] fp32 is updated in place.  expert_ids_out [L,B,k] or NULL.
+ */
+int moe_stack_forward(int L, const uint16_t* const* w_router, const float* const* logit_bias,
+                      const uint16_t* const* gate_up, const uint16_t* const* down, int B, int H,
+                      int I, int E, int top_k, float* x_inout, int32_t* expert_ids_out,
+                      uint32_t flags, void* workspace, size_t workspace_bytes,
+                      int32_t* dev_status, void* stream);
+
+/* moe_status_string -- static text for a moe_status code or MOE_DEV_* bit. */
+const char* moe_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

@@ -1,0 +1,224 @@
+"""Python binding of libmoe.so -- argument marshalling only.
+
+Every step of the layer runs in the CUDA library; this module allocates the
+output tensors and the workspace with torch (device memory and streams are
+all torch is used for) and passes raw pointers through the C ABI declared in
+``include/moe.h``.  It raises ImportError when the library has not been
+built: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+if not os.path.exists(_build.LIB):
+    raise ImportError(f"{_build.LIB} is missing: build it first with "
+                      "moe_decode_layer_gemv_gb300.build.build()")
+
+_lib = ctypes.CDLL(_build.LIB)
+LIB_PATH = _build.LIB
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_U = ctypes.c_uint32
+_S = ctypes.c_size_t
+
+_lib.moe_workspace_bytes.argtypes = [_I, _I, _I, _I, _I, ctypes.POINTER(_S)]
+_lib.moe_route.argtypes = [_P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _S, _P, _P]
+_lib.moe_group_by_expert.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]
+_lib.moe_expert_forward.argtypes = [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                    _P, _P, _U, _P, _S, _P, _P]
+_lib.moe_layer_forward.argtypes = [_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _U,
+                                   _P, _S, _P, _P]
+_lib.moe_stack_forward.argtypes = [_I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _U, _P, _S, _P, _P]
+_lib.moe_status_string.argtypes = [_I]
+_lib.moe_status_string.restype = ctypes.c_char_p
+for _f in ("moe_workspace_bytes", "moe_route", "moe_group_by_expert", "moe_expert_forward",
+           "moe_layer_forward", "moe_stack_forward"):
+    getattr(_lib, _f).restype = ctypes.c_int
+
+EXPORTED = ("moe_workspace_bytes", "moe_route", "moe_group_by_expert", "moe_expert_forward",
+            "moe_layer_forward", "moe_stack_forward", "moe_status_string")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = -1
+MOE_ERR_UNSUPPORTED = -2
+MOE_ERR_CUDA = -3
+MOE_ERR_WORKSPACE = -4
+MOE_DEV_TIMEOUT = 1
+MOE_DEV_BAD_EXPERT_ID = 2
+MOE_DEV_DUP_EXPERT = 4
+MOE_DEV_NONFINITE = 8
+MOE_DT_F32 = 0
+MOE_DT_BF16 = 1
+MOE_F_NO_DEDUP = 1
+MOE_F_UNFUSED = 2
+MAX_E, MAX_TOPK, MAX_B, MAX_DIM, MAX_LAYERS = 256, 8, 1024, 16384, 64
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__(f"{fn} returned {code}: {status_string(code)}")
+        self.code = code
+
+
+def status_string(code: int) -> str:
+    return _lib.moe_status_string(int(code)).decode()
+
+
+def _check(rc, fn):
+    if rc != MOE_OK:
+        raise MoeError(fn, rc)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _x_dtype(x):
+    if x.dtype == torch.float32:
+        return MOE_DT_F32
+    if x.dtype == torch.bfloat16:
+        return MOE_DT_BF16
+    raise TypeError("x must be float32 or bfloat16")
+
+
+def _need(t, dtype, name):
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+
+
+def workspace_bytes(B, H, I, E, top_k) -> int:
+    n = _S(0)
+    _check(_lib.moe_workspace_bytes(B, H, I, E, top_k, ctypes.byref(n)), "moe_workspace_bytes")
+    return n.value
+
+
+def new_workspace(B, H, I, E, top_k, device=None) -> torch.Tensor:
+    n = workspace_bytes(B, H, I, E, top_k)
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def new_status(device=None) -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def route(x, w_router, top_k, bias=None, stream=None, status=None):
+    """-> (expert_ids [B,k] int32, route_w [B,k] fp32, logits [B,E] fp32)."""
+    _need(w_router, torch.bfloat16, "w_router")
+    B, H = x.shape
+    E = w_router.shape[0]
+    ids = torch.empty((B, top_k), dtype=torch.int32, device=x.device)
+    w = torch.empty((B, top_k), dtype=torch.float32, device=x.device)
+    logits = torch.empty((B, E), dtype=torch.float32, device=x.device)
+    _check(_lib.moe_route(_ptr(x), _x_dtype(x), _ptr(w_router), _ptr(bias), B, H, E, top_k, _ptr(ids),
+                          _ptr(w), _ptr(logits), None, 0, _ptr(status), _stream(stream)), "moe_route")
+    return ids, w, logits
+
+
+def group_by_expert(expert_ids, E, stream=None, status=None):
+    """-> (offsets [E+1], route_idx [R], unique [E] (first num_unique valid), num_unique [1])."""
+    _need(expert_ids, torch.int32, "expert_ids")
+    B, k = expert_ids.shape
+    dev = expert_ids.device
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    ridx = torch.empty(max(B * k, 1), dtype=torch.int32, device=dev)
+    uniq = torch.empty(E, dtype=torch.int32, device=dev)
+    nu = torch.empty(1, dtype=torch.int32, device=dev)
+    _check(_lib.moe_group_by_expert(_ptr(expert_ids), B, k, E, _ptr(offsets), _ptr(ridx), _ptr(uniq),
+                                    _ptr(nu), _ptr(status), _stream(stream)), "moe_group_by_expert")
+    return offsets, ridx[:B * k], uniq, nu
+
+
+def expert_forward(x, gate_up, down, expert_ids, route_w, grouping, residual=None, flags=0,
+                   out=None, workspace=None, status=None, stream=None):
+    """y [B,H] fp32 = sum_j w * down_e(SiLU(gate_e x) * up_e x) (+ residual)."""
+    _need(gate_up, torch.bfloat16, "gate_up")
+    _need(down, torch.bfloat16, "down")
+    B, H = x.shape
+    E, twoI, _ = gate_up.shape
+    I = twoI // 2
+    k = expert_ids.shape[1]
+    offsets, ridx, uniq, nu = grouping
+    y = out if out is not None else torch.empty((B, H), dtype=torch.float32, device=x.device)
+    ws = workspace if workspace is not None else new_workspace(B, H, I, E, k, x.device)
+    _check(_lib.moe_expert_forward(_ptr(x), _x_dtype(x), _ptr(gate_up), _ptr(down), _ptr(expert_ids),
+                                   _ptr(route_w), _ptr(offsets), _ptr(ridx), _ptr(uniq), _ptr(nu), B, H,
+                                   I, E, k, _ptr(residual), _ptr(y), flags, _ptr(ws), ws.numel(),
+                                   _ptr(status), _stream(stream)), "moe_expert_forward")
+    return y
+
+
+def layer_forward(x, w_router, gate_up, down, top_k, bias=None, residual=None, flags=0, out=None,
+                  ids_out=None, w_out=None, workspace=None, status=None, stream=None):
+    """Whole layer -> (y [B,H] fp32, expert_ids [B,k], route_w [B,k])."""
+    for t, n in ((w_router, "w_router"), (gate_up, "gate_up"), (down, "down")):
+        _need(t, torch.bfloat16, n)
+    B, H = x.shape
+    E, twoI, _ = gate_up.shape
+    I = twoI // 2
+    dev = x.device
+    y = out if out is not None else torch.empty((B, H), dtype=torch.float32, device=dev)
+    ids = ids_out if ids_out is not None else torch.empty((B, top_k), dtype=torch.int32, device=dev)
+    w = w_out if w_out is not None else torch.empty((B, top_k), dtype=torch.float32, device=dev)
+    ws = workspace if workspace is not None else new_workspace(B, H, I, E, top_k, dev)
+    _check(_lib.moe_layer_forward(_ptr(x), _x_dtype(x), _ptr(w_router), _ptr(bias), _ptr(gate_up),
+                                  _ptr(down), B, H, I, E, top_k, _ptr(residual), _ptr(y), _ptr(ids),
+                                  _ptr(w), flags, _ptr(ws), ws.numel(), _ptr(status), _stream(stream)),
+           "moe_layer_forward")
+    return y, ids, w
+
+
+class StackWeights:
+    """Host pointer tables for moe_stack_forward (built once, reused)."""
+
+    def __init__(self, layers):
+        self.layers = layers
+        L = len(layers)
+        self.L = L
+        self.wr = (ctypes.c_void_p * L)(*[l["w_router"].data_ptr() for l in layers])
+        self.gu = (ctypes.c_void_p * L)(*[l["gate_up"].data_ptr() for l in layers])
+        self.dn = (ctypes.c_void_p * L)(*[l["down"].data_ptr() for l in layers])
+        has_bias = any(l.get("bias") is not None for l in layers)
+        self.bias = ((ctypes.c_void_p * L)(*[(l["bias"].data_ptr() if l.get("bias") is not None else None)
+                                             for l in layers]) if has_bias else None)
+        g = layers[0]["gate_up"]
+        self.E, twoI, self.H = g.shape
+        self.I = twoI // 2
+        for l in layers:
+            for n in ("w_router", "gate_up", "down"):
+                _need(l[n], torch.bfloat16, n)
+
+
+def stack_forward_(x, stack: StackWeights, top_k, flags=0, ids_out=None, workspace=None, status=None,
+                   stream=None):
+    """In place: x [B,H] fp32 <- x + layer_l(x) for every layer.  Returns x."""
+    _need(x, torch.float32, "x")
+    B, H = x.shape
+    ws = workspace if workspace is not None else new_workspace(B, H, stack.I, stack.E, top_k, x.device)
+    _check(_lib.moe_stack_forward(stack.L, ctypes.addressof(stack.wr),
+                                  ctypes.addressof(stack.bias) if stack.bias is not None else None,
+                                  ctypes.addressof(stack.gu), ctypes.addressof(stack.dn), B, H, stack.I,
+                                  stack.E, top_k, _ptr(x), _ptr(ids_out), flags, _ptr(ws), ws.numel(),
+                                  _ptr(status), _stream(stream)), "moe_stack_forward")
+    return x
+
+
+def stack_forward(x, layers, top_k, flags=0, stream=None, status=None):
+    """Out of place: returns (x_out, ids [L,B,k])."""
+    st = layers if isinstance(layers, StackWeights) else StackWeights(layers)
+    xo = x.to(torch.float32).clone()
+    ids = torch.empty((st.L, x.shape[0], top_k), dtype=torch.int32, device=x.device)
+    stack_forward_(xo, st, top_k, flags=flags, ids_out=ids, status=status, stream=stream)
+    return xo, ids

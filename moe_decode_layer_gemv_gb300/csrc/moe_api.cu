@@ -1,0 +1,530 @@
+// moe_api.cu -- the C ABI of libmoe.so (declared in include/moe.h): argument
+// checks, workspace layout and kernel launches.  The kernels are built from
+// the phase functions in moe_phases.cuh, either one kernel per phase or all
+// phases (and all layers of a stack) in one persistent cooperative kernel.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "moe.h"
+#include "moe_common.cuh"
+#include "moe_phases.cuh"
+
+namespace moe {
+
+// ------------------------------------------------------------ grid barrier
+// Device-wide barrier for the persistent kernel.  A monotonically increasing
+// arrival counter (zeroed by the host before the launch): barrier number n
+// completes when the counter reaches n * gridDim.x.  Every wait is bounded;
+// a CTA that gives up sets MOE_DEV_TIMEOUT and the abort word, and every
+// CTA then leaves the kernel at its next barrier.
+constexpr unsigned long long kSpinLimit = 1ull << 22;
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_add_u32(unsigned* p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ bool grid_sync(unsigned* bar, unsigned& epoch, int32_t* status) {
+    __shared__ int s_ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        epoch += 1;
+        const unsigned target = epoch * gridDim.x;
+        __threadfence();
+        red_release_add_u32(bar, 1u);
+        int ok = 1;
+        unsigned long long spins = 0;
+        while (ld_acquire_u32(bar) < target) {
+            ++spins;
+            if ((spins & 255ull) == 0 && ld_acquire_u32(bar + 1) != 0u) {
+                ok = 0;
+                break;
+            }
+            if (spins > kSpinLimit) {
+                set_status(status, MOE_DEV_TIMEOUT);
+                atomicExch(bar + 1, 1u);
+                ok = 0;
+                break;
+            }
+            if (spins > 32) __nanosleep(64);
+        }
+        __threadfence();
+        s_ok = ok;
+    }
+    __syncthreads();
+    return s_ok != 0;
+}
+
+// ----------------------------------------------------------------- kernels
+struct StackArgs {
+    LayerWeights layer[MOE_MAX_LAYERS];
+    int L;
+    int32_t* ids_out;  // [L, B, k] or nullptr
+};
+
+__global__ void __launch_bounds__(kThreads) router_kernel(Ctx c) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    router_item(c, blockIdx.x, reinterpret_cast<float*>(smem));
+}
+
+__global__ void __launch_bounds__(kThreads) topk_kernel(Ctx c) {
+    topk_item(c, blockIdx.x, c.ids, c.rw);
+}
+
+__global__ void __launch_bounds__(kThreads) group_kernel(const int32_t* ids, int B, int k, int E,
+                                                         int32_t* offsets, int32_t* route_idx,
+                                                         int32_t* unique, int32_t* num_unique,
+                                                         int32_t* status) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    group_cta(ids, B, k, E, offsets, route_idx, unique, num_unique, status,
+              reinterpret_cast<uint32_t*>(smem));
+}
+
+__device__ __forceinline__ void split_smem(const Ctx& c, unsigned char* smem, float*& act, int*& idx) {
+    const int dim = c.H > c.I ? c.H : c.I;
+    act = reinterpret_cast<float*>(smem);
+    idx = reinterpret_cast<int*>(smem + sizeof(float) * (size_t)c.nt_max * dim);
+}
+
+__global__ void __launch_bounds__(kThreads) gateup_kernel(Ctx c) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    float* xs;
+    int* tok;
+    split_smem(c, smem, xs, tok);
+    gateup_item(c, blockIdx.x, xs, tok);
+}
+
+__global__ void __launch_bounds__(kThreads) down_kernel(Ctx c) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    float* hs;
+    int* rts;
+    split_smem(c, smem, hs, rts);
+    down_item(c, blockIdx.x, hs, rts);
+}
+
+__global__ void __launch_bounds__(kThreads) combine_kernel(Ctx c) { combine_item(c, blockIdx.x); }
+
+// All phases of L layers in one launch.  For L > 1 (a stack) x, residual and
+// y all point at the fp32 residual stream, updated in place by the combine.
+__global__ void __launch_bounds__(kThreads) fused_kernel(Ctx c, StackArgs sa, unsigned* bar) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    float* act;
+    int* idx;
+    split_smem(c, smem, act, idx);
+    unsigned epoch = 0;
+    int32_t* ids_base = c.ids;
+    for (int l = 0; l < sa.L; ++l) {
+        c.w = sa.layer[l];
+        c.ids = sa.ids_out ? sa.ids_out + (size_t)l * c.B * c.k : ids_base;
+        for (int it = blockIdx.x; it < router_items(c); it += gridDim.x)
+            router_item(c, it, reinterpret_cast<float*>(smem));
+        if (!grid_sync(bar, epoch, c.status)) return;
+        for (int it = blockIdx.x; it < topk_items(c); it += gridDim.x) topk_item(c, it, c.ids, c.rw);
+        if (!grid_sync(bar, epoch, c.status)) return;
+        if (blockIdx.x == 0)
+            group_cta(c.ids, c.B, c.k, c.E, c.offsets, c.route_idx, c.unique, c.num_unique, c.status,
+                      reinterpret_cast<uint32_t*>(smem));
+        if (!grid_sync(bar, epoch, c.status)) return;
+        for (int it = blockIdx.x; it < gateup_items(c); it += gridDim.x) gateup_item(c, it, act, idx);
+        if (!grid_sync(bar, epoch, c.status)) return;
+        for (int it = blockIdx.x; it < down_items(c); it += gridDim.x) down_item(c, it, act, idx);
+        if (!grid_sync(bar, epoch, c.status)) return;
+        for (int it = blockIdx.x; it < combine_items(c); it += gridDim.x) combine_item(c, it);
+        if (l + 1 < sa.L && !grid_sync(bar, epoch, c.status)) return;
+    }
+}
+
+// -------------------------------------------------------------- host side
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct WsLayout {
+    size_t logits, ids, rw, offsets, route_idx, unique, num_unique, status, bar, h, o, total;
+};
+
+static WsLayout ws_layout(int B, int H, int I, int E, int k) {
+    WsLayout L;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + (bytes > 0 ? bytes : 1), 256);
+        return at;
+    };
+    const size_t R = (size_t)B * k;
+    L.logits = take(sizeof(float) * (size_t)B * E);
+    L.ids = take(sizeof(int32_t) * R);
+    L.rw = take(sizeof(float) * R);
+    L.offsets = take(sizeof(int32_t) * (E + 1));
+    L.route_idx = take(sizeof(int32_t) * R);
+    L.unique = take(sizeof(int32_t) * E);
+    L.num_unique = take(sizeof(int32_t));
+    L.status = take(sizeof(int32_t));
+    L.bar = take(sizeof(unsigned) * 2);
+    L.h = take(sizeof(float) * R * I);
+    L.o = take(sizeof(float) * R * H);
+    L.total = off;
+    return L;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int check_dims(int B, int H, int I, int E, int k, bool need_I) {
+    if (B < 0 || B > MOE_MAX_B) return MOE_ERR_INVALID_ARG;
+    if (E < 1 || E > MOE_MAX_E) return MOE_ERR_INVALID_ARG;
+    if (k < 1 || k > E || k > MOE_MAX_TOPK) return MOE_ERR_INVALID_ARG;
+    if (H < 8 || H > MOE_MAX_DIM || (H & 7)) return MOE_ERR_INVALID_ARG;
+    if (need_I && (I < 8 || I > MOE_MAX_DIM || (I & 7))) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+#define MOE_REQ(p) \
+    do {           \
+        if (!(p) || !aligned16(p)) return MOE_ERR_INVALID_ARG; \
+    } while (0)
+#define MOE_OPT(p) \
+    do {           \
+        if ((p) && !aligned16(p)) return MOE_ERR_INVALID_ARG; \
+    } while (0)
+
+static int nt_max_for(int H, int I) {
+    const int dim = H > I ? H : I;
+    int nt = 8;
+    while (nt > 1 && (size_t)nt * dim * sizeof(float) > 64 * 1024) nt >>= 1;
+    return nt;
+}
+
+static size_t act_smem(int H, int I) {
+    const int dim = H > I ? H : I;
+    return sizeof(float) * (size_t)nt_max_for(H, I) * dim + 64;
+}
+
+static size_t fused_smem(int B, int H, int I, int E) {
+    size_t s = act_smem(H, I);
+    if (kRouterSmem > s) s = kRouterSmem;
+    const size_t g = group_smem_bytes(B, E);
+    if (g > s) s = g;
+    return align_up(s, 16);
+}
+
+static int to_status(cudaError_t e) {
+    if (e == cudaSuccess) return MOE_OK;
+    return MOE_ERR_CUDA;
+}
+
+static int launch_check() { return to_status(cudaGetLastError()); }
+
+// dynamic shared memory above 48 KB needs an opt-in per kernel and device
+template <typename K>
+static int allow_smem(K kernel, size_t bytes) {
+    if (bytes <= 48 * 1024) return MOE_OK;
+    return to_status(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes));
+}
+
+static Ctx make_ctx(const void* x, int x_dtype, const float* residual, float* y, int B, int H, int I,
+                    int E, int k, unsigned flags, char* ws, const WsLayout& L, int32_t* status) {
+    Ctx c;
+    memset(&c, 0, sizeof c);
+    c.x = x;
+    c.x_bf16 = x_dtype == MOE_DT_BF16;
+    c.residual = residual;
+    c.y = y;
+    c.B = B;
+    c.H = H;
+    c.I = I;
+    c.E = E;
+    c.k = k;
+    c.flags = flags;
+    c.nt_max = nt_max_for(H, I);
+    if (ws) {
+        c.logits = reinterpret_cast<float*>(ws + L.logits);
+        c.ids = reinterpret_cast<int32_t*>(ws + L.ids);
+        c.rw = reinterpret_cast<float*>(ws + L.rw);
+        c.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+        c.route_idx = reinterpret_cast<int32_t*>(ws + L.route_idx);
+        c.unique = reinterpret_cast<int32_t*>(ws + L.unique);
+        c.num_unique = reinterpret_cast<int32_t*>(ws + L.num_unique);
+        c.h = reinterpret_cast<float*>(ws + L.h);
+        c.o = reinterpret_cast<float*>(ws + L.o);
+        c.status = status ? status : reinterpret_cast<int32_t*>(ws + L.status);
+    } else {
+        c.status = status;
+    }
+    return c;
+}
+
+static int launch_route(const Ctx& c, cudaStream_t st) {
+    int rc = allow_smem(router_kernel, kRouterSmem);
+    if (rc) return rc;
+    router_kernel<<<router_items(c), kThreads, kRouterSmem, st>>>(c);
+    if ((rc = launch_check())) return rc;
+    topk_kernel<<<topk_items(c), kThreads, 0, st>>>(c);
+    return launch_check();
+}
+
+static int launch_group(const int32_t* ids, int B, int k, int E, int32_t* offsets, int32_t* route_idx,
+                        int32_t* unique, int32_t* num_unique, int32_t* status, cudaStream_t st) {
+    const size_t smem = group_smem_bytes(B, E);
+    int rc = allow_smem(group_kernel, smem);
+    if (rc) return rc;
+    group_kernel<<<1, kThreads, smem, st>>>(ids, B, k, E, offsets, route_idx, unique, num_unique, status);
+    return launch_check();
+}
+
+static int launch_experts(const Ctx& c, cudaStream_t st) {
+    const size_t smem = act_smem(c.H, c.I);
+    int rc = allow_smem(gateup_kernel, smem);
+    if (rc) return rc;
+    if ((rc = allow_smem(down_kernel, smem))) return rc;
+    gateup_kernel<<<gateup_items(c), kThreads, smem, st>>>(c);
+    if ((rc = launch_check())) return rc;
+    down_kernel<<<down_items(c), kThreads, smem, st>>>(c);
+    if ((rc = launch_check())) return rc;
+    combine_kernel<<<combine_items(c), kThreads, 0, st>>>(c);
+    return launch_check();
+}
+
+static int launch_unfused_layer(const Ctx& c, cudaStream_t st) {
+    int rc = launch_route(c, st);
+    if (rc) return rc;
+    rc = launch_group(c.ids, c.B, c.k, c.E, c.offsets, c.route_idx, c.unique, c.num_unique, c.status, st);
+    if (rc) return rc;
+    return launch_experts(c, st);
+}
+
+static int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+static int launch_fused(const Ctx& c, const StackArgs& sa, unsigned* bar, cudaStream_t st) {
+    const size_t smem = fused_smem(c.B, c.H, c.I, c.E);
+    int rc = allow_smem(fused_kernel, smem);
+    if (rc) return rc;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_kernel, kThreads, smem) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    const int sms = sm_count();
+    if (per_sm < 1 || sms < 1) return MOE_ERR_UNSUPPORTED;
+    if (per_sm > 2) per_sm = 2;
+    if ((rc = to_status(cudaMemsetAsync(bar, 0, 2 * sizeof(unsigned), st)))) return rc;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)(sms * per_sm));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return to_status(cudaLaunchKernelEx(&cfg, fused_kernel, c, sa, bar));
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_workspace_bytes(int B, int H, int I, int E, int top_k, size_t* bytes) {
+    if (!bytes) return MOE_ERR_INVALID_ARG;
+    const int rc = check_dims(B, H, I, E, top_k, true);
+    if (rc) return rc;
+    *bytes = ws_layout(B, H, I, E, top_k).total;
+    return MOE_OK;
+}
+
+int moe_route(const void* x, int x_dtype, const uint16_t* w_router, const float* logit_bias, int B,
+              int H, int E, int top_k, int32_t* expert_ids, float* route_w, float* logits_out,
+              void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    int rc = check_dims(B, H, 8, E, top_k, false);
+    if (rc) return rc;
+    if (x_dtype != MOE_DT_F32 && x_dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
+    MOE_REQ(x);
+    MOE_REQ(w_router);
+    MOE_REQ(expert_ids);
+    MOE_REQ(route_w);
+    MOE_OPT(logit_bias);
+    MOE_OPT(logits_out);
+    MOE_OPT(workspace);
+    MOE_OPT(dev_status);
+    const WsLayout L = ws_layout(B, H, 8, E, top_k);
+    if (!logits_out && (!workspace || workspace_bytes < L.logits + sizeof(float) * (size_t)B * E))
+        return MOE_ERR_WORKSPACE;
+    if (B == 0) return MOE_OK;
+    Ctx c = make_ctx(x, x_dtype, nullptr, nullptr, B, H, 8, E, top_k, 0, nullptr, L, dev_status);
+    c.w.w_router = w_router;
+    c.w.bias = logit_bias;
+    c.logits = logits_out ? logits_out : reinterpret_cast<float*>(static_cast<char*>(workspace) + L.logits);
+    c.ids = expert_ids;
+    c.rw = route_w;
+    return launch_route(c, static_cast<cudaStream_t>(stream));
+}
+
+int moe_group_by_expert(const int32_t* expert_ids, int B, int top_k, int E, int32_t* offsets,
+                        int32_t* route_idx, int32_t* unique_experts, int32_t* num_unique,
+                        int32_t* dev_status, void* stream) {
+    int rc = check_dims(B, 8, 8, E, top_k, false);
+    if (rc) return rc;
+    MOE_REQ(expert_ids);
+    MOE_REQ(offsets);
+    MOE_REQ(route_idx);
+    MOE_REQ(unique_experts);
+    MOE_REQ(num_unique);
+    MOE_OPT(dev_status);
+    return launch_group(expert_ids, B, top_k, E, offsets, route_idx, unique_experts, num_unique, dev_status,
+                        static_cast<cudaStream_t>(stream));
+}
+
+int moe_expert_forward(const void* x, int x_dtype, const uint16_t* gate_up, const uint16_t* down,
+                       const int32_t* expert_ids, const float* route_w, const int32_t* offsets,
+                       const int32_t* route_idx, const int32_t* unique_experts,
+                       const int32_t* num_unique, int B, int H, int I, int E, int top_k,
+                       const float* residual, float* y, uint32_t flags, void* workspace,
+                       size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    int rc = check_dims(B, H, I, E, top_k, true);
+    if (rc) return rc;
+    if (x_dtype != MOE_DT_F32 && x_dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
+    if (flags & ~(MOE_F_NO_DEDUP | MOE_F_UNFUSED)) return MOE_ERR_INVALID_ARG;
+    MOE_REQ(x);
+    MOE_REQ(gate_up);
+    MOE_REQ(down);
+    MOE_REQ(expert_ids);
+    MOE_REQ(route_w);
+    MOE_REQ(offsets);
+    MOE_REQ(route_idx);
+    MOE_REQ(unique_experts);
+    MOE_REQ(num_unique);
+    MOE_REQ(y);
+    MOE_OPT(residual);
+    MOE_REQ(workspace);
+    MOE_OPT(dev_status);
+    const WsLayout L = ws_layout(B, H, I, E, top_k);
+    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+    if (B == 0) return MOE_OK;
+    Ctx c = make_ctx(x, x_dtype, residual, y, B, H, I, E, top_k, flags, static_cast<char*>(workspace), L,
+                     dev_status);
+    c.ids = const_cast<int32_t*>(expert_ids);
+    c.rw = const_cast<float*>(route_w);
+    c.offsets = const_cast<int32_t*>(offsets);
+    c.route_idx = const_cast<int32_t*>(route_idx);
+    c.unique = const_cast<int32_t*>(unique_experts);
+    c.num_unique = const_cast<int32_t*>(num_unique);
+    c.w.gate_up = gate_up;
+    c.w.down = down;
+    return launch_experts(c, static_cast<cudaStream_t>(stream));
+}
+
+int moe_layer_forward(const void* x, int x_dtype, const uint16_t* w_router, const float* logit_bias,
+                      const uint16_t* gate_up, const uint16_t* down, int B, int H, int I, int E,
+                      int top_k, const float* residual, float* y, int32_t* expert_ids_out,
+                      float* route_w_out, uint32_t flags, void* workspace, size_t workspace_bytes,
+                      int32_t* dev_status, void* stream) {
+    int rc = check_dims(B, H, I, E, top_k, true);
+    if (rc) return rc;
+    if (x_dtype != MOE_DT_F32 && x_dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
+    if (flags & ~(MOE_F_NO_DEDUP | MOE_F_UNFUSED)) return MOE_ERR_INVALID_ARG;
+    MOE_REQ(x);
+    MOE_REQ(w_router);
+    MOE_REQ(gate_up);
+    MOE_REQ(down);
+    MOE_REQ(y);
+    MOE_OPT(logit_bias);
+    MOE_OPT(residual);
+    MOE_OPT(expert_ids_out);
+    MOE_OPT(route_w_out);
+    MOE_REQ(workspace);
+    MOE_OPT(dev_status);
+    const WsLayout L = ws_layout(B, H, I, E, top_k);
+    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+    if (B == 0) return MOE_OK;
+    char* ws = static_cast<char*>(workspace);
+    Ctx c = make_ctx(x, x_dtype, residual, y, B, H, I, E, top_k, flags, ws, L, dev_status);
+    c.w.w_router = w_router;
+    c.w.bias = logit_bias;
+    c.w.gate_up = gate_up;
+    c.w.down = down;
+    if (expert_ids_out) c.ids = expert_ids_out;
+    if (route_w_out) c.rw = route_w_out;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (flags & MOE_F_UNFUSED) return launch_unfused_layer(c, st);
+    StackArgs sa;
+    memset(&sa, 0, sizeof sa);
+    sa.L = 1;
+    sa.layer[0] = c.w;
+    sa.ids_out = nullptr;
+    return launch_fused(c, sa, reinterpret_cast<unsigned*>(ws + L.bar), st);
+}
+
+int moe_stack_forward(int Lc, const uint16_t* const* w_router, const float* const* logit_bias,
+                      const uint16_t* const* gate_up, const uint16_t* const* down, int B, int H,
+                      int I, int E, int top_k, float* x_inout, int32_t* expert_ids_out,
+                      uint32_t flags, void* workspace, size_t workspace_bytes,
+                      int32_t* dev_status, void* stream) {
+    int rc = check_dims(B, H, I, E, top_k, true);
+    if (rc) return rc;
+    if (Lc < 1 || Lc > MOE_MAX_LAYERS) return MOE_ERR_INVALID_ARG;
+    if (flags & ~(MOE_F_NO_DEDUP | MOE_F_UNFUSED)) return MOE_ERR_INVALID_ARG;
+    if (!w_router || !gate_up || !down) return MOE_ERR_INVALID_ARG;
+    for (int l = 0; l < Lc; ++l) {
+        MOE_REQ(w_router[l]);
+        MOE_REQ(gate_up[l]);
+        MOE_REQ(down[l]);
+        if (logit_bias) MOE_OPT(logit_bias[l]);
+    }
+    MOE_REQ(x_inout);
+    MOE_OPT(expert_ids_out);
+    MOE_REQ(workspace);
+    MOE_OPT(dev_status);
+    const WsLayout L = ws_layout(B, H, I, E, top_k);
+    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+    if (B == 0) return MOE_OK;
+    char* ws = static_cast<char*>(workspace);
+    Ctx c = make_ctx(x_inout, MOE_DT_F32, x_inout, x_inout, B, H, I, E, top_k, flags, ws, L, dev_status);
+    StackArgs sa;
+    memset(&sa, 0, sizeof sa);
+    sa.L = Lc;
+    sa.ids_out = expert_ids_out;
+    for (int l = 0; l < Lc; ++l) {
+        sa.layer[l].w_router = w_router[l];
+        sa.layer[l].bias = logit_bias ? logit_bias[l] : nullptr;
+        sa.layer[l].gate_up = gate_up[l];
+        sa.layer[l].down = down[l];
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (flags & MOE_F_UNFUSED) {
+        int32_t* ids_ws = c.ids;
+        for (int l = 0; l < Lc; ++l) {
+            c.w = sa.layer[l];
+            c.ids = expert_ids_out ? expert_ids_out + (size_t)l * B * top_k : ids_ws;
+            if ((rc = launch_unfused_layer(c, st))) return rc;
+        }
+        return MOE_OK;
+    }
+    return launch_fused(c, sa, reinterpret_cast<unsigned*>(ws + L.bar), st);
+}
+
+const char* moe_status_string(int code) {
+    switch (code) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument (shape, limit, null or misaligned pointer)";
+        case MOE_ERR_UNSUPPORTED: return "unsupported configuration on this device";
+        case MOE_ERR_CUDA: return "CUDA launch or runtime error";
+        case MOE_ERR_WORKSPACE: return "workspace missing or smaller than moe_workspace_bytes()";
+        case MOE_DEV_TIMEOUT: return "device: a grid barrier timed out";
+        case MOE_DEV_BAD_EXPERT_ID: return "device: expert id outside [0, E)";
+        case MOE_DEV_DUP_EXPERT: return "device: a token lists the same expert twice";
+        case MOE_DEV_NONFINITE: return "device: non-finite router logit";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,119 @@
+// moe_common.cuh -- shared device helpers of the MoE decode library (sm_103a).
+//
+// Loads: weights are read once per step and never reused by the same SM, so
+// they go through the non-coherent path without L1 allocation and with a
+// 256-byte L2 prefetch; activations written earlier in the same launch (x of
+// a stacked layer, h, logits, ids) are read with ld.global.cg so that no SM
+// can see a stale L1 line after a device-wide barrier.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+constexpr int kThreads = 256;  // threads per CTA in every streaming phase
+constexpr int kWarps = kThreads / 32;
+
+__host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// ---------------------------------------------------------------- loads
+__device__ __forceinline__ uint4 ld_weight_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ float4 ld_act_f4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
+__device__ __forceinline__ uint4 ld_act_u4(const void* p) { return __ldcg(reinterpret_cast<const uint4*>(p)); }
+__device__ __forceinline__ float ld_act_f(const float* p) { return __ldcg(p); }
+__device__ __forceinline__ int ld_act_i(const int32_t* p) { return __ldcg(p); }
+
+// two bf16 packed in a 32-bit word -> (low element, high element) as fp32 (exact)
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t u) {
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+__device__ __forceinline__ void set_status(int32_t* status, int bits) {
+    if (status) atomicOr(status, bits);
+}
+
+// ------------------------------------------------------------ problem view
+struct LayerWeights {
+    const uint16_t* w_router;  // [E, H]
+    const float* bias;         // [E] or nullptr
+    const uint16_t* gate_up;   // [E, 2I, H]
+    const uint16_t* down;      // [E, H, I]
+};
+
+// Everything one layer step needs.  Built on the host, passed by value.
+struct Ctx {
+    const void* x;        // [B, H] fp32 or bf16
+    int x_bf16;
+    const float* residual;  // [B, H] or nullptr
+    float* y;               // [B, H]
+    LayerWeights w;
+    int B, H, I, E, k;
+    unsigned flags;
+    int nt_max;  // tokens staged per pass in the grouped GEMV phases (1, 2, 4 or 8)
+    // routing (device)
+    float* logits;       // [B, E]
+    int32_t* ids;        // [B, k]
+    float* rw;           // [B, k]
+    int32_t* offsets;    // [E + 1]
+    int32_t* route_idx;  // [R]
+    int32_t* unique;     // [E]
+    int32_t* num_unique; // [1]
+    // scratch (device)
+    float* h;  // [R, I]  per position in the grouped route list
+    float* o;  // [R, H]  per flat route r = t*k + j
+    int32_t* status;
+};
+
+// A segment is a run of routes that share one expert: one unique expert in
+// the grouped list, or (MOE_F_NO_DEDUP) a single route.
+struct Seg {
+    int e, p0, p1;
+};
+
+__host__ __device__ __forceinline__ bool no_dedup(const Ctx& c) { return (c.flags & MOE_F_NO_DEDUP) != 0; }
+
+__host__ __device__ __forceinline__ int max_segments(const Ctx& c) {
+    const int R = c.B * c.k;
+    return no_dedup(c) ? R : (R < c.E ? R : c.E);
+}
+
+__device__ __forceinline__ bool get_seg(const Ctx& c, int s, Seg& sg) {
+    if (no_dedup(c)) {
+        if (s >= c.B * c.k) return false;
+        sg.e = ld_act_i(c.ids + s);
+        sg.p0 = s;
+        sg.p1 = s + 1;
+    } else {
+        if (s >= ld_act_i(c.num_unique)) return false;
+        sg.e = ld_act_i(c.unique + s);
+        sg.p0 = ld_act_i(c.offsets + sg.e);
+        sg.p1 = ld_act_i(c.offsets + sg.e + 1);
+    }
+    // a grouping handed in by the caller is trusted only within bounds
+    return sg.e >= 0 && sg.e < c.E && sg.p0 >= 0 && sg.p1 > sg.p0 && sg.p1 <= c.B * c.k;
+}
+
+// flat route index r stored at position p of the (grouped) route list
+__device__ __forceinline__ int route_at(const Ctx& c, int p) {
+    return no_dedup(c) ? p : ld_act_i(c.route_idx + p);
+}
+
+}  // namespace moe

@@ -1,0 +1,503 @@
+// moe_phases.cuh -- the steps of one MoE layer as device functions over work
+// items.  Each phase is written as "process item i" so that it runs either
+// as its own kernel (one CTA per item) or inside the persistent fused kernel
+// (items strided over a grid of one CTA per SM, device-wide barriers between
+// phases).  All phases use kThreads = 256 threads per CTA.
+#pragma once
+
+#include "moe_common.cuh"
+
+namespace moe {
+
+// =================================================================== router
+// logits[t,e] = sum_h x[t,h] * W_r[e,h] (+ bias[e]).  ("MoE Performance
+// Optimization Analysis", Batch Router Design: [B,H] -> [B,E] on the GPU.)
+// Item = (8 experts, 8 tokens); one warp per expert row, x staged in shared
+// memory in chunks of kRouterHC columns and reused by all 8 warps.
+constexpr int kRouterTB = 8;
+constexpr int kRouterHC = 1024;
+constexpr size_t kRouterSmem = sizeof(float) * kRouterTB * kRouterHC;  // 32 KB
+
+__host__ __device__ __forceinline__ int router_items(const Ctx& c) {
+    return ceil_div(c.E, kWarps) * ceil_div(c.B, kRouterTB);
+}
+
+// Stage x[tok[q]][hc, hc+hn) (q < nq) into dst[q*ld + ...] as fp32; rows
+// nq..nfill-1 are zero-filled.  tok == nullptr means tok[q] = t0 + q.
+__device__ __forceinline__ void stage_x(const Ctx& c, const int* tok, int t0, int nq, int nfill,
+                                        int hc, int hn, float* dst, int ld) {
+    const int vpr = hn >> 3;  // 8-element vectors per row
+    for (int v = threadIdx.x; v < nfill * vpr; v += blockDim.x) {
+        const int q = v / vpr, i = (v - q * vpr) << 3;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+        if (q < nq) {
+            const int t = tok ? tok[q] : t0 + q;
+            const size_t off = (size_t)t * c.H + hc + i;
+            if (c.x_bf16) {
+                const uint4 u = ld_act_u4(static_cast<const uint16_t*>(c.x) + off);
+                const float2 f0 = bf16x2_to_f2(u.x), f1 = bf16x2_to_f2(u.y);
+                const float2 f2 = bf16x2_to_f2(u.z), f3 = bf16x2_to_f2(u.w);
+                a = make_float4(f0.x, f0.y, f1.x, f1.y);
+                b = make_float4(f2.x, f2.y, f3.x, f3.y);
+            } else {
+                const float* xp = static_cast<const float*>(c.x) + off;
+                a = ld_act_f4(xp);
+                b = ld_act_f4(xp + 4);
+            }
+        }
+        float4* d = reinterpret_cast<float4*>(dst + (size_t)q * ld + i);
+        d[0] = a;
+        d[1] = b;
+    }
+}
+
+__device__ void router_item(const Ctx& c, int item, float* smem) {
+    const int neb = ceil_div(c.E, kWarps);
+    const int eb = item % neb, tb = item / neb;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = eb * kWarps + warp;
+    const int t0 = tb * kRouterTB;
+    const int nt = min(kRouterTB, c.B - t0);
+    float2 acc[kRouterTB];
+#pragma unroll
+    for (int q = 0; q < kRouterTB; ++q) acc[q] = make_float2(0.f, 0.f);
+    for (int hc = 0; hc < c.H; hc += kRouterHC) {
+        const int hn = min(kRouterHC, c.H - hc);
+        __syncthreads();
+        stage_x(c, nullptr, t0, nt, kRouterTB, hc, hn, smem, kRouterHC);
+        __syncthreads();
+        if (e < c.E) {
+            const uint16_t* wrow = c.w.w_router + (size_t)e * c.H + hc;
+            for (int i = lane * 8; i < hn; i += 256) {
+                const uint4 wv = ld_weight_v4(wrow + i);
+                const float2 w0 = bf16x2_to_f2(wv.x), w1 = bf16x2_to_f2(wv.y);
+                const float2 w2 = bf16x2_to_f2(wv.z), w3 = bf16x2_to_f2(wv.w);
+#pragma unroll
+                for (int q = 0; q < kRouterTB; ++q) {
+                    const float4* xp = reinterpret_cast<const float4*>(smem + q * kRouterHC + i);
+                    const float4 xa = xp[0], xb = xp[1];
+                    acc[q] = ffma2(w0, make_float2(xa.x, xa.y), acc[q]);
+                    acc[q] = ffma2(w1, make_float2(xa.z, xa.w), acc[q]);
+                    acc[q] = ffma2(w2, make_float2(xb.x, xb.y), acc[q]);
+                    acc[q] = ffma2(w3, make_float2(xb.z, xb.w), acc[q]);
+                }
+            }
+        }
+    }
+    if (e < c.E) {
+        const float b = c.w.bias ? c.w.bias[e] : 0.f;
+#pragma unroll
+        for (int q = 0; q < kRouterTB; ++q) {
+            const float v = warp_sum(acc[q].x + acc[q].y);
+            if (lane == q && q < nt) c.logits[(size_t)(t0 + q) * c.E + e] = v + b;
+        }
+    }
+}
+
+// ==================================================================== top-k
+// p = softmax(logits[t,:]) in fp32; the k largest logits, descending, ties to
+// the lower expert id; w_j = p_j / sum of the selected p.  ("MoE Performance
+// Optimization Analysis", GPU Router Design: selection on the GPU.)
+// One warp per token; lane l holds experts l, l+32, ... (E <= 256).
+__host__ __device__ __forceinline__ int topk_items(const Ctx& c) { return ceil_div(c.B, kWarps); }
+
+__device__ void topk_item(const Ctx& c, int item, int32_t* ids_out, float* w_out) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = item * kWarps + warp;
+    if (t >= c.B) return;
+    const float* l = c.logits + (size_t)t * c.E;
+    float v[8];
+    bool bad = false;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+        const int e = lane + 32 * s;
+        v[s] = e < c.E ? ld_act_f(l + e) : -INFINITY;
+        if (e < c.E && !isfinite(v[s])) bad = true;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(c.status, MOE_DEV_NONFINITE);
+    unsigned taken = 0;
+    float selv[MOE_MAX_TOPK];
+    int seli[MOE_MAX_TOPK];
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_TOPK; ++j) {
+        selv[j] = -INFINITY;
+        seli[j] = 0;
+        if (j < c.k) {
+            float bv = -INFINITY;
+            int bi = 0x7fffffff;
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const int e = lane + 32 * s;
+                if (e < c.E && !((taken >> s) & 1u) && (v[s] > bv || (v[s] == bv && e < bi))) {
+                    bv = v[s];
+                    bi = e;
+                }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+                if (ov > bv || (ov == bv && oi < bi)) {
+                    bv = ov;
+                    bi = oi;
+                }
+            }
+            if (bi == 0x7fffffff) bi = 0;  // only with non-finite logits (flagged above)
+            if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+            selv[j] = bv;
+            seli[j] = bi;
+        }
+    }
+    const float m = selv[0];
+    float s = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        if (lane + 32 * q < c.E) s += expf(v[q] - m);
+    s = warp_sum(s);
+    if (lane == 0) {
+        float p[MOE_MAX_TOPK];
+        float ssel = 0.f;
+#pragma unroll
+        for (int j = 0; j < MOE_MAX_TOPK; ++j) {
+            p[j] = 0.f;
+            if (j < c.k) {
+                p[j] = expf(selv[j] - m) / s;
+                ssel += p[j];
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < MOE_MAX_TOPK; ++j) {
+            if (j < c.k) {
+                ids_out[(size_t)t * c.k + j] = seli[j];
+                w_out[(size_t)t * c.k + j] = p[j] / ssel;
+            }
+        }
+    }
+}
+
+// ================================================================= grouping
+// Stable counting sort of the flat routes r = t*k + j by expert id, in one
+// CTA.  ("perf(cpu-moe): dedup experts across the batch in pass 1 - #46",
+// commit message: group the routes by expert, counting sort over the ids.)
+// A token selects an expert at most once, so the rank of route (t, j) inside
+// expert e's group is the number of earlier tokens that chose e: a popcount
+// over a per-expert token bitmap.  Deterministic, no atomics-ordered scatter.
+__host__ __device__ __forceinline__ size_t group_smem_bytes(int B, int E) {
+    const int W = (B + 31) / 32;
+    return sizeof(uint32_t) * ((size_t)E * (W > 0 ? W : 1) + 2 * (size_t)E + 2);
+}
+
+__device__ void group_cta(const int32_t* ids, int B, int k, int E, int32_t* offsets,
+                          int32_t* route_idx, int32_t* unique, int32_t* num_unique,
+                          int32_t* status, uint32_t* smem) {
+    const int W = (B + 31) / 32 > 0 ? (B + 31) / 32 : 1;
+    uint32_t* bm = smem;                                  // [E][W]
+    int* cnt = reinterpret_cast<int*>(bm + (size_t)E * W);  // [E]
+    int* off = cnt + E;                                   // [E + 1]
+    const int R = B * k;
+    const int tid = threadIdx.x, nth = blockDim.x;
+    for (int i = tid; i < E * W; i += nth) bm[i] = 0u;
+    __syncthreads();
+    for (int r = tid; r < R; r += nth) {
+        const int e = ld_act_i(ids + r);
+        const int t = r / k;
+        if (e < 0 || e >= E) {
+            set_status(status, MOE_DEV_BAD_EXPERT_ID);
+            continue;
+        }
+        const uint32_t bit = 1u << (t & 31);
+        const uint32_t old = atomicOr(&bm[e * W + (t >> 5)], bit);
+        if (old & bit) set_status(status, MOE_DEV_DUP_EXPERT);
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += nth) {
+        int s = 0;
+        for (int w = 0; w < W; ++w) s += __popc(bm[e * W + w]);
+        cnt[e] = s;
+    }
+    __syncthreads();
+    if (tid < 32) {  // warp 0: exclusive scans of the counts and of the nonzero flags
+        const int lane = tid;
+        int loc[8], locu[8], sum = 0, sumu = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane * 8 + i;
+            const int v = e < E ? cnt[e] : 0;
+            loc[i] = sum;
+            locu[i] = sumu;
+            sum += v;
+            sumu += v > 0 ? 1 : 0;
+        }
+        int inc = sum, incu = sumu;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int a = __shfl_up_sync(0xffffffffu, inc, d);
+            const int b = __shfl_up_sync(0xffffffffu, incu, d);
+            if (lane >= d) {
+                inc += a;
+                incu += b;
+            }
+        }
+        const int ex = inc - sum, exu = incu - sumu;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane * 8 + i;
+            if (e < E) {
+                off[e] = ex + loc[i];
+                offsets[e] = ex + loc[i];
+                if (cnt[e] > 0) unique[exu + locu[i]] = e;
+            }
+        }
+        if (lane == 31) {
+            off[E] = inc;
+            offsets[E] = inc;
+            *num_unique = incu;
+        }
+    }
+    __syncthreads();
+    for (int r = tid; r < R; r += nth) {
+        const int e = ld_act_i(ids + r);
+        if (e < 0 || e >= E) continue;
+        const int t = r / k, w = t >> 5;
+        int rank = __popc(bm[e * W + w] & ((1u << (t & 31)) - 1u));
+        for (int ww = 0; ww < w; ++ww) rank += __popc(bm[e * W + ww]);
+        route_idx[off[e] + rank] = r;
+    }
+}
+
+// ============================================================ gate_up + SiLU
+// For each segment (expert e, its routes) and each gate/up row pair i:
+//   h[p, i] = SiLU(G_e[i,:] . x_t) * (U_e[i,:] . x_t)   for every route p of e.
+// ("perf(cpu-moe) ... #46": pass 1 reads gate_up [2I, H]; split by (unique
+// expert, row block) with the expert's routes as the inner loop, so each
+// weight row is read from memory once.)  Item = (segment, 8 row pairs); one
+// warp per row pair streams both rows with 16-byte loads; the routes' x rows
+// are staged in shared memory and the weights are reused from registers
+// across up to nt_max tokens per pass.
+constexpr int kGateUnroll = 4;
+
+__host__ __device__ __forceinline__ int gateup_items(const Ctx& c) {
+    return max_segments(c) * ceil_div(c.I, kWarps);
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+template <int NT>
+__device__ __forceinline__ void gateup_rowpair(const uint16_t* grow, const uint16_t* urow, int H,
+                                               const float* xs, int nq, float* hdst, int I) {
+    const int lane = threadIdx.x & 31;
+    float2 ag[NT], au[NT];
+#pragma unroll
+    for (int q = 0; q < NT; ++q) ag[q] = au[q] = make_float2(0.f, 0.f);
+    for (int base = 0; base < H; base += 256 * kGateUnroll) {
+        uint4 gv[kGateUnroll], uv[kGateUnroll];
+#pragma unroll
+        for (int u = 0; u < kGateUnroll; ++u) {
+            const int idx = base + u * 256 + lane * 8;
+            if (idx < H) {
+                gv[u] = ld_weight_v4(grow + idx);
+                uv[u] = ld_weight_v4(urow + idx);
+            } else {
+                gv[u] = uv[u] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kGateUnroll; ++u) {
+            const int idx = base + u * 256 + lane * 8;
+            if (idx < H) {
+                const float2 g0 = bf16x2_to_f2(gv[u].x), g1 = bf16x2_to_f2(gv[u].y);
+                const float2 g2 = bf16x2_to_f2(gv[u].z), g3 = bf16x2_to_f2(gv[u].w);
+                const float2 u0 = bf16x2_to_f2(uv[u].x), u1 = bf16x2_to_f2(uv[u].y);
+                const float2 u2 = bf16x2_to_f2(uv[u].z), u3 = bf16x2_to_f2(uv[u].w);
+#pragma unroll
+                for (int q = 0; q < NT; ++q) {
+                    const float4* xp = reinterpret_cast<const float4*>(xs + (size_t)q * H + idx);
+                    const float4 xa = xp[0], xb = xp[1];
+                    const float2 x0 = make_float2(xa.x, xa.y), x1 = make_float2(xa.z, xa.w);
+                    const float2 x2 = make_float2(xb.x, xb.y), x3 = make_float2(xb.z, xb.w);
+                    ag[q] = ffma2(g0, x0, ag[q]);
+                    au[q] = ffma2(u0, x0, au[q]);
+                    ag[q] = ffma2(g1, x1, ag[q]);
+                    au[q] = ffma2(u1, x1, au[q]);
+                    ag[q] = ffma2(g2, x2, ag[q]);
+                    au[q] = ffma2(u2, x2, au[q]);
+                    ag[q] = ffma2(g3, x3, ag[q]);
+                    au[q] = ffma2(u3, x3, au[q]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < NT; ++q) {
+        const float g = warp_sum(ag[q].x + ag[q].y);
+        const float u = warp_sum(au[q].x + au[q].y);
+        if (lane == q && q < nq) hdst[(size_t)q * I] = silu_mul(g, u);
+    }
+}
+
+// xs: nt_max * H floats of shared memory; tok: nt_max ints of shared memory.
+__device__ void gateup_item(const Ctx& c, int item, float* xs, int* tok) {
+    const int nib = ceil_div(c.I, kWarps);
+    const int s = item / nib, ib = item - s * nib;
+    Seg sg;
+    if (!get_seg(c, s, sg)) return;  // uniform over the CTA
+    const int warp = threadIdx.x >> 5;
+    const int i = ib * kWarps + warp;
+    const uint16_t* G = c.w.gate_up + (size_t)sg.e * 2 * c.I * c.H;
+    for (int g0 = sg.p0; g0 < sg.p1; g0 += c.nt_max) {
+        const int nq = min(c.nt_max, sg.p1 - g0);
+        __syncthreads();
+        if (threadIdx.x < nq) tok[threadIdx.x] = route_at(c, g0 + threadIdx.x) / c.k;
+        __syncthreads();
+        const int nfill = nq <= 1 ? 1 : nq <= 2 ? 2 : nq <= 4 ? 4 : 8;
+        stage_x(c, tok, 0, nq, nfill, 0, c.H, xs, c.H);
+        __syncthreads();
+        if (i < c.I) {
+            const uint16_t* grow = G + (size_t)i * c.H;
+            const uint16_t* urow = G + (size_t)(c.I + i) * c.H;
+            float* hdst = c.h + (size_t)g0 * c.I + i;
+            switch (nfill) {
+                case 1: gateup_rowpair<1>(grow, urow, c.H, xs, nq, hdst, c.I); break;
+                case 2: gateup_rowpair<2>(grow, urow, c.H, xs, nq, hdst, c.I); break;
+                case 4: gateup_rowpair<4>(grow, urow, c.H, xs, nq, hdst, c.I); break;
+                default: gateup_rowpair<8>(grow, urow, c.H, xs, nq, hdst, c.I); break;
+            }
+        }
+    }
+}
+
+// ===================================================================== down
+// o[r, j] = D_e[j,:] . h[p,:] for every route p (flat index r) of the segment.
+// ("perf(cpu-moe) ... #46": pass 2 reads down [H, I].)  Item = (segment,
+// 32 rows of D_e); one warp streams 4 rows; the segment's h rows are staged
+// in shared memory.
+constexpr int kDownRowsPerWarp = 4;
+constexpr int kDownRows = kWarps * kDownRowsPerWarp;
+constexpr int kDownUnroll = 2;
+
+__host__ __device__ __forceinline__ int down_items(const Ctx& c) {
+    return max_segments(c) * ceil_div(c.H, kDownRows);
+}
+
+template <int NT>
+__device__ __forceinline__ void down_rows(const uint16_t* D, int row0, int H, int I, const float* hs,
+                                          const int* rts, int nq, float* o) {
+    const int lane = threadIdx.x & 31;
+    float2 acc[kDownRowsPerWarp][NT];
+#pragma unroll
+    for (int rr = 0; rr < kDownRowsPerWarp; ++rr)
+#pragma unroll
+        for (int q = 0; q < NT; ++q) acc[rr][q] = make_float2(0.f, 0.f);
+    for (int base = 0; base < I; base += 256 * kDownUnroll) {
+        uint4 wv[kDownRowsPerWarp][kDownUnroll];
+#pragma unroll
+        for (int rr = 0; rr < kDownRowsPerWarp; ++rr)
+#pragma unroll
+            for (int u = 0; u < kDownUnroll; ++u) {
+                const int idx = base + u * 256 + lane * 8;
+                const int row = row0 + rr;
+                wv[rr][u] = (idx < I && row < H) ? ld_weight_v4(D + (size_t)row * I + idx)
+                                                 : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+        for (int u = 0; u < kDownUnroll; ++u) {
+            const int idx = base + u * 256 + lane * 8;
+            if (idx < I) {
+#pragma unroll
+                for (int q = 0; q < NT; ++q) {
+                    const float4* hp = reinterpret_cast<const float4*>(hs + (size_t)q * I + idx);
+                    const float4 ha = hp[0], hb = hp[1];
+                    const float2 h0 = make_float2(ha.x, ha.y), h1 = make_float2(ha.z, ha.w);
+                    const float2 h2 = make_float2(hb.x, hb.y), h3 = make_float2(hb.z, hb.w);
+#pragma unroll
+                    for (int rr = 0; rr < kDownRowsPerWarp; ++rr) {
+                        acc[rr][q] = ffma2(bf16x2_to_f2(wv[rr][u].x), h0, acc[rr][q]);
+                        acc[rr][q] = ffma2(bf16x2_to_f2(wv[rr][u].y), h1, acc[rr][q]);
+                        acc[rr][q] = ffma2(bf16x2_to_f2(wv[rr][u].z), h2, acc[rr][q]);
+                        acc[rr][q] = ffma2(bf16x2_to_f2(wv[rr][u].w), h3, acc[rr][q]);
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int rr = 0; rr < kDownRowsPerWarp; ++rr)
+#pragma unroll
+        for (int q = 0; q < NT; ++q) {
+            const float v = warp_sum(acc[rr][q].x + acc[rr][q].y);
+            const int row = row0 + rr;
+            if (lane == ((rr * NT + q) & 31) && q < nq && row < H) o[(size_t)rts[q] * H + row] = v;
+        }
+}
+
+// hs: nt_max * I floats of shared memory; rts: nt_max ints of shared memory.
+__device__ void down_item(const Ctx& c, int item, float* hs, int* rts) {
+    const int nrb = ceil_div(c.H, kDownRows);
+    const int s = item / nrb, rb = item - s * nrb;
+    Seg sg;
+    if (!get_seg(c, s, sg)) return;
+    const int warp = threadIdx.x >> 5;
+    const int row0 = rb * kDownRows + warp * kDownRowsPerWarp;
+    const uint16_t* D = c.w.down + (size_t)sg.e * c.H * c.I;
+    for (int g0 = sg.p0; g0 < sg.p1; g0 += c.nt_max) {
+        const int nq = min(c.nt_max, sg.p1 - g0);
+        const int nfill = nq <= 1 ? 1 : nq <= 2 ? 2 : nq <= 4 ? 4 : 8;
+        __syncthreads();
+        if (threadIdx.x < nq) rts[threadIdx.x] = route_at(c, g0 + threadIdx.x);
+        const int vpr = c.I >> 2;
+        for (int v = threadIdx.x; v < nfill * vpr; v += blockDim.x) {
+            const int q = v / vpr, i = (v - q * vpr) << 2;
+            float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (q < nq) val = ld_act_f4(c.h + (size_t)(g0 + q) * c.I + i);
+            *reinterpret_cast<float4*>(hs + (size_t)q * c.I + i) = val;
+        }
+        __syncthreads();
+        if (row0 < c.H) {
+            switch (nfill) {
+                case 1: down_rows<1>(D, row0, c.H, c.I, hs, rts, nq, c.o); break;
+                case 2: down_rows<2>(D, row0, c.H, c.I, hs, rts, nq, c.o); break;
+                case 4: down_rows<4>(D, row0, c.H, c.I, hs, rts, nq, c.o); break;
+                default: down_rows<8>(D, row0, c.H, c.I, hs, rts, nq, c.o); break;
+            }
+        }
+    }
+}
+
+// ================================================================== combine
+// y[t, :] = sum_j w[t,j] * o[t*k + j, :]  (j ascending)  (+ residual[t, :]).
+// ("MoE Performance Optimization Analysis", GPU Router Design: combination
+// on the GPU.)  Item = 1024 consecutive float4 of y.
+constexpr int kCombineVecs = kThreads * 4;
+
+__host__ __device__ __forceinline__ int combine_items(const Ctx& c) {
+    return ceil_div(c.B * (c.H >> 2), kCombineVecs);
+}
+
+__device__ void combine_item(const Ctx& c, int item) {
+    const int nv = c.B * (c.H >> 2);
+    const int hv = c.H >> 2;
+    for (int v = item * kCombineVecs + threadIdx.x; v < min(nv, (item + 1) * kCombineVecs);
+         v += blockDim.x) {
+        const int t = v / hv, col = (v - t * hv) << 2;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < c.k; ++j) {
+            const int r = t * c.k + j;
+            const float wj = ld_act_f(c.rw + r);
+            const float4 ov = ld_act_f4(c.o + (size_t)r * c.H + col);
+            acc.x = fmaf(wj, ov.x, acc.x);
+            acc.y = fmaf(wj, ov.y, acc.y);
+            acc.z = fmaf(wj, ov.z, acc.z);
+            acc.w = fmaf(wj, ov.w, acc.w);
+        }
+        if (c.residual) {
+            const float4 rv = ld_act_f4(c.residual + (size_t)t * c.H + col);
+            acc.x = rv.x + acc.x;
+            acc.y = rv.y + acc.y;
+            acc.z = rv.z + acc.z;
+            acc.w = rv.w + acc.w;
+        }
+        *reinterpret_cast<float4*>(c.y + (size_t)t * c.H + col) = acc;
+    }
+}
+
+}  // namespace moe

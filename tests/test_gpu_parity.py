@@ -1,0 +1,172 @@
+"""GPU path vs the CPU oracle, through the C ABI, on seeded inputs.
+
+Sizes span several tiles with ragged tails; the workloads' own shapes are
+covered at full size (sampled or whole where the oracle is fast enough).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_decode_layer_gemv_gb300 import synth
+from _parity import (check_route, check_y, layer_weights_np, np_x, oracle_layer_following)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def make_case(B, H, I, E, k, seed=0, sigma_r=None, bias=False, x_bf16=False, device="cpu"):
+    w = synth.Workload("case", B=B, H=H, I=I, E=E, top_k=k,
+                       sigma_router=sigma_r if sigma_r is not None else H ** -0.5,
+                       sigma_expert=0.02 if H >= 512 else 0.1, x_bf16=x_bf16, zipf_bias=bias)
+    lw = synth.make_layer(w, 0, seed=seed, device=device)
+    x = synth.make_x(w, 0, seed=seed, device=device)
+    return w, {n: (v.to(DEV) if v is not None else None) for n, v in lw.items()}, x.to(DEV)
+
+
+SHAPES = [
+    # B, H, I, E, k
+    (4, 64, 32, 8, 2),       # the tiny workload
+    (1, 2048, 768, 128, 2),  # one layer of the 30-layer stack
+    (5, 72, 40, 5, 3),       # ragged H and I (not multiples of 256), E < 32
+    (13, 264, 24, 17, 4),    # ragged everything
+    (9, 128, 64, 6, 6),      # top_k == E
+    (3, 128, 64, 1, 1),      # one expert: a dense SwiGLU MLP
+    (40, 256, 128, 12, 3),   # heavy reuse: many tokens per expert (> 8 per pass)
+]
+
+
+@pytest.mark.parametrize("B,H,I,E,k", SHAPES)
+def test_route_parity(cuda_lib, B, H, I, E, k):
+    _, lw, x = make_case(B, H, I, E, k, seed=B + H)
+    ids, w, logits = cuda_lib.route(x, lw["w_router"], k)
+    torch.cuda.synchronize()
+    check_route(x, lw["w_router"], None, k, ids, w, logits)
+
+
+@pytest.mark.parametrize("B,H,I,E,k", SHAPES)
+def test_group_parity_bit_exact(cuda_lib, B, H, I, E, k):
+    rng = np.random.default_rng(B * 7 + E)
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(B)]).astype(np.int32)
+    off_o, ridx_o, uniq_o = oracle.group(ids, E)
+    st = cuda_lib.new_status()
+    off, ridx, uniq, nu = cuda_lib.group_by_expert(torch.from_numpy(ids).to(DEV), E, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert np.array_equal(off.cpu().numpy(), off_o)
+    assert np.array_equal(ridx.cpu().numpy(), ridx_o)
+    n = int(nu.item())
+    assert n == len(uniq_o)
+    assert np.array_equal(uniq.cpu().numpy()[:n], uniq_o)
+
+
+@pytest.mark.parametrize("B", [1, 64, 300, 1024])
+def test_group_parity_large_batches(cuda_lib, B):
+    E, k = 256, 8
+    rng = np.random.default_rng(B)
+    # skewed: popular experts repeat heavily
+    p = 1.0 / np.arange(1, E + 1) ** 1.1
+    p /= p.sum()
+    ids = np.stack([rng.choice(E, k, replace=False, p=p) for _ in range(B)]).astype(np.int32)
+    off_o, ridx_o, uniq_o = oracle.group(ids, E)
+    off, ridx, uniq, nu = cuda_lib.group_by_expert(torch.from_numpy(ids).to(DEV), E)
+    torch.cuda.synchronize()
+    assert np.array_equal(off.cpu().numpy(), off_o)
+    assert np.array_equal(ridx.cpu().numpy(), ridx_o)
+    assert np.array_equal(uniq.cpu().numpy()[:int(nu.item())], uniq_o)
+
+
+def test_group_flags_bad_and_duplicate_ids(cuda_lib):
+    ids = torch.tensor([[0, 3], [2, 9], [1, 1]], dtype=torch.int32, device=DEV)
+    st = cuda_lib.new_status()
+    cuda_lib.group_by_expert(ids, 8, status=st)
+    torch.cuda.synchronize()
+    s = int(st.item())
+    assert s & cuda_lib.MOE_DEV_BAD_EXPERT_ID
+    assert s & cuda_lib.MOE_DEV_DUP_EXPERT
+
+
+@pytest.mark.parametrize("B,H,I,E,k", SHAPES)
+@pytest.mark.parametrize("flags", [0, 2, 1])  # fused, unfused, no-dedup
+def test_layer_parity(cuda_lib, B, H, I, E, k, flags):
+    _, lw, x = make_case(B, H, I, E, k, seed=3 * B + I)
+    st = cuda_lib.new_status()
+    y, ids, w = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k, flags=flags,
+                                       status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    lnp = layer_weights_np(lw)
+    y_o, _, _ = oracle_layer_following(x, lnp, k, ids)
+    check_y(y, y_o)
+    ids_g, w_g, logits_g = cuda_lib.route(x, lw["w_router"], k)
+    check_route(x, lw["w_router"], None, k, ids_g, w_g, logits_g)
+    assert torch.equal(ids_g, ids)
+
+
+def test_layer_with_bias_and_residual(cuda_lib):
+    B, H, I, E, k = 16, 256, 96, 24, 6
+    _, lw, x = make_case(B, H, I, E, k, seed=5, bias=True)
+    res = torch.randn(B, H, device=DEV)
+    y, ids, w = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k, bias=lw["bias"],
+                                       residual=res)
+    torch.cuda.synchronize()
+    y_o, _, _ = oracle_layer_following(x, layer_weights_np(lw), k, ids, residual=res.cpu().numpy())
+    check_y(y, y_o)
+
+
+def test_bf16_activations(cuda_lib):
+    B, H, I, E, k = 20, 512, 64, 16, 4
+    _, lw, x = make_case(B, H, I, E, k, seed=9, x_bf16=True)
+    assert x.dtype == torch.bfloat16
+    y, ids, w = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k)
+    torch.cuda.synchronize()
+    y_o, _, _ = oracle_layer_following(x, layer_weights_np(lw), k, ids)
+    check_y(y, y_o)
+
+
+def test_expert_forward_on_oracle_routing(cuda_lib):
+    """moe_expert_forward fed the oracle's own routing and grouping."""
+    B, H, I, E, k = 24, 320, 48, 10, 3
+    _, lw, x = make_case(B, H, I, E, k, seed=12)
+    lnp = layer_weights_np(lw)
+    lo = oracle.router(np_x(x), lnp["w_router"])
+    ids_o, w_o = oracle.topk(lo, k)
+    off, ridx, uniq = oracle.group(ids_o, E)
+    uniq_full = np.full(E, -1, np.int32)
+    uniq_full[:len(uniq)] = uniq
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    grouping = (t(off), t(ridx), t(uniq_full), t(np.array([len(uniq)], np.int32)))
+    for flags in (0, 1):
+        y = cuda_lib.expert_forward(x, lw["gate_up"], lw["down"], t(ids_o), t(w_o), grouping, flags=flags)
+        torch.cuda.synchronize()
+        y_o = oracle.experts(np_x(x), lnp["gate_up"], lnp["down"], ids_o, w_o, E)
+        check_y(y, y_o)
+
+
+def test_dedup_and_no_dedup_agree(cuda_lib):
+    B, H, I, E, k = 32, 512, 128, 8, 4
+    _, lw, x = make_case(B, H, I, E, k, seed=21)
+    y0, i0, _ = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k, flags=0)
+    y1, i1, _ = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k, flags=1)
+    torch.cuda.synchronize()
+    assert torch.equal(i0, i1)
+    assert torch.allclose(y0, y1, rtol=0, atol=1e-5 * float(y0.abs().max()))
+
+
+def test_empty_batch_is_a_no_op(cuda_lib):
+    B, H, I, E, k = 0, 64, 32, 8, 2
+    _, lw, _ = make_case(4, H, I, E, k)
+    x = torch.empty((0, H), device=DEV)
+    y, ids, w = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k)
+    torch.cuda.synchronize()
+    assert y.shape == (0, H)
+
+
+def test_deterministic_across_calls(cuda_lib):
+    B, H, I, E, k = 64, 2048, 768, 256, 8
+    _, lw, x = make_case(B, H, I, E, k, seed=1)
+    ya, ia, _ = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k)
+    yb, ib, _ = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k)
+    torch.cuda.synchronize()
+    assert torch.equal(ia, ib) and torch.equal(ya, yb)

@@ -1,0 +1,154 @@
+"""The five workloads at full size, in the launch configuration the benchmark
+times (the fused persistent kernel), against the CPU oracle.
+
+Weights are drawn on the GPU by torch's generator (synth recipe) and the
+oracle reads back exactly the tensors it needs: every router, and the
+experts its own routing selects.  Where the oracle would take minutes
+(prefill-sized layer), outputs are sampled token by token.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_decode_layer_gemv_gb300 import accounting, synth
+from _parity import (NEAR_TIE, check_route, check_y, margins, np_x, oracle_layer_following)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+class LazyExperts(dict):
+    """{e: uint16 array} filled on demand from a device tensor [E, ...]."""
+
+    def __init__(self, dev_tensor):
+        super().__init__()
+        self.t = dev_tensor
+
+    def need(self, ids):
+        for e in np.unique(ids):
+            e = int(e)
+            if e not in self:
+                self[e] = synth.bf16_bits(self.t[e])
+        return self
+
+
+def oracle_layer_lazy(x, lw, k, ids_gpu, residual=None, tokens=None):
+    """Oracle y for the given tokens (all by default), fetching only the
+    selected experts; near ties follow the GPU's ids."""
+    xn = np_x(x)
+    wr = synth.bf16_bits(lw["w_router"])
+    bias = None if lw.get("bias") is None else lw["bias"].cpu().numpy()
+    lo = oracle.router(xn, wr, bias)
+    ids_o, w_o = oracle.topk(lo, k)
+    ex = margins(lo, k) < NEAR_TIE
+    ig = ids_gpu.cpu().numpy()
+    tok = np.arange(xn.shape[0]) if tokens is None else np.asarray(tokens)
+    lnp = {"w_router": wr, "bias": bias,
+           "gate_up": LazyExperts(lw["gate_up"]), "down": LazyExperts(lw["down"])}
+    ids_use = np.where(ex[:, None], ig, ids_o)
+    lnp["gate_up"].need(ids_use[tok])
+    lnp["down"].need(ids_use[tok])
+    sub = {"w_router": wr, "bias": bias, "gate_up": lnp["gate_up"], "down": lnp["down"]}
+    res = None if residual is None else residual[tok]
+    xs = x[torch.as_tensor(tok, device=x.device)]
+    y, _, n_ex = oracle_layer_following(xs, sub, k, ids_gpu[torch.as_tensor(tok, device=x.device)],
+                                        residual=res)
+    return y, ids_o, ex
+
+
+def run_layer(cuda_lib, w, lw, x):
+    st = cuda_lib.new_status()
+    y, ids, rw = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], w.top_k,
+                                        bias=lw.get("bias"), status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return y, ids, rw
+
+
+@pytest.fixture(scope="module")
+def uniform_layer():
+    w = synth.UNIFORM
+    lw = synth.make_layer(w, 0, seed=0, device=DEV)
+    yield w, lw
+    del lw
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("B", synth.UNIFORM.batches)
+def test_uniform_routing_layer(cuda_lib, uniform_layer, B):
+    w, lw = uniform_layer
+    x = synth.make_x(w, 0, seed=0, device=DEV, B=B)
+    y, ids, rw = run_layer(cuda_lib, w, lw, x)
+    ids_r, w_r, lg = cuda_lib.route(x, lw["w_router"], w.top_k)
+    torch.cuda.synchronize()
+    check_route(x, lw["w_router"], None, w.top_k, ids_r, w_r, lg)
+    y_o, _, ex = oracle_layer_lazy(x, lw, w.top_k, ids)
+    check_y(y, y_o)
+    U = len(np.unique(ids.cpu().numpy()))
+    # unique count inside a generous band around the closed form
+    assert abs(U - accounting.expected_unique(256, 8, B)) <= 6 * np.sqrt(max(B, 1)) + 2
+
+
+@pytest.fixture(scope="module")
+def skewed_layer():
+    w = synth.SKEWED
+    lw = synth.make_layer(w, 0, seed=0, device=DEV)
+    yield w, lw
+    del lw
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("B", synth.SKEWED.batches)
+def test_skewed_routing_layer(cuda_lib, skewed_layer, B):
+    w, lw = skewed_layer
+    x = synth.make_x(w, 0, seed=0, device=DEV, B=B)
+    y, ids, rw = run_layer(cuda_lib, w, lw, x)
+    y_o, _, ex = oracle_layer_lazy(x, lw, w.top_k, ids)
+    check_y(y, y_o)
+    # the grouped route list of the layer's own ids, bit-exact
+    off, ridx, uniq, nu = cuda_lib.group_by_expert(ids, w.E)
+    torch.cuda.synchronize()
+    off_o, ridx_o, uniq_o = oracle.group(ids.cpu().numpy(), w.E)
+    assert np.array_equal(off.cpu().numpy(), off_o) and np.array_equal(ridx.cpu().numpy(), ridx_o)
+    assert np.array_equal(uniq.cpu().numpy()[:int(nu.item())], uniq_o)
+
+
+def test_prefill_sized_layer_sampled(cuda_lib):
+    w = synth.PREFILL
+    lw = synth.make_layer(w, 0, seed=0, device=DEV)
+    x = synth.make_x(w, 0, seed=0, device=DEV)
+    y, ids, rw = run_layer(cuda_lib, w, lw, x)
+    ids_r, w_r, lg = cuda_lib.route(x, lw["w_router"], w.top_k)
+    torch.cuda.synchronize()
+    check_route(x, lw["w_router"], None, w.top_k, ids_r, w_r, lg)
+    rng = np.random.default_rng(0)
+    tok = np.sort(np.concatenate([[0, w.B - 1], rng.choice(np.arange(1, w.B - 1), 10, replace=False)]))
+    y_o, _, _ = oracle_layer_lazy(x, lw, w.top_k, ids, tokens=tok)
+    yg = y[torch.as_tensor(tok, device=DEV)]
+    check_y(yg, y_o)
+    del lw
+    torch.cuda.empty_cache()
+
+
+def test_stack_of_30_layers_end_to_end(cuda_lib):
+    w = synth.STACK
+    layers = [synth.make_layer(w, l, seed=0, device=DEV) for l in range(w.layers)]
+    x0 = synth.make_x(w, 0, seed=0, device=DEV)
+    st = cuda_lib.new_status()
+    xs = cuda_lib.StackWeights(layers)
+    x_out, ids = cuda_lib.stack_forward(x0, xs, w.top_k, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    # oracle walks the same 30 layers, following the GPU only on near ties
+    x = x0.clone()
+    n_ties = 0
+    for l, lw in enumerate(layers):
+        y_o, ids_o, ex = oracle_layer_lazy(x, lw, w.top_k, ids[l], residual=x.cpu().numpy())
+        n_ties += int(ex.sum())
+        ig = ids[l].cpu().numpy()
+        assert np.array_equal(np.sort(ig[~ex], 1), np.sort(ids_o[~ex], 1)), l
+        x = torch.from_numpy(y_o).to(DEV)
+    check_y(x_out, x.cpu().numpy())
+    del layers
+    torch.cuda.empty_cache()
