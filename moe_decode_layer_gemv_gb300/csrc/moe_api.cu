@@ -348,6 +348,7 @@ int moe_route(const void* x, int x_dtype, const uint16_t* w_router, const float*
     int rc = check_dims(B, H, 8, E, top_k, false);
     if (rc) return rc;
     if (x_dtype != MOE_DT_F32 && x_dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
+    if (B == 0) return MOE_OK;  // nothing to do; empty tensors may carry null pointers
     MOE_REQ(x);
     MOE_REQ(w_router);
     MOE_REQ(expert_ids);
@@ -359,7 +360,6 @@ int moe_route(const void* x, int x_dtype, const uint16_t* w_router, const float*
     const WsLayout L = ws_layout(B, H, 8, E, top_k);
     if (!logits_out && (!workspace || workspace_bytes < L.logits + sizeof(float) * (size_t)B * E))
         return MOE_ERR_WORKSPACE;
-    if (B == 0) return MOE_OK;
     Ctx c = make_ctx(x, x_dtype, nullptr, nullptr, B, H, 8, E, top_k, 0, nullptr, L, dev_status);
     c.w.w_router = w_router;
     c.w.bias = logit_bias;
@@ -374,6 +374,7 @@ int moe_group_by_expert(const int32_t* expert_ids, int B, int top_k, int E, int3
                         int32_t* dev_status, void* stream) {
     int rc = check_dims(B, 8, 8, E, top_k, false);
     if (rc) return rc;
+    if (B == 0) return MOE_OK;
     MOE_REQ(expert_ids);
     MOE_REQ(offsets);
     MOE_REQ(route_idx);
@@ -394,6 +395,7 @@ int moe_expert_forward(const void* x, int x_dtype, const uint16_t* gate_up, cons
     if (rc) return rc;
     if (x_dtype != MOE_DT_F32 && x_dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
     if (flags & ~(MOE_F_NO_DEDUP | MOE_F_UNFUSED)) return MOE_ERR_INVALID_ARG;
+    if (B == 0) return MOE_OK;
     MOE_REQ(x);
     MOE_REQ(gate_up);
     MOE_REQ(down);
@@ -409,7 +411,6 @@ int moe_expert_forward(const void* x, int x_dtype, const uint16_t* gate_up, cons
     MOE_OPT(dev_status);
     const WsLayout L = ws_layout(B, H, I, E, top_k);
     if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
-    if (B == 0) return MOE_OK;
     Ctx c = make_ctx(x, x_dtype, residual, y, B, H, I, E, top_k, flags, static_cast<char*>(workspace), L,
                      dev_status);
     c.ids = const_cast<int32_t*>(expert_ids);
@@ -432,6 +433,7 @@ int moe_layer_forward(const void* x, int x_dtype, const uint16_t* w_router, cons
     if (rc) return rc;
     if (x_dtype != MOE_DT_F32 && x_dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
     if (flags & ~(MOE_F_NO_DEDUP | MOE_F_UNFUSED)) return MOE_ERR_INVALID_ARG;
+    if (B == 0) return MOE_OK;
     MOE_REQ(x);
     MOE_REQ(w_router);
     MOE_REQ(gate_up);
@@ -445,7 +447,6 @@ int moe_layer_forward(const void* x, int x_dtype, const uint16_t* w_router, cons
     MOE_OPT(dev_status);
     const WsLayout L = ws_layout(B, H, I, E, top_k);
     if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
-    if (B == 0) return MOE_OK;
     char* ws = static_cast<char*>(workspace);
     Ctx c = make_ctx(x, x_dtype, residual, y, B, H, I, E, top_k, flags, ws, L, dev_status);
     c.w.w_router = w_router;
@@ -473,6 +474,7 @@ int moe_stack_forward(int Lc, const uint16_t* const* w_router, const float* cons
     if (rc) return rc;
     if (Lc < 1 || Lc > MOE_MAX_LAYERS) return MOE_ERR_INVALID_ARG;
     if (flags & ~(MOE_F_NO_DEDUP | MOE_F_UNFUSED)) return MOE_ERR_INVALID_ARG;
+    if (B == 0) return MOE_OK;
     if (!w_router || !gate_up || !down) return MOE_ERR_INVALID_ARG;
     for (int l = 0; l < Lc; ++l) {
         MOE_REQ(w_router[l]);
@@ -486,7 +488,6 @@ int moe_stack_forward(int Lc, const uint16_t* const* w_router, const float* cons
     MOE_OPT(dev_status);
     const WsLayout L = ws_layout(B, H, I, E, top_k);
     if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
-    if (B == 0) return MOE_OK;
     char* ws = static_cast<char*>(workspace);
     Ctx c = make_ctx(x_inout, MOE_DT_F32, x_inout, x_inout, B, H, I, E, top_k, flags, ws, L, dev_status);
     StackArgs sa;
