@@ -49,6 +49,8 @@ def parse():
                     help="bound on the oracle's CPU sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layers", type=int, default=30,
+                    help="layers in the stack (30 = the workload; fewer only for profiling captures)")
     return ap.parse_args()
 
 
@@ -155,7 +157,7 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ oracle
-def oracle_stack_sample(layers_cpu_fn, x0_list, k, seconds):
+def oracle_stack_sample(layers_cpu_fn, x0_list, k, seconds, n_layers=30):
     """Run the CPU oracle on whole tokens through the stack until `seconds`
     of oracle time accumulate (at least one token).  layers_cpu_fn(l, ids)
     returns the layer's weights as the oracle takes them (host arrays),
@@ -165,7 +167,7 @@ def oracle_stack_sample(layers_cpu_fn, x0_list, k, seconds):
     done, spent = 0, 0.0
     for x0 in x0_list:
         x = np.array(x0, dtype=np.float32, copy=True)
-        for l in range(30):
+        for l in range(n_layers):
             wr, bias = layers_cpu_fn(l, None)
             t0 = time.perf_counter()
             lo = oracle.router(x, wr, bias)
@@ -258,6 +260,9 @@ def run_ours(args):
     build.build()
     from moe_decode_layer_gemv_gb300 import api
     w = synth.STACK
+    if args.layers != w.layers:
+        w = synth.Workload(f"stack{args.layers}_b1_h2048_i768_e128_k2", B=w.B, H=w.H, I=w.I, E=w.E,
+                           top_k=w.top_k, layers=args.layers, residual=True)
     flags = api.MOE_F_UNFUSED if args.mode == "unfused" else 0
     layers = [synth.make_layer(w, l, seed=args.seed + 7919 * rank, device=dev) for l in range(w.layers)]
     sw = api.StackWeights(layers)
@@ -288,6 +293,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         if pg:
             pg.barrier()
+        torch.cuda.nvtx.range_push("timed")
         for s in range(args.steps):
             i = args.warmup + s
             flush.zero_()
@@ -297,6 +303,7 @@ def run_ours(args):
                                stream=stream)
             ev[s][1].record(stream)
             uniq.append(ids.clone())
+        torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
         if pg:
             pg.barrier()
@@ -388,10 +395,10 @@ def run_ours(args):
             return gu, dn
 
         x_np = [xs[args.warmup + s].cpu().numpy() for s in range(args.steps)]
-        n, t = oracle_stack_sample(layer_cpu, x_np, w.top_k, args.cpu_seconds)
+        n, t = oracle_stack_sample(layer_cpu, x_np, w.top_k, args.cpu_seconds, w.layers)
         line["cpu_baseline"] = {"value": n * w.B / t, "unit": "tokens/s",
                                 "cores": int(os.environ["OMP_NUM_THREADS"]), "kind": "oracle",
-                                "sample": f"{n} whole tokens through all 30 layers (same weights, "
+                                "sample": f"{n} whole tokens through all {w.layers} layers (same weights, "
                                           f"{t:.1f} s of oracle time)"}
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -145,6 +145,33 @@ int moe_expert_forward(const void* x, int x_dtype, const uint16_t* gate_up, cons
                        size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /*
+ * moe_expert_forward_noalloc -- moe_expert_forward for callers that cannot
+ * allocate device memory (code inside a CUDA graph being captured or
+ * replayed, an allocator hook that must not re-enter the allocator, a
+ * runtime with a fixed memory budget).  The pages have no counterpart: this
+ * is an interface convenience, not part of the method.
+ * Same arguments and results as moe_expert_forward, minus the workspace:
+ * the scratch (h [R,I] and o [R,H], fp32) lives in one static device array
+ * of MOE_NOALLOC_SCRATCH_BYTES inside the library, held on every GPU that
+ * loads the library until the process exits.  Problems needing more than
+ * that (4*R*(I+H) bytes plus alignment, R = B*top_k) return
+ * MOE_ERR_WORKSPACE before anything is enqueued.  Nothing is allocated or
+ * freed.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call shares the one array, so calls
+ * that may overlap on the GPU (different streams, or concurrent graph
+ * replays) race on it: serialise them.
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES (16u << 20)
+int moe_expert_forward_noalloc(const void* x, int x_dtype, const uint16_t* gate_up,
+                               const uint16_t* down, const int32_t* expert_ids,
+                               const float* route_w, const int32_t* offsets,
+                               const int32_t* route_idx, const int32_t* unique_experts,
+                               const int32_t* num_unique, int B, int H, int I, int E, int top_k,
+                               const float* residual, float* y, uint32_t flags,
+                               int32_t* dev_status, void* stream);
+
+/*
  * moe_layer_forward -- the whole layer: moe_route, moe_group_by_expert and
  * moe_expert_forward in one enqueue.  Unless MOE_F_UNFUSED, the phases run in
  * one persistent cooperative kernel (one CTA per SM, device-wide barriers

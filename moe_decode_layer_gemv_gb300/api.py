@@ -32,17 +32,19 @@ _lib.moe_route.argtypes = [_P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _S, _
 _lib.moe_group_by_expert.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]
 _lib.moe_expert_forward.argtypes = [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                                     _P, _P, _U, _P, _S, _P, _P]
+_lib.moe_expert_forward_noalloc.argtypes = [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
+                                            _I, _P, _P, _U, _P, _P]
 _lib.moe_layer_forward.argtypes = [_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _U,
                                    _P, _S, _P, _P]
 _lib.moe_stack_forward.argtypes = [_I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _U, _P, _S, _P, _P]
 _lib.moe_status_string.argtypes = [_I]
 _lib.moe_status_string.restype = ctypes.c_char_p
 for _f in ("moe_workspace_bytes", "moe_route", "moe_group_by_expert", "moe_expert_forward",
-           "moe_layer_forward", "moe_stack_forward"):
+           "moe_expert_forward_noalloc", "moe_layer_forward", "moe_stack_forward"):
     getattr(_lib, _f).restype = ctypes.c_int
 
 EXPORTED = ("moe_workspace_bytes", "moe_route", "moe_group_by_expert", "moe_expert_forward",
-            "moe_layer_forward", "moe_stack_forward", "moe_status_string")
+            "moe_expert_forward_noalloc", "moe_layer_forward", "moe_stack_forward", "moe_status_string")
 
 MOE_OK = 0
 MOE_ERR_INVALID_ARG = -1
@@ -58,6 +60,7 @@ MOE_DT_BF16 = 1
 MOE_F_NO_DEDUP = 1
 MOE_F_UNFUSED = 2
 MAX_E, MAX_TOPK, MAX_B, MAX_DIM, MAX_LAYERS = 256, 8, 1024, 16384, 64
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class MoeError(RuntimeError):
@@ -157,6 +160,27 @@ def expert_forward(x, gate_up, down, expert_ids, route_w, grouping, residual=Non
                                    _ptr(route_w), _ptr(offsets), _ptr(ridx), _ptr(uniq), _ptr(nu), B, H,
                                    I, E, k, _ptr(residual), _ptr(y), flags, _ptr(ws), ws.numel(),
                                    _ptr(status), _stream(stream)), "moe_expert_forward")
+    return y
+
+
+def expert_forward_noalloc(x, gate_up, down, expert_ids, route_w, grouping, residual=None, flags=0,
+                           out=None, status=None, stream=None):
+    """expert_forward with the library's fixed scratch array instead of a
+    workspace: for callers that cannot allocate device memory.  `out` must
+    be given by such callers (it is allocated here only for convenience)."""
+    _need(gate_up, torch.bfloat16, "gate_up")
+    _need(down, torch.bfloat16, "down")
+    B, H = x.shape
+    E, twoI, _ = gate_up.shape
+    I = twoI // 2
+    k = expert_ids.shape[1]
+    offsets, ridx, uniq, nu = grouping
+    y = out if out is not None else torch.empty((B, H), dtype=torch.float32, device=x.device)
+    _check(_lib.moe_expert_forward_noalloc(_ptr(x), _x_dtype(x), _ptr(gate_up), _ptr(down),
+                                           _ptr(expert_ids), _ptr(route_w), _ptr(offsets), _ptr(ridx),
+                                           _ptr(uniq), _ptr(nu), B, H, I, E, k, _ptr(residual), _ptr(y),
+                                           flags, _ptr(status), _stream(stream)),
+           "moe_expert_forward_noalloc")
     return y
 
 

@@ -6,6 +6,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "moe.h"
 #include "moe_common.cuh"
 #include "moe_phases.cuh"
@@ -529,3 +531,86 @@ const char* moe_status_string(int code) {
 }
 
 }  // extern "C"
+
+// ----------------------------------------------------------------------------
+// moe_expert_forward_noalloc: moe_expert_forward with its scratch (the
+// intermediate h [R, I] and the per-route outputs o [R, H], fp32) in a fixed
+// device array owned by the library, for callers that cannot allocate device
+// memory: code running inside a CUDA graph that is being captured or
+// replayed, an allocator hook that must not re-enter the allocator, or an
+// embedding runtime whose memory budget is fixed up front.
+//
+// The array below is a file-scope __device__ array of MOE_NOALLOC_SCRATCH_BYTES
+// (16 MiB); every GPU that loads the library holds it until the process exits.
+// In host code its name is only a host-side stand-in, so the entry point looks
+// up its device address with cudaGetSymbolAddress once per device (on the
+// first call made with that device current) and hands that address to the
+// kernels.
+namespace moe {
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+static void* g_noalloc_ptr[kMaxDevices];
+static std::mutex g_noalloc_mu;
+
+static int noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return MOE_OK;
+}
+
+}  // namespace moe
+
+extern "C" int moe_expert_forward_noalloc(const void* x, int x_dtype, const uint16_t* gate_up,
+                                          const uint16_t* down, const int32_t* expert_ids,
+                                          const float* route_w, const int32_t* offsets,
+                                          const int32_t* route_idx, const int32_t* unique_experts,
+                                          const int32_t* num_unique, int B, int H, int I, int E,
+                                          int top_k, const float* residual, float* y, uint32_t flags,
+                                          int32_t* dev_status, void* stream) {
+    using namespace moe;
+    int rc = check_dims(B, H, I, E, top_k, true);
+    if (rc) return rc;
+    if (x_dtype != MOE_DT_F32 && x_dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
+    if (flags & ~(MOE_F_NO_DEDUP | MOE_F_UNFUSED)) return MOE_ERR_INVALID_ARG;
+    const size_t R = (size_t)B * top_k;
+    const size_t h_bytes = align_up(sizeof(float) * R * I, 256);
+    if (h_bytes + sizeof(float) * R * H > MOE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
+    if (B == 0) return MOE_OK;
+    MOE_REQ(x);
+    MOE_REQ(gate_up);
+    MOE_REQ(down);
+    MOE_REQ(expert_ids);
+    MOE_REQ(route_w);
+    MOE_REQ(offsets);
+    MOE_REQ(route_idx);
+    MOE_REQ(unique_experts);
+    MOE_REQ(num_unique);
+    MOE_REQ(y);
+    MOE_OPT(residual);
+    MOE_OPT(dev_status);
+    void* scratch = nullptr;
+    if ((rc = noalloc_scratch(&scratch))) return rc;
+    Ctx c = make_ctx(x, x_dtype, residual, y, B, H, I, E, top_k, flags, nullptr, WsLayout(), dev_status);
+    c.ids = const_cast<int32_t*>(expert_ids);
+    c.rw = const_cast<float*>(route_w);
+    c.offsets = const_cast<int32_t*>(offsets);
+    c.route_idx = const_cast<int32_t*>(route_idx);
+    c.unique = const_cast<int32_t*>(unique_experts);
+    c.num_unique = const_cast<int32_t*>(num_unique);
+    c.w.gate_up = gate_up;
+    c.w.down = down;
+    // every element of h and o is written before it is read, so the array's
+    // contents from an earlier call never need clearing
+    c.h = static_cast<float*>(scratch);
+    c.o = reinterpret_cast<float*>(static_cast<char*>(scratch) + h_bytes);
+    return launch_experts(c, static_cast<cudaStream_t>(stream));
+}
