@@ -11,6 +11,7 @@
 #include "moe.h"
 #include "moe_common.cuh"
 #include "moe_phases.cuh"
+#include "moe_decode.cuh"
 
 namespace moe {
 
@@ -71,7 +72,7 @@ struct StackArgs {
 };
 
 __global__ void __launch_bounds__(kThreads) router_kernel(Ctx c) {
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem[];
     router_item(c, blockIdx.x, reinterpret_cast<float*>(smem));
 }
 
@@ -83,7 +84,7 @@ __global__ void __launch_bounds__(kThreads) group_kernel(const int32_t* ids, int
                                                          int32_t* offsets, int32_t* route_idx,
                                                          int32_t* unique, int32_t* num_unique,
                                                          int32_t* status) {
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem[];
     group_cta(ids, B, k, E, offsets, route_idx, unique, num_unique, status,
               reinterpret_cast<uint32_t*>(smem));
 }
@@ -95,7 +96,7 @@ __device__ __forceinline__ void split_smem(const Ctx& c, unsigned char* smem, fl
 }
 
 __global__ void __launch_bounds__(kThreads) gateup_kernel(Ctx c) {
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem[];
     float* xs;
     int* tok;
     split_smem(c, smem, xs, tok);
@@ -103,7 +104,7 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(Ctx c) {
 }
 
 __global__ void __launch_bounds__(kThreads) down_kernel(Ctx c) {
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem[];
     float* hs;
     int* rts;
     split_smem(c, smem, hs, rts);
@@ -115,7 +116,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(Ctx c) { combine_item
 // All phases of L layers in one launch.  For L > 1 (a stack) x, residual and
 // y all point at the fp32 residual stream, updated in place by the combine.
 __global__ void __launch_bounds__(kThreads) fused_kernel(Ctx c, StackArgs sa, unsigned* bar) {
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem[];
     float* act;
     int* idx;
     split_smem(c, smem, act, idx);
@@ -146,7 +147,7 @@ __global__ void __launch_bounds__(kThreads) fused_kernel(Ctx c, StackArgs sa, un
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct WsLayout {
-    size_t logits, ids, rw, offsets, route_idx, unique, num_unique, status, bar, h, o, total;
+    size_t logits, ids, rw, offsets, route_idx, unique, num_unique, status, bar, acc, acc_end, h, o, total;
 };
 
 static WsLayout ws_layout(int B, int H, int I, int E, int k) {
@@ -167,6 +168,8 @@ static WsLayout ws_layout(int B, int H, int I, int E, int k) {
     L.num_unique = take(sizeof(int32_t));
     L.status = take(sizeof(int32_t));
     L.bar = take(sizeof(unsigned) * 2);
+    L.acc = take(sizeof(unsigned long long) * 2 * (size_t)B * E);  // right after bar: one memset clears both
+    L.acc_end = L.acc + sizeof(unsigned long long) * 2 * (size_t)B * E;
     L.h = take(sizeof(float) * R * I);
     L.o = take(sizeof(float) * R * H);
     L.total = off;
@@ -330,6 +333,77 @@ static int launch_fused(const Ctx& c, const StackArgs& sa, unsigned* bar, cudaSt
     return to_status(cudaLaunchKernelEx(&cfg, fused_kernel, c, sa, bar));
 }
 
+
+// ------------------------------------------------------ decode kernel plan
+// The decode kernel keeps x [B,H], h [R,I], the combine outputs and the next
+// router's column slice in shared memory and gives the rest to the weight
+// ring; it applies when B <= 4, B*k <= 32 and the ring gets >= 4 stages.
+static bool decode_plan(int B, int H, int I, int E, int k, int sms, DkParams& p, size_t& smem) {
+    const int R = B * k;
+    if (B < 1 || B > kDkMaxB || R > kDkMaxR || sms < 1) return false;
+    const int ng = H >> 3;
+    const int maxrows = 8 * ((ng + sms - 1) / sms);
+    size_t off = sizeof(uint64_t) * 2 * kDkMaxStages;
+    p.off_misc = (int)off;
+    off = align_up(off + sizeof(DkMisc) + sizeof(float) * (size_t)B * E, 128);
+    p.off_x = (int)off;
+    off = align_up(off + sizeof(float) * (size_t)B * H, 128);
+    p.off_h = (int)off;
+    off = align_up(off + sizeof(float) * (size_t)R * I, 128);
+    p.off_o = (int)off;
+    off = align_up(off + sizeof(float) * (size_t)R * maxrows, 128);
+    p.off_wr = (int)off;
+    off = align_up(off + sizeof(uint16_t) * (size_t)E * maxrows, 128);
+    p.off_ring = (int)off;
+    const size_t stage = align_up((size_t)(4 * H > 2 * I ? 4 * H : 2 * I), 128);
+    if (off >= (size_t)kDkSmemMax) return false;
+    size_t S = ((size_t)kDkSmemMax - off) / stage;
+    if (S > (size_t)kDkMaxStages) S = kDkMaxStages;
+    if (S < 4) return false;
+    p.S = (int)S;
+    p.stage_bytes = (int)stage;
+    p.maxrows = maxrows;
+    smem = off + S * stage;
+    return true;
+}
+
+static int launch_decode(DkParams& p, size_t smem, int sms, char* ws, const WsLayout& L, cudaStream_t st) {
+    int rc = allow_smem(decode_kernel, smem);
+    if (rc) return rc;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel, kDkThreads, smem) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (per_sm < 1) return MOE_ERR_UNSUPPORTED;
+    p.h = reinterpret_cast<float*>(ws + L.h);
+    p.acc = reinterpret_cast<unsigned long long*>(ws + L.acc);
+    p.bar = reinterpret_cast<unsigned*>(ws + L.bar);
+    if ((rc = to_status(cudaMemsetAsync(ws + L.bar, 0, L.acc_end - L.bar, st)))) return rc;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)sms);
+    cfg.blockDim = dim3(kDkThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return to_status(cudaLaunchKernelEx(&cfg, decode_kernel, p));
+}
+
+static void decode_common(DkParams& p, int B, int H, int I, int E, int k, int L, unsigned flags,
+                          int32_t* status) {
+    p.B = B;
+    p.H = H;
+    p.I = I;
+    p.E = E;
+    p.k = k;
+    p.L = L;
+    p.flags = flags;
+    p.status = status;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -459,6 +533,23 @@ int moe_layer_forward(const void* x, int x_dtype, const uint16_t* w_router, cons
     if (route_w_out) c.rw = route_w_out;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (flags & MOE_F_UNFUSED) return launch_unfused_layer(c, st);
+    {
+        DkParams dp;
+        memset(&dp, 0, sizeof dp);
+        size_t dsm = 0;
+        const int sms = sm_count();
+        if (decode_plan(B, H, I, E, top_k, sms, dp, dsm)) {
+            decode_common(dp, B, H, I, E, top_k, 1, flags, c.status);
+            dp.x_bf16 = x_dtype == MOE_DT_BF16;
+            dp.x_in = x;
+            dp.residual = residual;
+            dp.y = y;
+            dp.layer[0] = c.w;
+            dp.ids_out = c.ids;
+            dp.w_out = c.rw;
+            return launch_decode(dp, dsm, sms, ws, L, st);
+        }
+    }
     StackArgs sa;
     memset(&sa, 0, sizeof sa);
     sa.L = 1;
@@ -511,6 +602,23 @@ int moe_stack_forward(int Lc, const uint16_t* const* w_router, const float* cons
             if ((rc = launch_unfused_layer(c, st))) return rc;
         }
         return MOE_OK;
+    }
+    {
+        DkParams dp;
+        memset(&dp, 0, sizeof dp);
+        size_t dsm = 0;
+        const int sms = sm_count();
+        if (decode_plan(B, H, I, E, top_k, sms, dp, dsm)) {
+            decode_common(dp, B, H, I, E, top_k, Lc, flags, c.status);
+            dp.x_bf16 = 0;
+            dp.x_in = x_inout;
+            dp.residual = x_inout;
+            dp.y = x_inout;
+            for (int l = 0; l < Lc; ++l) dp.layer[l] = sa.layer[l];
+            dp.ids_out = expert_ids_out;
+            dp.w_out = nullptr;
+            return launch_decode(dp, dsm, sms, ws, L, st);
+        }
     }
     return launch_fused(c, sa, reinterpret_cast<unsigned*>(ws + L.bar), st);
 }
