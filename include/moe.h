@@ -202,6 +202,24 @@ int moe_stack_forward(int L, const uint16_t* const* w_router, const float* const
                       uint32_t flags, void* workspace, size_t workspace_bytes,
                       int32_t* dev_status, void* stream);
 
+/*
+ * moe_set_trace_buffer -- profiling aid.  While set, every launch of the
+ * persistent decode kernel records, per CTA, per layer and per phase
+ * boundary, a pair of 64-bit words (globaltimer ns, SM clock) into the device
+ * buffer `trace` of `words` words: word index ((l+1)*G + cta)*48 + ev*2 for
+ * layer l (-1 = the initial router step), G = grid size, event ev:
+ * 0 layer start, 1 routing done, 2 gate/up done, 3 after the mid-layer
+ * barrier, 4 down done, 5 layer work done, 6 after the end-of-layer barrier,
+ * 7 logits and x loaded, 8 top-k done, 9 grouping done, 10 combine done,
+ * 11 next router slice ready, 12 first gate/up chunk landed (leader warp),
+ * 13 first down chunk landed (leader warp), 16 last gate/up chunk landed,
+ * 17 last chunk landed, 18 producer issued every chunk, 19 first chunk
+ * landed (16..19 observed by the otherwise idle producer warp).
+ * Entries that do not fit are dropped.  trace == NULL with words == 0 turns
+ * it off (the default).  Host-only setting, not thread-safe.
+ */
+int moe_set_trace_buffer(unsigned long long* trace, int words);
+
 /* moe_status_string -- static text for a moe_status code or MOE_DEV_* bit. */
 const char* moe_status_string(int code);
 

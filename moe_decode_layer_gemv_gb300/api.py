@@ -37,6 +37,8 @@ _lib.moe_expert_forward_noalloc.argtypes = [_P, _I, _P, _P, _P, _P, _P, _P, _P, 
 _lib.moe_layer_forward.argtypes = [_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _U,
                                    _P, _S, _P, _P]
 _lib.moe_stack_forward.argtypes = [_I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _U, _P, _S, _P, _P]
+_lib.moe_set_trace_buffer.argtypes = [_P, _I]
+_lib.moe_set_trace_buffer.restype = ctypes.c_int
 _lib.moe_status_string.argtypes = [_I]
 _lib.moe_status_string.restype = ctypes.c_char_p
 for _f in ("moe_workspace_bytes", "moe_route", "moe_group_by_expert", "moe_expert_forward",
@@ -44,7 +46,8 @@ for _f in ("moe_workspace_bytes", "moe_route", "moe_group_by_expert", "moe_exper
     getattr(_lib, _f).restype = ctypes.c_int
 
 EXPORTED = ("moe_workspace_bytes", "moe_route", "moe_group_by_expert", "moe_expert_forward",
-            "moe_expert_forward_noalloc", "moe_layer_forward", "moe_stack_forward", "moe_status_string")
+            "moe_expert_forward_noalloc", "moe_layer_forward", "moe_stack_forward", "moe_set_trace_buffer",
+            "moe_status_string")
 
 MOE_OK = 0
 MOE_ERR_INVALID_ARG = -1
@@ -100,6 +103,16 @@ def _need(t, dtype, name):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous CUDA tensor")
+
+
+def set_trace_buffer(buf):
+    """Record phase timestamps of the persistent decode kernel into `buf`
+    (a CUDA int64 tensor) on every following launch; None turns it off."""
+    if buf is None:
+        _check(_lib.moe_set_trace_buffer(None, 0), "moe_set_trace_buffer")
+    else:
+        _need(buf, torch.int64, "trace buffer")
+        _check(_lib.moe_set_trace_buffer(_ptr(buf), buf.numel()), "moe_set_trace_buffer")
 
 
 def workspace_bytes(B, H, I, E, top_k) -> int:

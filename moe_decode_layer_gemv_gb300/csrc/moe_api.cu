@@ -167,9 +167,9 @@ static WsLayout ws_layout(int B, int H, int I, int E, int k) {
     L.unique = take(sizeof(int32_t) * E);
     L.num_unique = take(sizeof(int32_t));
     L.status = take(sizeof(int32_t));
-    L.bar = take(sizeof(unsigned) * 2);
-    L.acc = take(sizeof(unsigned long long) * 2 * (size_t)B * E);  // right after bar: one memset clears both
-    L.acc_end = L.acc + sizeof(unsigned long long) * 2 * (size_t)B * E;
+    L.bar = take(sizeof(unsigned) * 1056);  // abort/counter words + one barrier flag per CTA (<= 1024)
+    L.acc = take(sizeof(unsigned long long) * 2 * 8 * (size_t)B * E);  // right after bar: one memset clears both
+    L.acc_end = L.acc + sizeof(unsigned long long) * 2 * 8 * (size_t)B * E;
     L.h = take(sizeof(float) * R * I);
     L.o = take(sizeof(float) * R * H);
     L.total = off;
@@ -340,12 +340,12 @@ static int launch_fused(const Ctx& c, const StackArgs& sa, unsigned* bar, cudaSt
 // ring; it applies when B <= 4, B*k <= 32 and the ring gets >= 4 stages.
 static bool decode_plan(int B, int H, int I, int E, int k, int sms, DkParams& p, size_t& smem) {
     const int R = B * k;
-    if (B < 1 || B > kDkMaxB || R > kDkMaxR || sms < 1) return false;
+    if (B < 1 || B > kDkMaxB || R > kDkMaxR || sms < 1 || sms > 1024) return false;
     const int ng = H >> 3;
     const int maxrows = 8 * ((ng + sms - 1) / sms);
     size_t off = sizeof(uint64_t) * 2 * kDkMaxStages;
     p.off_misc = (int)off;
-    off = align_up(off + sizeof(DkMisc) + sizeof(float) * (size_t)B * E, 128);
+    off = align_up(off + sizeof(DkMisc) + sizeof(float) * (size_t)B * ((E + 7) & ~7), 128);
     p.off_x = (int)off;
     off = align_up(off + sizeof(float) * (size_t)B * H, 128);
     p.off_h = (int)off;
@@ -360,6 +360,10 @@ static bool decode_plan(int B, int H, int I, int E, int k, int sms, DkParams& p,
     size_t S = ((size_t)kDkSmemMax - off) / stage;
     if (S > (size_t)kDkMaxStages) S = kDkMaxStages;
     if (S < 4) return false;
+    // stage s is always consumed by warp s % W, so S must be a multiple of W
+    const size_t W = S < (size_t)kDkConsumers ? S : (size_t)kDkConsumers;
+    S = W * (S / W);
+    p.W = (int)W;
     p.S = (int)S;
     p.stage_bytes = (int)stage;
     p.maxrows = maxrows;
@@ -392,8 +396,13 @@ static int launch_decode(DkParams& p, size_t smem, int sms, char* ws, const WsLa
     return to_status(cudaLaunchKernelEx(&cfg, decode_kernel, p));
 }
 
+static unsigned long long* g_trace = nullptr;
+static int g_trace_words = 0;
+
 static void decode_common(DkParams& p, int B, int H, int I, int E, int k, int L, unsigned flags,
                           int32_t* status) {
+    p.trace = g_trace;
+    p.trace_words = g_trace_words;
     p.B = B;
     p.H = H;
     p.I = I;
@@ -621,6 +630,13 @@ int moe_stack_forward(int Lc, const uint16_t* const* w_router, const float* cons
         }
     }
     return launch_fused(c, sa, reinterpret_cast<unsigned*>(ws + L.bar), st);
+}
+
+int moe_set_trace_buffer(unsigned long long* trace, int words) {
+    if ((trace == nullptr) != (words == 0) || words < 0) return MOE_ERR_INVALID_ARG;
+    g_trace = trace;
+    g_trace_words = words;
+    return MOE_OK;
 }
 
 const char* moe_status_string(int code) {

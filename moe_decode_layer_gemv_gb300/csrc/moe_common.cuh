@@ -40,6 +40,9 @@ __device__ __forceinline__ float2 bf16x2_to_f2(uint32_t u) {
 
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
+// SiLU(g) * u with SiLU(z) = z / (1 + e^-z), fp32
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);

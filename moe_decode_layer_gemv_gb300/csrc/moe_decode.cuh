@@ -28,7 +28,7 @@
 
 namespace moe {
 
-constexpr int kDkConsumers = 8;                    // consumer warps
+constexpr int kDkConsumers = 12;                   // consumer warps
 constexpr int kDkThreads = 32 * (kDkConsumers + 1);  // + one producer warp
 constexpr int kDkMaxB = 4;
 constexpr int kDkMaxR = 32;
@@ -49,23 +49,28 @@ struct DkParams {
     int32_t* ids_out;  // [L, B, k] or nullptr
     float* w_out;      // [B, k] (single layer) or nullptr
     float* h;          // [R, I] exchange buffer
-    unsigned long long* acc;  // [2][B][E] fixed-point logits
+    unsigned long long* acc;  // [2][kDkShadows][B][E] fixed-point logits
     unsigned* bar;            // [0] arrival counter, [1] abort word
     int32_t* status;
     int S, stage_bytes, maxrows;
+    int W;  // consumer warps that take chunks: stage s always goes to warp s % W (S % W == 0)
+    unsigned long long* trace;  // optional phase timestamps (see dk_trace), or nullptr
+    int trace_words;
     int off_misc, off_x, off_h, off_o, off_wr, off_ring;
 };
 
-struct DkMisc {
+struct __align__(16) DkMisc {
     int abort_flag;
     int sync_ok;
     int U;
     int ids[kDkMaxR];
+    float selv[kDkMaxR];  // selected logits, rank order
     float w[kDkMaxR];
     int pos[kDkMaxR];   // position of route r in the grouped list
     int rat[kDkMaxR];   // route at position p
     int seg_e[kDkMaxR];
     int seg_p[kDkMaxR + 1];
+    int last_pos[kDkMaxStages];  // latest ring position armed in each stage (-1: none)
 };
 
 // --------------------------------------------------------- work partition
@@ -78,44 +83,75 @@ __device__ __forceinline__ void dk_rows(int c, int G, int H, int& h0, int& h1) {
 }
 
 // First gate/up row pair of CTA c (pairs are numbered segment-major).  The
-// split balances each CTA's total bytes (its gate/up pairs plus its down rows
-// of every selected expert).  Ranges [start(c), max(start(c), start(c+1)))
-// cover every pair even where start() is not monotonic (tiny H).
-__device__ __forceinline__ long long dk_gate_start(int c, int G, int U, int H, int I) {
-    const long long P = (long long)U * I;
+// split balances each CTA's total bytes: its gate/up pairs (4H bytes each)
+// plus its down rows of every selected expert (2I bytes per row and expert):
+//   start(c) = floor(U * N_c / D),  N_c = 6HI*c - 2I*G*h0(c),  D = 4HG,
+// with start(0) = 0 and start(G) = P = U*I (integer arithmetic only: this
+// GPU's FP64 rate is low).  N_c does not depend on the routing, so it is
+// computed once per launch; every CTA evaluates the same expression for the
+// same c, so neighbouring ranges agree, and the ranges
+// [start(c), max(start(c), start(c+1))) cover every pair even where start()
+// is not monotonic (tiny H).
+__device__ __forceinline__ long long dk_gate_num(int c, int G, int H, int I) {
+    const long long h0 = 8LL * ((long long)c * (H >> 3) / G);
+    return 6LL * H * I * c - 2LL * I * G * h0;
+}
+
+__device__ __forceinline__ int dk_gate_start(int c, int G, int U, int I, long long num, long long den) {
+    const int P = U * I;
     if (c <= 0) return 0;
     if (c >= G) return P;
-    const long long h0 = 8LL * ((long long)c * (H >> 3) / G);
-    const long long target = (long long)c * U * I * 6LL * H / G;
-    long long v = (target - h0 * U * 2LL * I) / (4LL * H);
-    return v < 0 ? 0 : (v > P ? P : v);
+    if (num <= 0) return 0;
+    const long long v = (long long)U * num / den;
+    return v > P ? P : (int)v;
 }
 
 struct DkWork {
-    long long ga, gb;  // gate/up pairs [ga, gb)
+    int ga, gb;  // gate/up pairs [ga, gb)
     int h0, h1, nr, nd_per_u, ng, n;
 };
 
-__device__ __forceinline__ DkWork dk_work(const DkParams& p, int U) {
-    DkWork w;
+// rows, down-chunk size and down chunks per expert are fixed per launch
+// (template `base`); only the gate/up range depends on the routing.
+__device__ __forceinline__ DkWork dk_work(const DkWork& base, int U, int I, long long n0, long long n1,
+                                          long long den) {
+    DkWork w = base;
     const int G = gridDim.x, c = blockIdx.x;
-    w.ga = dk_gate_start(c, G, U, p.H, p.I);
-    const long long nb = dk_gate_start(c + 1, G, U, p.H, p.I);
+    w.ga = dk_gate_start(c, G, U, I, n0, den);
+    const int nb = dk_gate_start(c + 1, G, U, I, n1, den);
     w.gb = nb > w.ga ? nb : w.ga;
-    dk_rows(c, G, p.H, w.h0, w.h1);
-    int nr = p.stage_bytes / (2 * p.I);
-    if (nr < 1) nr = 1;
-    w.nr = nr;
-    w.nd_per_u = w.h1 > w.h0 ? (w.h1 - w.h0 + nr - 1) / nr : 0;
-    w.ng = (int)(w.gb - w.ga);
+    w.ng = w.gb - w.ga;
     w.n = w.ng + U * w.nd_per_u;
     return w;
 }
 
 // ------------------------------------------------------------- barriers
 // Device-wide barrier among the threads of named barrier `bar_id`
-// (`nthreads` of them) in every CTA; thread kDkLeader does the arrive/wait.
+// (`nthreads` of them) in every CTA: after the CTA-wide barrier the leader
+// thread adds 1 to a shared arrival counter with a release atomic and polls
+// it until it reaches epoch * G, then an acquire fence.  (Measured on GB300
+// with 152 CTAs: ~1.15 us; a flag per CTA polled by every CTA, a master-
+// released flag array and a two-level counter tree were all slower.)  Every
+// thread that wrote global memory with relaxed reductions fences before
+// entering, since the release orders only the leader's own accesses.
+// p.bar[0] = counter, p.bar[1] = abort word.  Bounded: after kDkSpinLimit
+// polls the CTA sets MOE_DEV_TIMEOUT and the abort word and reports failure.
 constexpr int kDkLeader = 32;  // first consumer thread
+constexpr int kDkShadows = 8;  // copies of the logit accumulator (spread the atomics)
+
+__device__ __forceinline__ unsigned atom_add_release_gpu(unsigned* p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.add.release.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 __device__ __forceinline__ bool dk_grid_sync(const DkParams& p, unsigned& epoch, DkMisc* m, int bar_id,
                                              int nthreads) {
@@ -123,33 +159,35 @@ __device__ __forceinline__ bool dk_grid_sync(const DkParams& p, unsigned& epoch,
     if (threadIdx.x == kDkLeader) {
         epoch += 1;
         const unsigned target = epoch * gridDim.x;
-        __threadfence();
-        red_release_gpu_add(p.bar, 1u);
         int ok = 1;
-        unsigned long long spins = 0;
-        while (ld_acquire_gpu(p.bar) < target) {
-            ++spins;
-            if ((spins & 127ull) == 0 && ld_acquire_gpu(p.bar + 1) != 0u) {
-                ok = 0;
-                break;
+        const unsigned old = atom_add_release_gpu(p.bar, 1u);
+        if (old + 1u < target) {
+            unsigned long long spins = 0;
+            while (ld_relaxed_gpu(p.bar) < target) {
+                ++spins;
+                if ((spins & 63ull) == 0 && ld_relaxed_gpu(p.bar + 1) != 0u) {
+                    ok = 0;
+                    break;
+                }
+                if (spins > kDkSpinLimit) {
+                    set_status(p.status, MOE_DEV_TIMEOUT);
+                    atomicExch(p.bar + 1, 1u);
+                    ok = 0;
+                    break;
+                }
             }
-            if (spins > kDkSpinLimit) {
-                set_status(p.status, MOE_DEV_TIMEOUT);
-                atomicExch(p.bar + 1, 1u);
-                ok = 0;
-                break;
-            }
-            if (spins > 256) __nanosleep(32);
         }
-        __threadfence();
+        fence_acq_rel_gpu();
         m->sync_ok = ok;
         if (!ok) m->abort_flag = 1;
     }
+    __syncwarp();
     named_sync(bar_id, nthreads);
     return m->sync_ok != 0;
 }
 
-// mbarrier wait that also gives up when the CTA has aborted
+// mbarrier wait that also gives up when the CTA has aborted; bounded by
+// kDkWaitLimit tries.
 __device__ __forceinline__ bool dk_wait(uint64_t* bar, uint32_t parity, DkMisc* m, const DkParams& p) {
     for (uint32_t i = 0; i < kDkWaitLimit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -161,94 +199,130 @@ __device__ __forceinline__ bool dk_wait(uint64_t* bar, uint32_t parity, DkMisc* 
     return false;
 }
 
+// Phase timestamps for profiling: word pair (globaltimer ns, SM clock) of
+// event `ev` (0..23) of layer `l` (-1 = the initial router step) of this CTA.
+__device__ __forceinline__ void dk_trace(const DkParams& p, int l, int ev) {
+    if (p.trace == nullptr) return;
+    const long long idx = (((long long)(l + 1) * gridDim.x + blockIdx.x) * 24 + ev) * 2;
+    if (idx + 1 >= p.trace_words) return;
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    p.trace[idx] = t;
+    p.trace[idx + 1] = (unsigned long long)clock64();
+}
+
 // ----------------------------------------------------------- small steps
 __device__ __forceinline__ float fix_to_float(unsigned long long v) {
-    return (float)((double)(long long)v * (1.0 / 4294967296.0));
+    return __ll2float_rn((long long)v) * (1.0f / kFixScale);
 }
 
 __device__ __forceinline__ unsigned long long float_to_fix(float v) {
     return (unsigned long long)__float2ll_rn(v * kFixScale);
 }
 
-// top-k of one token's logits held in shared memory (one warp); same rule
-// as the stand-alone top-k phase: ties to the lower id, fp32 softmax,
-// renormalised over the selected experts.
-__device__ void dk_topk_token(const float* lg, int E, int k, int t, DkMisc* m, int32_t* status) {
+// Top-k of one token (one warp; lane l holds experts l, l+32, ...; E <= 256).
+// Each logit becomes an order-preserving unsigned key; every round takes the
+// largest key over the warp with one warp-wide max reduction and, among the
+// lanes holding it, the lowest expert id with one min reduction -- "logit
+// descending, ties to the lower id" -- and the owning lane marks it taken.
+// The routing weights follow: the fp32 softmax over all E logits followed by
+// renormalisation over the selection equals the softmax over the selected
+// logits alone (the full denominator cancels), w_j = e^(l_j - l_0) / sum.
+__device__ __forceinline__ unsigned order_key(float f) {
+    const unsigned b = __float_as_uint(f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(unsigned k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+__device__ void dk_topk_warp(const float* lg, int E, int k, int t, DkMisc* m, int32_t* status) {
     const int lane = threadIdx.x & 31;
-    float v[8];
+    unsigned key[8];
     bool bad = false;
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
         const int e = lane + 32 * s;
-        v[s] = e < E ? lg[e] : -INFINITY;
-        if (e < E && !isfinite(v[s])) bad = true;
+        const float v = e < E ? lg[e] : 0.f;
+        if (e < E && !isfinite(v)) bad = true;
+        key[s] = e < E ? order_key(v) : 0u;  // 0 is below every real key
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(status, MOE_DEV_NONFINITE);
     unsigned taken = 0;
-    float selv[MOE_MAX_TOPK];
-    int seli[MOE_MAX_TOPK];
+    int my_id = 0;
+    float my_l = 0.f, l0 = 0.f;
+    for (int j = 0; j < k; ++j) {
+        unsigned kb = 0u;
+        int ib = 0x7fffffff;
 #pragma unroll
-    for (int j = 0; j < MOE_MAX_TOPK; ++j) {
-        selv[j] = -INFINITY;
-        seli[j] = 0;
-        if (j < k) {
-            float bv = -INFINITY;
-            int bi = 0x7fffffff;
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const int e = lane + 32 * s;
-                if (e < E && !((taken >> s) & 1u) && (v[s] > bv || (v[s] == bv && e < bi))) {
-                    bv = v[s];
-                    bi = e;
-                }
+        for (int s = 0; s < 8; ++s)
+            if (!((taken >> s) & 1u) && key[s] > kb) {  // strictly greater keeps the lower id
+                kb = key[s];
+                ib = lane + 32 * s;
             }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                if (ov > bv || (ov == bv && oi < bi)) {
-                    bv = ov;
-                    bi = oi;
-                }
-            }
-            if (bi == 0x7fffffff) bi = 0;
-            if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-            selv[j] = bv;
-            seli[j] = bi;
+        const unsigned km = __reduce_max_sync(0xffffffffu, kb);
+        const int win = (int)__reduce_min_sync(0xffffffffu, kb == km ? (unsigned)ib : 0x7fffffffu);
+        if ((win & 31) == lane && win < E) taken |= 1u << (win >> 5);
+        const float lv = key_value(km);
+        if (j == 0) l0 = lv;
+        if (lane == j) {
+            my_id = win < E ? win : 0;
+            my_l = lv;
         }
     }
-    const float mx = selv[0];
-    float s = 0.f;
+    const float ex = lane < k ? expf(my_l - l0) : 0.f;
+    float den = ex;
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
-        if (lane + 32 * q < E) s += expf(v[q] - mx);
-    s = warp_sum(s);
-    if (lane == 0) {
-        float pr[MOE_MAX_TOPK];
-        float ssel = 0.f;
-#pragma unroll
-        for (int j = 0; j < MOE_MAX_TOPK; ++j) {
-            pr[j] = 0.f;
-            if (j < k) {
-                pr[j] = expf(selv[j] - mx) / s;
-                ssel += pr[j];
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < MOE_MAX_TOPK; ++j)
-            if (j < k) {
-                m->ids[t * k + j] = seli[j];
-                m->w[t * k + j] = pr[j] / ssel;
-            }
+    for (int off = 4; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);  // lanes 0..7
+    if (lane < k) {
+        m->ids[t * k + lane] = my_id;
+        m->selv[t * k + lane] = my_l;
+        m->w[t * k + lane] = ex / den;
     }
+}
+
+// Router partial sums of this CTA's hidden rows [h0, h0+nrows) for every
+// (token, expert): one thread per pair, rows in 8-wide vectors from shared
+// memory, the result added to shadow copy (CTA mod kDkShadows) of the
+// fixed-point accumulator.
+__device__ __forceinline__ void dk_router_partials(const uint16_t* wrs, int maxrows, const float* xs, int H,
+                                                   int h0, int nrows, int B, int E,
+                                                   unsigned long long* acc, int t0, int nth) {
+    unsigned long long* sh = acc + (size_t)(blockIdx.x % kDkShadows) * B * E;
+    for (int v = t0; v < B * E; v += nth) {
+        const int t = v / E, e = v - t * E;
+        const uint16_t* wrow = wrs + e * maxrows;
+        const float* xr = xs + (size_t)t * H + h0;
+        float2 a = make_float2(0.f, 0.f);
+        for (int r = 0; r < nrows; r += 8) {
+            const uint4 wv = *reinterpret_cast<const uint4*>(wrow + r);
+            const float4 xa = *reinterpret_cast<const float4*>(xr + r);
+            const float4 xb = *reinterpret_cast<const float4*>(xr + r + 4);
+            a = ffma2(bf16x2_to_f2(wv.x), make_float2(xa.x, xa.y), a);
+            a = ffma2(bf16x2_to_f2(wv.y), make_float2(xa.z, xa.w), a);
+            a = ffma2(bf16x2_to_f2(wv.z), make_float2(xb.x, xb.y), a);
+            a = ffma2(bf16x2_to_f2(wv.w), make_float2(xb.z, xb.w), a);
+        }
+        red_add_u64(sh + v, float_to_fix(a.x + a.y));
+    }
+    __threadfence();  // the reductions are performed before this thread reaches the next barrier
 }
 
 // Stable grouping of R <= 32 routes by expert in one warp: the position of
 // route r is (#routes with a smaller expert) + (#earlier routes with the
 // same expert) -- the counting sort's result, computed directly.
-__device__ void dk_group(DkMisc* m, int R, bool no_dedup) {
+__device__ void dk_group(DkMisc* m, int R, int E, bool no_dedup) {
     const int lane = threadIdx.x & 31;
-    const int e = lane < R ? m->ids[lane] : 0x7fffffff;
+    int e = 0x7fffffff;
+    if (lane < R) {  // only non-finite logits can leave an entry out of range
+        e = m->ids[lane];
+        if (e < 0 || e >= E) {
+            e = 0;
+            m->ids[lane] = 0;
+        }
+    }
+    __syncwarp();
     int pos = 0;
     for (int r = 0; r < R; ++r) {
         const int er = __shfl_sync(0xffffffffu, e, r);
@@ -278,6 +352,119 @@ __device__ void dk_group(DkMisc* m, int R, bool no_dedup) {
     __syncwarp();
 }
 
+// Sum of N values held by every lane over the 32 lanes of a warp; the N
+// butterflies are interleaved so the latency is that of one.
+template <int N>
+__device__ __forceinline__ void warp_sum_n(float (&v)[N]) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+        for (int j = 0; j < N; ++j) v[j] += __shfl_xor_sync(0xffffffffu, v[j], off);
+}
+
+// One gate/up row pair held in a ring stage (gate row, then up row, H bf16
+// each) against NQ tokens' x rows in shared memory.  Four 16-byte vectors
+// per lane are loaded before they are used.  Result: g[q], u[q] summed over
+// the warp.
+template <int NQ>
+__device__ __forceinline__ void dk_gate_pair(const unsigned char* st, const float* xs, const int (&tok)[4], int H,
+                                             float (&gu)[2 * NQ]) {
+    const int lane = threadIdx.x & 31;
+    float2 ag[NQ], au[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) ag[q] = au[q] = make_float2(0.f, 0.f);
+    const int nv = H >> 3;
+    auto step = [&](const uint4& gw, const uint4& uw, int v) {
+        const float2 g0 = bf16x2_to_f2(gw.x), g1 = bf16x2_to_f2(gw.y);
+        const float2 g2 = bf16x2_to_f2(gw.z), g3 = bf16x2_to_f2(gw.w);
+        const float2 u0 = bf16x2_to_f2(uw.x), u1 = bf16x2_to_f2(uw.y);
+        const float2 u2 = bf16x2_to_f2(uw.z), u3 = bf16x2_to_f2(uw.w);
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            const float4* xp = reinterpret_cast<const float4*>(xs + (size_t)tok[q] * H + 8 * v);
+            const float4 xa = xp[0], xb = xp[1];
+            ag[q] = ffma2(g0, make_float2(xa.x, xa.y), ag[q]);
+            au[q] = ffma2(u0, make_float2(xa.x, xa.y), au[q]);
+            ag[q] = ffma2(g1, make_float2(xa.z, xa.w), ag[q]);
+            au[q] = ffma2(u1, make_float2(xa.z, xa.w), au[q]);
+            ag[q] = ffma2(g2, make_float2(xb.x, xb.y), ag[q]);
+            au[q] = ffma2(u2, make_float2(xb.x, xb.y), au[q]);
+            ag[q] = ffma2(g3, make_float2(xb.z, xb.w), ag[q]);
+            au[q] = ffma2(u3, make_float2(xb.z, xb.w), au[q]);
+        }
+    };
+    int v = lane;
+    for (; v + 96 < nv; v += 128) {
+        uint4 gw[4], uw[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            gw[j] = *reinterpret_cast<const uint4*>(st + 16 * (v + 32 * j));
+            uw[j] = *reinterpret_cast<const uint4*>(st + 2 * H + 16 * (v + 32 * j));
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) step(gw[j], uw[j], v + 32 * j);
+    }
+    for (; v < nv; v += 32)
+        step(*reinterpret_cast<const uint4*>(st + 16 * v), *reinterpret_cast<const uint4*>(st + 2 * H + 16 * v), v);
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+        gu[2 * q] = ag[q].x + ag[q].y;
+        gu[2 * q + 1] = au[q].x + au[q].y;
+    }
+    warp_sum_n<2 * NQ>(gu);
+}
+
+// Down rows [0, nrc) of a ring stage (each I bf16) against NQ routes' h rows
+// in shared memory (hrow = h of the first route, consecutive routes I apart),
+// four rows at a time with independent accumulators; results to
+// os[q * ld + orow0 + r].
+template <int NQ>
+__device__ __forceinline__ void dk_down_rows(const unsigned char* st, int nrc, int I, const float* hrow,
+                                             float* os, int ld, int orow0) {
+    const int lane = threadIdx.x & 31;
+    const int nv = I >> 3;
+    for (int rb = 0; rb < nrc; rb += 4) {
+        const int n4 = min(4, nrc - rb);
+        float2 acc[4][NQ];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) acc[j][q] = make_float2(0.f, 0.f);
+        for (int v = lane; v < nv; v += 32) {
+            uint4 wv[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                wv[j] = j < n4 ? *reinterpret_cast<const uint4*>(st + (size_t)(rb + j) * 2 * I + 16 * v)
+                               : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                const float4* hp = reinterpret_cast<const float4*>(hrow + (size_t)q * I + 8 * v);
+                const float4 ha = hp[0], hb = hp[1];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    acc[j][q] = ffma2(bf16x2_to_f2(wv[j].x), make_float2(ha.x, ha.y), acc[j][q]);
+                    acc[j][q] = ffma2(bf16x2_to_f2(wv[j].y), make_float2(ha.z, ha.w), acc[j][q]);
+                    acc[j][q] = ffma2(bf16x2_to_f2(wv[j].z), make_float2(hb.x, hb.y), acc[j][q]);
+                    acc[j][q] = ffma2(bf16x2_to_f2(wv[j].w), make_float2(hb.z, hb.w), acc[j][q]);
+                }
+            }
+        }
+        float red[4 * NQ];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) red[j * NQ + q] = acc[j][q].x + acc[j][q].y;
+        warp_sum_n<4 * NQ>(red);
+        if (lane == 0) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (j < n4)
+#pragma unroll
+                    for (int q = 0; q < NQ; ++q) os[(size_t)q * ld + orow0 + rb + j] = red[j * NQ + q];
+        }
+    }
+}
+
 // ------------------------------------------------------------ the kernel
 __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -289,7 +476,8 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
     float* os = reinterpret_cast<float*>(smem + p.off_o);   // [R][maxrows]
     uint16_t* wrs = reinterpret_cast<uint16_t*>(smem + p.off_wr);  // [E][maxrows]
     unsigned char* ring = smem + p.off_ring;
-    float* lg = reinterpret_cast<float*>(smem + p.off_misc + sizeof(DkMisc));  // [B][E]
+    float* lg = reinterpret_cast<float*>(smem + p.off_misc + sizeof(DkMisc));  // [B][Ep]
+    const int Ep = (p.E + 7) & ~7;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = p.B, H = p.H, I = p.I, E = p.E, k = p.k, R = B * k;
@@ -297,6 +485,16 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
     int h0, h1;
     dk_rows(blockIdx.x, gridDim.x, H, h0, h1);
     const int nrows = h1 - h0;
+    const long long gN0 = dk_gate_num(blockIdx.x, gridDim.x, H, I);
+    const long long gN1 = dk_gate_num(blockIdx.x + 1, gridDim.x, H, I);
+    const long long gDen = 4LL * H * gridDim.x;
+    DkWork wbase;
+    wbase.h0 = h0;
+    wbase.h1 = h1;
+    wbase.nr = max(1, p.stage_bytes / (2 * I));
+    if (wbase.nr >= 4) wbase.nr &= ~3;  // whole 4-row groups in the down compute
+    wbase.nd_per_u = nrows > 0 ? (nrows + wbase.nr - 1) / wbase.nr : 0;
+    wbase.ga = wbase.gb = wbase.ng = wbase.n = 0;
 
     if (tid == 0) {
         for (int s = 0; s < p.S; ++s) {
@@ -304,14 +502,20 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
             mbar_init(&empty[s], 1);
         }
         m->abort_flag = 0;
+        for (int q = 0; q < kDkMaxStages; ++q) m->last_pos[q] = -1;
         fence_mbar_init();
     }
     __syncthreads();
 
     unsigned epoch = 0;        // barrier count (leader thread only)
-    long long ring_pos = 0;    // chunks through the ring so far (all threads agree)
-    long long issued = 0;      // producer: chunks issued
+    // Ring cursor: chunks through the ring so far, as (stage, phase parity) of
+    // the next chunk -- advanced incrementally, no division per chunk.
+    int ring_pos = 0;
+    int rs = 0;
+    uint32_t rph = 0;
 
+
+    if (tid == kDkLeader) dk_trace(p, -1, 0);
     // ---- router of layer 0: partial dot products over this CTA's rows
     {
         const LayerWeights& w0 = p.layer[0];
@@ -328,29 +532,28 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
         }
         cp_async_wait_all();
         __syncthreads();
-        if (nrows > 0) {
-            for (int q = warp; q < B * E; q += blockDim.x >> 5) {
-                const int t = q / E, e = q - t * E;
-                float part = 0.f;
-                for (int r = lane; r < nrows; r += 32)
-                    part = fmaf(__uint_as_float((uint32_t)wrs[e * p.maxrows + r] << 16), xs[t * H + h0 + r], part);
-                part = warp_sum(part);
-                if (lane == 0) red_add_u64(p.acc + (size_t)t * E + e, float_to_fix(part));
-            }
-        }
+        if (nrows > 0) dk_router_partials(wrs, p.maxrows, xs, H, h0, nrows, B, E, p.acc, tid, blockDim.x);
     }
+    if (tid == kDkLeader) dk_trace(p, -1, 1);
     dk_grid_sync(p, epoch, m, 0, kDkThreads);
 
     for (int l = 0; l < p.L && !*(volatile int*)&m->abort_flag; ++l) {
         const LayerWeights& lw = p.layer[l];
         const bool has_next = l + 1 < p.L;
-        unsigned long long* acc_now = p.acc + (size_t)(l & 1) * B * E;
-        unsigned long long* acc_next = p.acc + (size_t)((l + 1) & 1) * B * E;
+        unsigned long long* acc_now = p.acc + (size_t)(l & 1) * kDkShadows * B * E;
+        unsigned long long* acc_next = p.acc + (size_t)((l + 1) & 1) * kDkShadows * B * E;
         // ---- A0: logits, x, next router slice
-        for (int v = tid; v < B * E; v += blockDim.x) {
-            const int e = v % E;
-            float val = fix_to_float(__ldcg(acc_now + v));
-            if (lw.bias) val += lw.bias[e];
+        if (tid == kDkLeader) dk_trace(p, l, 0);
+        for (int v = tid; v < B * Ep; v += blockDim.x) {
+            const int t = v / Ep, e = v - t * Ep;
+            float val = -INFINITY;
+            if (e < E) {
+                unsigned long long sum = 0ull;  // integer sum: exact in any order
+#pragma unroll
+                for (int sh = 0; sh < kDkShadows; ++sh) sum += __ldcg(acc_now + ((size_t)sh * B + t) * E + e);
+                val = fix_to_float(sum);
+                if (lw.bias) val += lw.bias[e];
+            }
             lg[v] = val;
         }
         if (l > 0 || !p.x_bf16) {
@@ -370,197 +573,220 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
             cp_async_commit();
         }
         __syncthreads();
-        if (warp < B) dk_topk_token(lg + warp * E, E, k, warp, m, p.status);
+        if (tid == kDkLeader) dk_trace(p, l, 7);
+        if (warp < B) dk_topk_warp(lg + warp * Ep, E, k, warp, m, p.status);
         __syncthreads();
-        if (warp == 0) dk_group(m, R, no_dedup);
+        if (tid == kDkLeader) dk_trace(p, l, 8);
+        if (warp == 0) dk_group(m, R, E, no_dedup);
         __syncthreads();
+        if (tid == kDkLeader) dk_trace(p, l, 9);
         if (blockIdx.x == 0) {
             if (p.ids_out && tid < R) p.ids_out[(size_t)l * R + tid] = m->ids[tid];
             if (p.w_out && tid < R) p.w_out[tid] = m->w[tid];
         }
         const int U = m->U;
-        const DkWork wk = dk_work(p, U);
+        const DkWork wk = dk_work(wbase, U, I, gN0, gN1, gDen);
+        if (tid == kDkLeader) dk_trace(p, l, 1);
 
         if (warp == 0) {
-            // ================= producer: one lane issues every chunk in order
-            if (lane == 0) {
+            // ================= producer: lane s owns ring stage s (S <= 32) and
+            // issues that stage's chunks of the layer in order, so the lanes
+            // overlap the cost of issuing bulk copies while each stage is still
+            // armed strictly in sequence (a stage is re-armed only after its
+            // previous chunk was released, and the wait parity never aliases).
+            // Every stage is free at the start of a layer (all of the last
+            // layer's chunks were consumed before its final barrier), so only a
+            // chunk that reuses a stage within this layer waits for the release.
+            if (lane == 0) dk_trace(p, l, 15);
+            const int s = lane;
+            const int c_first = lane < p.S ? ((s - rs) % p.S + p.S) % p.S : wk.n;
+            for (int c = c_first; c < wk.n; c += p.S) {
+                const int n = ring_pos + c;
+                const uint32_t ph = rph ^ (uint32_t)(((rs + c) / p.S) & 1);
+                if (c >= p.S && !dk_wait(&empty[s], ph ^ 1u, m, p)) break;
+                unsigned char* dst = ring + (size_t)s * p.stage_bytes;
+                if (c < wk.ng) {
+                    const int pq = wk.ga + c;
+                    const int u = pq / I, i = pq - u * I;
+                    const uint16_t* G = lw.gate_up + (size_t)m->seg_e[u] * 2 * I * H;
+                    mbar_arrive_expect_tx(&full[s], 4u * H);
+                    bulk_g2s(dst, G + (size_t)i * H, 2u * H, &full[s]);
+                    bulk_g2s(dst + 2 * H, G + (size_t)(I + i) * H, 2u * H, &full[s]);
+                } else {
+                    const int mm = c - wk.ng;
+                    const int u = mm / wk.nd_per_u, sub = mm - u * wk.nd_per_u;
+                    const int r0 = wk.h0 + sub * wk.nr;
+                    const int r1 = min(wk.h1, r0 + wk.nr);
+                    const uint16_t* D = lw.down + (size_t)m->seg_e[u] * H * I;
+                    const uint32_t bytes = 2u * (r1 - r0) * I;
+                    mbar_arrive_expect_tx(&full[s], bytes);
+                    bulk_g2s(dst, D + (size_t)r0 * I, bytes, &full[s]);
+                }
+                m->last_pos[s] = n;
+            }
+            __syncwarp();
+            if (lane == 0 && p.trace) {  // profiling only: when did the first, the last gate/up and the last chunk land?
+                dk_trace(p, l, 18);
                 for (int c = 0; c < wk.n; ++c) {
-                    const long long n = ring_pos + c;
-                    const int s = (int)(n % p.S);
-                    const uint32_t ph = (uint32_t)((n / p.S) & 1);
-                    if (!dk_wait(&empty[s], ph ^ 1u, m, p)) break;
-                    unsigned char* dst = ring + (size_t)s * p.stage_bytes;
-                    if (c < wk.ng) {
-                        const long long q = wk.ga + c;
-                        const int u = (int)(q / I), i = (int)(q - (long long)u * I);
-                        const uint16_t* G = lw.gate_up + (size_t)m->seg_e[u] * 2 * I * H;
-                        mbar_arrive_expect_tx(&full[s], 4u * H);
-                        bulk_g2s(dst, G + (size_t)i * H, 2u * H, &full[s]);
-                        bulk_g2s(dst + 2 * H, G + (size_t)(I + i) * H, 2u * H, &full[s]);
-                    } else {
-                        const int mm = c - wk.ng;
-                        const int u = mm / wk.nd_per_u, sub = mm - u * wk.nd_per_u;
-                        const int r0 = wk.h0 + sub * wk.nr;
-                        const int r1 = min(wk.h1, r0 + wk.nr);
-                        const uint16_t* D = lw.down + (size_t)m->seg_e[u] * H * I;
-                        const uint32_t bytes = 2u * (r1 - r0) * I;
-                        mbar_arrive_expect_tx(&full[s], bytes);
-                        bulk_g2s(dst, D + (size_t)r0 * I, bytes, &full[s]);
-                    }
-                    issued = n + 1;
+                    const int n = ring_pos + c;
+                    mbar_wait(&full[n % p.S], (uint32_t)((n / p.S) & 1), kDkWaitLimit);
+                    if (c == 0) dk_trace(p, l, 19);
+                    if (c == wk.ng - 1) dk_trace(p, l, 16);
+                    if (c == wk.n - 1) dk_trace(p, l, 17);
                 }
             }
         } else {
             // ================= consumers: gate/up pairs
+            // Chunk c sits in stage (ring_pos + c) % S and is consumed by warp
+            // (ring_pos + c) % W; since S % W == 0, every use of a stage goes to
+            // the same warp, in order, so a warp never waits on a stage phase
+            // whose predecessor it has not consumed itself (mbarrier parity
+            // waits would alias otherwise).
             const int cw = warp - 1;
-            for (int c = cw; c < wk.ng; c += kDkConsumers) {
+            const bool consumes = cw < p.W;
+            int s, q0, c0;
+            uint32_t ph;
+            c0 = ((cw - rs % p.W) % p.W + p.W) % p.W;
+            q0 = (rs + c0) / p.S;
+            s = rs + c0 - q0 * p.S;
+            ph = rph ^ (uint32_t)(q0 & 1);
+            for (int c = c0; consumes && c < wk.ng; c += p.W) {
                 if (*(volatile int*)&m->abort_flag) break;
-                const long long n = ring_pos + c;
-                const int s = (int)(n % p.S);
-                if (!dk_wait(&full[s], (uint32_t)((n / p.S) & 1), m, p)) break;
-                const long long q = wk.ga + c;
-                const int u = (int)(q / I), i = (int)(q - (long long)u * I);
+                if (!dk_wait(&full[s], ph, m, p)) break;
+                if (tid == kDkLeader && c == c0) dk_trace(p, l, 12);
+                const int q = wk.ga + c;
+                const int u = q / I, i = q - u * I;
                 const unsigned char* st = ring + (size_t)s * p.stage_bytes;
                 const int p0 = m->seg_p[u], p1 = m->seg_p[u + 1];
                 int tok[kDkMaxB];
 #pragma unroll
                 for (int qq = 0; qq < kDkMaxB; ++qq) tok[qq] = p0 + qq < p1 ? m->rat[p0 + qq] / k : 0;
-                float2 ag[kDkMaxB], au[kDkMaxB];
-#pragma unroll
-                for (int qq = 0; qq < kDkMaxB; ++qq) ag[qq] = au[qq] = make_float2(0.f, 0.f);
                 const int nq = p1 - p0;
-                for (int v = lane; v < (H >> 3); v += 32) {
-                    const uint4 gw = *reinterpret_cast<const uint4*>(st + 16 * v);
-                    const uint4 uw = *reinterpret_cast<const uint4*>(st + 2 * H + 16 * v);
-                    const float2 g0 = bf16x2_to_f2(gw.x), g1 = bf16x2_to_f2(gw.y);
-                    const float2 g2 = bf16x2_to_f2(gw.z), g3 = bf16x2_to_f2(gw.w);
-                    const float2 u0 = bf16x2_to_f2(uw.x), u1 = bf16x2_to_f2(uw.y);
-                    const float2 u2 = bf16x2_to_f2(uw.z), u3 = bf16x2_to_f2(uw.w);
+                float gu[2 * kDkMaxB];
+                switch (nq) {
+                    case 1: { float r[2]; dk_gate_pair<1>(st, xs, tok, H, r); gu[0] = r[0]; gu[1] = r[1]; } break;
+                    case 2: { float r[4]; dk_gate_pair<2>(st, xs, tok, H, r);
 #pragma unroll
-                    for (int qq = 0; qq < kDkMaxB; ++qq) {
-                        if (qq < nq) {
-                            const float4* xp = reinterpret_cast<const float4*>(xs + (size_t)tok[qq] * H + 8 * v);
-                            const float4 xa = xp[0], xb = xp[1];
-                            ag[qq] = ffma2(g0, make_float2(xa.x, xa.y), ag[qq]);
-                            au[qq] = ffma2(u0, make_float2(xa.x, xa.y), au[qq]);
-                            ag[qq] = ffma2(g1, make_float2(xa.z, xa.w), ag[qq]);
-                            au[qq] = ffma2(u1, make_float2(xa.z, xa.w), au[qq]);
-                            ag[qq] = ffma2(g2, make_float2(xb.x, xb.y), ag[qq]);
-                            au[qq] = ffma2(u2, make_float2(xb.x, xb.y), au[qq]);
-                            ag[qq] = ffma2(g3, make_float2(xb.z, xb.w), ag[qq]);
-                            au[qq] = ffma2(u3, make_float2(xb.z, xb.w), au[qq]);
-                        }
-                    }
+                              for (int j = 0; j < 4; ++j) gu[j] = r[j]; } break;
+                    case 3: { float r[6]; dk_gate_pair<3>(st, xs, tok, H, r);
+#pragma unroll
+                              for (int j = 0; j < 6; ++j) gu[j] = r[j]; } break;
+                    default: dk_gate_pair<4>(st, xs, tok, H, gu); break;
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
+                if (lane < nq) {
+                    float g = gu[0], uu = gu[1];
 #pragma unroll
-                for (int qq = 0; qq < kDkMaxB; ++qq) {
-                    if (qq < nq) {
-                        const float g = warp_sum(ag[qq].x + ag[qq].y);
-                        const float uu = warp_sum(au[qq].x + au[qq].y);
-                        if (lane == 0) p.h[(size_t)(p0 + qq) * I + i] = silu_mul(g, uu);
-                    }
+                    for (int qq = 1; qq < kDkMaxB; ++qq)
+                        if (lane == qq) {
+                            g = gu[2 * qq];
+                            uu = gu[2 * qq + 1];
+                        }
+                    p.h[(size_t)(p0 + lane) * I + i] = silu_mul(g, uu);
+                }
+                s += p.W;
+                if (s >= p.S) {
+                    s -= p.S;
+                    ph ^= 1u;
                 }
             }
             // ---- all gate/up pairs of every CTA done
+            if (tid == kDkLeader) dk_trace(p, l, 2);
             const bool ok = dk_grid_sync(p, epoch, m, 1, 32 * kDkConsumers);
             // ---- B: down rows of every selected expert for this CTA's rows
             if (ok) {
             for (int v = tid - 32; v < (R * I) >> 2; v += 32 * kDkConsumers)
                 reinterpret_cast<float4*>(hs)[v] = ld_act_f4(p.h + 4 * (size_t)v);
             named_sync(1, 32 * kDkConsumers);
-            for (int c = wk.ng + cw; c < wk.n; c += kDkConsumers) {
+            if (tid == kDkLeader) dk_trace(p, l, 3);
+            c0 = wk.ng + ((cw - (rs + wk.ng) % p.W) % p.W + p.W) % p.W;
+            q0 = (rs + c0) / p.S;
+            s = rs + c0 - q0 * p.S;
+            ph = rph ^ (uint32_t)(q0 & 1);
+            for (int c = c0; consumes && c < wk.n; c += p.W) {
                 if (*(volatile int*)&m->abort_flag) break;
-                const long long n = ring_pos + c;
-                const int s = (int)(n % p.S);
-                if (!dk_wait(&full[s], (uint32_t)((n / p.S) & 1), m, p)) break;
+                if (!dk_wait(&full[s], ph, m, p)) break;
+
                 const int mm = c - wk.ng;
                 const int u = mm / wk.nd_per_u, sub = mm - u * wk.nd_per_u;
                 const int r0 = wk.h0 + sub * wk.nr;
                 const int r1 = min(wk.h1, r0 + wk.nr);
                 const unsigned char* st = ring + (size_t)s * p.stage_bytes;
                 const int p0 = m->seg_p[u], p1 = m->seg_p[u + 1];
-                for (int r = r0; r < r1; ++r) {
-                    const unsigned char* row = st + (size_t)(r - r0) * 2 * I;
-                    float2 acc[kDkMaxB];
-#pragma unroll
-                    for (int qq = 0; qq < kDkMaxB; ++qq) acc[qq] = make_float2(0.f, 0.f);
-                    for (int v = lane; v < (I >> 3); v += 32) {
-                        const uint4 dw = *reinterpret_cast<const uint4*>(row + 16 * v);
-                        const float2 d0 = bf16x2_to_f2(dw.x), d1 = bf16x2_to_f2(dw.y);
-                        const float2 d2 = bf16x2_to_f2(dw.z), d3 = bf16x2_to_f2(dw.w);
-#pragma unroll
-                        for (int qq = 0; qq < kDkMaxB; ++qq) {
-                            if (p0 + qq < p1) {
-                                const float4* hp = reinterpret_cast<const float4*>(hs + (size_t)(p0 + qq) * I + 8 * v);
-                                const float4 ha = hp[0], hb = hp[1];
-                                acc[qq] = ffma2(d0, make_float2(ha.x, ha.y), acc[qq]);
-                                acc[qq] = ffma2(d1, make_float2(ha.z, ha.w), acc[qq]);
-                                acc[qq] = ffma2(d2, make_float2(hb.x, hb.y), acc[qq]);
-                                acc[qq] = ffma2(d3, make_float2(hb.z, hb.w), acc[qq]);
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int qq = 0; qq < kDkMaxB; ++qq) {
-                        if (p0 + qq < p1) {
-                            const float o = warp_sum(acc[qq].x + acc[qq].y);
-                            if (lane == 0) os[(p0 + qq) * p.maxrows + (r - h0)] = o;
-                        }
-                    }
+                const float* hrow = hs + (size_t)p0 * I;
+                float* orow = os + (size_t)p0 * p.maxrows;
+                switch (p1 - p0) {
+                    case 1: dk_down_rows<1>(st, r1 - r0, I, hrow, orow, p.maxrows, r0 - h0); break;
+                    case 2: dk_down_rows<2>(st, r1 - r0, I, hrow, orow, p.maxrows, r0 - h0); break;
+                    case 3: dk_down_rows<3>(st, r1 - r0, I, hrow, orow, p.maxrows, r0 - h0); break;
+                    default: dk_down_rows<4>(st, r1 - r0, I, hrow, orow, p.maxrows, r0 - h0); break;
                 }
                 __syncwarp();
+                if (c == c0 && cw == 0 && lane == 0) dk_trace(p, l, 13);
                 if (lane == 0) mbar_arrive(&empty[s]);
+                s += p.W;
+                if (s >= p.S) {
+                    s -= p.S;
+                    ph ^= 1u;
+                }
             }
             named_sync(1, 32 * kDkConsumers);
-            // ---- combine (+ residual) for this CTA's rows, j ascending
+            if (tid == kDkLeader) dk_trace(p, l, 4);
+            // ---- combine (+ residual) for this CTA's rows, j ascending.  When the
+            // residual is the layer input itself (a stack) it is already in xs.
+            const bool res_in_xs = p.residual != nullptr && p.residual == p.x_in && !p.x_bf16;
             for (int v = tid - 32; v < B * nrows; v += 32 * kDkConsumers) {
                 const int t = v / nrows, r = v - t * nrows;
                 float a = 0.f;
                 for (int j = 0; j < k; ++j)
                     a = fmaf(m->w[t * k + j], os[m->pos[t * k + j] * p.maxrows + r], a);
                 const size_t gi = (size_t)t * H + h0 + r;
-                if (p.residual) a = ld_act_f(p.residual + gi) + a;
+                if (res_in_xs)
+                    a = xs[t * H + h0 + r] + a;
+                else if (p.residual)
+                    a = ld_act_f(p.residual + gi) + a;
                 p.y[gi] = a;
                 xs[t * H + h0 + r] = a;  // x_{l+1} rows for the next router
             }
             if (blockIdx.x == 0) {  // acc_now was read by every CTA before the last barrier
-                for (int v = tid - 32; v < B * E; v += 32 * kDkConsumers) acc_now[v] = 0ull;
+                for (int v = tid - 32; v < kDkShadows * B * E; v += 32 * kDkConsumers) acc_now[v] = 0ull;
             }
+            if (tid == kDkLeader) dk_trace(p, l, 10);
             if (has_next) cp_async_wait_all();
             named_sync(1, 32 * kDkConsumers);
+            if (tid == kDkLeader) dk_trace(p, l, 11);
             // ---- router of layer l+1: partial dot products over this CTA's rows
-            if (has_next && nrows > 0) {
-                const float* bx = xs;
-                for (int q = cw; q < B * E; q += kDkConsumers) {
-                    const int t = q / E, e = q - t * E;
-                    float part = 0.f;
-                    for (int r = lane; r < nrows; r += 32)
-                        part = fmaf(__uint_as_float((uint32_t)wrs[e * p.maxrows + r] << 16), bx[t * H + h0 + r], part);
-                    part = warp_sum(part);
-                    if (lane == 0) red_add_u64(acc_next + (size_t)t * E + e, float_to_fix(part));
-                }
-            }
+            if (has_next && nrows > 0)
+                dk_router_partials(wrs, p.maxrows, xs, H, h0, nrows, B, E, acc_next, tid - 32,
+                                   32 * kDkConsumers);
             }  // ok
             if (has_next) cp_async_wait_all();
         }
         ring_pos += wk.n;
+        {
+            const int t = rs + wk.n, q = t / p.S;
+            rs = t - q * p.S;
+            rph ^= (uint32_t)(q & 1);
+        }
+        if (tid == kDkLeader) dk_trace(p, l, 5);
         __syncthreads();
         // every thread reads the same flag: nobody writes it between the two
         // barriers around this read
         const bool aborted = *(volatile int*)&m->abort_flag != 0;
         if (has_next && !aborted) dk_grid_sync(p, epoch, m, 0, kDkThreads);
+        if (tid == kDkLeader) dk_trace(p, l, 6);
         __syncthreads();
     }
-    // leave only after this CTA's own copies in flight have landed (they all
-    // have, unless a wait gave up)
+    // leave only after this CTA's own copies in flight have landed: the latest
+    // phase armed in each stage is the only one that can still be in flight
+    // (they have all landed already unless a wait gave up)
     __syncthreads();
-    if (warp == 0 && lane == 0) {
-        const long long first = issued > p.S ? issued - p.S : 0;
-        for (long long n = first; n < issued; ++n)
-            mbar_wait(&full[(int)(n % p.S)], (uint32_t)((n / p.S) & 1), kDkWaitLimit);
-    }
+    if (warp == 0)
+        for (int st = lane; st < p.S; st += 32) {
+            const int n = m->last_pos[st];
+            if (n >= 0) mbar_wait(&full[st], (uint32_t)((n / p.S) & 1), kDkWaitLimit);
+        }
     __syncthreads();
 }
 

@@ -280,7 +280,6 @@ __host__ __device__ __forceinline__ int gateup_items(const Ctx& c) {
     return max_segments(c) * ceil_div(c.I, kWarps);
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
 template <int NT>
 __device__ __forceinline__ void gateup_rowpair(const uint16_t* grow, const uint16_t* urow, int H,

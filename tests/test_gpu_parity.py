@@ -170,3 +170,37 @@ def test_deterministic_across_calls(cuda_lib):
     yb, ib, _ = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k)
     torch.cuda.synchronize()
     assert torch.equal(ia, ib) and torch.equal(ya, yb)
+
+
+@pytest.mark.parametrize("B,k,E", [(1, 2, 128), (4, 8, 256), (3, 6, 256), (2, 8, 64)])
+def test_persistent_decode_kernel_is_stable_over_repeated_runs(cuda_lib, B, k, E):
+    """The small-batch layer runs in one persistent kernel whose phases hand
+    data over through device-wide barriers; a missing ordering would show up
+    as an occasional wrong token.  Many seeds, compared with the phase-by-phase
+    kernels (each checked against the oracle above)."""
+    H, I = 2048, 768
+    w = synth.Workload("rep", B=B, H=H, I=I, E=E, top_k=k, sigma_router=H ** -0.5)
+    lw = synth.make_layer(w, 0, seed=7, device=DEV)
+    for step in range(40):
+        x = synth.make_x(w, step, seed=7, device=DEV)
+        y0, i0, w0 = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k)
+        y1, i1, w1 = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k,
+                                            flags=cuda_lib.MOE_F_UNFUSED)
+        torch.cuda.synchronize()
+        assert torch.equal(i0, i1), step
+        assert float((w0 - w1).abs().max()) <= 1e-6
+        assert float((y0 - y1).abs().max()) <= 1e-5 * float(y1.abs().max()), step
+
+
+def test_persistent_stack_is_stable_over_repeated_runs(cuda_lib):
+    H, I, E, k, L = 2048, 768, 128, 2, 6
+    w = synth.Workload("rep", B=1, H=H, I=I, E=E, top_k=k, layers=L)
+    layers = [synth.make_layer(w, l, seed=3, device=DEV) for l in range(L)]
+    sw = cuda_lib.StackWeights(layers)
+    for step in range(30):
+        x = synth.make_x(w, step, seed=3, device=DEV)
+        xa, ia = cuda_lib.stack_forward(x, sw, k)
+        xb, ib = cuda_lib.stack_forward(x, sw, k, flags=cuda_lib.MOE_F_UNFUSED)
+        torch.cuda.synchronize()
+        assert torch.equal(ia, ib), step
+        assert float((xa - xb).abs().max()) <= 1e-5 * float(xb.abs().max()), step
