@@ -51,6 +51,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=30,
                     help="layers in the stack (30 = the workload; fewer only for profiling captures)")
+    ap.add_argument("--workload", default="stack", choices=["stack", "uniform", "skewed", "prefill", "tiny"],
+                    help="stack = the 30-layer decode stack (the headline); the others time one layer")
+    ap.add_argument("--batch", type=int, default=None, help="tokens per step for a single-layer workload")
     return ap.parse_args()
 
 
@@ -244,6 +247,75 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------ single layer
+def run_layer_workload(args):
+    """One MoE layer per step (uniform / skewed / prefill-sized / tiny)."""
+    rank, world, local = dist_env()
+    import numpy as np
+    import torch
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from moe_decode_layer_gemv_gb300 import accounting, build, synth
+    build.build()
+    from moe_decode_layer_gemv_gb300 import api
+    base = {"uniform": synth.UNIFORM, "skewed": synth.SKEWED, "prefill": synth.PREFILL,
+            "tiny": synth.TINY}[args.workload]
+    w = base.with_batch(args.batch) if args.batch else base
+    flags = api.MOE_F_UNFUSED if args.mode == "unfused" else 0
+    lw = synth.make_layer(w, 0, seed=args.seed, device=dev)
+    nsteps = args.warmup + args.steps
+    xs = [synth.make_x(w, s, seed=args.seed, device=dev) for s in range(nsteps)]
+    y = torch.empty((w.B, w.H), dtype=torch.float32, device=dev)
+    ids = torch.empty((w.B, w.top_k), dtype=torch.int32, device=dev)
+    rw = torch.empty((w.B, w.top_k), dtype=torch.float32, device=dev)
+    ws = api.new_workspace(w.B, w.H, w.I, w.E, w.top_k, dev)
+    status = api.new_status(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        api.layer_forward(xs[i], lw["w_router"], lw["gate_up"], lw["down"], w.top_k, bias=lw["bias"],
+                          flags=flags, out=y, ids_out=ids, w_out=rw, workspace=ws, status=status,
+                          stream=stream)
+
+    for i in range(args.warmup):
+        flush.zero_()
+        step(i)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    uniq = []
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        for s in range(args.steps):
+            flush.zero_()
+            ev[s][0].record(stream)
+            step(args.warmup + s)
+            ev[s][1].record(stream)
+            uniq.append(ids.clone())
+        torch.cuda.synchronize()
+    st = int(status.item())
+    if st != 0:
+        raise SystemExit(f"device status {st}: {api.status_string(st)}")
+    times_ms = [a.elapsed_time(b) for a, b in ev]
+    mean_ms = statistics.mean(times_ms)
+    us = [len(np.unique(u.cpu().numpy())) for u in uniq]
+    bytes_step = statistics.mean(accounting.layer_bytes(w.H, w.I, w.E, u) for u in us)
+    achieved = bytes_step / (mean_ms / 1e3) / 1e9
+    peak, peak_src = hbm_peak()
+    line = {"metric": METRIC, "value": w.B * args.steps / (sum(times_ms) / 1e3), "unit": "tokens/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "weights_dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "I": w.I, "E": w.E, "top_k": w.top_k,
+                       "mode": args.mode, "l2": "flushed before every timed step"},
+            "unique_experts_mean": statistics.mean(us), "hbm_gbs": achieved,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_src, "traffic": None,
+                         "bytes_per_launch": bytes_step},
+            "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
 # -------------------------------------------------------------------- ours
 def run_ours(args):
     rank, world, local = dist_env()
@@ -410,6 +482,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload != "stack":
+        run_layer_workload(args)
     else:
         run_ours(args)
 

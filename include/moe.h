@@ -81,6 +81,11 @@ typedef enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 } moe_dtype;
                                dedup page; results are identical */
 #define MOE_F_UNFUSED 2u    /* layer/stack: run the phases as separate kernels
                                instead of the persistent fused kernel */
+#define MOE_F_FORCE_TC 4u   /* every expert with any route uses the tensor-core
+                               GEMMs (testing; needs H % 128 == 0, I % 64 == 0) */
+#define MOE_F_NO_TC 8u      /* never use the tensor-core GEMMs */
+#define MOE_TC_MIN_ROUTES 8 /* by default an expert chosen by at least this many
+                               routes runs on the tensor cores */
 
 /*
  * moe_workspace_bytes -- size of the scratch buffer the forward entry points

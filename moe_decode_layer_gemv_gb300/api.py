@@ -62,6 +62,9 @@ MOE_DT_F32 = 0
 MOE_DT_BF16 = 1
 MOE_F_NO_DEDUP = 1
 MOE_F_UNFUSED = 2
+MOE_F_FORCE_TC = 4
+MOE_F_NO_TC = 8
+TC_MIN_ROUTES = 8
 MAX_E, MAX_TOPK, MAX_B, MAX_DIM, MAX_LAYERS = 256, 8, 1024, 16384, 64
 NOALLOC_SCRATCH_BYTES = 16 << 20
 

@@ -12,6 +12,7 @@
 #include "moe_common.cuh"
 #include "moe_phases.cuh"
 #include "moe_decode.cuh"
+#include "moe_tc.cuh"
 
 namespace moe {
 
@@ -147,7 +148,8 @@ __global__ void __launch_bounds__(kThreads) fused_kernel(Ctx c, StackArgs sa, un
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct WsLayout {
-    size_t logits, ids, rw, offsets, route_idx, unique, num_unique, status, bar, acc, acc_end, h, o, total;
+    size_t logits, ids, rw, offsets, route_idx, unique, num_unique, status, bar, acc, acc_end, h, o;
+    size_t x_hi, x_lo, h_hi, h_lo, total;
 };
 
 static WsLayout ws_layout(int B, int H, int I, int E, int k) {
@@ -172,6 +174,10 @@ static WsLayout ws_layout(int B, int H, int I, int E, int k) {
     L.acc_end = L.acc + sizeof(unsigned long long) * 2 * 8 * (size_t)B * E;
     L.h = take(sizeof(float) * R * I);
     L.o = take(sizeof(float) * R * H);
+    L.x_hi = take(sizeof(uint16_t) * R * H);  // tensor-core activation operands (bf16 hi/lo)
+    L.x_lo = take(sizeof(uint16_t) * R * H);
+    L.h_hi = take(sizeof(uint16_t) * R * I);
+    L.h_lo = take(sizeof(uint16_t) * R * I);
     L.total = off;
     return L;
 }
@@ -230,6 +236,8 @@ static int allow_smem(K kernel, size_t bytes) {
     return to_status(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes));
 }
 
+static int tc_threshold_for(unsigned flags, int H, int I);
+
 static Ctx make_ctx(const void* x, int x_dtype, const float* residual, float* y, int B, int H, int I,
                     int E, int k, unsigned flags, char* ws, const WsLayout& L, int32_t* status) {
     Ctx c;
@@ -256,8 +264,10 @@ static Ctx make_ctx(const void* x, int x_dtype, const float* residual, float* y,
         c.h = reinterpret_cast<float*>(ws + L.h);
         c.o = reinterpret_cast<float*>(ws + L.o);
         c.status = status ? status : reinterpret_cast<int32_t*>(ws + L.status);
+        c.tc_threshold = tc_threshold_for(flags, H, I);
     } else {
         c.status = status;
+        c.tc_threshold = 0;  // the tensor-core path needs workspace for its operands
     }
     return c;
 }
@@ -280,25 +290,117 @@ static int launch_group(const int32_t* ids, int B, int k, int E, int32_t* offset
     return launch_check();
 }
 
-static int launch_experts(const Ctx& c, cudaStream_t st) {
+
+// ------------------------------------------------------- tensor-core path
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+// 2-D bf16 tensor [rows, inner] (row-major), 128-byte swizzled boxes of
+// {64, box_rows}; rows beyond the tensor read as zeros.
+static bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {inner * 2};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static bool tc_shape_ok(int H, int I) { return H >= 128 && (H % 128) == 0 && I >= 64 && (I % 64) == 0; }
+
+static int tc_threshold_for(unsigned flags, int H, int I) {
+    if ((flags & MOE_F_NO_TC) || !tc_shape_ok(H, I)) return 0;
+    if (flags & MOE_F_FORCE_TC) return 1;
+    return MOE_TC_MIN_ROUTES;
+}
+
+static int launch_tc(const Ctx& c, char* ws, const WsLayout& L, cudaStream_t st) {
+    int rc = allow_smem(tc_gemm_kernel, kTcSmem);
+    if (rc) return rc;
+    const int R = c.B * c.k;
+    uint16_t* x_hi = reinterpret_cast<uint16_t*>(ws + L.x_hi);
+    uint16_t* x_lo = reinterpret_cast<uint16_t*>(ws + L.x_lo);
+    TcParams tp;
+    memset(&tp, 0, sizeof tp);
+    tp.c = c;
+    tp.threshold = c.tc_threshold;
+    tp.h_hi = reinterpret_cast<uint16_t*>(ws + L.h_hi);
+    tp.h_lo = reinterpret_cast<uint16_t*>(ws + L.h_lo);
+    tp.with_lo = c.x_bf16 ? 0 : 1;
+    tc_split_x_kernel<<<R, kThreads, 0, st>>>(c, x_hi, x_lo);
+    if ((rc = launch_check())) return rc;
+    const int nseg = max_segments(c);
+    const int nchunk = (c.B + kTcMaxN - 1) / kTcMaxN;
+    // gate/up: A = gate_up viewed as [E*2I, H], 64-row boxes
+    if (!encode_bf16_2d(&tp.ta, c.w.gate_up, c.H, (uint64_t)c.E * 2 * c.I, 64) ||
+        !encode_bf16_2d(&tp.tb_hi, x_hi, c.H, R, kTcBoxN) || !encode_bf16_2d(&tp.tb_lo, x_lo, c.H, R, kTcBoxN))
+        return MOE_ERR_UNSUPPORTED;
+    tp.gate = 1;
+    tc_gemm_kernel<<<dim3(nseg, c.I / 64, nchunk), kTcThreads, kTcSmem, st>>>(tp);
+    if ((rc = launch_check())) return rc;
+    return MOE_OK;
+}
+
+static int launch_tc_down(const Ctx& c, char* ws, const WsLayout& L, cudaStream_t st) {
+    const int R = c.B * c.k;
+    TcParams tp;
+    memset(&tp, 0, sizeof tp);
+    tp.c = c;
+    tp.threshold = c.tc_threshold;
+    tp.with_lo = 1;  // h is fp32: always split
+    const uint16_t* h_hi = reinterpret_cast<const uint16_t*>(ws + L.h_hi);
+    const uint16_t* h_lo = reinterpret_cast<const uint16_t*>(ws + L.h_lo);
+    if (!encode_bf16_2d(&tp.ta, c.w.down, c.I, (uint64_t)c.E * c.H, 128) ||
+        !encode_bf16_2d(&tp.tb_hi, h_hi, c.I, R, kTcBoxN) || !encode_bf16_2d(&tp.tb_lo, h_lo, c.I, R, kTcBoxN))
+        return MOE_ERR_UNSUPPORTED;
+    tp.gate = 0;
+    const int nseg = max_segments(c);
+    const int nchunk = (c.B + kTcMaxN - 1) / kTcMaxN;
+    tc_gemm_kernel<<<dim3(nseg, c.H / 128, nchunk), kTcThreads, kTcSmem, st>>>(tp);
+    return launch_check();
+}
+
+static int launch_experts(const Ctx& c, cudaStream_t st, char* ws = nullptr, const WsLayout* L = nullptr) {
     const size_t smem = act_smem(c.H, c.I);
     int rc = allow_smem(gateup_kernel, smem);
     if (rc) return rc;
     if ((rc = allow_smem(down_kernel, smem))) return rc;
+    const bool tc = c.tc_threshold > 0 && ws != nullptr;
+    if (tc && (rc = launch_tc(c, ws, *L, st))) return rc;
     gateup_kernel<<<gateup_items(c), kThreads, smem, st>>>(c);
     if ((rc = launch_check())) return rc;
+    if (tc && (rc = launch_tc_down(c, ws, *L, st))) return rc;
     down_kernel<<<down_items(c), kThreads, smem, st>>>(c);
     if ((rc = launch_check())) return rc;
     combine_kernel<<<combine_items(c), kThreads, 0, st>>>(c);
     return launch_check();
 }
 
-static int launch_unfused_layer(const Ctx& c, cudaStream_t st) {
+static int launch_unfused_layer(const Ctx& c, cudaStream_t st, char* ws, const WsLayout& L) {
     int rc = launch_route(c, st);
     if (rc) return rc;
     rc = launch_group(c.ids, c.B, c.k, c.E, c.offsets, c.route_idx, c.unique, c.num_unique, c.status, st);
     if (rc) return rc;
-    return launch_experts(c, st);
+    return launch_experts(c, st, ws, &L);
 }
 
 static int sm_count() {
@@ -479,7 +581,7 @@ int moe_expert_forward(const void* x, int x_dtype, const uint16_t* gate_up, cons
     int rc = check_dims(B, H, I, E, top_k, true);
     if (rc) return rc;
     if (x_dtype != MOE_DT_F32 && x_dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
-    if (flags & ~(MOE_F_NO_DEDUP | MOE_F_UNFUSED)) return MOE_ERR_INVALID_ARG;
+    if (flags & ~(MOE_F_NO_DEDUP | MOE_F_UNFUSED | MOE_F_FORCE_TC | MOE_F_NO_TC)) return MOE_ERR_INVALID_ARG;
     if (B == 0) return MOE_OK;
     MOE_REQ(x);
     MOE_REQ(gate_up);
@@ -506,7 +608,7 @@ int moe_expert_forward(const void* x, int x_dtype, const uint16_t* gate_up, cons
     c.num_unique = const_cast<int32_t*>(num_unique);
     c.w.gate_up = gate_up;
     c.w.down = down;
-    return launch_experts(c, static_cast<cudaStream_t>(stream));
+    return launch_experts(c, static_cast<cudaStream_t>(stream), static_cast<char*>(workspace), &L);
 }
 
 int moe_layer_forward(const void* x, int x_dtype, const uint16_t* w_router, const float* logit_bias,
@@ -517,7 +619,7 @@ int moe_layer_forward(const void* x, int x_dtype, const uint16_t* w_router, cons
     int rc = check_dims(B, H, I, E, top_k, true);
     if (rc) return rc;
     if (x_dtype != MOE_DT_F32 && x_dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
-    if (flags & ~(MOE_F_NO_DEDUP | MOE_F_UNFUSED)) return MOE_ERR_INVALID_ARG;
+    if (flags & ~(MOE_F_NO_DEDUP | MOE_F_UNFUSED | MOE_F_FORCE_TC | MOE_F_NO_TC)) return MOE_ERR_INVALID_ARG;
     if (B == 0) return MOE_OK;
     MOE_REQ(x);
     MOE_REQ(w_router);
@@ -541,7 +643,7 @@ int moe_layer_forward(const void* x, int x_dtype, const uint16_t* w_router, cons
     if (expert_ids_out) c.ids = expert_ids_out;
     if (route_w_out) c.rw = route_w_out;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (flags & MOE_F_UNFUSED) return launch_unfused_layer(c, st);
+    if (flags & MOE_F_UNFUSED) return launch_unfused_layer(c, st, ws, L);
     {
         DkParams dp;
         memset(&dp, 0, sizeof dp);
@@ -559,6 +661,7 @@ int moe_layer_forward(const void* x, int x_dtype, const uint16_t* w_router, cons
             return launch_decode(dp, dsm, sms, ws, L, st);
         }
     }
+    if (c.tc_threshold > 0) return launch_unfused_layer(c, st, ws, L);  // grouped GEMMs need their own grids
     StackArgs sa;
     memset(&sa, 0, sizeof sa);
     sa.L = 1;
@@ -575,7 +678,7 @@ int moe_stack_forward(int Lc, const uint16_t* const* w_router, const float* cons
     int rc = check_dims(B, H, I, E, top_k, true);
     if (rc) return rc;
     if (Lc < 1 || Lc > MOE_MAX_LAYERS) return MOE_ERR_INVALID_ARG;
-    if (flags & ~(MOE_F_NO_DEDUP | MOE_F_UNFUSED)) return MOE_ERR_INVALID_ARG;
+    if (flags & ~(MOE_F_NO_DEDUP | MOE_F_UNFUSED | MOE_F_FORCE_TC | MOE_F_NO_TC)) return MOE_ERR_INVALID_ARG;
     if (B == 0) return MOE_OK;
     if (!w_router || !gate_up || !down) return MOE_ERR_INVALID_ARG;
     for (int l = 0; l < Lc; ++l) {
@@ -608,7 +711,7 @@ int moe_stack_forward(int Lc, const uint16_t* const* w_router, const float* cons
         for (int l = 0; l < Lc; ++l) {
             c.w = sa.layer[l];
             c.ids = expert_ids_out ? expert_ids_out + (size_t)l * B * top_k : ids_ws;
-            if ((rc = launch_unfused_layer(c, st))) return rc;
+            if ((rc = launch_unfused_layer(c, st, ws, L))) return rc;
         }
         return MOE_OK;
     }
@@ -628,6 +731,15 @@ int moe_stack_forward(int Lc, const uint16_t* const* w_router, const float* cons
             dp.w_out = nullptr;
             return launch_decode(dp, dsm, sms, ws, L, st);
         }
+    }
+    if (c.tc_threshold > 0) {  // grouped GEMMs need their own grids: one sequence per layer
+        int32_t* ids_ws = c.ids;
+        for (int l = 0; l < Lc; ++l) {
+            c.w = sa.layer[l];
+            c.ids = expert_ids_out ? expert_ids_out + (size_t)l * B * top_k : ids_ws;
+            if ((rc = launch_unfused_layer(c, st, ws, L))) return rc;
+        }
+        return MOE_OK;
     }
     return launch_fused(c, sa, reinterpret_cast<unsigned*>(ws + L.bar), st);
 }
@@ -704,7 +816,7 @@ extern "C" int moe_expert_forward_noalloc(const void* x, int x_dtype, const uint
     int rc = check_dims(B, H, I, E, top_k, true);
     if (rc) return rc;
     if (x_dtype != MOE_DT_F32 && x_dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
-    if (flags & ~(MOE_F_NO_DEDUP | MOE_F_UNFUSED)) return MOE_ERR_INVALID_ARG;
+    if (flags & ~(MOE_F_NO_DEDUP | MOE_F_UNFUSED | MOE_F_FORCE_TC | MOE_F_NO_TC)) return MOE_ERR_INVALID_ARG;
     const size_t R = (size_t)B * top_k;
     const size_t h_bytes = align_up(sizeof(float) * R * I, 256);
     if (h_bytes + sizeof(float) * R * H > MOE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;

@@ -71,6 +71,7 @@ struct Ctx {
     int B, H, I, E, k;
     unsigned flags;
     int nt_max;  // tokens staged per pass in the grouped GEMV phases (1, 2, 4 or 8)
+    int tc_threshold;  // segments with at least this many routes go to the tensor-core kernels (0: none)
     // routing (device)
     float* logits;       // [B, E]
     int32_t* ids;        // [B, k]

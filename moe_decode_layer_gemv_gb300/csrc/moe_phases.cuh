@@ -340,6 +340,7 @@ __device__ void gateup_item(const Ctx& c, int item, float* xs, int* tok) {
     const int s = item / nib, ib = item - s * nib;
     Seg sg;
     if (!get_seg(c, s, sg)) return;  // uniform over the CTA
+    if (c.tc_threshold > 0 && sg.p1 - sg.p0 >= c.tc_threshold) return;  // tensor-core path
     const int warp = threadIdx.x >> 5;
     const int i = ib * kWarps + warp;
     const uint16_t* G = c.w.gate_up + (size_t)sg.e * 2 * c.I * c.H;
@@ -435,6 +436,7 @@ __device__ void down_item(const Ctx& c, int item, float* hs, int* rts) {
     const int s = item / nrb, rb = item - s * nrb;
     Seg sg;
     if (!get_seg(c, s, sg)) return;
+    if (c.tc_threshold > 0 && sg.p1 - sg.p0 >= c.tc_threshold) return;  // tensor-core path
     const int warp = threadIdx.x >> 5;
     const int row0 = rb * kDownRows + warp * kDownRowsPerWarp;
     const uint16_t* D = c.w.down + (size_t)sg.e * c.H * c.I;

@@ -1,0 +1,68 @@
+"""The tensor-core (tcgen05) grouped GEMM path against the CPU oracle.
+
+Experts chosen by at least MOE_TC_MIN_ROUTES routes run as grouped GEMMs on
+the tensor cores; MOE_F_FORCE_TC sends every expert there.  Shapes cover
+several M tiles, K steps, token tiles (more than 128 routes on one expert)
+and both activation dtypes.
+"""
+import numpy as np
+import pytest
+import torch
+
+from moe_decode_layer_gemv_gb300 import synth
+from _parity import check_y, layer_weights_np, oracle_layer_following
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _case(B, H, I, E, k, seed, x_bf16=False, skew=False):
+    w = synth.Workload("tc", B=B, H=H, I=I, E=E, top_k=k, sigma_router=H ** -0.5, sigma_expert=0.05,
+                       x_bf16=x_bf16, zipf_bias=skew)
+    lw = {n: (v.to(DEV) if v is not None else None) for n, v in synth.make_layer(w, 0, seed=seed).items()}
+    x = synth.make_x(w, 0, seed=seed).to(DEV)
+    return lw, x
+
+
+@pytest.mark.parametrize("B,H,I,E,k,x_bf16", [
+    (16, 256, 128, 4, 2, False),
+    (40, 512, 192, 6, 3, False),
+    (64, 2048, 768, 8, 4, False),
+    (24, 1024, 256, 5, 2, True),
+    (300, 256, 64, 3, 2, False),   # > 128 routes on one expert: several token tiles
+])
+def test_forced_tensor_core_layer_matches_oracle(cuda_lib, B, H, I, E, k, x_bf16):
+    lw, x = _case(B, H, I, E, k, seed=B + I, x_bf16=x_bf16)
+    st = cuda_lib.new_status()
+    y, ids, w = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k,
+                                       flags=cuda_lib.MOE_F_FORCE_TC, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    y_o, _, _ = oracle_layer_following(x, layer_weights_np(lw), k, ids)
+    rel = check_y(y, y_o)
+    assert rel < 1e-4  # hi/lo split activations keep near-fp32 accuracy
+
+
+def test_mixed_dispatch_skewed_routing(cuda_lib):
+    """Skewed routing: popular experts (>= 8 routes) on the tensor cores, the
+    rest on the CUDA-core GEMV, in one layer."""
+    B, H, I, E, k = 96, 1024, 256, 32, 4
+    lw, x = _case(B, H, I, E, k, seed=4, skew=True)
+    y, ids, w = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k, bias=lw["bias"])
+    torch.cuda.synchronize()
+    counts = np.bincount(ids.cpu().numpy().ravel(), minlength=E)
+    assert counts.max() >= cuda_lib.TC_MIN_ROUTES and (counts[counts > 0] < cuda_lib.TC_MIN_ROUTES).any()
+    y_o, _, _ = oracle_layer_following(x, layer_weights_np(lw), k, ids)
+    check_y(y, y_o)
+
+
+def test_tensor_core_and_gemv_paths_agree(cuda_lib):
+    B, H, I, E, k = 128, 2048, 768, 16, 4
+    lw, x = _case(B, H, I, E, k, seed=9)
+    ya, ia, _ = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k,
+                                       flags=cuda_lib.MOE_F_FORCE_TC)
+    yb, ib, _ = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k,
+                                       flags=cuda_lib.MOE_F_NO_TC)
+    torch.cuda.synchronize()
+    assert torch.equal(ia, ib)
+    assert float((ya - yb).abs().max()) <= 1e-4 * float(yb.abs().max())
