@@ -286,12 +286,14 @@ def run_layer_workload(args):
     uniq = []
     with ClockSampler(local) as clk:
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("timed")
         for s in range(args.steps):
             flush.zero_()
             ev[s][0].record(stream)
             step(args.warmup + s)
             ev[s][1].record(stream)
             uniq.append(ids.clone())
+        torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
     st = int(status.item())
     if st != 0:

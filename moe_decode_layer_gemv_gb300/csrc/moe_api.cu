@@ -101,7 +101,8 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(Ctx c) {
     float* xs;
     int* tok;
     split_smem(c, smem, xs, tok);
-    gateup_item(c, blockIdx.x, xs, tok);
+    const int n = c.seg_list ? ld_act_i(c.seg_count) * ceil_div(c.I, kWarps) : gateup_items(c);
+    for (int it = blockIdx.x; it < n; it += gridDim.x) gateup_item(c, it, xs, tok);
 }
 
 __global__ void __launch_bounds__(kThreads) down_kernel(Ctx c) {
@@ -109,8 +110,11 @@ __global__ void __launch_bounds__(kThreads) down_kernel(Ctx c) {
     float* hs;
     int* rts;
     split_smem(c, smem, hs, rts);
-    down_item(c, blockIdx.x, hs, rts);
+    const int n = c.seg_list ? ld_act_i(c.seg_count) * ceil_div(c.H, kDownRows) : down_items(c);
+    for (int it = blockIdx.x; it < n; it += gridDim.x) down_item(c, it, hs, rts);
 }
+
+__global__ void classify_kernel(Ctx c) { classify_warp(c); }
 
 __global__ void __launch_bounds__(kThreads) combine_kernel(Ctx c) { combine_item(c, blockIdx.x); }
 
@@ -149,7 +153,7 @@ static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct WsLayout {
     size_t logits, ids, rw, offsets, route_idx, unique, num_unique, status, bar, acc, acc_end, h, o;
-    size_t x_hi, x_lo, h_hi, h_lo, total;
+    size_t x_hi, x_lo, h_hi, h_lo, seg_list, seg_count, total;
 };
 
 static WsLayout ws_layout(int B, int H, int I, int E, int k) {
@@ -178,6 +182,8 @@ static WsLayout ws_layout(int B, int H, int I, int E, int k) {
     L.x_lo = take(sizeof(uint16_t) * R * H);
     L.h_hi = take(sizeof(uint16_t) * R * I);
     L.h_lo = take(sizeof(uint16_t) * R * I);
+    L.seg_list = take(sizeof(int32_t) * 2 * (R > (size_t)E ? R : (size_t)E));
+    L.seg_count = take(sizeof(int32_t) * 2);
     L.total = off;
     return L;
 }
@@ -291,6 +297,8 @@ static int launch_group(const int32_t* ids, int B, int k, int E, int32_t* offset
 }
 
 
+static int sm_count();
+
 // ------------------------------------------------------- tensor-core path
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -355,7 +363,10 @@ static int launch_tc(const Ctx& c, char* ws, const WsLayout& L, cudaStream_t st)
         !encode_bf16_2d(&tp.tb_hi, x_hi, c.H, R, kTcBoxN) || !encode_bf16_2d(&tp.tb_lo, x_lo, c.H, R, kTcBoxN))
         return MOE_ERR_UNSUPPORTED;
     tp.gate = 1;
-    tc_gemm_kernel<<<dim3(nseg, c.I / 64, nchunk), kTcThreads, kTcSmem, st>>>(tp);
+    const int grid = sm_count() > 0 ? sm_count() : 1;
+    (void)nseg;
+    (void)nchunk;
+    tc_gemm_kernel<<<grid, kTcThreads, kTcSmem, st>>>(tp);
     if ((rc = launch_check())) return rc;
     return MOE_OK;
 }
@@ -373,23 +384,47 @@ static int launch_tc_down(const Ctx& c, char* ws, const WsLayout& L, cudaStream_
         !encode_bf16_2d(&tp.tb_hi, h_hi, c.I, R, kTcBoxN) || !encode_bf16_2d(&tp.tb_lo, h_lo, c.I, R, kTcBoxN))
         return MOE_ERR_UNSUPPORTED;
     tp.gate = 0;
-    const int nseg = max_segments(c);
-    const int nchunk = (c.B + kTcMaxN - 1) / kTcMaxN;
-    tc_gemm_kernel<<<dim3(nseg, c.H / 128, nchunk), kTcThreads, kTcSmem, st>>>(tp);
+    tc_gemm_kernel<<<sm_count() > 0 ? sm_count() : 1, kTcThreads, kTcSmem, st>>>(tp);
     return launch_check();
 }
 
-static int launch_experts(const Ctx& c, cudaStream_t st, char* ws = nullptr, const WsLayout* L = nullptr) {
+// Resident CTAs of a kernel on the whole GPU (at least 1).
+template <typename K>
+static int resident_grid(K kernel, int threads, size_t smem) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    const int sms = sm_count();
+    return (sms > 0 ? sms : 1) * per_sm;
+}
+
+// The expert pass.  With a workspace the segments are first split on the
+// device into a CUDA-core list and a tensor-core list, and every kernel
+// walks only its own list with a resident grid; without one (the fixed-
+// scratch entry point) the GEMV kernels take every segment.
+static int launch_experts(const Ctx& c0, cudaStream_t st, char* ws = nullptr, const WsLayout* L = nullptr) {
+    Ctx c = c0;
     const size_t smem = act_smem(c.H, c.I);
     int rc = allow_smem(gateup_kernel, smem);
     if (rc) return rc;
     if ((rc = allow_smem(down_kernel, smem))) return rc;
+    int g_items = gateup_items(c), d_items = down_items(c);
+    if (ws) {
+        c.seg_list = reinterpret_cast<int32_t*>(ws + L->seg_list);
+        c.seg_count = reinterpret_cast<int32_t*>(ws + L->seg_count);
+        classify_kernel<<<1, 32, 0, st>>>(c);
+        if ((rc = launch_check())) return rc;
+        const int rg = resident_grid(gateup_kernel, kThreads, smem);
+        const int rd = resident_grid(down_kernel, kThreads, smem);
+        g_items = g_items < rg ? g_items : rg;
+        d_items = d_items < rd ? d_items : rd;
+    }
     const bool tc = c.tc_threshold > 0 && ws != nullptr;
     if (tc && (rc = launch_tc(c, ws, *L, st))) return rc;
-    gateup_kernel<<<gateup_items(c), kThreads, smem, st>>>(c);
+    gateup_kernel<<<g_items, kThreads, smem, st>>>(c);
     if ((rc = launch_check())) return rc;
     if (tc && (rc = launch_tc_down(c, ws, *L, st))) return rc;
-    down_kernel<<<down_items(c), kThreads, smem, st>>>(c);
+    down_kernel<<<d_items, kThreads, smem, st>>>(c);
     if ((rc = launch_check())) return rc;
     combine_kernel<<<combine_items(c), kThreads, 0, st>>>(c);
     return launch_check();

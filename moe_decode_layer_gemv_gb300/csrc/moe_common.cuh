@@ -72,6 +72,12 @@ struct Ctx {
     unsigned flags;
     int nt_max;  // tokens staged per pass in the grouped GEMV phases (1, 2, 4 or 8)
     int tc_threshold;  // segments with at least this many routes go to the tensor-core kernels (0: none)
+    // Work lists built on the device by classify_kernel (nullptr: iterate over
+    // every segment directly): seg_list[0 .. seg_count[0]) are the segments
+    // for the CUDA-core GEMV, seg_list[max_segments .. + seg_count[1]) those
+    // for the tensor-core GEMMs.
+    int32_t* seg_list;
+    int32_t* seg_count;
     // routing (device)
     float* logits;       // [B, E]
     int32_t* ids;        // [B, k]

@@ -265,6 +265,37 @@ __device__ void group_cta(const int32_t* ids, int B, int k, int E, int32_t* offs
     }
 }
 
+// ================================================================ classify
+// Split the segments into the CUDA-core list and the tensor-core list (one
+// warp, order kept): a segment with at least tc_threshold routes goes to the
+// tensor cores.  Writes c.seg_list / c.seg_count.
+__device__ void classify_warp(const Ctx& c) {
+    const int lane = threadIdx.x & 31;
+    const int nseg = no_dedup(c) ? c.B * c.k : ld_act_i(c.num_unique);
+    const int maxseg = max_segments(c);
+    int ng = 0, nt = 0;
+    for (int base = 0; base < nseg; base += 32) {
+        const int s = base + lane;
+        bool valid = false, tc = false;
+        if (s < nseg) {
+            Seg sg;
+            valid = get_seg(c, s, sg);
+            tc = valid && c.tc_threshold > 0 && sg.p1 - sg.p0 >= c.tc_threshold;
+        }
+        const unsigned bt = __ballot_sync(0xffffffffu, tc);
+        const unsigned bg = __ballot_sync(0xffffffffu, valid && !tc);
+        const unsigned below = (1u << lane) - 1u;
+        if (tc) c.seg_list[maxseg + nt + __popc(bt & below)] = s;
+        if (valid && !tc) c.seg_list[ng + __popc(bg & below)] = s;
+        nt += __popc(bt);
+        ng += __popc(bg);
+    }
+    if (lane == 0) {
+        c.seg_count[0] = ng;
+        c.seg_count[1] = nt;
+    }
+}
+
 // ============================================================ gate_up + SiLU
 // For each segment (expert e, its routes) and each gate/up row pair i:
 //   h[p, i] = SiLU(G_e[i,:] . x_t) * (U_e[i,:] . x_t)   for every route p of e.
@@ -337,7 +368,8 @@ __device__ __forceinline__ void gateup_rowpair(const uint16_t* grow, const uint1
 // xs: nt_max * H floats of shared memory; tok: nt_max ints of shared memory.
 __device__ void gateup_item(const Ctx& c, int item, float* xs, int* tok) {
     const int nib = ceil_div(c.I, kWarps);
-    const int s = item / nib, ib = item - s * nib;
+    const int sl = item / nib, ib = item - sl * nib;
+    const int s = c.seg_list ? ld_act_i(c.seg_list + sl) : sl;
     Seg sg;
     if (!get_seg(c, s, sg)) return;  // uniform over the CTA
     if (c.tc_threshold > 0 && sg.p1 - sg.p0 >= c.tc_threshold) return;  // tensor-core path
@@ -433,7 +465,8 @@ __device__ __forceinline__ void down_rows(const uint16_t* D, int row0, int H, in
 // hs: nt_max * I floats of shared memory; rts: nt_max ints of shared memory.
 __device__ void down_item(const Ctx& c, int item, float* hs, int* rts) {
     const int nrb = ceil_div(c.H, kDownRows);
-    const int s = item / nrb, rb = item - s * nrb;
+    const int sl = item / nrb, rb = item - sl * nrb;
+    const int s = c.seg_list ? ld_act_i(c.seg_list + sl) : sl;
     Seg sg;
     if (!get_seg(c, s, sg)) return;
     if (c.tc_threshold > 0 && sg.p1 - sg.p0 >= c.tc_threshold) return;  // tensor-core path

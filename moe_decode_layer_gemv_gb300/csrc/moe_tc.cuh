@@ -157,8 +157,10 @@ __global__ void __launch_bounds__(kThreads) tc_split_x_kernel(Ctx c, uint16_t* x
 }
 
 // ------------------------------------------------------------ the GEMM
-// grid: x = segment, y = M tile (64 pairs of gate/up rows, or 128 down rows),
-// z = 128-token chunk of the segment.
+// Persistent: one CTA per SM walks the items of the tensor-core segment
+// list; an item is (segment, M tile of 64 gate/up row pairs or 128 down rows,
+// 128-token chunk).  The ring position and the accumulator phase carry over
+// from item to item; TMEM and the barriers are set up once.
 __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ __align__(1024) unsigned char tc_smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -171,16 +173,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
 
     const Ctx& c = p.c;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    Seg sg;
-    if (!get_seg(c, blockIdx.x, sg)) return;  // uniform over the CTA
-    if (sg.p1 - sg.p0 < p.threshold) return;
-    const int q0 = sg.p0 + blockIdx.z * kTcMaxN;
-    if (q0 >= sg.p1) return;
-    const int n = min(kTcMaxN, sg.p1 - q0);
-    const int n_pad = (n + kTcBoxN - 1) / kTcBoxN * kTcBoxN;
     const int K = p.gate ? c.H : c.I;
     const int nk = K / kTcBK;
-    const int mt = blockIdx.y;
+    const int mtiles = p.gate ? c.I / 64 : c.H / 128;
+    const int nchunk = (c.B + kTcMaxN - 1) / kTcMaxN;
+    const int maxseg = max_segments(c);
+    const int n_items = ld_act_i(c.seg_count + 1) * mtiles * nchunk;
+    if ((int)blockIdx.x >= n_items) return;  // uniform: nothing for this CTA
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTcStages; ++s) {
@@ -196,104 +195,136 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    float* epi = reinterpret_cast<float*>(smem);  // [128][kTcEpiLd]: stage memory, idle during the epilogue
 
-    if (warp == 0 && lane == 0) {
-        // ---------------- TMA producer
-        const uint32_t bytes = kTcATile + (uint32_t)n_pad * 128u * (p.with_lo ? 2u : 1u);
-        int arow0, arow1 = 0;
-        if (p.gate) {
-            arow0 = sg.e * 2 * c.I + mt * 64;
-            arow1 = arow0 + c.I;
-        } else {
-            arow0 = sg.e * c.H + mt * 128;
-        }
-        for (int kc = 0; kc < nk; ++kc) {
-            const int s = kc % kTcStages;
-            const uint32_t ph = (uint32_t)((kc / kTcStages) & 1);
-            if (kc >= kTcStages && !tc_wait(&empty[s], ph ^ 1u)) {
-                *(volatile int*)ok_flag = 0;
-                break;
-            }
-            unsigned char* st = smem + (size_t)s * kTcStageBytes;
-            mbar_arrive_expect_tx(&full[s], bytes);
+    int g = 0;     // k-steps through the ring so far (same in every thread)
+    int done = 0;  // items finished (accumulator phases)
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+        // the token chunk varies slowest: items of later chunks (which exist
+        // only for segments with more than 128 routes) come after every
+        // first chunk, so no CTA draws only empty items
+        const int per_chunk = n_items / nchunk;
+        const int nc = item / per_chunk;
+        const int rem = item - nc * per_chunk;
+        const int sl = rem / mtiles, mt = rem - sl * mtiles;
+        Seg sg;
+        if (!get_seg(c, ld_act_i(c.seg_list + maxseg + sl), sg)) continue;  // uniform
+        const int q0 = sg.p0 + nc * kTcMaxN;
+        if (q0 >= sg.p1) continue;
+        const int n = min(kTcMaxN, sg.p1 - q0);
+        const int n_pad = (n + kTcBoxN - 1) / kTcBoxN * kTcBoxN;
+
+        if (warp == 0 && lane == 0) {
+            // ---------------- TMA producer
+            const uint32_t bytes = kTcATile + (uint32_t)n_pad * 128u * (p.with_lo ? 2u : 1u);
+            int arow0, arow1 = 0;
             if (p.gate) {
-                tma_load_2d(st, &p.ta, kc * kTcBK, arow0, &full[s]);
-                tma_load_2d(st + 8192, &p.ta, kc * kTcBK, arow1, &full[s]);
+                arow0 = sg.e * 2 * c.I + mt * 64;
+                arow1 = arow0 + c.I;
             } else {
-                tma_load_2d(st, &p.ta, kc * kTcBK, arow0, &full[s]);
+                arow0 = sg.e * c.H + mt * 128;
             }
-            for (int r = 0; r < n_pad; r += kTcBoxN) {
-                tma_load_2d(st + kTcATile + r * 128, &p.tb_hi, kc * kTcBK, q0 + r, &full[s]);
-                if (p.with_lo) tma_load_2d(st + kTcATile + kTcBTile + r * 128, &p.tb_lo, kc * kTcBK, q0 + r, &full[s]);
+            for (int kc = 0; kc < nk; ++kc) {
+                const int gk = g + kc;
+                const int s = gk % kTcStages;
+                const uint32_t ph = (uint32_t)((gk / kTcStages) & 1);
+                if (gk >= kTcStages && !tc_wait(&empty[s], ph ^ 1u)) {
+                    *(volatile int*)ok_flag = 0;
+                    break;
+                }
+                unsigned char* st = smem + (size_t)s * kTcStageBytes;
+                mbar_arrive_expect_tx(&full[s], bytes);
+                if (p.gate) {
+                    tma_load_2d(st, &p.ta, kc * kTcBK, arow0, &full[s]);
+                    tma_load_2d(st + 8192, &p.ta, kc * kTcBK, arow1, &full[s]);
+                } else {
+                    tma_load_2d(st, &p.ta, kc * kTcBK, arow0, &full[s]);
+                }
+                for (int r = 0; r < n_pad; r += kTcBoxN) {
+                    tma_load_2d(st + kTcATile + r * 128, &p.tb_hi, kc * kTcBK, q0 + r, &full[s]);
+                    if (p.with_lo)
+                        tma_load_2d(st + kTcATile + kTcBTile + r * 128, &p.tb_lo, kc * kTcBK, q0 + r, &full[s]);
+                }
             }
-        }
-    } else if (warp == 1 && lane == 0) {
-        // ---------------- MMA issuer (one thread)
-        const uint32_t idesc = umma_idesc_bf16(128, n_pad);
-        bool good = true;
-        for (int kc = 0; kc < nk && good; ++kc) {
-            const int s = kc % kTcStages;
-            const uint32_t ph = (uint32_t)((kc / kTcStages) & 1);
-            if (!tc_wait(&full[s], ph)) {
-                *(volatile int*)ok_flag = 0;
-                good = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t a_addr = smem_u32(smem + (size_t)s * kTcStageBytes);
-            const uint32_t bh_addr = a_addr + kTcATile;
-            const uint32_t bl_addr = bh_addr + kTcBTile;
+        } else if (warp == 1 && lane == 0) {
+            // ---------------- MMA issuer (one thread)
+            const uint32_t idesc = umma_idesc_bf16(128, n_pad);
+            for (int kc = 0; kc < nk; ++kc) {
+                const int gk = g + kc;
+                const int s = gk % kTcStages;
+                const uint32_t ph = (uint32_t)((gk / kTcStages) & 1);
+                if (!tc_wait(&full[s], ph)) {
+                    *(volatile int*)ok_flag = 0;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(smem + (size_t)s * kTcStageBytes);
+                const uint32_t bh_addr = a_addr + kTcATile;
+                const uint32_t bl_addr = bh_addr + kTcBTile;
 #pragma unroll
-            for (int kk = 0; kk < kTcBK / 16; ++kk) {
-                const uint64_t ad = umma_sdesc(a_addr + kk * 32);
-                umma_bf16(tmem, ad, umma_sdesc(bh_addr + kk * 32), idesc, (kc > 0 || kk > 0) ? 1u : 0u);
-                if (p.with_lo) umma_bf16(tmem, ad, umma_sdesc(bl_addr + kk * 32), idesc, 1u);
+                for (int kk = 0; kk < kTcBK / 16; ++kk) {
+                    const uint64_t ad = umma_sdesc(a_addr + kk * 32);
+                    umma_bf16(tmem, ad, umma_sdesc(bh_addr + kk * 32), idesc, (kc > 0 || kk > 0) ? 1u : 0u);
+                    if (p.with_lo) umma_bf16(tmem, ad, umma_sdesc(bl_addr + kk * 32), idesc, 1u);
+                }
+                umma_commit(&empty[s]);  // the stage is free once these MMAs have read it
             }
-            umma_commit(&empty[s]);  // the stage is free once these MMAs have read it
+            umma_commit(accum);  // every MMA issued so far is complete when this arrives
         }
-        umma_commit(accum);  // every MMA issued so far is complete when this arrives
-    }
-    __syncwarp();
+        __syncwarp();
 
-    // ---------------- epilogue (all four warps)
-    const bool acc_ok = tc_wait(accum, 0);
-    tc_fence_after();
-    __syncthreads();
-    const bool good = acc_ok && *(volatile int*)ok_flag;
-    float* epi = reinterpret_cast<float*>(smem);  // [128][kTcEpiLd], the stages are idle now
-    if (good) {
-        const uint32_t row_addr = tmem + ((uint32_t)(warp * 32) << 16);
-        for (int col = 0; col < n_pad; col += 16) {
-            float v[16];
-            tmem_ld16(row_addr + col, v);
+        // ---------------- epilogue (all four warps)
+        if (!tc_wait(accum, (uint32_t)(done & 1))) *(volatile int*)ok_flag = 0;
+        tc_fence_after();
+        __syncthreads();
+        const bool good = *(volatile int*)ok_flag != 0;  // the same in every thread
+        if (good) {
+            const uint32_t row_addr = tmem + ((uint32_t)(warp * 32) << 16);
+            for (int col = 0; col < n_pad; col += 16) {
+                float v[16];
+                tmem_ld16(row_addr + col, v);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) epi[threadIdx.x * kTcEpiLd + col + j] = v[j];
-        }
-    } else if (threadIdx.x == 0) {
-        set_status(c.status, MOE_DEV_TIMEOUT);
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (good) {
-        if (p.gate) {
-            const int i0 = mt * 64;
-            for (int v = threadIdx.x; v < 64 * n; v += kTcThreads) {
-                const int i = v & 63, j = v >> 6;
-                const float hv = silu_mul(epi[i * kTcEpiLd + j], epi[(64 + i) * kTcEpiLd + j]);
-                const uint16_t hi = f2bf_bits(hv);
-                const size_t at = (size_t)(q0 + j) * c.I + i0 + i;
-                p.h_hi[at] = hi;
-                p.h_lo[at] = f2bf_bits(hv - bf_bits2f(hi));
-            }
-        } else {
-            const int r0 = mt * 128;
-            for (int v = threadIdx.x; v < 128 * n; v += kTcThreads) {
-                const int row = v & 127, j = v >> 7;
-                const int r = route_at(c, q0 + j);
-                c.o[(size_t)r * c.H + r0 + row] = epi[row * kTcEpiLd + j];
+                for (int j = 0; j < 16; ++j) epi[threadIdx.x * kTcEpiLd + col + j] = v[j];
             }
         }
+        tc_fence_before();
+        __syncthreads();
+        if (good) {
+            if (p.gate) {
+                const int i0 = mt * 64;
+                for (int v = threadIdx.x; v < 64 * n; v += kTcThreads) {
+                    const int i = v & 63, j = v >> 6;
+                    const float hv = silu_mul(epi[i * kTcEpiLd + j], epi[(64 + i) * kTcEpiLd + j]);
+                    const uint16_t hi = f2bf_bits(hv);
+                    const size_t at = (size_t)(q0 + j) * c.I + i0 + i;
+                    p.h_hi[at] = hi;
+                    p.h_lo[at] = f2bf_bits(hv - bf_bits2f(hi));
+                }
+            } else {
+                const int r0 = mt * 128;
+                for (int v = threadIdx.x; v < 128 * n; v += kTcThreads) {
+                    const int row = v & 127, j = v >> 7;
+                    const int r = route_at(c, q0 + j);
+                    c.o[(size_t)r * c.H + r0 + row] = epi[row * kTcEpiLd + j];
+                }
+            }
+        }
+        // the next item's loads and MMAs reuse the stages and TMEM only after
+        // every thread is done with this item's epilogue
+        __syncthreads();
+        g += nk;
+        ++done;
+        if (!good) {
+            if (threadIdx.x == 0) set_status(c.status, MOE_DEV_TIMEOUT);
+            break;
+        }
     }
+    // leave with no copy in flight: the latest phase of every stage has landed
+    if (warp == 0 && lane == 0)
+        for (int s = 0; s < kTcStages; ++s) {
+            const int last = g - 1 - ((g - 1 - s) % kTcStages + kTcStages) % kTcStages;  // last k-step in stage s
+            if (last >= 0) tc_wait(&full[s], (uint32_t)((last / kTcStages) & 1));
+        }
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
