@@ -153,7 +153,7 @@ static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct WsLayout {
     size_t logits, ids, rw, offsets, route_idx, unique, num_unique, status, bar, acc, acc_end, h, o;
-    size_t x_hi, x_lo, h_hi, h_lo, seg_list, seg_count, total;
+    size_t x_hi, x_lo, h_hi, h_lo, seg_list, seg_count, alog, total;
 };
 
 static WsLayout ws_layout(int B, int H, int I, int E, int k) {
@@ -184,6 +184,7 @@ static WsLayout ws_layout(int B, int H, int I, int E, int k) {
     L.h_lo = take(sizeof(uint16_t) * R * I);
     L.seg_list = take(sizeof(int32_t) * 2 * (R > (size_t)E ? R : (size_t)E));
     L.seg_count = take(sizeof(int32_t) * 2);
+    L.alog = take(sizeof(float) * (size_t)B * E);
     L.total = off;
     return L;
 }
@@ -480,7 +481,7 @@ static bool decode_plan(int B, int H, int I, int E, int k, int sms, DkParams& p,
     if (B < 1 || B > kDkMaxB || R > kDkMaxR || sms < 1 || sms > 1024) return false;
     const int ng = H >> 3;
     const int maxrows = 8 * ((ng + sms - 1) / sms);
-    size_t off = sizeof(uint64_t) * 2 * kDkMaxStages;
+    size_t off = 1024;  // ring barriers (2 x kDkMaxStages) and the two direct-mode barriers
     p.off_misc = (int)off;
     off = align_up(off + sizeof(DkMisc) + sizeof(float) * (size_t)B * ((E + 7) & ~7), 128);
     p.off_x = (int)off;
@@ -516,6 +517,16 @@ static int launch_decode(DkParams& p, size_t smem, int sms, char* ws, const WsLa
         return MOE_ERR_CUDA;
     if (per_sm < 1) return MOE_ERR_UNSUPPORTED;
     p.h = reinterpret_cast<float*>(ws + L.h);
+    p.alog = reinterpret_cast<float*>(ws + L.alog);
+    // next-layer L2 prefetch: single-token decode, top (k + 1) experts while
+    // that stays within 64 MB of weights (a stack only: L > 1)
+    p.prefetch_k = 0;
+    if (p.B == 1 && p.L > 1) {
+        const unsigned long long per_e = 6ull * p.I * p.H;
+        int kp = p.k + 1 < p.E ? p.k + 1 : p.E;
+        while (kp > p.k && per_e * kp > (64ull << 20)) --kp;
+        if (per_e * kp <= (64ull << 20) && kp <= 32) p.prefetch_k = kp;
+    }
     p.acc = reinterpret_cast<unsigned long long*>(ws + L.acc);
     p.bar = reinterpret_cast<unsigned*>(ws + L.bar);
     if ((rc = to_status(cudaMemsetAsync(ws + L.bar, 0, L.acc_end - L.bar, st)))) return rc;

@@ -50,6 +50,8 @@ struct DkParams {
     float* w_out;      // [B, k] (single layer) or nullptr
     float* h;          // [R, I] exchange buffer
     unsigned long long* acc;  // [2][kDkShadows][B][E] fixed-point logits
+    float* alog;              // [B][E] next layer's logits predicted from this layer's input
+    int prefetch_k;           // experts per token to prefetch into L2 for the next layer (0: off)
     unsigned* bar;            // [0] arrival counter, [1] abort word
     int32_t* status;
     int S, stage_bytes, maxrows;
@@ -71,6 +73,7 @@ struct __align__(16) DkMisc {
     int seg_e[kDkMaxR];
     int seg_p[kDkMaxR + 1];
     int last_pos[kDkMaxStages];  // latest ring position armed in each stage (-1: none)
+    int mid_epoch;               // layers whose mid-layer barrier has completed (for the producer warp)
 };
 
 // --------------------------------------------------------- work partition
@@ -362,13 +365,13 @@ __device__ __forceinline__ void warp_sum_n(float (&v)[N]) {
         for (int j = 0; j < N; ++j) v[j] += __shfl_xor_sync(0xffffffffu, v[j], off);
 }
 
-// One gate/up row pair held in a ring stage (gate row, then up row, H bf16
-// each) against NQ tokens' x rows in shared memory.  Four 16-byte vectors
+// One gate/up row pair in shared memory (gate row at grow, up row at urow,
+// H bf16 each) against NQ tokens' x rows in shared memory.  Four 16-byte vectors
 // per lane are loaded before they are used.  Result: g[q], u[q] summed over
 // the warp.
 template <int NQ>
-__device__ __forceinline__ void dk_gate_pair(const unsigned char* st, const float* xs, const int (&tok)[4], int H,
-                                             float (&gu)[2 * NQ]) {
+__device__ __forceinline__ void dk_gate_pair(const unsigned char* grow, const unsigned char* urow, const float* xs,
+                                             const int (&tok)[4], int H, float (&gu)[2 * NQ]) {
     const int lane = threadIdx.x & 31;
     float2 ag[NQ], au[NQ];
 #pragma unroll
@@ -398,14 +401,14 @@ __device__ __forceinline__ void dk_gate_pair(const unsigned char* st, const floa
         uint4 gw[4], uw[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            gw[j] = *reinterpret_cast<const uint4*>(st + 16 * (v + 32 * j));
-            uw[j] = *reinterpret_cast<const uint4*>(st + 2 * H + 16 * (v + 32 * j));
+            gw[j] = *reinterpret_cast<const uint4*>(grow + 16 * (v + 32 * j));
+            uw[j] = *reinterpret_cast<const uint4*>(urow + 16 * (v + 32 * j));
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) step(gw[j], uw[j], v + 32 * j);
     }
     for (; v < nv; v += 32)
-        step(*reinterpret_cast<const uint4*>(st + 16 * v), *reinterpret_cast<const uint4*>(st + 2 * H + 16 * v), v);
+        step(*reinterpret_cast<const uint4*>(grow + 16 * v), *reinterpret_cast<const uint4*>(urow + 16 * v), v);
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
         gu[2 * q] = ag[q].x + ag[q].y;
@@ -465,11 +468,149 @@ __device__ __forceinline__ void dk_down_rows(const unsigned char* st, int nrc, i
     }
 }
 
+// Gate/up pair q of the layer (segment u, row i) from shared-memory rows:
+// h[p, i] = SiLU(g) * u for every route p of the segment.
+__device__ __forceinline__ void dk_pair_compute(const DkMisc* m, const unsigned char* grow, const unsigned char* urow,
+                                                const float* xs, int H, int I, int k, int u, int i, float* h) {
+    const int lane = threadIdx.x & 31;
+    const int p0 = m->seg_p[u], p1 = m->seg_p[u + 1];
+    int tok[kDkMaxB];
+#pragma unroll
+    for (int qq = 0; qq < kDkMaxB; ++qq) tok[qq] = p0 + qq < p1 ? m->rat[p0 + qq] / k : 0;
+    const int nq = p1 - p0;
+    float gu[2 * kDkMaxB];
+    switch (nq) {
+        case 1: { float r[2]; dk_gate_pair<1>(grow, urow, xs, tok, H, r); gu[0] = r[0]; gu[1] = r[1]; } break;
+        case 2: { float r[4]; dk_gate_pair<2>(grow, urow, xs, tok, H, r);
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) gu[j] = r[j]; } break;
+        case 3: { float r[6]; dk_gate_pair<3>(grow, urow, xs, tok, H, r);
+#pragma unroll
+                  for (int j = 0; j < 6; ++j) gu[j] = r[j]; } break;
+        default: dk_gate_pair<4>(grow, urow, xs, tok, H, gu); break;
+    }
+    if (lane < nq) {
+        float g = gu[0], uu = gu[1];
+#pragma unroll
+        for (int qq = 1; qq < kDkMaxB; ++qq)
+            if (lane == qq) {
+                g = gu[2 * qq];
+                uu = gu[2 * qq + 1];
+            }
+        h[(size_t)(p0 + lane) * I + i] = silu_mul(g, uu);
+    }
+}
+
+// Down rows [r0, r1) of segment u from shared memory (row r at base + (r -
+// r0) * 2I) into os (j-th route of the segment at row p0 + j).
+__device__ __forceinline__ void dk_down_compute(const DkMisc* m, const unsigned char* base, int r0, int r1, int I,
+                                                const float* hs, float* os, int maxrows, int h0, int u) {
+    const int p0 = m->seg_p[u], p1 = m->seg_p[u + 1];
+    const float* hrow = hs + (size_t)p0 * I;
+    float* orow = os + (size_t)p0 * maxrows;
+    switch (p1 - p0) {
+        case 1: dk_down_rows<1>(base, r1 - r0, I, hrow, orow, maxrows, r0 - h0); break;
+        case 2: dk_down_rows<2>(base, r1 - r0, I, hrow, orow, maxrows, r0 - h0); break;
+        case 3: dk_down_rows<3>(base, r1 - r0, I, hrow, orow, maxrows, r0 - h0); break;
+        default: dk_down_rows<4>(base, r1 - r0, I, hrow, orow, maxrows, r0 - h0); break;
+    }
+}
+
+// ------------------------------------------------- next-layer L2 prefetch
+// While layer l runs, the next layer's router can already be applied to
+// layer l's input x_l (its true input is x_l + y_l).  The top experts of
+// those predicted logits usually contain the next layer's choice, so their
+// weights are prefetched into L2 during the rest of layer l and the next
+// layer's bulk copies mostly hit L2.  Only a prefetch: the real routing is
+// computed exactly as before and any miss is served from HBM.
+//
+// Predicted logits of this CTA's experts (e = blockIdx.x, + G, ...) for
+// token 0 (one warp).
+__device__ __forceinline__ void dk_predict_logits(const LayerWeights& wn, const float* xs, int H, int E, float* alog) {
+    const int lane = threadIdx.x & 31;
+    for (int e = blockIdx.x; e < E; e += gridDim.x) {
+        const uint16_t* wrow = wn.w_router + (size_t)e * H;
+        float2 a = make_float2(0.f, 0.f);
+        for (int v = lane; v < (H >> 3); v += 32) {
+            const uint4 wv = ld_weight_v4(wrow + 8 * v);
+            const float4 xa = *reinterpret_cast<const float4*>(xs + 8 * v);
+            const float4 xb = *reinterpret_cast<const float4*>(xs + 8 * v + 4);
+            a = ffma2(bf16x2_to_f2(wv.x), make_float2(xa.x, xa.y), a);
+            a = ffma2(bf16x2_to_f2(wv.y), make_float2(xa.z, xa.w), a);
+            a = ffma2(bf16x2_to_f2(wv.z), make_float2(xb.x, xb.y), a);
+            a = ffma2(bf16x2_to_f2(wv.w), make_float2(xb.z, xb.w), a);
+        }
+        const float v = warp_sum(a.x + a.y);
+        if (lane == 0) alog[e] = v + (wn.bias ? wn.bias[e] : 0.f);
+    }
+}
+
+// One warp: top-kp experts of the predicted logits (all CTAs' values, read
+// after the mid-layer barrier), then this CTA's 1/G share of their weight
+// bytes (gate_up block, then down block, expert after expert) prefetched
+// into L2, one bulk prefetch per contiguous piece.
+__device__ __forceinline__ void dk_prefetch_next(const LayerWeights& wn, const float* alog, int H, int I, int E,
+                                                 int kp) {
+    const int lane = threadIdx.x & 31;
+    unsigned key[8];
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+        const int e = lane + 32 * s;
+        key[s] = e < E ? order_key(__ldcg(alog + e)) : 0u;
+    }
+    unsigned taken = 0;
+    int my_e = -1;
+    for (int j = 0; j < kp; ++j) {
+        unsigned kb = 0u;
+        int ib = 0x7fffffff;
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+            if (!((taken >> s) & 1u) && key[s] > kb) {
+                kb = key[s];
+                ib = lane + 32 * s;
+            }
+        const unsigned km = __reduce_max_sync(0xffffffffu, kb);
+        const int win = (int)__reduce_min_sync(0xffffffffu, kb == km ? (unsigned)ib : 0x7fffffffu);
+        if ((win & 31) == lane && win < E) taken |= 1u << (win >> 5);
+        if (lane == j) my_e = win < E ? win : -1;
+    }
+    // bytes of one expert: gate_up 4IH, down 2IH
+    const unsigned long long per_e = 6ull * I * H;
+    const unsigned long long total = per_e * (unsigned long long)kp;
+    const unsigned long long b0 = total * blockIdx.x / gridDim.x, b1 = total * (blockIdx.x + 1) / gridDim.x;
+    // lane j < kp prefetches the part of [b0, b1) that falls in expert j's bytes
+    if (lane < kp && my_e >= 0) {
+        const unsigned long long e0 = per_e * lane, e1 = e0 + per_e;
+        unsigned long long lo = b0 > e0 ? b0 : e0, hi = b1 < e1 ? b1 : e1;
+        lo = (lo + 15) & ~15ull;
+        hi &= ~15ull;
+        const unsigned long long gsz = 4ull * I * H;
+        while (lo < hi) {
+            const unsigned long long off = lo - e0;
+            const char* src;
+            unsigned long long lim;
+            if (off < gsz) {
+                src = reinterpret_cast<const char*>(wn.gate_up + (size_t)my_e * 2 * I * H) + off;
+                lim = gsz - off;
+            } else {
+                src = reinterpret_cast<const char*>(wn.down + (size_t)my_e * H * I) + (off - gsz);
+                lim = per_e - off;
+            }
+            unsigned long long n = hi - lo;
+            if (n > lim) n = lim;
+            if (n > (2ull << 20)) n = 2ull << 20;
+            bulk_prefetch_l2(src, (uint32_t)n);
+            lo += n;
+        }
+    }
+}
+
 // ------------------------------------------------------------ the kernel
 __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + kDkMaxStages;
+    uint64_t* dbar = empty + kDkMaxStages;  // direct mode: [0] gate/up rows landed, [1] down rows landed
     DkMisc* m = reinterpret_cast<DkMisc*>(smem + p.off_misc);
     float* xs = reinterpret_cast<float*>(smem + p.off_x);   // [B][H]
     float* hs = reinterpret_cast<float*>(smem + p.off_h);   // [R][I]
@@ -501,7 +642,10 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
+        mbar_init(&dbar[0], 1);
+        mbar_init(&dbar[1], 1);
         m->abort_flag = 0;
+        m->mid_epoch = 0;
         for (int q = 0; q < kDkMaxStages; ++q) m->last_pos[q] = -1;
         fence_mbar_init();
     }
@@ -513,6 +657,9 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
     int ring_pos = 0;
     int rs = 0;
     uint32_t rph = 0;
+    // Direct mode (a CTA's whole layer share fits in the ring area): phases
+    // armed so far on the two direct-mode barriers (same in every thread)
+    int dg_count = 0, dd_count = 0;
 
 
     if (tid == kDkLeader) dk_trace(p, -1, 0);
@@ -587,8 +734,40 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
         const int U = m->U;
         const DkWork wk = dk_work(wbase, U, I, gN0, gN1, gDen);
         if (tid == kDkLeader) dk_trace(p, l, 1);
+        // Direct mode: when this CTA's gate/up rows and down rows of the layer
+        // fit in the ring area together, they are fetched by a handful of
+        // large bulk copies (rows of one expert are contiguous) onto two
+        // barriers instead of chunk by chunk through the ring.
+        const uint32_t d_gate_bytes = (uint32_t)wk.ng * 4u * (uint32_t)H;
+        const uint32_t d_down_bytes = (uint32_t)U * (uint32_t)nrows * 2u * (uint32_t)I;
+        const bool direct = (size_t)d_gate_bytes + d_down_bytes <= (size_t)p.S * p.stage_bytes &&
+                            d_gate_bytes < (1u << 20) && d_down_bytes < (1u << 20);
+        const bool d_gate = direct && wk.ng > 0, d_down = direct && d_down_bytes > 0;
+        unsigned char* d_g = ring;                                       // [ng][2H] gate rows
+        unsigned char* d_u = ring + (size_t)wk.ng * 2 * H;               // [ng][2H] up rows
+        unsigned char* d_d = ring + (size_t)wk.ng * 4 * H;               // [U][nrows][2I] down rows
 
-        if (warp == 0) {
+        if (warp == 0 && direct) {
+            // ================= producer, direct mode
+            if (lane == 0 && d_gate) {
+                mbar_arrive_expect_tx(&dbar[0], d_gate_bytes);
+                for (int q = wk.ga; q < wk.gb;) {
+                    const int u = q / I, i = q - u * I;
+                    const int qe = min(wk.gb, (u + 1) * I);
+                    const uint16_t* G = lw.gate_up + (size_t)m->seg_e[u] * 2 * I * H;
+                    const uint32_t bytes = (uint32_t)(qe - q) * 2u * H;
+                    bulk_g2s(d_g + (size_t)(q - wk.ga) * 2 * H, G + (size_t)i * H, bytes, &dbar[0]);
+                    bulk_g2s(d_u + (size_t)(q - wk.ga) * 2 * H, G + (size_t)(I + i) * H, bytes, &dbar[0]);
+                    q = qe;
+                }
+            } else if (lane == 1 && d_down) {
+                mbar_arrive_expect_tx(&dbar[1], d_down_bytes);
+                for (int u = 0; u < U; ++u)
+                    bulk_g2s(d_d + (size_t)u * nrows * 2 * I, lw.down + (size_t)m->seg_e[u] * H * I + (size_t)h0 * I,
+                             (uint32_t)nrows * 2u * I, &dbar[1]);
+            }
+            __syncwarp();
+        } else if (warp == 0) {
             // ================= producer: lane s owns ring stage s (S <= 32) and
             // issues that stage's chunks of the layer in order, so the lanes
             // overlap the cost of issuing bulk copies while each stage is still
@@ -635,7 +814,24 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                     if (c == wk.n - 1) dk_trace(p, l, 17);
                 }
             }
-        } else {
+        }
+        if (warp == 0 && p.prefetch_k > 0 && has_next) {
+            // ================= producer warp, once the mid-layer barrier is
+            // through: predicted next-layer experts into L2
+            bool seen = false;
+            for (uint32_t it = 0; it < kDkWaitLimit; ++it) {
+                uint32_t v;
+                asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(&m->mid_epoch)) : "memory");
+                if ((int)v >= l + 1) {
+                    seen = true;
+                    break;
+                }
+                if (*(volatile int*)&m->abort_flag) break;
+                __nanosleep(64);
+            }
+            if (__all_sync(0xffffffffu, seen)) dk_prefetch_next(p.layer[l + 1], p.alog, H, I, E, p.prefetch_k);
+        }
+        if (warp != 0) {
             // ================= consumers: gate/up pairs
             // Chunk c sits in stage (ring_pos + c) % S and is consumed by warp
             // (ring_pos + c) % W; since S % W == 0, every use of a stage goes to
@@ -650,41 +846,31 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
             q0 = (rs + c0) / p.S;
             s = rs + c0 - q0 * p.S;
             ph = rph ^ (uint32_t)(q0 & 1);
-            for (int c = c0; consumes && c < wk.ng; c += p.W) {
+            const bool predicting = p.prefetch_k > 0 && has_next && cw == kDkConsumers - 1;
+            if (predicting) dk_predict_logits(p.layer[l + 1], xs, H, E, p.alog);
+            if (d_gate) {
+                bool landed = false;
+                for (int c = cw; c < wk.ng; c += kDkConsumers) {
+                    if (!landed) {
+                        if (!dk_wait(&dbar[0], (uint32_t)(dg_count & 1), m, p)) break;
+                        landed = true;
+                        if (tid == kDkLeader) dk_trace(p, l, 12);
+                    }
+                    const int q = wk.ga + c;
+                    const int u = q / I, i = q - u * I;
+                    dk_pair_compute(m, d_g + (size_t)c * 2 * H, d_u + (size_t)c * 2 * H, xs, H, I, k, u, i, p.h);
+                }
+            }
+            for (int c = c0; !direct && consumes && c < wk.ng; c += p.W) {
                 if (*(volatile int*)&m->abort_flag) break;
                 if (!dk_wait(&full[s], ph, m, p)) break;
                 if (tid == kDkLeader && c == c0) dk_trace(p, l, 12);
                 const int q = wk.ga + c;
                 const int u = q / I, i = q - u * I;
                 const unsigned char* st = ring + (size_t)s * p.stage_bytes;
-                const int p0 = m->seg_p[u], p1 = m->seg_p[u + 1];
-                int tok[kDkMaxB];
-#pragma unroll
-                for (int qq = 0; qq < kDkMaxB; ++qq) tok[qq] = p0 + qq < p1 ? m->rat[p0 + qq] / k : 0;
-                const int nq = p1 - p0;
-                float gu[2 * kDkMaxB];
-                switch (nq) {
-                    case 1: { float r[2]; dk_gate_pair<1>(st, xs, tok, H, r); gu[0] = r[0]; gu[1] = r[1]; } break;
-                    case 2: { float r[4]; dk_gate_pair<2>(st, xs, tok, H, r);
-#pragma unroll
-                              for (int j = 0; j < 4; ++j) gu[j] = r[j]; } break;
-                    case 3: { float r[6]; dk_gate_pair<3>(st, xs, tok, H, r);
-#pragma unroll
-                              for (int j = 0; j < 6; ++j) gu[j] = r[j]; } break;
-                    default: dk_gate_pair<4>(st, xs, tok, H, gu); break;
-                }
+                dk_pair_compute(m, st, st + 2 * H, xs, H, I, k, u, i, p.h);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
-                if (lane < nq) {
-                    float g = gu[0], uu = gu[1];
-#pragma unroll
-                    for (int qq = 1; qq < kDkMaxB; ++qq)
-                        if (lane == qq) {
-                            g = gu[2 * qq];
-                            uu = gu[2 * qq + 1];
-                        }
-                    p.h[(size_t)(p0 + lane) * I + i] = silu_mul(g, uu);
-                }
                 s += p.W;
                 if (s >= p.S) {
                     s -= p.S;
@@ -700,11 +886,28 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                 reinterpret_cast<float4*>(hs)[v] = ld_act_f4(p.h + 4 * (size_t)v);
             named_sync(1, 32 * kDkConsumers);
             if (tid == kDkLeader) dk_trace(p, l, 3);
+            if (tid == kDkLeader) {  // tell the producer warp that every CTA's predicted logits are visible
+                asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(&m->mid_epoch)), "r"(l + 1)
+                             : "memory");
+            }
+            if (d_down) {
+                const int ng4 = (nrows + 3) >> 2;
+                bool landed = false;
+                for (int j = cw; j < U * ng4; j += kDkConsumers) {
+                    if (!landed) {
+                        if (!dk_wait(&dbar[1], (uint32_t)(dd_count & 1), m, p)) break;
+                        landed = true;
+                    }
+                    const int u = j / ng4, rg = j - u * ng4;
+                    const int r0 = h0 + 4 * rg, r1 = min(h1, r0 + 4);
+                    dk_down_compute(m, d_d + ((size_t)u * nrows + 4 * rg) * 2 * I, r0, r1, I, hs, os, p.maxrows, h0, u);
+                }
+            }
             c0 = wk.ng + ((cw - (rs + wk.ng) % p.W) % p.W + p.W) % p.W;
             q0 = (rs + c0) / p.S;
             s = rs + c0 - q0 * p.S;
             ph = rph ^ (uint32_t)(q0 & 1);
-            for (int c = c0; consumes && c < wk.n; c += p.W) {
+            for (int c = c0; !direct && consumes && c < wk.n; c += p.W) {
                 if (*(volatile int*)&m->abort_flag) break;
                 if (!dk_wait(&full[s], ph, m, p)) break;
 
@@ -713,15 +916,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                 const int r0 = wk.h0 + sub * wk.nr;
                 const int r1 = min(wk.h1, r0 + wk.nr);
                 const unsigned char* st = ring + (size_t)s * p.stage_bytes;
-                const int p0 = m->seg_p[u], p1 = m->seg_p[u + 1];
-                const float* hrow = hs + (size_t)p0 * I;
-                float* orow = os + (size_t)p0 * p.maxrows;
-                switch (p1 - p0) {
-                    case 1: dk_down_rows<1>(st, r1 - r0, I, hrow, orow, p.maxrows, r0 - h0); break;
-                    case 2: dk_down_rows<2>(st, r1 - r0, I, hrow, orow, p.maxrows, r0 - h0); break;
-                    case 3: dk_down_rows<3>(st, r1 - r0, I, hrow, orow, p.maxrows, r0 - h0); break;
-                    default: dk_down_rows<4>(st, r1 - r0, I, hrow, orow, p.maxrows, r0 - h0); break;
-                }
+                dk_down_compute(m, st, r0, r1, I, hs, os, p.maxrows, h0, u);
                 __syncwarp();
                 if (c == c0 && cw == 0 && lane == 0) dk_trace(p, l, 13);
                 if (lane == 0) mbar_arrive(&empty[s]);
@@ -763,12 +958,14 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
             }  // ok
             if (has_next) cp_async_wait_all();
         }
-        ring_pos += wk.n;
-        {
+        if (!direct) {
+            ring_pos += wk.n;
             const int t = rs + wk.n, q = t / p.S;
             rs = t - q * p.S;
             rph ^= (uint32_t)(q & 1);
         }
+        dg_count += d_gate ? 1 : 0;
+        dd_count += d_down ? 1 : 0;
         if (tid == kDkLeader) dk_trace(p, l, 5);
         __syncthreads();
         // every thread reads the same flag: nobody writes it between the two
@@ -782,11 +979,14 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
     // phase armed in each stage is the only one that can still be in flight
     // (they have all landed already unless a wait gave up)
     __syncthreads();
-    if (warp == 0)
+    if (warp == 0) {
         for (int st = lane; st < p.S; st += 32) {
             const int n = m->last_pos[st];
             if (n >= 0) mbar_wait(&full[st], (uint32_t)((n / p.S) & 1), kDkWaitLimit);
         }
+        if (lane == 0 && dg_count > 0) mbar_wait(&dbar[0], (uint32_t)((dg_count - 1) & 1), kDkWaitLimit);
+        if (lane == 1 && dd_count > 0) mbar_wait(&dbar[1], (uint32_t)((dd_count - 1) & 1), kDkWaitLimit);
+    }
     __syncthreads();
 }
 
