@@ -64,6 +64,20 @@ def dist_env():
     return rank, world, local
 
 
+def job_throughput(local_ms, units_per_rank, pg=None, device="cpu"):
+    """Whole-job throughput of N replicas: every rank processed
+    `units_per_rank` units in `local_ms`; the job took the slowest rank's
+    time.  Returns (max-over-ranks ms, units of all ranks per second)."""
+    import torch
+    world = 1
+    if pg is not None:
+        world = pg.get_world_size()
+        t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        local_ms = float(t.item())
+    return local_ms, units_per_rank * world / (local_ms / 1000.0)
+
+
 def hbm_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -161,15 +175,16 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ oracle
 def oracle_stack_sample(layers_cpu_fn, x0_list, k, seconds, n_layers=30):
-    """Run the CPU oracle on whole tokens through the stack until `seconds`
-    of oracle time accumulate (at least one token).  layers_cpu_fn(l, ids)
+    """Run the CPU oracle on whole tokens through the stack (cycling through
+    x0_list) until `seconds` of oracle time accumulate (at least one token).  layers_cpu_fn(l, ids)
     returns the layer's weights as the oracle takes them (host arrays),
     fetching only the experts in ids.  Returns (tokens, oracle_seconds)."""
     import numpy as np
     import oracle
     done, spent = 0, 0.0
-    for x0 in x0_list:
-        x = np.array(x0, dtype=np.float32, copy=True)
+    # cycle through the given tokens until the time is spent
+    for i in range(100000):
+        x = np.array(x0_list[i % len(x0_list)], dtype=np.float32, copy=True)
         for l in range(n_layers):
             wr, bias = layers_cpu_fn(l, None)
             t0 = time.perf_counter()
@@ -385,13 +400,7 @@ def run_ours(args):
     st = int(status.item())
     if st != 0:
         raise SystemExit(f"device status {st}: {api.status_string(st)}")
-    total_ms = sum(times_ms)
-    if pg:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
-    tokens = w.B * args.steps * world
-    value = tokens / (total_ms / 1000.0)
+    total_ms, value = job_throughput(sum(times_ms), w.B * args.steps, pg, dev)
     # algorithmic bytes: per layer the router + each unique selected expert once
     bytes_steps = []
     for u in uniq:
@@ -444,7 +453,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_src,
                      "traffic": recorded_traffic("moe_stack_fused", w.name),
-                     "kernel": "fused_kernel (one launch = 30 layers)",
+                     "kernel": "decode_kernel (one launch = 30 layers)",
                      "bytes_per_launch": bytes_per_launch},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,

@@ -225,6 +225,19 @@ int moe_stack_forward(int L, const uint16_t* const* w_router, const float* const
  */
 int moe_set_trace_buffer(unsigned long long* trace, int words);
 
+/*
+ * moe_inject_barrier_stall -- fault injection for the failure path.  While
+ * extra_arrivals > 0, every device-wide barrier of the persistent kernels
+ * (moe_layer_forward / moe_stack_forward without MOE_F_UNFUSED) waits for
+ * that many arrivals beyond the grid, which never come: the first barrier's
+ * bounded wait runs out (about a second), the CTA sets MOE_DEV_TIMEOUT in
+ * dev_status and the abort word, every CTA leaves the kernel after its own
+ * copies in flight have landed, and the launch completes with the context
+ * still usable.  0 (the default) turns it off.  Returns MOE_ERR_INVALID_ARG
+ * outside [0, 1024].  Host-only setting, not thread-safe.
+ */
+int moe_inject_barrier_stall(int extra_arrivals);
+
 /* moe_status_string -- static text for a moe_status code or MOE_DEV_* bit. */
 const char* moe_status_string(int code);
 

@@ -39,6 +39,8 @@ _lib.moe_layer_forward.argtypes = [_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _
 _lib.moe_stack_forward.argtypes = [_I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _U, _P, _S, _P, _P]
 _lib.moe_set_trace_buffer.argtypes = [_P, _I]
 _lib.moe_set_trace_buffer.restype = ctypes.c_int
+_lib.moe_inject_barrier_stall.argtypes = [_I]
+_lib.moe_inject_barrier_stall.restype = ctypes.c_int
 _lib.moe_status_string.argtypes = [_I]
 _lib.moe_status_string.restype = ctypes.c_char_p
 for _f in ("moe_workspace_bytes", "moe_route", "moe_group_by_expert", "moe_expert_forward",
@@ -47,7 +49,7 @@ for _f in ("moe_workspace_bytes", "moe_route", "moe_group_by_expert", "moe_exper
 
 EXPORTED = ("moe_workspace_bytes", "moe_route", "moe_group_by_expert", "moe_expert_forward",
             "moe_expert_forward_noalloc", "moe_layer_forward", "moe_stack_forward", "moe_set_trace_buffer",
-            "moe_status_string")
+            "moe_inject_barrier_stall", "moe_status_string")
 
 MOE_OK = 0
 MOE_ERR_INVALID_ARG = -1
@@ -116,6 +118,13 @@ def set_trace_buffer(buf):
     else:
         _need(buf, torch.int64, "trace buffer")
         _check(_lib.moe_set_trace_buffer(_ptr(buf), buf.numel()), "moe_set_trace_buffer")
+
+
+def inject_barrier_stall(extra_arrivals: int):
+    """Fault injection: while > 0 the persistent kernels' device-wide
+    barriers wait for arrivals that never come, time out (about a second),
+    set MOE_DEV_TIMEOUT in the status word and return; 0 turns it off."""
+    _check(_lib.moe_inject_barrier_stall(int(extra_arrivals)), "moe_inject_barrier_stall")
 
 
 def workspace_bytes(B, H, I, E, top_k) -> int:

@@ -34,12 +34,12 @@ __device__ __forceinline__ void red_release_add_u32(unsigned* p, unsigned v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-__device__ bool grid_sync(unsigned* bar, unsigned& epoch, int32_t* status) {
+__device__ bool grid_sync(unsigned* bar, unsigned& epoch, int32_t* status, unsigned extra) {
     __shared__ int s_ok;
     __syncthreads();
     if (threadIdx.x == 0) {
         epoch += 1;
-        const unsigned target = epoch * gridDim.x;
+        const unsigned target = epoch * (gridDim.x + extra);
         __threadfence();
         red_release_add_u32(bar, 1u);
         int ok = 1;
@@ -70,6 +70,7 @@ struct StackArgs {
     LayerWeights layer[MOE_MAX_LAYERS];
     int L;
     int32_t* ids_out;  // [L, B, k] or nullptr
+    unsigned bar_extra;  // arrivals a barrier waits for beyond the grid (0; > 0 only to test the timeout)
 };
 
 __global__ void __launch_bounds__(kThreads) router_kernel(Ctx c) {
@@ -132,19 +133,19 @@ __global__ void __launch_bounds__(kThreads) fused_kernel(Ctx c, StackArgs sa, un
         c.ids = sa.ids_out ? sa.ids_out + (size_t)l * c.B * c.k : ids_base;
         for (int it = blockIdx.x; it < router_items(c); it += gridDim.x)
             router_item(c, it, reinterpret_cast<float*>(smem));
-        if (!grid_sync(bar, epoch, c.status)) return;
+        if (!grid_sync(bar, epoch, c.status, sa.bar_extra)) return;
         for (int it = blockIdx.x; it < topk_items(c); it += gridDim.x) topk_item(c, it, c.ids, c.rw);
-        if (!grid_sync(bar, epoch, c.status)) return;
+        if (!grid_sync(bar, epoch, c.status, sa.bar_extra)) return;
         if (blockIdx.x == 0)
             group_cta(c.ids, c.B, c.k, c.E, c.offsets, c.route_idx, c.unique, c.num_unique, c.status,
                       reinterpret_cast<uint32_t*>(smem));
-        if (!grid_sync(bar, epoch, c.status)) return;
+        if (!grid_sync(bar, epoch, c.status, sa.bar_extra)) return;
         for (int it = blockIdx.x; it < gateup_items(c); it += gridDim.x) gateup_item(c, it, act, idx);
-        if (!grid_sync(bar, epoch, c.status)) return;
+        if (!grid_sync(bar, epoch, c.status, sa.bar_extra)) return;
         for (int it = blockIdx.x; it < down_items(c); it += gridDim.x) down_item(c, it, act, idx);
-        if (!grid_sync(bar, epoch, c.status)) return;
+        if (!grid_sync(bar, epoch, c.status, sa.bar_extra)) return;
         for (int it = blockIdx.x; it < combine_items(c); it += gridDim.x) combine_item(c, it);
-        if (l + 1 < sa.L && !grid_sync(bar, epoch, c.status)) return;
+        if (l + 1 < sa.L && !grid_sync(bar, epoch, c.status, sa.bar_extra)) return;
     }
 }
 
@@ -546,6 +547,7 @@ static int launch_decode(DkParams& p, size_t smem, int sms, char* ws, const WsLa
 
 static unsigned long long* g_trace = nullptr;
 static int g_trace_words = 0;
+static unsigned g_bar_extra = 0;  // moe_inject_barrier_stall
 
 static void decode_common(DkParams& p, int B, int H, int I, int E, int k, int L, unsigned flags,
                           int32_t* status) {
@@ -559,6 +561,7 @@ static void decode_common(DkParams& p, int B, int H, int I, int E, int k, int L,
     p.L = L;
     p.flags = flags;
     p.status = status;
+    p.bar_extra = g_bar_extra;
 }
 
 }  // namespace moe
@@ -711,6 +714,7 @@ int moe_layer_forward(const void* x, int x_dtype, const uint16_t* w_router, cons
     StackArgs sa;
     memset(&sa, 0, sizeof sa);
     sa.L = 1;
+    sa.bar_extra = g_bar_extra;
     sa.layer[0] = c.w;
     sa.ids_out = nullptr;
     return launch_fused(c, sa, reinterpret_cast<unsigned*>(ws + L.bar), st);
@@ -744,6 +748,7 @@ int moe_stack_forward(int Lc, const uint16_t* const* w_router, const float* cons
     StackArgs sa;
     memset(&sa, 0, sizeof sa);
     sa.L = Lc;
+    sa.bar_extra = g_bar_extra;
     sa.ids_out = expert_ids_out;
     for (int l = 0; l < Lc; ++l) {
         sa.layer[l].w_router = w_router[l];
@@ -788,6 +793,12 @@ int moe_stack_forward(int Lc, const uint16_t* const* w_router, const float* cons
         return MOE_OK;
     }
     return launch_fused(c, sa, reinterpret_cast<unsigned*>(ws + L.bar), st);
+}
+
+int moe_inject_barrier_stall(int extra_arrivals) {
+    if (extra_arrivals < 0 || extra_arrivals > 1024) return MOE_ERR_INVALID_ARG;
+    g_bar_extra = (unsigned)extra_arrivals;
+    return MOE_OK;
 }
 
 int moe_set_trace_buffer(unsigned long long* trace, int words) {

@@ -53,6 +53,7 @@ struct DkParams {
     float* alog;              // [B][E] next layer's logits predicted from this layer's input
     int prefetch_k;           // experts per token to prefetch into L2 for the next layer (0: off)
     unsigned* bar;            // [0] arrival counter, [1] abort word
+    unsigned bar_extra;       // arrivals a barrier waits for beyond the grid (0; > 0 only to test the timeout)
     int32_t* status;
     int S, stage_bytes, maxrows;
     int W;  // consumer warps that take chunks: stage s always goes to warp s % W (S % W == 0)
@@ -161,7 +162,7 @@ __device__ __forceinline__ bool dk_grid_sync(const DkParams& p, unsigned& epoch,
     named_sync(bar_id, nthreads);
     if (threadIdx.x == kDkLeader) {
         epoch += 1;
-        const unsigned target = epoch * gridDim.x;
+        const unsigned target = epoch * (gridDim.x + p.bar_extra);
         int ok = 1;
         const unsigned old = atom_add_release_gpu(p.bar, 1u);
         if (old + 1u < target) {

@@ -69,6 +69,13 @@ def test_bad_arguments_are_rejected_before_any_launch(lib):
                                  None, None) == -1
 
 
+def test_injection_hook_range_checked(lib):
+    lib.moe_inject_barrier_stall.argtypes = [ctypes.c_int]
+    assert lib.moe_inject_barrier_stall(-1) == -1
+    assert lib.moe_inject_barrier_stall(1025) == -1
+    assert lib.moe_inject_barrier_stall(0) == 0
+
+
 def test_status_strings(lib):
     lib.moe_status_string.restype = ctypes.c_char_p
     assert b"invalid" in lib.moe_status_string(-1)
