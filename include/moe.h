@@ -215,7 +215,8 @@ int moe_stack_forward(int L, const uint16_t* const* w_router, const float* const
  * layer l (-1 = the initial router step), G = grid size, event ev:
  * 0 layer start, 1 routing done, 2 gate/up done, 3 after the mid-layer
  * barrier, 4 down done, 5 layer work done, 6 after the end-of-layer barrier,
- * 7 logits and x loaded, 8 top-k done, 9 grouping done, 10 combine done,
+ * 7 top-k done (router warp), 8 x staged (consumers), 9 grouping done
+ * (router warp), 10 combine done,
  * 11 next router slice ready, 12 first gate/up chunk landed (leader warp),
  * 13 first down chunk landed (leader warp), 16 last gate/up chunk landed,
  * 17 last chunk landed, 18 producer issued every chunk, 19 first chunk

@@ -484,7 +484,7 @@ static bool decode_plan(int B, int H, int I, int E, int k, int sms, DkParams& p,
     const int maxrows = 8 * ((ng + sms - 1) / sms);
     size_t off = 1024;  // ring barriers (2 x kDkMaxStages) and the two direct-mode barriers
     p.off_misc = (int)off;
-    off = align_up(off + sizeof(DkMisc) + sizeof(float) * (size_t)B * ((E + 7) & ~7), 128);
+    off = align_up(off + sizeof(DkMisc), 128);
     p.off_x = (int)off;
     off = align_up(off + sizeof(float) * (size_t)B * H, 128);
     p.off_h = (int)off;
@@ -519,13 +519,14 @@ static int launch_decode(DkParams& p, size_t smem, int sms, char* ws, const WsLa
     if (per_sm < 1) return MOE_ERR_UNSUPPORTED;
     p.h = reinterpret_cast<float*>(ws + L.h);
     p.alog = reinterpret_cast<float*>(ws + L.alog);
-    // next-layer L2 prefetch: single-token decode, top (k + 1) experts while
-    // that stays within 64 MB of weights (a stack only: L > 1)
+    // next-layer L2 prefetch: single-token decode, the top k experts of the
+    // predicted logits while that stays within 64 MB of weights (a stack
+    // only: L > 1).  (Measured on the 30-layer stack: top k beats top k+1,
+    // whose extra expert costs more HBM time than its hits save.)
     p.prefetch_k = 0;
     if (p.B == 1 && p.L > 1) {
         const unsigned long long per_e = 6ull * p.I * p.H;
-        int kp = p.k + 1 < p.E ? p.k + 1 : p.E;
-        while (kp > p.k && per_e * kp > (64ull << 20)) --kp;
+        const int kp = p.k;
         if (per_e * kp <= (64ull << 20) && kp <= 32) p.prefetch_k = kp;
     }
     p.acc = reinterpret_cast<unsigned long long*>(ws + L.acc);

@@ -75,6 +75,8 @@ struct __align__(16) DkMisc {
     int seg_p[kDkMaxR + 1];
     int last_pos[kDkMaxStages];  // latest ring position armed in each stage (-1: none)
     int mid_epoch;               // layers whose mid-layer barrier has completed (for the producer warp)
+    int ga_tab[kDkMaxR + 1];     // this CTA's gate/up pair range [ga_tab[U], gb_tab[U]) for U segments
+    int gb_tab[kDkMaxR + 1];
 };
 
 // --------------------------------------------------------- work partition
@@ -86,44 +88,30 @@ __device__ __forceinline__ void dk_rows(int c, int G, int H, int& h0, int& h1) {
     h1 = 8 * (int)((long long)(c + 1) * ng / G);
 }
 
-// First gate/up row pair of CTA c (pairs are numbered segment-major).  The
-// split balances each CTA's total bytes: its gate/up pairs (4H bytes each)
-// plus its down rows of every selected expert (2I bytes per row and expert):
-//   start(c) = floor(U * N_c / D),  N_c = 6HI*c - 2I*G*h0(c),  D = 4HG,
-// with start(0) = 0 and start(G) = P = U*I (integer arithmetic only: this
-// GPU's FP64 rate is low).  N_c does not depend on the routing, so it is
-// computed once per launch; every CTA evaluates the same expression for the
-// same c, so neighbouring ranges agree, and the ranges
-// [start(c), max(start(c), start(c+1))) cover every pair even where start()
-// is not monotonic (tiny H).
-__device__ __forceinline__ long long dk_gate_num(int c, int G, int H, int I) {
-    const long long h0 = 8LL * ((long long)c * (H >> 3) / G);
-    return 6LL * H * I * c - 2LL * I * G * h0;
-}
-
-__device__ __forceinline__ int dk_gate_start(int c, int G, int U, int I, long long num, long long den) {
-    const int P = U * I;
-    if (c <= 0) return 0;
-    if (c >= G) return P;
-    if (num <= 0) return 0;
-    const long long v = (long long)U * num / den;
-    return v > P ? P : (int)v;
-}
-
 struct DkWork {
     int ga, gb;  // gate/up pairs [ga, gb)
     int h0, h1, nr, nd_per_u, ng, n;
 };
 
-// rows, down-chunk size and down chunks per expert are fixed per launch
-// (template `base`); only the gate/up range depends on the routing.
-__device__ __forceinline__ DkWork dk_work(const DkWork& base, int U, int I, long long n0, long long n1,
-                                          long long den) {
+// Rows, down-chunk size and down chunks per expert are fixed per launch
+// (template `base`); only the gate/up range depends on the routing, through
+// the number of segments U, so it is tabulated for every U at the start.
+// The U*I gate/up row pairs (numbered segment-major) are split into equal
+// counts: CTA c takes [floor(c*U*I/G), floor((c+1)*U*I/G)).  (The down rows
+// are split evenly too, in 8-row groups.  Equal pair counts beat an equal
+// split of each CTA's total bytes, gate/up plus down: the gate/up pass ends
+// at a device-wide barrier, so its slowest CTA sets the pace, while the
+// down rows land during that pass anyway.)
+__device__ __forceinline__ void dk_work_range(int U, int I, int& ga, int& gb) {
+    const long long G = gridDim.x, c = blockIdx.x, P = (long long)U * I;
+    ga = (int)(c * P / G);
+    gb = (int)((c + 1) * P / G);
+}
+
+__device__ __forceinline__ DkWork dk_work(const DkWork& base, int U, const DkMisc* m) {
     DkWork w = base;
-    const int G = gridDim.x, c = blockIdx.x;
-    w.ga = dk_gate_start(c, G, U, I, n0, den);
-    const int nb = dk_gate_start(c + 1, G, U, I, n1, den);
-    w.gb = nb > w.ga ? nb : w.ga;
+    w.ga = m->ga_tab[U];
+    w.gb = m->gb_tab[U];
     w.ng = w.gb - w.ga;
     w.n = w.ng + U * w.nd_per_u;
     return w;
@@ -241,16 +229,38 @@ __device__ __forceinline__ float key_value(unsigned k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-__device__ void dk_topk_warp(const float* lg, int E, int k, int t, DkMisc* m, int32_t* status) {
+// Routing of token t by one warp, straight from the fixed-point shadow
+// accumulators of its logits: lane L holds experts L + 32 s (s < 8); every
+// load of a batch of four slots is issued before the first sum (the shadows
+// add up exactly, in any order), then the top-k and the weights.
+__device__ __forceinline__ void dk_route_warp(const unsigned long long* acc, const float* bias, int B, int E, int k,
+                                              int t, DkMisc* m, int32_t* status) {
     const int lane = threadIdx.x & 31;
     unsigned key[8];
     bool bad = false;
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-        const int e = lane + 32 * s;
-        const float v = e < E ? lg[e] : 0.f;
-        if (e < E && !isfinite(v)) bad = true;
-        key[s] = e < E ? order_key(v) : 0u;  // 0 is below every real key
+    for (int s0 = 0; s0 < 8; s0 += 4) {
+        unsigned long long sum[4] = {0ull, 0ull, 0ull, 0ull};
+        if (32 * s0 < E) {
+#pragma unroll
+            for (int sh = 0; sh < kDkShadows; ++sh)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int e = lane + 32 * (s0 + j);
+                    if (e < E) sum[j] += __ldcg(acc + ((size_t)sh * B + t) * E + e);
+                }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int e = lane + 32 * (s0 + j);
+            float v = 0.f;
+            if (e < E) {
+                v = fix_to_float(sum[j]);
+                if (bias) v += __ldg(bias + e);
+                if (!isfinite(v)) bad = true;
+            }
+            key[s0 + j] = e < E ? order_key(v) : 0u;  // 0 is below every real key
+        }
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(status, MOE_DEV_NONFINITE);
     unsigned taken = 0;
@@ -284,6 +294,7 @@ __device__ void dk_topk_warp(const float* lg, int E, int k, int t, DkMisc* m, in
         m->selv[t * k + lane] = my_l;
         m->w[t * k + lane] = ex / den;
     }
+    __syncwarp();
 }
 
 // Router partial sums of this CTA's hidden rows [h0, h0+nrows) for every
@@ -546,12 +557,10 @@ __device__ __forceinline__ void dk_predict_logits(const LayerWeights& wn, const 
     }
 }
 
-// One warp: top-kp experts of the predicted logits (all CTAs' values, read
-// after the mid-layer barrier), then this CTA's 1/G share of their weight
-// bytes (gate_up block, then down block, expert after expert) prefetched
-// into L2, one bulk prefetch per contiguous piece.
-__device__ __forceinline__ void dk_prefetch_next(const LayerWeights& wn, const float* alog, int H, int I, int E,
-                                                 int kp) {
+// One warp: the top-kp experts of the predicted logits (all CTAs' values,
+// read after the mid-layer barrier); lane j < kp returns the j-th best
+// (-1 elsewhere).
+__device__ __forceinline__ int dk_predict_top(const float* alog, int E, int kp) {
     const int lane = threadIdx.x & 31;
     unsigned key[8];
 #pragma unroll
@@ -575,17 +584,23 @@ __device__ __forceinline__ void dk_prefetch_next(const LayerWeights& wn, const f
         if ((win & 31) == lane && win < E) taken |= 1u << (win >> 5);
         if (lane == j) my_e = win < E ? win : -1;
     }
-    // bytes of one expert: gate_up 4IH, down 2IH
-    const unsigned long long per_e = 6ull * I * H;
+    return my_e;
+}
+
+// This CTA's 1/G share of the predicted experts' weight bytes prefetched
+// into L2, one bulk prefetch per contiguous piece: lane j < kp covers expert
+// j (my_e), its gate_up block then its down block.
+__device__ __forceinline__ void dk_prefetch_l2(const LayerWeights& wn, int my_e, int H, int I, int kp) {
+    const int lane = threadIdx.x & 31;
+    const unsigned long long gsz = 4ull * I * H;  // gate_up bytes of one expert; down: 2IH
+    const unsigned long long per_e = gsz + 2ull * I * H;
     const unsigned long long total = per_e * (unsigned long long)kp;
     const unsigned long long b0 = total * blockIdx.x / gridDim.x, b1 = total * (blockIdx.x + 1) / gridDim.x;
-    // lane j < kp prefetches the part of [b0, b1) that falls in expert j's bytes
     if (lane < kp && my_e >= 0) {
         const unsigned long long e0 = per_e * lane, e1 = e0 + per_e;
         unsigned long long lo = b0 > e0 ? b0 : e0, hi = b1 < e1 ? b1 : e1;
         lo = (lo + 15) & ~15ull;
         hi &= ~15ull;
-        const unsigned long long gsz = 4ull * I * H;
         while (lo < hi) {
             const unsigned long long off = lo - e0;
             const char* src;
@@ -606,6 +621,23 @@ __device__ __forceinline__ void dk_prefetch_next(const LayerWeights& wn, const f
     }
 }
 
+// Gate/up rows [ga, gb) of the pair list (segment u = q / I, row i = q - u*I,
+// expert seg_e[u]) by bulk copies onto `bar` (armed by the caller with
+// (gb - ga) * 4H bytes): per run of one segment, the gate rows to
+// dg + (q - ga)*2H and the up rows to du + (q - ga)*2H.
+__device__ __forceinline__ void dk_gate_runs(const uint16_t* gate_up, const int* seg_e, int ga, int gb, int H, int I,
+                                             unsigned char* dg, unsigned char* du, uint64_t* bar) {
+    for (int q = ga; q < gb;) {
+        const int u = q / I, i = q - u * I;
+        const int qe = min(gb, (u + 1) * I);
+        const uint32_t bytes = (uint32_t)(qe - q) * 2u * H;
+        const uint16_t* G = gate_up + (size_t)seg_e[u] * 2 * I * H;
+        bulk_g2s(dg + (size_t)(q - ga) * 2 * H, G + (size_t)i * H, bytes, bar);
+        bulk_g2s(du + (size_t)(q - ga) * 2 * H, G + (size_t)(I + i) * H, bytes, bar);
+        q = qe;
+    }
+}
+
 // ------------------------------------------------------------ the kernel
 __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -618,8 +650,6 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
     float* os = reinterpret_cast<float*>(smem + p.off_o);   // [R][maxrows]
     uint16_t* wrs = reinterpret_cast<uint16_t*>(smem + p.off_wr);  // [E][maxrows]
     unsigned char* ring = smem + p.off_ring;
-    float* lg = reinterpret_cast<float*>(smem + p.off_misc + sizeof(DkMisc));  // [B][Ep]
-    const int Ep = (p.E + 7) & ~7;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = p.B, H = p.H, I = p.I, E = p.E, k = p.k, R = B * k;
@@ -627,9 +657,6 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
     int h0, h1;
     dk_rows(blockIdx.x, gridDim.x, H, h0, h1);
     const int nrows = h1 - h0;
-    const long long gN0 = dk_gate_num(blockIdx.x, gridDim.x, H, I);
-    const long long gN1 = dk_gate_num(blockIdx.x + 1, gridDim.x, H, I);
-    const long long gDen = 4LL * H * gridDim.x;
     DkWork wbase;
     wbase.h0 = h0;
     wbase.h1 = h1;
@@ -649,6 +676,10 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
         m->mid_epoch = 0;
         for (int q = 0; q < kDkMaxStages; ++q) m->last_pos[q] = -1;
         fence_mbar_init();
+    }
+    if (tid >= 32 && tid <= 32 + kDkMaxR) {  // gate/up pair range for U = 0 .. kDkMaxR segments
+        const int U = tid - 32;
+        dk_work_range(U, I, m->ga_tab[U], m->gb_tab[U]);
     }
     __syncthreads();
 
@@ -690,50 +721,60 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
         const bool has_next = l + 1 < p.L;
         unsigned long long* acc_now = p.acc + (size_t)(l & 1) * kDkShadows * B * E;
         unsigned long long* acc_next = p.acc + (size_t)((l + 1) & 1) * kDkShadows * B * E;
-        // ---- A0: logits, x, next router slice
+        // ---- A0: the router warps (token t: warp t) route straight from the
+        // logit accumulators while the consumers stage x and the next router
+        // slice; the producer warp then groups, hands the routing over (named
+        // barrier 4: it arrives, the consumers wait) and goes on to issue the
+        // copies at once
         if (tid == kDkLeader) dk_trace(p, l, 0);
-        for (int v = tid; v < B * Ep; v += blockDim.x) {
-            const int t = v / Ep, e = v - t * Ep;
-            float val = -INFINITY;
-            if (e < E) {
-                unsigned long long sum = 0ull;  // integer sum: exact in any order
-#pragma unroll
-                for (int sh = 0; sh < kDkShadows; ++sh) sum += __ldcg(acc_now + ((size_t)sh * B + t) * E + e);
-                val = fix_to_float(sum);
-                if (lw.bias) val += lw.bias[e];
+        if (warp < B) {
+            dk_route_warp(acc_now, lw.bias, B, E, k, warp, m, p.status);
+            if (tid == 0) dk_trace(p, l, 7);
+            if (B > 1) {  // warp 0 groups every token's selection
+                if (warp == 0)
+                    named_sync(3, 32 * B);
+                else
+                    named_arrive(3, 32 * B);
             }
-            lg[v] = val;
         }
-        if (l > 0 || !p.x_bf16) {
-            const float* xsrc = (l > 0) ? p.y : static_cast<const float*>(p.x_in);
-            for (int v = tid; v < (B * H) >> 2; v += blockDim.x)
-                reinterpret_cast<float4*>(xs)[v] = ld_act_f4(xsrc + 4 * (size_t)v);
+        if (warp == 0) {
+            dk_group(m, R, E, no_dedup);
+            if (blockIdx.x == 0) {
+                if (p.ids_out && lane < R) p.ids_out[(size_t)l * R + lane] = m->ids[lane];
+                if (p.w_out && lane < R) p.w_out[lane] = m->w[lane];
+            }
+            if (tid == 0) dk_trace(p, l, 9);
+            named_arrive(4, kDkThreads);
         } else {
-            const uint16_t* xb = static_cast<const uint16_t*>(p.x_in);
-            for (int v = tid; v < B * H; v += blockDim.x) xs[v] = __uint_as_float((uint32_t)xb[v] << 16);
-        }
-        if (has_next && tid >= 32) {
-            const LayerWeights& wn = p.layer[l + 1];
-            for (int v = tid - 32; v < E * (nrows >> 3); v += 32 * kDkConsumers) {
-                const int e = v / (nrows >> 3), c8 = (v - e * (nrows >> 3)) << 3;
-                cp_async16(wrs + e * p.maxrows + c8, wn.w_router + (size_t)e * H + h0 + c8);
+            const int ct = tid - 32, nct = 32 * kDkConsumers;
+            if (l > 0 || !p.x_bf16) {
+                // both loads of a thread in flight before either store
+                const float* xsrc = (l > 0) ? p.y : static_cast<const float*>(p.x_in);
+                const int nv4 = (B * H) >> 2;
+                for (int v0 = ct; v0 < nv4; v0 += 2 * nct) {
+                    const int v1 = v0 + nct;
+                    const float4 a = ld_act_f4(xsrc + 4 * (size_t)v0);
+                    const float4 b = v1 < nv4 ? ld_act_f4(xsrc + 4 * (size_t)v1) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    reinterpret_cast<float4*>(xs)[v0] = a;
+                    if (v1 < nv4) reinterpret_cast<float4*>(xs)[v1] = b;
+                }
+            } else {
+                const uint16_t* xb = static_cast<const uint16_t*>(p.x_in);
+                for (int v = ct; v < B * H; v += nct) xs[v] = __uint_as_float((uint32_t)xb[v] << 16);
             }
-            cp_async_commit();
-        }
-        __syncthreads();
-        if (tid == kDkLeader) dk_trace(p, l, 7);
-        if (warp < B) dk_topk_warp(lg + warp * Ep, E, k, warp, m, p.status);
-        __syncthreads();
-        if (tid == kDkLeader) dk_trace(p, l, 8);
-        if (warp == 0) dk_group(m, R, E, no_dedup);
-        __syncthreads();
-        if (tid == kDkLeader) dk_trace(p, l, 9);
-        if (blockIdx.x == 0) {
-            if (p.ids_out && tid < R) p.ids_out[(size_t)l * R + tid] = m->ids[tid];
-            if (p.w_out && tid < R) p.w_out[tid] = m->w[tid];
+            if (has_next) {
+                const LayerWeights& wn = p.layer[l + 1];
+                for (int v = ct; v < E * (nrows >> 3); v += nct) {
+                    const int e = v / (nrows >> 3), c8 = (v - e * (nrows >> 3)) << 3;
+                    cp_async16(wrs + e * p.maxrows + c8, wn.w_router + (size_t)e * H + h0 + c8);
+                }
+                cp_async_commit();
+            }
+            if (tid == kDkLeader) dk_trace(p, l, 8);
+            named_sync(4, kDkThreads);
         }
         const int U = m->U;
-        const DkWork wk = dk_work(wbase, U, I, gN0, gN1, gDen);
+        const DkWork wk = dk_work(wbase, U, m);
         if (tid == kDkLeader) dk_trace(p, l, 1);
         // Direct mode: when this CTA's gate/up rows and down rows of the layer
         // fit in the ring area together, they are fetched by a handful of
@@ -752,15 +793,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
             // ================= producer, direct mode
             if (lane == 0 && d_gate) {
                 mbar_arrive_expect_tx(&dbar[0], d_gate_bytes);
-                for (int q = wk.ga; q < wk.gb;) {
-                    const int u = q / I, i = q - u * I;
-                    const int qe = min(wk.gb, (u + 1) * I);
-                    const uint16_t* G = lw.gate_up + (size_t)m->seg_e[u] * 2 * I * H;
-                    const uint32_t bytes = (uint32_t)(qe - q) * 2u * H;
-                    bulk_g2s(d_g + (size_t)(q - wk.ga) * 2 * H, G + (size_t)i * H, bytes, &dbar[0]);
-                    bulk_g2s(d_u + (size_t)(q - wk.ga) * 2 * H, G + (size_t)(I + i) * H, bytes, &dbar[0]);
-                    q = qe;
-                }
+                dk_gate_runs(lw.gate_up, m->seg_e, wk.ga, wk.gb, H, I, d_g, d_u, &dbar[0]);
             } else if (lane == 1 && d_down) {
                 mbar_arrive_expect_tx(&dbar[1], d_down_bytes);
                 for (int u = 0; u < U; ++u)
@@ -818,7 +851,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
         }
         if (warp == 0 && p.prefetch_k > 0 && has_next) {
             // ================= producer warp, once the mid-layer barrier is
-            // through: predicted next-layer experts into L2
+            // through: the next layer's predicted experts prefetched into L2
             bool seen = false;
             for (uint32_t it = 0; it < kDkWaitLimit; ++it) {
                 uint32_t v;
@@ -830,7 +863,10 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                 if (*(volatile int*)&m->abort_flag) break;
                 __nanosleep(64);
             }
-            if (__all_sync(0xffffffffu, seen)) dk_prefetch_next(p.layer[l + 1], p.alog, H, I, E, p.prefetch_k);
+            if (__all_sync(0xffffffffu, seen)) {
+                const int my_e = dk_predict_top(p.alog, E, p.prefetch_k);
+                dk_prefetch_l2(p.layer[l + 1], my_e, H, I, p.prefetch_k);
+            }
         }
         if (warp != 0) {
             // ================= consumers: gate/up pairs

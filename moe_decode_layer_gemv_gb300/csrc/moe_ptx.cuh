@@ -98,6 +98,12 @@ __device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Arrive at named barrier `id` without waiting (the producer side of a
+// hand-off: the consumers wait with named_sync on the same id and count).
+__device__ __forceinline__ void named_arrive(uint32_t id, uint32_t nthreads) {
+    asm volatile("barrier.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // --------------------------------------------------- gpu-scope atomics
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
     unsigned v;

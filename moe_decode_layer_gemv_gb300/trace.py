@@ -40,25 +40,41 @@ def trace_stack(api, x, stack, top_k, sms=None, flags=0):
         d = lambda a, b: (ev[:, b] - ev[:, a]).tolist()
         row = {}
         for name, a, b in (("route", 0, 1), ("gate", 1, 2), ("mid", 2, 3), ("down", 3, 4),
-                           ("tail", 4, 5), ("end", 5, 6), ("load", 0, 7), ("topk", 7, 8), ("group", 8, 9),
-                           ("plan", 9, 1), ("combine", 4, 10), ("cpwait", 10, 11), ("partial", 11, 5),
+                           ("tail", 4, 5), ("end", 5, 6), ("topk", 0, 7), ("xload", 0, 8), ("group", 7, 9),
+                           ("handoff", 9, 1), ("combine", 4, 10), ("cpwait", 10, 11), ("partial", 11, 5),
                            ("gate1st", 1, 12), ("issued", 1, 18), ("land0", 1, 19), ("gate_land", 1, 16), ("all_land", 1, 17)):
             v = d(a, b)
             row[name] = (statistics.median(v), max(v))
         row["wall"] = float(ev[:, 6].max() - ev[:, 0].min()) if l < L else float(ev[:, 5].max() - ev[:, 0].min())
         c = cyc[l]
         row["route_cycles"] = statistics.median((c[:, 1] - c[:, 0]).tolist())
+        # SM-clock intervals (same SM, any warps): exact where globaltimer is coarse
+        for name, a, b in (("cy_land", 1, 16), ("cy_after_land", 16, 2), ("cy_lead_wait", 1, 12),
+                           ("cy_lead_compute", 12, 2), ("cy_mid", 2, 3), ("cy_down", 3, 4),
+                           ("cy_combine", 4, 10), ("cy_partial", 11, 5), ("cy_end", 5, 6), ("cy_topk", 0, 7),
+                           ("cy_group", 7, 9), ("cy_xload", 0, 8), ("cy_route", 0, 1)):
+            v = (c[:, b] - c[:, a]).tolist()
+            row[name] = (statistics.median(v), max(v))
         out.append(row)
     init = t[0]
     return {"layers": out, "init_wall": float(init[:, 1].max() - init[:, 0].min())}
 
 
 def format_detail(res) -> str:
-    names = ("load", "topk", "plan", "partial", "issued", "land0", "gate_land", "all_land")
+    names = ("topk", "xload", "group", "handoff", "combine", "partial", "issued", "gate_land", "all_land")
     lines = ["layer  " + "  ".join(f"{n:>11s}" for n in names) + "  route_cycles"]
     for l, r in enumerate(res["layers"]):
         lines.append(f"{l:5d}  " + "  ".join(f"{r[n][0]:5.2f}/{r[n][1]:5.2f}" for n in names)
                      + f"  {r['route_cycles']:.0f}")
+    return "\n".join(lines)
+
+
+def format_cycles(res) -> str:
+    names = ("cy_topk", "cy_group", "cy_xload", "cy_route", "cy_land", "cy_after_land", "cy_lead_wait", "cy_lead_compute", "cy_mid", "cy_down",
+             "cy_combine", "cy_partial", "cy_end")
+    lines = ["layer " + " ".join(f"{n[3:]:>15s}" for n in names) + "   (SM cycles, median/max)"]
+    for l, r in enumerate(res["layers"]):
+        lines.append(f"{l:5d} " + " ".join(f"{r[n][0]:7.0f}/{r[n][1]:7.0f}" for n in names))
     return "\n".join(lines)
 
 
