@@ -487,6 +487,8 @@ static bool decode_plan(int B, int H, int I, int E, int k, int sms, DkParams& p,
     off = align_up(off + sizeof(DkMisc), 128);
     p.off_x = (int)off;
     off = align_up(off + sizeof(float) * (size_t)B * H, 128);
+    p.off_xq = (int)off;
+    off = align_up(off + sizeof(float) * (size_t)B * dk_hq(H), 128);
     p.off_h = (int)off;
     off = align_up(off + sizeof(float) * (size_t)R * I, 128);
     p.off_o = (int)off;

@@ -59,7 +59,7 @@ struct DkParams {
     int W;  // consumer warps that take chunks: stage s always goes to warp s % W (S % W == 0)
     unsigned long long* trace;  // optional phase timestamps (see dk_trace), or nullptr
     int trace_words;
-    int off_misc, off_x, off_h, off_o, off_wr, off_ring;
+    int off_misc, off_x, off_xq, off_h, off_o, off_wr, off_ring;
 };
 
 struct __align__(16) DkMisc {
@@ -377,18 +377,38 @@ __device__ __forceinline__ void warp_sum_n(float (&v)[N]) {
         for (int j = 0; j < N; ++j) v[j] += __shfl_xor_sync(0xffffffffu, v[j], off);
 }
 
+// x rows are also kept "lane-blocked" in shared memory (xq, token stride
+// dk_hq(H)): the 8 values of column group g = 32*b + L (columns 8g..8g+7)
+// sit at 256*b + 4*L (first four) and 256*b + 128 + 4*L (last four), so the
+// 16-byte loads of a warp walking the groups g = 32*b + lane cover 512
+// contiguous bytes -- one shared-memory wavefront per 128 bytes, where the
+// natural layout (32-byte lane stride) needs two.
+__host__ __device__ __forceinline__ int dk_hq(int H) { return (H + 255) & ~255; }
+
+__device__ __forceinline__ int dk_xq_index(int c) {  // column c (a multiple of 4) -> its float4 in xq
+    const int g = c >> 3;
+    return ((g >> 5) << 8) + ((c >> 2) & 1) * 128 + ((g & 31) << 2);
+}
+
+// Four x values at flat index f = t*H + c (c a multiple of 4) into both copies.
+__device__ __forceinline__ void dk_store_x(float* xs, float* xq, int H, int f, float4 v) {
+    *reinterpret_cast<float4*>(xs + f) = v;
+    const int t = f / H, c = f - t * H;
+    *reinterpret_cast<float4*>(xq + (size_t)t * dk_hq(H) + dk_xq_index(c)) = v;
+}
+
 // One gate/up row pair in shared memory (gate row at grow, up row at urow,
-// H bf16 each) against NQ tokens' x rows in shared memory.  Four 16-byte vectors
-// per lane are loaded before they are used.  Result: g[q], u[q] summed over
-// the warp.
+// H bf16 each) against NQ tokens' x rows (lane-blocked copy xq).  Four
+// 16-byte vectors per lane are loaded before they are used.  Result: g[q],
+// u[q] summed over the warp.
 template <int NQ>
-__device__ __forceinline__ void dk_gate_pair(const unsigned char* grow, const unsigned char* urow, const float* xs,
+__device__ __forceinline__ void dk_gate_pair(const unsigned char* grow, const unsigned char* urow, const float* xq,
                                              const int (&tok)[4], int H, float (&gu)[2 * NQ]) {
     const int lane = threadIdx.x & 31;
     float2 ag[NQ], au[NQ];
 #pragma unroll
     for (int q = 0; q < NQ; ++q) ag[q] = au[q] = make_float2(0.f, 0.f);
-    const int nv = H >> 3;
+    const int nv = H >> 3, hq = dk_hq(H);
     auto step = [&](const uint4& gw, const uint4& uw, int v) {
         const float2 g0 = bf16x2_to_f2(gw.x), g1 = bf16x2_to_f2(gw.y);
         const float2 g2 = bf16x2_to_f2(gw.z), g3 = bf16x2_to_f2(gw.w);
@@ -396,8 +416,9 @@ __device__ __forceinline__ void dk_gate_pair(const unsigned char* grow, const un
         const float2 u2 = bf16x2_to_f2(uw.z), u3 = bf16x2_to_f2(uw.w);
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
-            const float4* xp = reinterpret_cast<const float4*>(xs + (size_t)tok[q] * H + 8 * v);
-            const float4 xa = xp[0], xb = xp[1];
+            const float* xp = xq + (size_t)tok[q] * hq + ((v >> 5) << 8) + ((v & 31) << 2);
+            const float4 xa = *reinterpret_cast<const float4*>(xp);
+            const float4 xb = *reinterpret_cast<const float4*>(xp + 128);
             ag[q] = ffma2(g0, make_float2(xa.x, xa.y), ag[q]);
             au[q] = ffma2(u0, make_float2(xa.x, xa.y), au[q]);
             ag[q] = ffma2(g1, make_float2(xa.z, xa.w), ag[q]);
@@ -483,7 +504,7 @@ __device__ __forceinline__ void dk_down_rows(const unsigned char* st, int nrc, i
 // Gate/up pair q of the layer (segment u, row i) from shared-memory rows:
 // h[p, i] = SiLU(g) * u for every route p of the segment.
 __device__ __forceinline__ void dk_pair_compute(const DkMisc* m, const unsigned char* grow, const unsigned char* urow,
-                                                const float* xs, int H, int I, int k, int u, int i, float* h) {
+                                                const float* xq, int H, int I, int k, int u, int i, float* h) {
     const int lane = threadIdx.x & 31;
     const int p0 = m->seg_p[u], p1 = m->seg_p[u + 1];
     int tok[kDkMaxB];
@@ -492,14 +513,14 @@ __device__ __forceinline__ void dk_pair_compute(const DkMisc* m, const unsigned 
     const int nq = p1 - p0;
     float gu[2 * kDkMaxB];
     switch (nq) {
-        case 1: { float r[2]; dk_gate_pair<1>(grow, urow, xs, tok, H, r); gu[0] = r[0]; gu[1] = r[1]; } break;
-        case 2: { float r[4]; dk_gate_pair<2>(grow, urow, xs, tok, H, r);
+        case 1: { float r[2]; dk_gate_pair<1>(grow, urow, xq, tok, H, r); gu[0] = r[0]; gu[1] = r[1]; } break;
+        case 2: { float r[4]; dk_gate_pair<2>(grow, urow, xq, tok, H, r);
 #pragma unroll
                   for (int j = 0; j < 4; ++j) gu[j] = r[j]; } break;
-        case 3: { float r[6]; dk_gate_pair<3>(grow, urow, xs, tok, H, r);
+        case 3: { float r[6]; dk_gate_pair<3>(grow, urow, xq, tok, H, r);
 #pragma unroll
                   for (int j = 0; j < 6; ++j) gu[j] = r[j]; } break;
-        default: dk_gate_pair<4>(grow, urow, xs, tok, H, gu); break;
+        default: dk_gate_pair<4>(grow, urow, xq, tok, H, gu); break;
     }
     if (lane < nq) {
         float g = gu[0], uu = gu[1];
@@ -538,15 +559,16 @@ __device__ __forceinline__ void dk_down_compute(const DkMisc* m, const unsigned 
 //
 // Predicted logits of this CTA's experts (e = blockIdx.x, + G, ...) for
 // token 0 (one warp).
-__device__ __forceinline__ void dk_predict_logits(const LayerWeights& wn, const float* xs, int H, int E, float* alog) {
+__device__ __forceinline__ void dk_predict_logits(const LayerWeights& wn, const float* xq, int H, int E, float* alog) {
     const int lane = threadIdx.x & 31;
     for (int e = blockIdx.x; e < E; e += gridDim.x) {
         const uint16_t* wrow = wn.w_router + (size_t)e * H;
         float2 a = make_float2(0.f, 0.f);
         for (int v = lane; v < (H >> 3); v += 32) {
             const uint4 wv = ld_weight_v4(wrow + 8 * v);
-            const float4 xa = *reinterpret_cast<const float4*>(xs + 8 * v);
-            const float4 xb = *reinterpret_cast<const float4*>(xs + 8 * v + 4);
+            const float* xp = xq + ((v >> 5) << 8) + ((v & 31) << 2);
+            const float4 xa = *reinterpret_cast<const float4*>(xp);
+            const float4 xb = *reinterpret_cast<const float4*>(xp + 128);
             a = ffma2(bf16x2_to_f2(wv.x), make_float2(xa.x, xa.y), a);
             a = ffma2(bf16x2_to_f2(wv.y), make_float2(xa.z, xa.w), a);
             a = ffma2(bf16x2_to_f2(wv.z), make_float2(xb.x, xb.y), a);
@@ -646,6 +668,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
     uint64_t* dbar = empty + kDkMaxStages;  // direct mode: [0] gate/up rows landed, [1] down rows landed
     DkMisc* m = reinterpret_cast<DkMisc*>(smem + p.off_misc);
     float* xs = reinterpret_cast<float*>(smem + p.off_x);   // [B][H]
+    float* xq = reinterpret_cast<float*>(smem + p.off_xq);  // [B][dk_hq(H)] lane-blocked copy of xs
     float* hs = reinterpret_cast<float*>(smem + p.off_h);   // [R][I]
     float* os = reinterpret_cast<float*>(smem + p.off_o);   // [R][maxrows]
     uint16_t* wrs = reinterpret_cast<uint16_t*>(smem + p.off_wr);  // [E][maxrows]
@@ -755,12 +778,16 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                     const int v1 = v0 + nct;
                     const float4 a = ld_act_f4(xsrc + 4 * (size_t)v0);
                     const float4 b = v1 < nv4 ? ld_act_f4(xsrc + 4 * (size_t)v1) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    reinterpret_cast<float4*>(xs)[v0] = a;
-                    if (v1 < nv4) reinterpret_cast<float4*>(xs)[v1] = b;
+                    dk_store_x(xs, xq, H, 4 * v0, a);
+                    if (v1 < nv4) dk_store_x(xs, xq, H, 4 * v1, b);
                 }
             } else {
                 const uint16_t* xb = static_cast<const uint16_t*>(p.x_in);
-                for (int v = ct; v < B * H; v += nct) xs[v] = __uint_as_float((uint32_t)xb[v] << 16);
+                for (int v = ct; v < (B * H) >> 2; v += nct) {
+                    const uint2 w = *reinterpret_cast<const uint2*>(xb + 4 * (size_t)v);
+                    const float2 lo = bf16x2_to_f2(w.x), hi = bf16x2_to_f2(w.y);
+                    dk_store_x(xs, xq, H, 4 * v, make_float4(lo.x, lo.y, hi.x, hi.y));
+                }
             }
             if (has_next) {
                 const LayerWeights& wn = p.layer[l + 1];
@@ -794,7 +821,12 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
             if (lane == 0 && d_gate) {
                 mbar_arrive_expect_tx(&dbar[0], d_gate_bytes);
                 dk_gate_runs(lw.gate_up, m->seg_e, wk.ga, wk.gb, H, I, d_g, d_u, &dbar[0]);
-            } else if (lane == 1 && d_down) {
+            }
+            __syncwarp();
+            if (lane == 1 && d_down) {
+                // the gate/up rows first: the down rows are needed only after
+                // the mid-layer barrier, so they do not share the bandwidth
+                if (d_gate) dk_wait(&dbar[0], (uint32_t)(dg_count & 1), m, p);
                 mbar_arrive_expect_tx(&dbar[1], d_down_bytes);
                 for (int u = 0; u < U; ++u)
                     bulk_g2s(d_d + (size_t)u * nrows * 2 * I, lw.down + (size_t)m->seg_e[u] * H * I + (size_t)h0 * I,
@@ -884,7 +916,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
             s = rs + c0 - q0 * p.S;
             ph = rph ^ (uint32_t)(q0 & 1);
             const bool predicting = p.prefetch_k > 0 && has_next && cw == kDkConsumers - 1;
-            if (predicting) dk_predict_logits(p.layer[l + 1], xs, H, E, p.alog);
+            if (predicting) dk_predict_logits(p.layer[l + 1], xq, H, E, p.alog);
             if (d_gate) {
                 bool landed = false;
                 for (int c = cw; c < wk.ng; c += kDkConsumers) {
@@ -895,7 +927,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                     }
                     const int q = wk.ga + c;
                     const int u = q / I, i = q - u * I;
-                    dk_pair_compute(m, d_g + (size_t)c * 2 * H, d_u + (size_t)c * 2 * H, xs, H, I, k, u, i, p.h);
+                    dk_pair_compute(m, d_g + (size_t)c * 2 * H, d_u + (size_t)c * 2 * H, xq, H, I, k, u, i, p.h);
                 }
             }
             for (int c = c0; !direct && consumes && c < wk.ng; c += p.W) {
@@ -905,7 +937,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                 const int q = wk.ga + c;
                 const int u = q / I, i = q - u * I;
                 const unsigned char* st = ring + (size_t)s * p.stage_bytes;
-                dk_pair_compute(m, st, st + 2 * H, xs, H, I, k, u, i, p.h);
+                dk_pair_compute(m, st, st + 2 * H, xq, H, I, k, u, i, p.h);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
                 s += p.W;
