@@ -13,6 +13,7 @@
 #include "moe_phases.cuh"
 #include "moe_decode.cuh"
 #include "moe_tc.cuh"
+#include "moe_stream.cuh"
 
 namespace moe {
 
@@ -390,6 +391,51 @@ static int launch_tc_down(const Ctx& c, char* ws, const WsLayout& L, cudaStream_
     return launch_check();
 }
 
+// Geometry of a streaming grouped-GEMV pass; false when it does not apply
+// (segments may exceed kSgMaxTok routes, or the rows do not fit).
+static bool stream_plan(const Ctx& c, int gate, SgParams& P, size_t& smem) {
+    if (c.tc_threshold != MOE_TC_MIN_ROUTES || c.seg_list == nullptr) return false;
+    memset(&P, 0, sizeof P);
+    P.c = c;
+    P.gate = gate;
+    if (gate) {
+        P.rpi = kSgStageTarget / (4 * c.H);
+        if (P.rpi < 1) P.rpi = 1;
+        P.ips = ceil_div(c.I, P.rpi);
+        P.dim = c.H;
+        P.stage_bytes = (int)align_up((size_t)P.rpi * 4 * c.H, 128);
+    } else {
+        P.rpi = kSgStageTarget / (2 * c.I);
+        if (P.rpi < 1) P.rpi = 1;
+        if (P.rpi > 4) P.rpi &= ~3;  // whole 4-row groups
+        P.ips = ceil_div(c.H, P.rpi);
+        P.dim = c.I;
+        P.stage_bytes = (int)align_up((size_t)P.rpi * 2 * c.I, 128);
+    }
+    const size_t off_act = align_up(sizeof(SgMisc), 128);
+    const size_t off_ring = align_up(off_act + sizeof(float) * kSgMaxTok * (size_t)lb_stride(P.dim), 128);
+    const size_t limit = 227 * 1024;
+    if (off_ring + 2 * (size_t)P.stage_bytes > limit) return false;
+    size_t S = (limit - off_ring) / P.stage_bytes;
+    if (S > (size_t)kSgMaxStages) S = kSgMaxStages;
+    const size_t W = S < (size_t)kSgConsumers ? S : (size_t)kSgConsumers;
+    S = W * (S / W);
+    P.S = (int)S;
+    P.W = (int)W;
+    P.off_act = (int)off_act;
+    P.off_ring = (int)off_ring;
+    smem = off_ring + S * P.stage_bytes;
+    return true;
+}
+
+static int launch_stream(const SgParams& P, size_t smem, cudaStream_t st) {
+    int rc = allow_smem(stream_gemv_kernel, smem);
+    if (rc) return rc;
+    const int sms = sm_count();
+    stream_gemv_kernel<<<sms > 0 ? sms : 1, kSgThreads, smem, st>>>(P);
+    return launch_check();
+}
+
 // Resident CTAs of a kernel on the whole GPU (at least 1).
 template <typename K>
 static int resident_grid(K kernel, int threads, size_t smem) {
@@ -422,12 +468,24 @@ static int launch_experts(const Ctx& c0, cudaStream_t st, char* ws = nullptr, co
         d_items = d_items < rd ? d_items : rd;
     }
     const bool tc = c.tc_threshold > 0 && ws != nullptr;
+    SgParams sg_gate, sg_down;
+    size_t sg_gate_smem = 0, sg_down_smem = 0;
+    const bool streamed = ws != nullptr && stream_plan(c, 1, sg_gate, sg_gate_smem) &&
+                          stream_plan(c, 0, sg_down, sg_down_smem);
     if (tc && (rc = launch_tc(c, ws, *L, st))) return rc;
-    gateup_kernel<<<g_items, kThreads, smem, st>>>(c);
-    if ((rc = launch_check())) return rc;
+    if (streamed) {
+        if ((rc = launch_stream(sg_gate, sg_gate_smem, st))) return rc;
+    } else {
+        gateup_kernel<<<g_items, kThreads, smem, st>>>(c);
+        if ((rc = launch_check())) return rc;
+    }
     if (tc && (rc = launch_tc_down(c, ws, *L, st))) return rc;
-    down_kernel<<<d_items, kThreads, smem, st>>>(c);
-    if ((rc = launch_check())) return rc;
+    if (streamed) {
+        if ((rc = launch_stream(sg_down, sg_down_smem, st))) return rc;
+    } else {
+        down_kernel<<<d_items, kThreads, smem, st>>>(c);
+        if ((rc = launch_check())) return rc;
+    }
     combine_kernel<<<combine_items(c), kThreads, 0, st>>>(c);
     return launch_check();
 }

@@ -49,6 +49,24 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Lane-blocked layout of an fp32 activation row in shared memory: the 8
+// values of column group g = 32*b + L (columns 8g..8g+7) sit at 256*b + 4*L
+// (first four) and 256*b + 128 + 4*L (last four).  A warp that walks the
+// groups g = 32*b + lane then loads 512 contiguous bytes with each 16-byte
+// load -- one shared-memory wavefront per 128 bytes, where the natural
+// layout (a 32-byte lane stride) needs two.  Rows are lb_stride(n) floats
+// apart.
+__host__ __device__ __forceinline__ int lb_stride(int n) { return (n + 255) & ~255; }
+
+__device__ __forceinline__ int lb_index(int c) {  // column c (a multiple of 4) -> its float4
+    const int g = c >> 3;
+    return ((g >> 5) << 8) + ((c >> 2) & 1) * 128 + ((g & 31) << 2);
+}
+
+// first float of column group v (8 columns) in a lane-blocked row; the other
+// four are 128 floats further
+__device__ __forceinline__ int lb_group(int v) { return ((v >> 5) << 8) + ((v & 31) << 2); }
+
 __device__ __forceinline__ void set_status(int32_t* status, int bits) {
     if (status) atomicOr(status, bits);
 }

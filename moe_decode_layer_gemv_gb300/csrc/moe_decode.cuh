@@ -377,18 +377,11 @@ __device__ __forceinline__ void warp_sum_n(float (&v)[N]) {
         for (int j = 0; j < N; ++j) v[j] += __shfl_xor_sync(0xffffffffu, v[j], off);
 }
 
-// x rows are also kept "lane-blocked" in shared memory (xq, token stride
-// dk_hq(H)): the 8 values of column group g = 32*b + L (columns 8g..8g+7)
-// sit at 256*b + 4*L (first four) and 256*b + 128 + 4*L (last four), so the
-// 16-byte loads of a warp walking the groups g = 32*b + lane cover 512
-// contiguous bytes -- one shared-memory wavefront per 128 bytes, where the
-// natural layout (32-byte lane stride) needs two.
-__host__ __device__ __forceinline__ int dk_hq(int H) { return (H + 255) & ~255; }
-
-__device__ __forceinline__ int dk_xq_index(int c) {  // column c (a multiple of 4) -> its float4 in xq
-    const int g = c >> 3;
-    return ((g >> 5) << 8) + ((c >> 2) & 1) * 128 + ((g & 31) << 2);
-}
+// x rows are also kept lane-blocked in shared memory (xq, token stride
+// lb_stride(H); see lb_index): conflict-free 16-byte loads for the warps
+// that walk column groups lane by lane.
+__host__ __device__ __forceinline__ int dk_hq(int H) { return lb_stride(H); }
+__device__ __forceinline__ int dk_xq_index(int c) { return lb_index(c); }
 
 // Four x values at flat index f = t*H + c (c a multiple of 4) into both copies.
 __device__ __forceinline__ void dk_store_x(float* xs, float* xq, int H, int f, float4 v) {
@@ -1015,6 +1008,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
             }
             if (blockIdx.x == 0) {  // acc_now was read by every CTA before the last barrier
                 for (int v = tid - 32; v < kDkShadows * B * E; v += 32 * kDkConsumers) acc_now[v] = 0ull;
+                __threadfence();  // performed before this CTA reaches the end-of-layer barrier
             }
             if (tid == kDkLeader) dk_trace(p, l, 10);
             if (has_next) cp_async_wait_all();

@@ -204,3 +204,38 @@ def test_persistent_stack_is_stable_over_repeated_runs(cuda_lib):
         torch.cuda.synchronize()
         assert torch.equal(ia, ib), step
         assert float((xa - xb).abs().max()) <= 1e-5 * float(xb.abs().max()), step
+
+
+def test_stack_captured_in_a_cuda_graph(cuda_lib):
+    """No host synchronisation anywhere in a stack forward: the whole call
+    (the workspace clear and the persistent kernel) is captured into a CUDA
+    graph, and each replay gives the direct call's result on new inputs."""
+    H, I, E, k, L = 2048, 768, 128, 2, 4
+    w = synth.Workload("graph", B=1, H=H, I=I, E=E, top_k=k, layers=L)
+    layers = [synth.make_layer(w, l, seed=5, device=DEV) for l in range(L)]
+    sw = cuda_lib.StackWeights(layers)
+    ws = cuda_lib.new_workspace(1, H, I, E, k, DEV)
+    st = cuda_lib.new_status(DEV)
+    xbuf = torch.empty((1, H), dtype=torch.float32, device=DEV)
+    ids = torch.empty((L, 1, k), dtype=torch.int32, device=DEV)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm-up outside the capture
+        xbuf.copy_(synth.make_x(w, 0, seed=5, device=DEV))
+        cuda_lib.stack_forward_(xbuf, sw, k, ids_out=ids, workspace=ws, status=st, stream=side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cuda_lib.stack_forward_(xbuf, sw, k, ids_out=ids, workspace=ws, status=st,
+                                stream=torch.cuda.current_stream())
+    for step in range(1, 4):
+        x = synth.make_x(w, step, seed=5, device=DEV)
+        xbuf.copy_(x)
+        g.replay()
+        torch.cuda.synchronize()
+        xr, ir = cuda_lib.stack_forward(x, sw, k)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        assert torch.equal(ids, ir), step
+        assert torch.equal(xbuf, xr), step
