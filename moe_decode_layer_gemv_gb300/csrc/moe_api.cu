@@ -571,10 +571,12 @@ static bool decode_plan(int B, int H, int I, int E, int k, int sms, DkParams& p,
 }
 
 static int launch_decode(DkParams& p, size_t smem, int sms, char* ws, const WsLayout& L, cudaStream_t st) {
-    int rc = allow_smem(decode_kernel, smem);
+    void (*kernel)(DkParams) = p.trace ? (p.B == 1 ? decode_kernel<true, 1> : decode_kernel<true, 4>)
+                                       : (p.B == 1 ? decode_kernel<false, 1> : decode_kernel<false, 4>);
+    int rc = allow_smem(kernel, smem);
     if (rc) return rc;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel, kDkThreads, smem) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kDkThreads, smem) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (per_sm < 1) return MOE_ERR_UNSUPPORTED;
     p.h = reinterpret_cast<float*>(ws + L.h);
@@ -603,7 +605,7 @@ static int launch_decode(DkParams& p, size_t smem, int sms, char* ws, const WsLa
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return to_status(cudaLaunchKernelEx(&cfg, decode_kernel, p));
+    return to_status(cudaLaunchKernelEx(&cfg, kernel, p));
 }
 
 static unsigned long long* g_trace = nullptr;

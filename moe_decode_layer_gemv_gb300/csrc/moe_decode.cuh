@@ -193,8 +193,12 @@ __device__ __forceinline__ bool dk_wait(uint64_t* bar, uint32_t parity, DkMisc* 
 
 // Phase timestamps for profiling: word pair (globaltimer ns, SM clock) of
 // event `ev` (0..23) of layer `l` (-1 = the initial router step) of this CTA.
+// The kernel is compiled twice: without any of this code (the default) and
+// with it (only while a trace buffer is set), so that the untraced kernel's
+// instruction footprint stays small.
+template <bool kTrace>
 __device__ __forceinline__ void dk_trace(const DkParams& p, int l, int ev) {
-    if (p.trace == nullptr) return;
+    if (!kTrace || p.trace == nullptr) return;
     const long long idx = (((long long)(l + 1) * gridDim.x + blockIdx.x) * 24 + ev) * 2;
     if (idx + 1 >= p.trace_words) return;
     unsigned long long t;
@@ -496,6 +500,7 @@ __device__ __forceinline__ void dk_down_rows(const unsigned char* st, int nrc, i
 
 // Gate/up pair q of the layer (segment u, row i) from shared-memory rows:
 // h[p, i] = SiLU(g) * u for every route p of the segment.
+template <int kNQ>
 __device__ __forceinline__ void dk_pair_compute(const DkMisc* m, const unsigned char* grow, const unsigned char* urow,
                                                 const float* xq, int H, int I, int k, int u, int i, float* h) {
     const int lane = threadIdx.x & 31;
@@ -503,9 +508,9 @@ __device__ __forceinline__ void dk_pair_compute(const DkMisc* m, const unsigned 
     int tok[kDkMaxB];
 #pragma unroll
     for (int qq = 0; qq < kDkMaxB; ++qq) tok[qq] = p0 + qq < p1 ? m->rat[p0 + qq] / k : 0;
-    const int nq = p1 - p0;
+    const int nq = kNQ == 1 ? 1 : p1 - p0;
     float gu[2 * kDkMaxB];
-    switch (nq) {
+    switch (kNQ == 1 ? 1 : nq) {
         case 1: { float r[2]; dk_gate_pair<1>(grow, urow, xq, tok, H, r); gu[0] = r[0]; gu[1] = r[1]; } break;
         case 2: { float r[4]; dk_gate_pair<2>(grow, urow, xq, tok, H, r);
 #pragma unroll
@@ -529,12 +534,13 @@ __device__ __forceinline__ void dk_pair_compute(const DkMisc* m, const unsigned 
 
 // Down rows [r0, r1) of segment u from shared memory (row r at base + (r -
 // r0) * 2I) into os (j-th route of the segment at row p0 + j).
+template <int kNQ>
 __device__ __forceinline__ void dk_down_compute(const DkMisc* m, const unsigned char* base, int r0, int r1, int I,
                                                 const float* hs, float* os, int maxrows, int h0, int u) {
     const int p0 = m->seg_p[u], p1 = m->seg_p[u + 1];
     const float* hrow = hs + (size_t)p0 * I;
     float* orow = os + (size_t)p0 * maxrows;
-    switch (p1 - p0) {
+    switch (kNQ == 1 ? 1 : p1 - p0) {
         case 1: dk_down_rows<1>(base, r1 - r0, I, hrow, orow, maxrows, r0 - h0); break;
         case 2: dk_down_rows<2>(base, r1 - r0, I, hrow, orow, maxrows, r0 - h0); break;
         case 3: dk_down_rows<3>(base, r1 - r0, I, hrow, orow, maxrows, r0 - h0); break;
@@ -654,6 +660,10 @@ __device__ __forceinline__ void dk_gate_runs(const uint16_t* gate_up, const int*
 }
 
 // ------------------------------------------------------------ the kernel
+// kNQ = 1: a single token (every segment has one route), so only the
+// one-token variants of the gate/up and down loops are compiled in; 4: any
+// batch up to kDkMaxB.
+template <bool kTrace, int kNQ>
 __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -710,7 +720,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
     int dg_count = 0, dd_count = 0;
 
 
-    if (tid == kDkLeader) dk_trace(p, -1, 0);
+    if (tid == kDkLeader) dk_trace<kTrace>(p, -1, 0);
     // ---- router of layer 0: partial dot products over this CTA's rows
     {
         const LayerWeights& w0 = p.layer[0];
@@ -729,7 +739,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
         __syncthreads();
         if (nrows > 0) dk_router_partials(wrs, p.maxrows, xs, H, h0, nrows, B, E, p.acc, tid, blockDim.x);
     }
-    if (tid == kDkLeader) dk_trace(p, -1, 1);
+    if (tid == kDkLeader) dk_trace<kTrace>(p, -1, 1);
     dk_grid_sync(p, epoch, m, 0, kDkThreads);
 
     for (int l = 0; l < p.L && !*(volatile int*)&m->abort_flag; ++l) {
@@ -742,10 +752,10 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
         // slice; the producer warp then groups, hands the routing over (named
         // barrier 4: it arrives, the consumers wait) and goes on to issue the
         // copies at once
-        if (tid == kDkLeader) dk_trace(p, l, 0);
+        if (tid == kDkLeader) dk_trace<kTrace>(p, l, 0);
         if (warp < B) {
             dk_route_warp(acc_now, lw.bias, B, E, k, warp, m, p.status);
-            if (tid == 0) dk_trace(p, l, 7);
+            if (tid == 0) dk_trace<kTrace>(p, l, 7);
             if (B > 1) {  // warp 0 groups every token's selection
                 if (warp == 0)
                     named_sync(3, 32 * B);
@@ -759,7 +769,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                 if (p.ids_out && lane < R) p.ids_out[(size_t)l * R + lane] = m->ids[lane];
                 if (p.w_out && lane < R) p.w_out[lane] = m->w[lane];
             }
-            if (tid == 0) dk_trace(p, l, 9);
+            if (tid == 0) dk_trace<kTrace>(p, l, 9);
             named_arrive(4, kDkThreads);
         } else {
             const int ct = tid - 32, nct = 32 * kDkConsumers;
@@ -790,12 +800,12 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                 }
                 cp_async_commit();
             }
-            if (tid == kDkLeader) dk_trace(p, l, 8);
+            if (tid == kDkLeader) dk_trace<kTrace>(p, l, 8);
             named_sync(4, kDkThreads);
         }
         const int U = m->U;
         const DkWork wk = dk_work(wbase, U, m);
-        if (tid == kDkLeader) dk_trace(p, l, 1);
+        if (tid == kDkLeader) dk_trace<kTrace>(p, l, 1);
         // Direct mode: when this CTA's gate/up rows and down rows of the layer
         // fit in the ring area together, they are fetched by a handful of
         // large bulk copies (rows of one expert are contiguous) onto two
@@ -835,7 +845,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
             // Every stage is free at the start of a layer (all of the last
             // layer's chunks were consumed before its final barrier), so only a
             // chunk that reuses a stage within this layer waits for the release.
-            if (lane == 0) dk_trace(p, l, 15);
+            if (lane == 0) dk_trace<kTrace>(p, l, 15);
             const int s = lane;
             const int c_first = lane < p.S ? ((s - rs) % p.S + p.S) % p.S : wk.n;
             for (int c = c_first; c < wk.n; c += p.S) {
@@ -864,13 +874,13 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
             }
             __syncwarp();
             if (lane == 0 && p.trace) {  // profiling only: when did the first, the last gate/up and the last chunk land?
-                dk_trace(p, l, 18);
+                dk_trace<kTrace>(p, l, 18);
                 for (int c = 0; c < wk.n; ++c) {
                     const int n = ring_pos + c;
                     mbar_wait(&full[n % p.S], (uint32_t)((n / p.S) & 1), kDkWaitLimit);
-                    if (c == 0) dk_trace(p, l, 19);
-                    if (c == wk.ng - 1) dk_trace(p, l, 16);
-                    if (c == wk.n - 1) dk_trace(p, l, 17);
+                    if (c == 0) dk_trace<kTrace>(p, l, 19);
+                    if (c == wk.ng - 1) dk_trace<kTrace>(p, l, 16);
+                    if (c == wk.n - 1) dk_trace<kTrace>(p, l, 17);
                 }
             }
         }
@@ -916,21 +926,21 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                     if (!landed) {
                         if (!dk_wait(&dbar[0], (uint32_t)(dg_count & 1), m, p)) break;
                         landed = true;
-                        if (tid == kDkLeader) dk_trace(p, l, 12);
+                        if (tid == kDkLeader) dk_trace<kTrace>(p, l, 12);
                     }
                     const int q = wk.ga + c;
                     const int u = q / I, i = q - u * I;
-                    dk_pair_compute(m, d_g + (size_t)c * 2 * H, d_u + (size_t)c * 2 * H, xq, H, I, k, u, i, p.h);
+                    dk_pair_compute<kNQ>(m, d_g + (size_t)c * 2 * H, d_u + (size_t)c * 2 * H, xq, H, I, k, u, i, p.h);
                 }
             }
             for (int c = c0; !direct && consumes && c < wk.ng; c += p.W) {
                 if (*(volatile int*)&m->abort_flag) break;
                 if (!dk_wait(&full[s], ph, m, p)) break;
-                if (tid == kDkLeader && c == c0) dk_trace(p, l, 12);
+                if (tid == kDkLeader && c == c0) dk_trace<kTrace>(p, l, 12);
                 const int q = wk.ga + c;
                 const int u = q / I, i = q - u * I;
                 const unsigned char* st = ring + (size_t)s * p.stage_bytes;
-                dk_pair_compute(m, st, st + 2 * H, xq, H, I, k, u, i, p.h);
+                dk_pair_compute<kNQ>(m, st, st + 2 * H, xq, H, I, k, u, i, p.h);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
                 s += p.W;
@@ -940,14 +950,14 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                 }
             }
             // ---- all gate/up pairs of every CTA done
-            if (tid == kDkLeader) dk_trace(p, l, 2);
+            if (tid == kDkLeader) dk_trace<kTrace>(p, l, 2);
             const bool ok = dk_grid_sync(p, epoch, m, 1, 32 * kDkConsumers);
             // ---- B: down rows of every selected expert for this CTA's rows
             if (ok) {
             for (int v = tid - 32; v < (R * I) >> 2; v += 32 * kDkConsumers)
                 reinterpret_cast<float4*>(hs)[v] = ld_act_f4(p.h + 4 * (size_t)v);
             named_sync(1, 32 * kDkConsumers);
-            if (tid == kDkLeader) dk_trace(p, l, 3);
+            if (tid == kDkLeader) dk_trace<kTrace>(p, l, 3);
             if (tid == kDkLeader) {  // tell the producer warp that every CTA's predicted logits are visible
                 asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(&m->mid_epoch)), "r"(l + 1)
                              : "memory");
@@ -962,7 +972,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                     }
                     const int u = j / ng4, rg = j - u * ng4;
                     const int r0 = h0 + 4 * rg, r1 = min(h1, r0 + 4);
-                    dk_down_compute(m, d_d + ((size_t)u * nrows + 4 * rg) * 2 * I, r0, r1, I, hs, os, p.maxrows, h0, u);
+                    dk_down_compute<kNQ>(m, d_d + ((size_t)u * nrows + 4 * rg) * 2 * I, r0, r1, I, hs, os, p.maxrows, h0, u);
                 }
             }
             c0 = wk.ng + ((cw - (rs + wk.ng) % p.W) % p.W + p.W) % p.W;
@@ -978,9 +988,9 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                 const int r0 = wk.h0 + sub * wk.nr;
                 const int r1 = min(wk.h1, r0 + wk.nr);
                 const unsigned char* st = ring + (size_t)s * p.stage_bytes;
-                dk_down_compute(m, st, r0, r1, I, hs, os, p.maxrows, h0, u);
+                dk_down_compute<kNQ>(m, st, r0, r1, I, hs, os, p.maxrows, h0, u);
                 __syncwarp();
-                if (c == c0 && cw == 0 && lane == 0) dk_trace(p, l, 13);
+                if (c == c0 && cw == 0 && lane == 0) dk_trace<kTrace>(p, l, 13);
                 if (lane == 0) mbar_arrive(&empty[s]);
                 s += p.W;
                 if (s >= p.S) {
@@ -989,7 +999,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                 }
             }
             named_sync(1, 32 * kDkConsumers);
-            if (tid == kDkLeader) dk_trace(p, l, 4);
+            if (tid == kDkLeader) dk_trace<kTrace>(p, l, 4);
             // ---- combine (+ residual) for this CTA's rows, j ascending.  When the
             // residual is the layer input itself (a stack) it is already in xs.
             const bool res_in_xs = p.residual != nullptr && p.residual == p.x_in && !p.x_bf16;
@@ -1010,10 +1020,10 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                 for (int v = tid - 32; v < kDkShadows * B * E; v += 32 * kDkConsumers) acc_now[v] = 0ull;
                 __threadfence();  // performed before this CTA reaches the end-of-layer barrier
             }
-            if (tid == kDkLeader) dk_trace(p, l, 10);
+            if (tid == kDkLeader) dk_trace<kTrace>(p, l, 10);
             if (has_next) cp_async_wait_all();
             named_sync(1, 32 * kDkConsumers);
-            if (tid == kDkLeader) dk_trace(p, l, 11);
+            if (tid == kDkLeader) dk_trace<kTrace>(p, l, 11);
             // ---- router of layer l+1: partial dot products over this CTA's rows
             if (has_next && nrows > 0)
                 dk_router_partials(wrs, p.maxrows, xs, H, h0, nrows, B, E, acc_next, tid - 32,
@@ -1029,13 +1039,13 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
         }
         dg_count += d_gate ? 1 : 0;
         dd_count += d_down ? 1 : 0;
-        if (tid == kDkLeader) dk_trace(p, l, 5);
+        if (tid == kDkLeader) dk_trace<kTrace>(p, l, 5);
         __syncthreads();
         // every thread reads the same flag: nobody writes it between the two
         // barriers around this read
         const bool aborted = *(volatile int*)&m->abort_flag != 0;
         if (has_next && !aborted) dk_grid_sync(p, epoch, m, 0, kDkThreads);
-        if (tid == kDkLeader) dk_trace(p, l, 6);
+        if (tid == kDkLeader) dk_trace<kTrace>(p, l, 6);
         __syncthreads();
     }
     // leave only after this CTA's own copies in flight have landed: the latest
