@@ -571,8 +571,19 @@ static bool decode_plan(int B, int H, int I, int E, int k, int sms, DkParams& p,
 }
 
 static int launch_decode(DkParams& p, size_t smem, int sms, char* ws, const WsLayout& L, cudaStream_t st) {
-    void (*kernel)(DkParams) = p.trace ? (p.B == 1 ? decode_kernel<true, 1> : decode_kernel<true, 4>)
-                                       : (p.B == 1 ? decode_kernel<false, 1> : decode_kernel<false, 4>);
+    // direct mode for every layer: a CTA's largest share -- ceil(U*I/G) gate/up
+    // pairs and maxrows down rows of U experts, U <= R -- fits in the ring area
+    const size_t Ru = (size_t)p.B * p.k;
+    const size_t g_max = ((Ru * p.I + sms - 1) / sms) * 4 * (size_t)p.H;
+    const size_t d_max = Ru * p.maxrows * 2 * (size_t)p.I;
+    const bool all_direct = g_max + d_max <= (size_t)p.S * p.stage_bytes && g_max < (1u << 20) && d_max < (1u << 20);
+    void (*kernel)(DkParams);
+    if (p.B == 1 && all_direct)
+        kernel = p.trace ? decode_kernel<true, 1, true> : decode_kernel<false, 1, true>;
+    else if (p.B == 1)
+        kernel = p.trace ? decode_kernel<true, 1, false> : decode_kernel<false, 1, false>;
+    else
+        kernel = p.trace ? decode_kernel<true, 4, false> : decode_kernel<false, 4, false>;
     int rc = allow_smem(kernel, smem);
     if (rc) return rc;
     int per_sm = 0;

@@ -662,8 +662,13 @@ __device__ __forceinline__ void dk_gate_runs(const uint16_t* gate_up, const int*
 // ------------------------------------------------------------ the kernel
 // kNQ = 1: a single token (every segment has one route), so only the
 // one-token variants of the gate/up and down loops are compiled in; 4: any
-// batch up to kDkMaxB.
-template <bool kTrace, int kNQ>
+// batch up to kDkMaxB.  kDirect: every layer takes direct mode (the host
+// has checked that a CTA's largest possible share fits), so the ring code
+// is compiled out.  Each variant that is not needed is left out of the
+// instruction stream: the kernel runs every phase of a layer once per
+// layer, so its speed depends on how much code it streams through the
+// instruction caches.
+template <bool kTrace, int kNQ, bool kDirect>
 __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -812,7 +817,8 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
         // barriers instead of chunk by chunk through the ring.
         const uint32_t d_gate_bytes = (uint32_t)wk.ng * 4u * (uint32_t)H;
         const uint32_t d_down_bytes = (uint32_t)U * (uint32_t)nrows * 2u * (uint32_t)I;
-        const bool direct = (size_t)d_gate_bytes + d_down_bytes <= (size_t)p.S * p.stage_bytes &&
+        // (kDirect: the host has checked that every CTA's share fits for any routing)
+        const bool direct = kDirect || (size_t)d_gate_bytes + d_down_bytes <= (size_t)p.S * p.stage_bytes &&
                             d_gate_bytes < (1u << 20) && d_down_bytes < (1u << 20);
         const bool d_gate = direct && wk.ng > 0, d_down = direct && d_down_bytes > 0;
         unsigned char* d_g = ring;                                       // [ng][2H] gate rows
