@@ -542,7 +542,7 @@ static bool decode_plan(int B, int H, int I, int E, int k, int sms, DkParams& p,
     const int maxrows = 8 * ((ng + sms - 1) / sms);
     size_t off = 1024;  // ring barriers (2 x kDkMaxStages) and the two direct-mode barriers
     p.off_misc = (int)off;
-    off = align_up(off + sizeof(DkMisc), 128);
+    off = align_up(off + sizeof(DkMisc) + sizeof(float) * (size_t)B * ((E + 7) & ~7), 128);
     p.off_x = (int)off;
     off = align_up(off + sizeof(float) * (size_t)B * H, 128);
     p.off_xq = (int)off;

@@ -233,38 +233,20 @@ __device__ __forceinline__ float key_value(unsigned k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// Routing of token t by one warp, straight from the fixed-point shadow
-// accumulators of its logits: lane L holds experts L + 32 s (s < 8); every
-// load of a batch of four slots is issued before the first sum (the shadows
-// add up exactly, in any order), then the top-k and the weights.
-__device__ __forceinline__ void dk_route_warp(const unsigned long long* acc, const float* bias, int B, int E, int k,
-                                              int t, DkMisc* m, int32_t* status) {
+// Top-k of token t's logits in shared memory (lg[e], e < E) by one warp:
+// lane L holds experts L + 32 s (s < 8) as order-preserving keys; k rounds
+// of a max reduction (and a min reduction over the ids holding it: ties to
+// the lower id), then the weights.
+__device__ __forceinline__ void dk_topk_smem(const float* lg, int E, int k, int t, DkMisc* m, int32_t* status) {
     const int lane = threadIdx.x & 31;
     unsigned key[8];
     bool bad = false;
 #pragma unroll
-    for (int s0 = 0; s0 < 8; s0 += 4) {
-        unsigned long long sum[4] = {0ull, 0ull, 0ull, 0ull};
-        if (32 * s0 < E) {
-#pragma unroll
-            for (int sh = 0; sh < kDkShadows; ++sh)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int e = lane + 32 * (s0 + j);
-                    if (e < E) sum[j] += __ldcg(acc + ((size_t)sh * B + t) * E + e);
-                }
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int e = lane + 32 * (s0 + j);
-            float v = 0.f;
-            if (e < E) {
-                v = fix_to_float(sum[j]);
-                if (bias) v += __ldg(bias + e);
-                if (!isfinite(v)) bad = true;
-            }
-            key[s0 + j] = e < E ? order_key(v) : 0u;  // 0 is below every real key
-        }
+    for (int s = 0; s < 8; ++s) {
+        const int e = lane + 32 * s;
+        const float v = e < E ? lg[e] : 0.f;
+        if (e < E && !isfinite(v)) bad = true;
+        key[s] = e < E ? order_key(v) : 0u;
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(status, MOE_DEV_NONFINITE);
     unsigned taken = 0;
@@ -275,7 +257,7 @@ __device__ __forceinline__ void dk_route_warp(const unsigned long long* acc, con
         int ib = 0x7fffffff;
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-            if (!((taken >> s) & 1u) && key[s] > kb) {  // strictly greater keeps the lower id
+            if (!((taken >> s) & 1u) && key[s] > kb) {
                 kb = key[s];
                 ib = lane + 32 * s;
             }
@@ -292,7 +274,7 @@ __device__ __forceinline__ void dk_route_warp(const unsigned long long* acc, con
     const float ex = lane < k ? expf(my_l - l0) : 0.f;
     float den = ex;
 #pragma unroll
-    for (int off = 4; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);  // lanes 0..7
+    for (int off = 4; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
     if (lane < k) {
         m->ids[t * k + lane] = my_id;
         m->selv[t * k + lane] = my_l;
@@ -611,12 +593,20 @@ __device__ __forceinline__ int dk_predict_top(const float* alog, int E, int kp) 
 // This CTA's 1/G share of the predicted experts' weight bytes prefetched
 // into L2, one bulk prefetch per contiguous piece: lane j < kp covers expert
 // j (my_e), its gate_up block then its down block.
-__device__ __forceinline__ void dk_prefetch_l2(const LayerWeights& wn, int my_e, int H, int I, int kp) {
+// [b0, b1): this CTA's byte range of the kp experts' concatenated bytes
+// (fixed per launch, computed once).
+__device__ __forceinline__ void dk_prefetch_range(int H, int I, int kp, unsigned long long& b0,
+                                                  unsigned long long& b1) {
+    const unsigned long long total = 6ull * I * H * (unsigned long long)kp;
+    b0 = total * blockIdx.x / gridDim.x;
+    b1 = total * (blockIdx.x + 1) / gridDim.x;
+}
+
+__device__ __forceinline__ void dk_prefetch_l2(const LayerWeights& wn, int my_e, int H, int I, int kp,
+                                               unsigned long long b0, unsigned long long b1) {
     const int lane = threadIdx.x & 31;
     const unsigned long long gsz = 4ull * I * H;  // gate_up bytes of one expert; down: 2IH
     const unsigned long long per_e = gsz + 2ull * I * H;
-    const unsigned long long total = per_e * (unsigned long long)kp;
-    const unsigned long long b0 = total * blockIdx.x / gridDim.x, b1 = total * (blockIdx.x + 1) / gridDim.x;
     if (lane < kp && my_e >= 0) {
         const unsigned long long e0 = per_e * lane, e1 = e0 + per_e;
         unsigned long long lo = b0 > e0 ? b0 : e0, hi = b1 < e1 ? b1 : e1;
@@ -681,12 +671,17 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
     float* os = reinterpret_cast<float*>(smem + p.off_o);   // [R][maxrows]
     uint16_t* wrs = reinterpret_cast<uint16_t*>(smem + p.off_wr);  // [E][maxrows]
     unsigned char* ring = smem + p.off_ring;
+    float* lg = reinterpret_cast<float*>(smem + p.off_misc + sizeof(DkMisc));  // [B][Ep] logits
+    const int Ep = (p.E + 7) & ~7;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int B = p.B, H = p.H, I = p.I, E = p.E, k = p.k, R = B * k;
+    const int B = kNQ == 1 ? 1 : p.B;  // a compile-time constant for one token
+    const int H = p.H, I = p.I, E = p.E, k = p.k, R = B * k;
     const bool no_dedup = (p.flags & MOE_F_NO_DEDUP) != 0;
     int h0, h1;
     dk_rows(blockIdx.x, gridDim.x, H, h0, h1);
+    unsigned long long pf_b0 = 0, pf_b1 = 0;  // next-layer prefetch range (producer warp)
+    if (warp == 0 && p.prefetch_k > 0) dk_prefetch_range(H, I, p.prefetch_k, pf_b0, pf_b1);
     const int nrows = h1 - h0;
     DkWork wbase;
     wbase.h0 = h0;
@@ -752,14 +747,32 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
         const bool has_next = l + 1 < p.L;
         unsigned long long* acc_now = p.acc + (size_t)(l & 1) * kDkShadows * B * E;
         unsigned long long* acc_next = p.acc + (size_t)((l + 1) & 1) * kDkShadows * B * E;
-        // ---- A0: the router warps (token t: warp t) route straight from the
-        // logit accumulators while the consumers stage x and the next router
-        // slice; the producer warp then groups, hands the routing over (named
-        // barrier 4: it arrives, the consumers wait) and goes on to issue the
-        // copies at once
+        // ---- A0: the consumers sum the logit accumulators into lg; the
+        // router warps (token t: warp t) take the top-k while the consumers
+        // stage x and the next router slice; the producer warp then groups,
+        // hands the routing over (named barrier 4: it arrives, the consumers
+        // wait) and goes on to issue the copies at once
         if (tid == kDkLeader) dk_trace<kTrace>(p, l, 0);
+        if (warp >= 1) {
+            // consumers: every (token, expert) logit from the shadow
+            // accumulators (an integer sum: exact in any order) into lg
+            const int ct = tid - 32, nct = 32 * kDkConsumers;
+            for (int v = ct; v < B * Ep; v += nct) {
+                const int t = v / Ep, e = v - t * Ep;
+                float val = -INFINITY;
+                if (e < E) {
+                    unsigned long long sum = 0ull;
+#pragma unroll
+                    for (int sh = 0; sh < kDkShadows; ++sh) sum += __ldcg(acc_now + ((size_t)sh * B + t) * E + e);
+                    val = fix_to_float(sum);
+                    if (lw.bias) val += __ldg(lw.bias + e);
+                }
+                lg[v] = val;
+            }
+        }
+        __syncthreads();
         if (warp < B) {
-            dk_route_warp(acc_now, lw.bias, B, E, k, warp, m, p.status);
+            dk_topk_smem(lg + warp * Ep, E, k, warp, m, p.status);
             if (tid == 0) dk_trace<kTrace>(p, l, 7);
             if (B > 1) {  // warp 0 groups every token's selection
                 if (warp == 0)
@@ -906,7 +919,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
             }
             if (__all_sync(0xffffffffu, seen)) {
                 const int my_e = dk_predict_top(p.alog, E, p.prefetch_k);
-                dk_prefetch_l2(p.layer[l + 1], my_e, H, I, p.prefetch_k);
+                dk_prefetch_l2(p.layer[l + 1], my_e, H, I, p.prefetch_k, pf_b0, pf_b1);
             }
         }
         if (warp != 0) {
