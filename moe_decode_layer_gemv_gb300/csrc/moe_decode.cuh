@@ -129,7 +129,7 @@ __device__ __forceinline__ DkWork dk_work(const DkWork& base, int U, const DkMis
 // p.bar[0] = counter, p.bar[1] = abort word.  Bounded: after kDkSpinLimit
 // polls the CTA sets MOE_DEV_TIMEOUT and the abort word and reports failure.
 constexpr int kDkLeader = 32;  // first consumer thread
-constexpr int kDkShadows = 8;  // copies of the logit accumulator (spread the atomics)
+constexpr int kDkShadows = 2;  // copies of the logit accumulator (spread the atomics; 2 measured best of 1, 2, 4, 8)
 
 __device__ __forceinline__ unsigned atom_add_release_gpu(unsigned* p, unsigned v) {
     unsigned old;
@@ -593,42 +593,22 @@ __device__ __forceinline__ int dk_predict_top(const float* alog, int E, int kp) 
 // This CTA's 1/G share of the predicted experts' weight bytes prefetched
 // into L2, one bulk prefetch per contiguous piece: lane j < kp covers expert
 // j (my_e), its gate_up block then its down block.
-// [b0, b1): this CTA's byte range of the kp experts' concatenated bytes
-// (fixed per launch, computed once).
-__device__ __forceinline__ void dk_prefetch_range(int H, int I, int kp, unsigned long long& b0,
-                                                  unsigned long long& b1) {
-    const unsigned long long total = 6ull * I * H * (unsigned long long)kp;
-    b0 = total * blockIdx.x / gridDim.x;
-    b1 = total * (blockIdx.x + 1) / gridDim.x;
-}
-
-__device__ __forceinline__ void dk_prefetch_l2(const LayerWeights& wn, int my_e, int H, int I, int kp,
-                                               unsigned long long b0, unsigned long long b1) {
+// This CTA's 1/G share of each predicted expert's weights prefetched into
+// L2: lane j < kp takes expert j (my_e) and issues two bulk prefetches, its
+// piece of the gate_up block and its piece of the down block (pieces of
+// equal 16-byte-aligned size, the last CTA taking the remainder).
+__device__ __forceinline__ void dk_prefetch_l2(const LayerWeights& wn, int my_e, int H, int I, int kp) {
     const int lane = threadIdx.x & 31;
-    const unsigned long long gsz = 4ull * I * H;  // gate_up bytes of one expert; down: 2IH
-    const unsigned long long per_e = gsz + 2ull * I * H;
     if (lane < kp && my_e >= 0) {
-        const unsigned long long e0 = per_e * lane, e1 = e0 + per_e;
-        unsigned long long lo = b0 > e0 ? b0 : e0, hi = b1 < e1 ? b1 : e1;
-        lo = (lo + 15) & ~15ull;
-        hi &= ~15ull;
-        while (lo < hi) {
-            const unsigned long long off = lo - e0;
-            const char* src;
-            unsigned long long lim;
-            if (off < gsz) {
-                src = reinterpret_cast<const char*>(wn.gate_up + (size_t)my_e * 2 * I * H) + off;
-                lim = gsz - off;
-            } else {
-                src = reinterpret_cast<const char*>(wn.down + (size_t)my_e * H * I) + (off - gsz);
-                lim = per_e - off;
-            }
-            unsigned long long n = hi - lo;
-            if (n > lim) n = lim;
-            if (n > (2ull << 20)) n = 2ull << 20;
-            bulk_prefetch_l2(src, (uint32_t)n);
-            lo += n;
-        }
+        const unsigned G = gridDim.x, c = blockIdx.x;
+        const unsigned gsz = 4u * (unsigned)I * (unsigned)H, dsz = 2u * (unsigned)I * (unsigned)H;
+        const unsigned gp = (gsz / G) & ~15u, dp = (dsz / G) & ~15u;
+        const unsigned g0 = c * gp, d0 = c * dp;
+        const unsigned gn = c + 1 == G ? gsz - g0 : gp, dn = c + 1 == G ? dsz - d0 : dp;
+        const char* ge = reinterpret_cast<const char*>(wn.gate_up + (size_t)my_e * 2 * I * H);
+        const char* de = reinterpret_cast<const char*>(wn.down + (size_t)my_e * H * I);
+        if (gn > 0) bulk_prefetch_l2(ge + g0, gn);
+        if (dn > 0) bulk_prefetch_l2(de + d0, dn);
     }
 }
 
@@ -680,8 +660,6 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
     const bool no_dedup = (p.flags & MOE_F_NO_DEDUP) != 0;
     int h0, h1;
     dk_rows(blockIdx.x, gridDim.x, H, h0, h1);
-    unsigned long long pf_b0 = 0, pf_b1 = 0;  // next-layer prefetch range (producer warp)
-    if (warp == 0 && p.prefetch_k > 0) dk_prefetch_range(H, I, p.prefetch_k, pf_b0, pf_b1);
     const int nrows = h1 - h0;
     DkWork wbase;
     wbase.h0 = h0;
@@ -919,7 +897,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
             }
             if (__all_sync(0xffffffffu, seen)) {
                 const int my_e = dk_predict_top(p.alog, E, p.prefetch_k);
-                dk_prefetch_l2(p.layer[l + 1], my_e, H, I, p.prefetch_k, pf_b0, pf_b1);
+                dk_prefetch_l2(p.layer[l + 1], my_e, H, I, p.prefetch_k);
             }
         }
         if (warp != 0) {
