@@ -80,7 +80,7 @@ typedef enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 } moe_dtype;
                                its expert's weights): the A/B baseline of the
                                dedup page; results are identical */
 #define MOE_F_UNFUSED 2u    /* layer/stack: run the phases as separate kernels
-                               instead of the persistent fused kernel */
+                               instead of a persistent kernel */
 #define MOE_F_FORCE_TC 4u   /* every expert with any route uses the tensor-core
                                GEMMs (testing; needs H % 128 == 0, I % 64 == 0) */
 #define MOE_F_NO_TC 8u      /* never use the tensor-core GEMMs */
@@ -178,9 +178,12 @@ int moe_expert_forward_noalloc(const void* x, int x_dtype, const uint16_t* gate_
 
 /*
  * moe_layer_forward -- the whole layer: moe_route, moe_group_by_expert and
- * moe_expert_forward in one enqueue.  Unless MOE_F_UNFUSED, the phases run in
- * one persistent cooperative kernel (one CTA per SM, device-wide barriers
- * with a bounded wait).
+ * moe_expert_forward in one enqueue.  Unless MOE_F_UNFUSED, batches of up to
+ * 4 tokens and 32 routes run in one persistent cooperative kernel (one CTA
+ * per SM, device-wide barriers with a bounded wait); larger batches run the
+ * phases as separate kernels (streaming GEMV for experts with few routes,
+ * tensor-core GEMMs for the others), or, when no expert goes to the tensor
+ * cores, all phases in one persistent fused kernel.
  * Out: y [B,H] fp32 (may alias residual); expert_ids_out / route_w_out
  *      [B,k] (may be NULL).
  */

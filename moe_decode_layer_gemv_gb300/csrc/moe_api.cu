@@ -1,7 +1,11 @@
 // moe_api.cu -- the C ABI of libmoe.so (declared in include/moe.h): argument
-// checks, workspace layout and kernel launches.  The kernels are built from
-// the phase functions in moe_phases.cuh, either one kernel per phase or all
-// phases (and all layers of a stack) in one persistent cooperative kernel.
+// checks, workspace layout and kernel launches.  Kernels: the persistent
+// decode kernel for batches of up to 4 tokens (moe_decode.cuh, whole layers
+// or stacks in one launch); for larger batches the phase kernels of
+// moe_phases.cuh (router, top-k, grouping, combine), the streaming grouped
+// GEMV passes (moe_stream.cuh) and the tensor-core GEMMs (moe_tc.cuh), or
+// all phases in one persistent fused kernel when no expert needs the tensor
+// cores.
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>

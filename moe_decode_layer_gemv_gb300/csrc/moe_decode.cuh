@@ -590,9 +590,6 @@ __device__ __forceinline__ int dk_predict_top(const float* alog, int E, int kp) 
     return my_e;
 }
 
-// This CTA's 1/G share of the predicted experts' weight bytes prefetched
-// into L2, one bulk prefetch per contiguous piece: lane j < kp covers expert
-// j (my_e), its gate_up block then its down block.
 // This CTA's 1/G share of each predicted expert's weights prefetched into
 // L2: lane j < kp takes expert j (my_e) and issues two bulk prefetches, its
 // piece of the gate_up block and its piece of the down block (pieces of
