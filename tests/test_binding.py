@@ -1,0 +1,59 @@
+"""The Python binding on the CPU: it marshals arguments only, so every check
+it makes happens before any launch, and it never computes a result itself
+(a CPU tensor is refused, not evaluated)."""
+import re
+import os
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def api():
+    from moe_decode_layer_gemv_gb300 import build
+    build.build()
+    from moe_decode_layer_gemv_gb300 import api as a
+    return a
+
+
+def test_binding_names_every_declared_entry_point(api):
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    declared = set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(moe_\w+)\s*\(", src, flags=re.M))
+    assert declared == set(api.EXPORTED)
+
+
+def test_cpu_tensors_are_refused_not_computed(api):
+    B, H, I, E, k = 2, 64, 32, 8, 2
+    x = torch.zeros(B, H)
+    wr = torch.zeros(E, H, dtype=torch.bfloat16)
+    gu = torch.zeros(E, 2 * I, H, dtype=torch.bfloat16)
+    dn = torch.zeros(E, H, I, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        api.layer_forward(x, wr, gu, dn, k)
+    with pytest.raises(TypeError):  # weights must be bf16
+        api.layer_forward(x, wr.float(), gu, dn, k)
+
+
+def test_host_errors_raise_with_their_status(api):
+    with pytest.raises(api.MoeError) as e:
+        api.workspace_bytes(4, 2048, 768, 300, 8)  # E above the maximum
+    assert e.value.code == api.MOE_ERR_INVALID_ARG
+    with pytest.raises(api.MoeError):
+        api.inject_barrier_stall(-1)
+    api.inject_barrier_stall(0)
+
+
+def test_workspace_grows_with_the_batch(api):
+    a = api.workspace_bytes(1, 2048, 768, 128, 2)
+    b = api.workspace_bytes(64, 2048, 768, 256, 8)
+    assert 0 < a < b
+    # at least the per-route scratch: h [R, I] and o [R, H] in fp32
+    assert b >= 64 * 8 * (768 + 2048) * 4
+
+
+def test_status_strings_name_the_device_bits(api):
+    assert "timed out" in api.status_string(api.MOE_DEV_TIMEOUT)
+    assert api.status_string(api.MOE_OK)
