@@ -316,6 +316,20 @@ def run_layer_workload(args):
     times_ms = [a.elapsed_time(b) for a, b in ev]
     mean_ms = statistics.mean(times_ms)
     us = [len(np.unique(u.cpu().numpy())) for u in uniq]
+    # routing statistics of the timed inputs, outside the timed region: tokens
+    # whose k-th and (k+1)-th logits are within 1e-5 (near ties)
+    near_ties = None
+    if w.top_k < w.E:
+        try:
+            near_ties = 0
+            for s in range(args.steps):
+                _, _, lg = api.route(xs[args.warmup + s], lw["w_router"], w.top_k, bias=lw["bias"], stream=stream)
+                srt = torch.sort(lg, dim=1, descending=True).values
+                near_ties += int(((srt[:, w.top_k - 1] - srt[:, w.top_k]) < 1e-5).sum())
+            torch.cuda.synchronize()
+        except Exception as exc:  # statistics only: never fail the timing line
+            print(f"near-tie count skipped: {exc}", file=sys.stderr)
+            near_ties = None
     bytes_step = statistics.mean(accounting.layer_bytes(w.H, w.I, w.E, u) for u in us)
     achieved = bytes_step / (mean_ms / 1e3) / 1e9
     peak, peak_src = hbm_peak()
@@ -325,7 +339,9 @@ def run_layer_workload(args):
             "weights_dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "I": w.I, "E": w.E, "top_k": w.top_k,
                        "mode": args.mode, "l2": "flushed before every timed step"},
-            "unique_experts_mean": statistics.mean(us), "hbm_gbs": achieved,
+            "unique_experts_mean": statistics.mean(us),
+            "reuse_mean": statistics.mean(w.B * w.top_k / u for u in us),
+            "near_tie_tokens": near_ties, "hbm_gbs": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_src, "traffic": None,
                          "bytes_per_launch": bytes_step},
