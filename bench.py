@@ -78,16 +78,32 @@ def job_throughput(local_ms, units_per_rank, pg=None, device="cpu"):
     return local_ms, units_per_rank * world / (local_ms / 1000.0)
 
 
-def hbm_peak():
-    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(p):
-        try:
-            d = json.load(open(p))
-            for key in ("hbm_gbs", "hbm_copy_gbs"):
-                if key in d:
-                    return float(d[key]), "measured"
-        except Exception:
-            pass
+def hbm_peak(path=None):
+    """HBM roofline peak in GB/s: the measured copy bandwidth from
+    MEASURED_PEAKS.json (a numeric entry whose key path names HBM and a
+    bandwidth, the burst figure first: kernels here are timed per launch; a
+    value below 100 is taken as TB/s), else the fallback."""
+    p = path or os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p)) if os.path.exists(p) else None
+    except Exception:
+        d = None
+    found = []
+
+    def walk(o, key_path):
+        if isinstance(o, dict):
+            for k, v in o.items():
+                walk(v, key_path + "/" + str(k).lower())
+        elif isinstance(o, (int, float)) and not isinstance(o, bool) and o > 0:
+            found.append((key_path, float(o)))
+
+    walk(d, "")
+    unrelated = ("clock", "mhz", "freq", "mib", "size", "bytes", "count", "util", "pct", "frac")
+    cands = [(k, v) for k, v in found if "hbm" in k and not any(u in k for u in unrelated)]
+    if cands:
+        cands.sort(key=lambda kv: ("burst" not in kv[0], "sustain" in kv[0], kv[0]))
+        v = cands[0][1]
+        return (v * 1000.0 if v < 100 else v), "measured"
     return FALLBACK_HBM_GBS, "fallback"
 
 
