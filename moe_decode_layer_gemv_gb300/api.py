@@ -110,6 +110,25 @@ def _need(t, dtype, name):
         raise ValueError(f"{name} must be a contiguous CUDA tensor")
 
 
+def _opt(t, dtype, name, device):
+    """Optional tensor argument: None, or a contiguous CUDA tensor of dtype on
+    x's device (a host tensor's address must never reach a kernel)."""
+    if t is None:
+        return
+    if dtype is not None:
+        _need(t, dtype, name)
+    elif not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, x on {device}")
+
+
+def _need_x(x):
+    _x_dtype(x)
+    if not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA tensor")
+
+
 def set_trace_buffer(buf):
     """Record phase timestamps of the persistent decode kernel into `buf`
     (a CUDA int64 tensor) on every following launch; None turns it off."""
@@ -144,7 +163,10 @@ def new_status(device=None) -> torch.Tensor:
 
 def route(x, w_router, top_k, bias=None, stream=None, status=None):
     """-> (expert_ids [B,k] int32, route_w [B,k] fp32, logits [B,E] fp32)."""
+    _need_x(x)
     _need(w_router, torch.bfloat16, "w_router")
+    _opt(bias, torch.float32, "bias", x.device)
+    _opt(status, torch.int32, "status", x.device)
     B, H = x.shape
     E = w_router.shape[0]
     ids = torch.empty((B, top_k), dtype=torch.int32, device=x.device)
@@ -160,6 +182,7 @@ def group_by_expert(expert_ids, E, stream=None, status=None):
     _need(expert_ids, torch.int32, "expert_ids")
     B, k = expert_ids.shape
     dev = expert_ids.device
+    _opt(status, torch.int32, "status", dev)
     offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
     ridx = torch.empty(max(B * k, 1), dtype=torch.int32, device=dev)
     uniq = torch.empty(E, dtype=torch.int32, device=dev)
@@ -169,11 +192,25 @@ def group_by_expert(expert_ids, E, stream=None, status=None):
     return offsets, ridx[:B * k], uniq, nu
 
 
+def _check_expert_args(x, gate_up, down, expert_ids, route_w, grouping, residual, out, status):
+    _need_x(x)
+    _need(gate_up, torch.bfloat16, "gate_up")
+    _need(down, torch.bfloat16, "down")
+    dev = x.device
+    _opt(expert_ids, torch.int32, "expert_ids", dev)
+    _opt(route_w, torch.float32, "route_w", dev)
+    for t, n in zip(grouping, ("offsets", "route_idx", "unique_experts", "num_unique")):
+        _opt(t, torch.int32, n, dev)
+    _opt(residual, torch.float32, "residual", dev)
+    _opt(out, torch.float32, "out", dev)
+    _opt(status, torch.int32, "status", dev)
+
+
 def expert_forward(x, gate_up, down, expert_ids, route_w, grouping, residual=None, flags=0,
                    out=None, workspace=None, status=None, stream=None):
     """y [B,H] fp32 = sum_j w * down_e(SiLU(gate_e x) * up_e x) (+ residual)."""
-    _need(gate_up, torch.bfloat16, "gate_up")
-    _need(down, torch.bfloat16, "down")
+    _check_expert_args(x, gate_up, down, expert_ids, route_w, grouping, residual, out, status)
+    _opt(workspace, torch.uint8, "workspace", x.device)
     B, H = x.shape
     E, twoI, _ = gate_up.shape
     I = twoI // 2
@@ -193,8 +230,7 @@ def expert_forward_noalloc(x, gate_up, down, expert_ids, route_w, grouping, resi
     """expert_forward with the library's fixed scratch array instead of a
     workspace: for callers that cannot allocate device memory.  `out` must
     be given by such callers (it is allocated here only for convenience)."""
-    _need(gate_up, torch.bfloat16, "gate_up")
-    _need(down, torch.bfloat16, "down")
+    _check_expert_args(x, gate_up, down, expert_ids, route_w, grouping, residual, out, status)
     B, H = x.shape
     E, twoI, _ = gate_up.shape
     I = twoI // 2
@@ -212,8 +248,14 @@ def expert_forward_noalloc(x, gate_up, down, expert_ids, route_w, grouping, resi
 def layer_forward(x, w_router, gate_up, down, top_k, bias=None, residual=None, flags=0, out=None,
                   ids_out=None, w_out=None, workspace=None, status=None, stream=None):
     """Whole layer -> (y [B,H] fp32, expert_ids [B,k], route_w [B,k])."""
+    _need_x(x)
     for t, n in ((w_router, "w_router"), (gate_up, "gate_up"), (down, "down")):
         _need(t, torch.bfloat16, n)
+    for t, dt, n in ((bias, torch.float32, "bias"), (residual, torch.float32, "residual"),
+                     (out, torch.float32, "out"), (ids_out, torch.int32, "ids_out"),
+                     (w_out, torch.float32, "w_out"), (workspace, torch.uint8, "workspace"),
+                     (status, torch.int32, "status")):
+        _opt(t, dt, n, x.device)
     B, H = x.shape
     E, twoI, _ = gate_up.shape
     I = twoI // 2
@@ -248,12 +290,17 @@ class StackWeights:
         for l in layers:
             for n in ("w_router", "gate_up", "down"):
                 _need(l[n], torch.bfloat16, n)
+            if l.get("bias") is not None:
+                _need(l["bias"], torch.float32, "bias")
 
 
 def stack_forward_(x, stack: StackWeights, top_k, flags=0, ids_out=None, workspace=None, status=None,
                    stream=None):
     """In place: x [B,H] fp32 <- x + layer_l(x) for every layer.  Returns x."""
     _need(x, torch.float32, "x")
+    for t, dt, n in ((ids_out, torch.int32, "ids_out"), (workspace, torch.uint8, "workspace"),
+                     (status, torch.int32, "status")):
+        _opt(t, dt, n, x.device)
     B, H = x.shape
     ws = workspace if workspace is not None else new_workspace(B, H, stack.I, stack.E, top_k, x.device)
     _check(_lib.moe_stack_forward(stack.L, ctypes.addressof(stack.wr),

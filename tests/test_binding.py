@@ -33,8 +33,30 @@ def test_cpu_tensors_are_refused_not_computed(api):
     dn = torch.zeros(E, H, I, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         api.layer_forward(x, wr, gu, dn, k)
-    with pytest.raises(TypeError):  # weights must be bf16
-        api.layer_forward(x, wr.float(), gu, dn, k)
+    with pytest.raises(TypeError):  # x must be fp32 or bf16
+        api.layer_forward(x.double(), wr, gu, dn, k)
+
+
+def test_every_entry_point_checks_its_tensors_before_any_launch(api):
+    B, H, I, E, k = 2, 64, 32, 8, 2
+    x = torch.zeros(B, H)
+    wr = torch.zeros(E, H, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        api.route(x, wr, k)
+    with pytest.raises(ValueError):
+        api.group_by_expert(torch.zeros(B, k, dtype=torch.int32), E)
+    with pytest.raises(ValueError):
+        api.stack_forward_(x, None, k)
+    gu = torch.zeros(E, 2 * I, H, dtype=torch.bfloat16)
+    dn = torch.zeros(E, H, I, dtype=torch.bfloat16)
+    ids = torch.zeros(B, k, dtype=torch.int32)
+    grouping = tuple(torch.zeros(n, dtype=torch.int32) for n in (E + 1, B * k, E, 1))
+    with pytest.raises(ValueError):
+        api.expert_forward(x, gu, dn, ids, torch.zeros(B, k), grouping)
+    with pytest.raises(ValueError):
+        api.expert_forward_noalloc(x, gu, dn, ids, torch.zeros(B, k), grouping)
+    with pytest.raises(TypeError):  # x must be fp32 or bf16
+        api.route(x.double(), wr, k)
 
 
 def test_host_errors_raise_with_their_status(api):
