@@ -58,10 +58,13 @@ static float load_x(const void* x, int x_dtype, size_t idx) {
     return ((const float*)x)[idx];
 }
 
-/* Router GEMV: logits[t,e] = sum_h x[t,h]*Wr[e,h], h ascending, + bias[e]. */
+/* Router GEMV: logits[t,e] = sum_h x[t,h]*Wr[e,h], h ascending, + bias[e].
+ * The (token, expert) pairs are independent sums, so they are spread over
+ * threads; each sum still runs in h order. */
 int oracle_router(const void* x, int x_dtype, const uint16_t* wr, const float* bias,
                   int B, int H, int E, float* logits) {
     if (B < 0 || H <= 0 || E <= 0 || !x || !wr || !logits) return OR_BAD_ARG;
+#pragma omp parallel for collapse(2) schedule(static)
     for (int t = 0; t < B; ++t) {
         for (int e = 0; e < E; ++e) {
             float acc = 0.0f;
@@ -137,11 +140,12 @@ int oracle_group(const int32_t* ids, int B, int k, int E, int32_t* offsets,
     return OR_OK;
 }
 
-/* One expert on one token: h = SiLU(G x) * (U x), o = D h.
- * gate_up_e: [2I, H] bf16 (rows [0,I) gate, [I,2I) up); down_e: [H, I] bf16. */
-static void expert_one(const void* x, int x_dtype, size_t x_off, const uint16_t* gate_up_e,
-                       const uint16_t* down_e, int H, int I, float* hbuf, float* o) {
-    for (int i = 0; i < I; ++i) {
+/* Pass 1 of one expert on one token, gate/up rows [i0, i1):
+ * h[i] = SiLU(G_i . x) * (U_i . x), each dot product in h order.
+ * gate_up_e: [2I, H] bf16 (rows [0,I) gate, [I,2I) up). */
+static void expert_gate_rows(const void* x, int x_dtype, size_t x_off, const uint16_t* gate_up_e,
+                             int H, int I, int i0, int i1, float* hbuf) {
+    for (int i = i0; i < i1; ++i) {
         float g = 0.0f, u = 0.0f;
         const uint16_t* grow = gate_up_e + (size_t)i * H;
         const uint16_t* urow = gate_up_e + (size_t)(I + i) * H;
@@ -153,13 +157,29 @@ static void expert_one(const void* x, int x_dtype, size_t x_off, const uint16_t*
         float silu = g / (1.0f + expf(-g));
         hbuf[i] = silu * u;
     }
-    for (int r = 0; r < H; ++r) {
+}
+
+/* Pass 2 of one expert on one token, down rows [r0, r1): o[r] = D_r . h,
+ * each dot product in i order.  down_e: [H, I] bf16. */
+static void expert_down_rows(const uint16_t* down_e, int I, int r0, int r1, const float* hbuf,
+                             float* o) {
+    for (int r = r0; r < r1; ++r) {
         float acc = 0.0f;
         const uint16_t* drow = down_e + (size_t)r * I;
         for (int i = 0; i < I; ++i) acc += bf16_to_f32(drow[i]) * hbuf[i];
         o[r] = acc;
     }
 }
+
+/* One expert on one token: h = SiLU(G x) * (U x), o = D h. */
+static void expert_one(const void* x, int x_dtype, size_t x_off, const uint16_t* gate_up_e,
+                       const uint16_t* down_e, int H, int I, float* hbuf, float* o) {
+    expert_gate_rows(x, x_dtype, x_off, gate_up_e, H, I, 0, I, hbuf);
+    expert_down_rows(down_e, I, 0, H, hbuf, o);
+}
+
+/* rows per work item of the dedup passes */
+#define ORACLE_ROW_BLOCK 64
 
 /* Expert pass for given routing.  gate_up_ptrs[e] / down_ptrs[e] point at
  * expert e's weights (host memory); experts that no route selects may be
@@ -198,15 +218,37 @@ int oracle_experts(const void* x, int x_dtype, const uint16_t* const* gate_up_pt
         int32_t* uniq = (int32_t*)malloc(sizeof(int32_t) * (size_t)E);
         int32_t nu = 0;
         oracle_group(ids, B, k, E, offsets, ridx, uniq, &nu);
-        /* parallel over unique experts: each route's result is written to
-         * its own row, so the order the experts run in changes nothing */
-#pragma omp parallel for schedule(dynamic, 1)
+        /* The #46 loop order, split by (unique expert, row block): pass 1
+         * over the gate/up rows, then pass 2 over the down rows.  Every h[r,i]
+         * and o[r,c] is one dot product written to its own place, computed
+         * exactly as in expert_one, so neither the split nor the order the
+         * items run in changes a bit of the result. */
+        const int nib = (I + ORACLE_ROW_BLOCK - 1) / ORACLE_ROW_BLOCK;
+        const int nrb = (H + ORACLE_ROW_BLOCK - 1) / ORACLE_ROW_BLOCK;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
         for (int u = 0; u < nu; ++u) {
-            int e = uniq[u];
-            for (int q = offsets[e]; q < offsets[e + 1]; ++q) {
-                int r = ridx[q], t = r / k;
-                expert_one(x, x_dtype, (size_t)t * H, gate_up_ptrs[e], down_ptrs[e], H, I,
-                           hb + (size_t)r * I, o + (size_t)r * H);
+            for (int ib = 0; ib < nib; ++ib) {
+                int e = uniq[u];
+                int i0 = ib * ORACLE_ROW_BLOCK;
+                int i1 = i0 + ORACLE_ROW_BLOCK < I ? i0 + ORACLE_ROW_BLOCK : I;
+                for (int q = offsets[e]; q < offsets[e + 1]; ++q) {
+                    int r = ridx[q], t = r / k;
+                    expert_gate_rows(x, x_dtype, (size_t)t * H, gate_up_ptrs[e], H, I, i0, i1,
+                                     hb + (size_t)r * I);
+                }
+            }
+        }
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+        for (int u = 0; u < nu; ++u) {
+            for (int rb = 0; rb < nrb; ++rb) {
+                int e = uniq[u];
+                int r0 = rb * ORACLE_ROW_BLOCK;
+                int r1 = r0 + ORACLE_ROW_BLOCK < H ? r0 + ORACLE_ROW_BLOCK : H;
+                for (int q = offsets[e]; q < offsets[e + 1]; ++q) {
+                    int r = ridx[q];
+                    expert_down_rows(down_ptrs[e], I, r0, r1, hb + (size_t)r * I,
+                                     o + (size_t)r * H);
+                }
             }
         }
         free(offsets);
