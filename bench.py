@@ -13,9 +13,15 @@ and combine, with the residual add), one fused persistent kernel launch.
   roofline  algorithmic bytes per launch (each layer's bf16 router plus each
             unique selected expert once) / mean launch time, against the
             measured HBM copy bandwidth;
-  cpu_baseline  the CPU oracle on a bounded sample of the same workload.
+  cpu_baseline  the CPU oracle on a bounded sample of the same workload;
+  configs   sub-records measured in the same run for the other workloads
+            (tiny layer, uniform-routing sweep B = 1..64, skewed-routing
+            sweep B = 1..128, prefill-sized layer): ms, tokens/s, algorithmic
+            bytes, GB/s and fraction of the peak, unique experts, reuse,
+            near-tie tokens and kernel launches per step.
 
 --impl reference times the CPU oracle itself on this workload (rank 0 only).
+--workload {uniform,skewed,prefill,tiny} times one layer of that workload.
 """
 from __future__ import annotations
 
@@ -54,6 +60,9 @@ def parse():
     ap.add_argument("--workload", default="stack", choices=["stack", "uniform", "skewed", "prefill", "tiny"],
                     help="stack = the 30-layer decode stack (the headline); the others time one layer")
     ap.add_argument("--batch", type=int, default=None, help="tokens per step for a single-layer workload")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the sub-records of the other workloads in the default run")
+    ap.add_argument("--config-steps", type=int, default=10, help="timed steps per sub-record")
     return ap.parse_args()
 
 
@@ -217,6 +226,18 @@ def oracle_stack_sample(layers_cpu_fn, x0_list, k, seconds, n_layers=30):
     return done, spent
 
 
+def cpu_model():
+    try:
+        for ln in open("/proc/cpuinfo"):
+            k = ln.split(":")[0].strip().lower()
+            if k in ("model name", "cpu part", "hardware"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
+
+
 def cpu_threads():
     try:
         return len(os.sched_getaffinity(0))
@@ -272,6 +293,7 @@ def run_reference(args):
         "data": "synthetic", "config": {"workload": w.name, "layers": w.layers, "B": w.B, "H": w.H,
                                          "I": w.I, "E": w.E, "top_k": w.top_k},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "cpu": cpu_model(),
                          "sample": f"{total_tok} whole tokens through all 30 layers (CPU-drawn weights)"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -279,10 +301,83 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------ single layer
+def near_tie_count(api, xs, lw, k, stream):
+    """Tokens whose k-th and (k+1)-th router logits are within 1e-5 (the
+    near ties the parity rules exempt), over the given inputs; None when
+    k == E.  Statistics only, computed outside any timed region."""
+    import torch
+    E = lw["w_router"].shape[0]
+    if k >= E:
+        return None
+    n = 0
+    for x in xs:
+        _, _, lg = api.route(x, lw["w_router"], k, bias=lw.get("bias"), stream=stream)
+        srt = torch.sort(lg, dim=1, descending=True).values
+        n += int(((srt[:, k - 1] - srt[:, k]) < 1e-5).sum())
+    return n
+
+
+def measure_layer(api, accounting, synth, w, dev, steps, warmup, flags=0, seed=0, flush=None, lw=None):
+    """One MoE layer per step on fresh inputs, L2 flushed before each timed
+    step, CUDA events on the launching stream.  Returns the sub-record."""
+    import numpy as np
+    import torch
+    lw = lw if lw is not None else synth.make_layer(w, 0, seed=seed, device=dev)
+    nsteps = warmup + steps
+    xs = [synth.make_x(w, s, seed=seed, device=dev) for s in range(nsteps)]
+    y = torch.empty((w.B, w.H), dtype=torch.float32, device=dev)
+    ids = torch.empty((w.B, w.top_k), dtype=torch.int32, device=dev)
+    rw = torch.empty((w.B, w.top_k), dtype=torch.float32, device=dev)
+    ws = api.new_workspace(w.B, w.H, w.I, w.E, w.top_k, dev)
+    status = api.new_status(dev)
+    flush = flush if flush is not None else torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        api.layer_forward(xs[i], lw["w_router"], lw["gate_up"], lw["down"], w.top_k, bias=lw["bias"],
+                          flags=flags, out=y, ids_out=ids, w_out=rw, workspace=ws, status=status,
+                          stream=stream)
+
+    for i in range(warmup):
+        flush.zero_()
+        step(i)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    uniq = []
+    launches = 0
+    for s in range(steps):
+        flush.zero_()
+        n0 = api.launch_count()
+        ev[s][0].record(stream)
+        step(warmup + s)
+        ev[s][1].record(stream)
+        launches += api.launch_count() - n0
+        uniq.append(ids.clone())
+    torch.cuda.synchronize()
+    st = int(status.item())
+    if st != 0:
+        raise SystemExit(f"{w.name} B={w.B}: device status {st}: {api.status_string(st)}")
+    times_ms = [a.elapsed_time(b) for a, b in ev]
+    mean_ms = statistics.mean(times_ms)
+    us = [len(np.unique(u.cpu().numpy())) for u in uniq]
+    bytes_step = statistics.mean(accounting.layer_bytes(w.H, w.I, w.E, u) for u in us)
+    achieved = bytes_step / (mean_ms / 1e3) / 1e9
+    peak, _ = hbm_peak()
+    try:
+        ties = near_tie_count(api, xs[warmup:], lw, w.top_k, stream)
+    except Exception as exc:  # statistics only: never fail the timing
+        print(f"near-tie count skipped: {exc}", file=sys.stderr)
+        ties = None
+    return {"workload": w.name, "B": w.B, "H": w.H, "I": w.I, "E": w.E, "top_k": w.top_k,
+            "ms": mean_ms, "tokens_per_s": w.B / (mean_ms / 1e3), "bytes_per_step": bytes_step,
+            "hbm_gbs": achieved, "frac": achieved / peak, "unique_experts": statistics.mean(us),
+            "reuse": statistics.mean(w.B * w.top_k / u for u in us), "near_tie_tokens": ties,
+            "launches_per_step": launches / steps, "steps": steps}
+
+
 def run_layer_workload(args):
     """One MoE layer per step (uniform / skewed / prefill-sized / tiny)."""
     rank, world, local = dist_env()
-    import numpy as np
     import torch
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -293,79 +388,63 @@ def run_layer_workload(args):
             "tiny": synth.TINY}[args.workload]
     w = base.with_batch(args.batch) if args.batch else base
     flags = api.MOE_F_UNFUSED if args.mode == "unfused" else 0
-    lw = synth.make_layer(w, 0, seed=args.seed, device=dev)
-    nsteps = args.warmup + args.steps
-    xs = [synth.make_x(w, s, seed=args.seed, device=dev) for s in range(nsteps)]
-    y = torch.empty((w.B, w.H), dtype=torch.float32, device=dev)
-    ids = torch.empty((w.B, w.top_k), dtype=torch.int32, device=dev)
-    rw = torch.empty((w.B, w.top_k), dtype=torch.float32, device=dev)
-    ws = api.new_workspace(w.B, w.H, w.I, w.E, w.top_k, dev)
-    status = api.new_status(dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
-    def step(i):
-        api.layer_forward(xs[i], lw["w_router"], lw["gate_up"], lw["down"], w.top_k, bias=lw["bias"],
-                          flags=flags, out=y, ids_out=ids, w_out=rw, workspace=ws, status=status,
-                          stream=stream)
-
-    for i in range(args.warmup):
-        flush.zero_()
-        step(i)
-    torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    uniq = []
     with ClockSampler(local) as clk:
-        torch.cuda.synchronize()
-        torch.cuda.nvtx.range_push("timed")
-        for s in range(args.steps):
-            flush.zero_()
-            ev[s][0].record(stream)
-            step(args.warmup + s)
-            ev[s][1].record(stream)
-            uniq.append(ids.clone())
-        torch.cuda.nvtx.range_pop()
-        torch.cuda.synchronize()
-    st = int(status.item())
-    if st != 0:
-        raise SystemExit(f"device status {st}: {api.status_string(st)}")
-    times_ms = [a.elapsed_time(b) for a, b in ev]
-    mean_ms = statistics.mean(times_ms)
-    us = [len(np.unique(u.cpu().numpy())) for u in uniq]
-    # routing statistics of the timed inputs, outside the timed region: tokens
-    # whose k-th and (k+1)-th logits are within 1e-5 (near ties)
-    near_ties = None
-    if w.top_k < w.E:
-        try:
-            near_ties = 0
-            for s in range(args.steps):
-                _, _, lg = api.route(xs[args.warmup + s], lw["w_router"], w.top_k, bias=lw["bias"], stream=stream)
-                srt = torch.sort(lg, dim=1, descending=True).values
-                near_ties += int(((srt[:, w.top_k - 1] - srt[:, w.top_k]) < 1e-5).sum())
-            torch.cuda.synchronize()
-        except Exception as exc:  # statistics only: never fail the timing line
-            print(f"near-tie count skipped: {exc}", file=sys.stderr)
-            near_ties = None
-    bytes_step = statistics.mean(accounting.layer_bytes(w.H, w.I, w.E, u) for u in us)
-    achieved = bytes_step / (mean_ms / 1e3) / 1e9
+        rec = measure_layer(api, accounting, synth, w, dev, args.steps, args.warmup, flags, args.seed)
     peak, peak_src = hbm_peak()
-    line = {"metric": METRIC, "value": w.B * args.steps / (sum(times_ms) / 1e3), "unit": "tokens/s",
-            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "weights_dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "H": w.H, "I": w.I, "E": w.E, "top_k": w.top_k,
-                       "mode": args.mode, "l2": "flushed before every timed step"},
-            "unique_experts_mean": statistics.mean(us),
-            "reuse_mean": statistics.mean(w.B * w.top_k / u for u in us),
-            "near_tie_tokens": near_ties, "hbm_gbs": achieved,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_source": peak_src, "traffic": None,
-                         "bytes_per_launch": bytes_step},
+    line = {"metric": METRIC, "value": rec["tokens_per_s"], "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": rec["ms"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "weights_dtype": "bf16",
+            "data": "synthetic", "mode": args.mode, "l2_flush": "256 MiB memset before every timed step",
+            "config": {"workload": w.name, "layers": 1, "B": w.B, "H": w.H, "I": w.I, "E": w.E,
+                       "top_k": w.top_k},
+            "unique_experts_mean": rec["unique_experts"], "reuse_mean": rec["reuse"],
+            "near_tie_tokens": rec["near_tie_tokens"], "hbm_gbs": rec["hbm_gbs"],
+            "roofline": {"bound": "hbm", "achieved": rec["hbm_gbs"], "peak": peak, "unit": "GB/s",
+                         "frac": rec["frac"], "peak_source": peak_src, "traffic": None,
+                         "bytes_per_launch": rec["bytes_per_step"]},
+            "gpu_launches": int(round(rec["launches_per_step"] * args.steps)),
             "clocks": clk.summary()}
     print(json.dumps(line), flush=True)
 
 
+def config_records(api, accounting, synth, dev, steps, warmup, seed=0):
+    """Sub-records for every workload besides the stack: the tiny layer, the
+    uniform-routing sweep, the skewed-routing sweep and the prefill-sized
+    layer (one layer per step each, measured in this run)."""
+    import torch
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    out = {}
+    out["tiny"] = measure_layer(api, accounting, synth, synth.TINY, dev, steps, warmup, 0, seed, flush)
+    for base in (synth.UNIFORM, synth.SKEWED):
+        lw = synth.make_layer(base, 0, seed=seed, device=dev)
+        for B in base.batches:
+            key = f"{'uniform' if base is synth.UNIFORM else 'skewed'}_B{B}"
+            out[key] = measure_layer(api, accounting, synth, base.with_batch(B), dev, steps, warmup, 0, seed,
+                                     flush, lw=lw)
+        del lw
+        torch.cuda.empty_cache()
+    out["prefill"] = measure_layer(api, accounting, synth, synth.PREFILL, dev, steps, warmup, 0, seed, flush)
+    torch.cuda.empty_cache()
+    return out
+
+
 # -------------------------------------------------------------------- ours
+def stack_near_ties(api, sw, layers, x0, k, stream):
+    """Near ties along one token's path through the stack (layer by layer,
+    outside the timed region): tokens x layers whose k-th and (k+1)-th logits
+    are within 1e-5."""
+    import torch
+    x = x0.clone()
+    n = 0
+    for lw in layers:
+        n += near_tie_count(api, [x], lw, k, stream) or 0
+        y, _, _ = api.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k, bias=lw.get("bias"),
+                                    residual=x, stream=stream)
+        x = y
+    torch.cuda.synchronize()
+    return n
+
+
 def run_ours(args):
     rank, world, local = dist_env()
     import numpy as np
@@ -410,6 +489,7 @@ def run_ours(args):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     uniq = []
+    launches = 0
     with ClockSampler(local) as clk:
         torch.cuda.synchronize()
         if pg:
@@ -419,10 +499,12 @@ def run_ours(args):
             i = args.warmup + s
             flush.zero_()
             xbuf.copy_(xs[i])
+            n0 = api.launch_count()
             ev[s][0].record(stream)
             api.stack_forward_(xbuf, sw, w.top_k, flags=flags, ids_out=ids, workspace=ws, status=status,
                                stream=stream)
             ev[s][1].record(stream)
+            launches += api.launch_count() - n0
             uniq.append(ids.clone())
         torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
@@ -434,18 +516,28 @@ def run_ours(args):
         raise SystemExit(f"device status {st}: {api.status_string(st)}")
     total_ms, value = job_throughput(sum(times_ms), w.B * args.steps, pg, dev)
     # algorithmic bytes: per layer the router + each unique selected expert once
-    bytes_steps = []
+    bytes_steps, u_layers = [], []
     for u in uniq:
         un = u.cpu().numpy()
-        bytes_steps.append(sum(accounting.layer_bytes(w.H, w.I, w.E, len(np.unique(un[l])))
-                               for l in range(w.layers)))
+        ul = [len(np.unique(un[l])) for l in range(w.layers)]
+        u_layers += ul
+        bytes_steps.append(sum(accounting.layer_bytes(w.H, w.I, w.E, n) for n in ul))
     bytes_per_launch = statistics.mean(bytes_steps)
     mean_ms = statistics.mean(times_ms)
     achieved = bytes_per_launch / (mean_ms / 1000.0) / 1e9
     peak, peak_src = hbm_peak()
     clocks = clk.summary()
+    ties = None
+    if rank == 0:
+        try:
+            ties = sum(stack_near_ties(api, sw, layers, xs[args.warmup + s], w.top_k, stream)
+                       for s in range(min(args.steps, 5)))
+        except Exception as exc:  # statistics only
+            print(f"near-tie count skipped: {exc}", file=sys.stderr)
 
-    # ---- e2e: public API, pinned host buffers, copies inside the timed region
+    # ---- e2e: public API, pinned host buffers, copies inside the timed
+    # region; no L2 flush (a user's call has none, and every step reads
+    # 582 MB of weights, over four times the 129 MB L2)
     e2e = None
     if not args.no_e2e:
         xh = [xs[args.warmup + s].cpu().pin_memory() for s in range(args.steps)]
@@ -453,41 +545,35 @@ def run_ours(args):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for s in range(args.steps):
-            flush.zero_()
             xbuf.copy_(xh[s], non_blocking=True)
             api.stack_forward_(xbuf, sw, w.top_k, flags=flags, ids_out=ids, workspace=ws, status=status,
                                stream=stream)
             out_h.copy_(xbuf, non_blocking=True)
             stream.synchronize()
         e2e_s = time.perf_counter() - t0
-        # the L2 flush is not part of the user's call: subtract its device time
-        fe = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-        fe[0].record(stream)
-        for _ in range(args.steps):
-            flush.zero_()
-        fe[1].record(stream)
-        torch.cuda.synchronize()
-        e2e_s -= fe[0].elapsed_time(fe[1]) / 1000.0
         nbytes = xh[0].numel() * 4
         e2e = {"value": w.B * args.steps * world / e2e_s, "unit": "tokens/s",
-               "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes}
+               "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes,
+               "l2_flush": "none (per-step weights exceed L2)"}
 
-    launches_per_step = 1 if args.mode == "fused" else 6 * w.layers
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "weights_dtype": "bf16", "data": "synthetic",
+        "mode": args.mode, "l2_flush": "256 MiB memset before every timed step, outside the events",
         "config": {"workload": w.name, "layers": w.layers, "B": w.B, "H": w.H, "I": w.I, "E": w.E,
-                   "top_k": w.top_k, "mode": args.mode,
-                   "l2": "flushed before every timed step (256 MiB memset, outside the events)"},
+                   "top_k": w.top_k},
         "hbm_gbs": achieved,
         "us_per_layer": 1000.0 * mean_ms / w.layers,
+        "unique_experts_per_layer": statistics.mean(u_layers),
+        "reuse": w.B * w.top_k / statistics.mean(u_layers),
+        "near_tie_token_layers": ties,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_src,
                      "traffic": recorded_traffic("moe_stack_fused", w.name),
                      "kernel": "decode_kernel (one launch = 30 layers)",
                      "bytes_per_launch": bytes_per_launch},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": launches,
         "clocks": clocks,
         "e2e": e2e,
     }
@@ -513,8 +599,13 @@ def run_ours(args):
         n, t = oracle_stack_sample(layer_cpu, x_np, w.top_k, args.cpu_seconds, w.layers)
         line["cpu_baseline"] = {"value": n * w.B / t, "unit": "tokens/s",
                                 "cores": int(os.environ["OMP_NUM_THREADS"]), "kind": "oracle",
+                                "cpu": cpu_model(),
                                 "sample": f"{n} whole tokens through all {w.layers} layers (same weights, "
                                           f"{t:.1f} s of oracle time)"}
+    if rank == 0 and not args.no_configs and world == 1:
+        del layers, sw
+        torch.cuda.empty_cache()
+        line["configs"] = config_records(api, accounting, synth, dev, args.config_steps, 3, args.seed)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg:

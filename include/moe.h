@@ -64,6 +64,7 @@ typedef enum {
 #define MOE_DEV_BAD_EXPERT_ID 2  /* an expert id outside [0, E)              */
 #define MOE_DEV_DUP_EXPERT 4     /* one token lists the same expert twice    */
 #define MOE_DEV_NONFINITE 8      /* a router logit was NaN or infinite       */
+#define MOE_DEV_BAD_ROUTE 16     /* a route_idx entry outside [0, B*top_k)    */
 
 /* activation dtypes */
 typedef enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 } moe_dtype;
@@ -141,6 +142,10 @@ int moe_group_by_expert(const int32_t* expert_ids, int B, int top_k, int E, int3
  *      the grouping from moe_group_by_expert (offsets, route_idx,
  *      unique_experts, num_unique), residual [B,H] fp32 or NULL.
  * Out: y [B,H] fp32.  y may alias residual (in-place residual add).
+ * A grouping handed in is used only within bounds: a unique-expert count
+ * above min(B*top_k, E), expert ids outside [0, E) and offsets outside
+ * [0, B*top_k] drop the segment; a route_idx entry outside [0, B*top_k) sets
+ * MOE_DEV_BAD_ROUTE (route 0 is used in its place).  y is then not valid.
  */
 int moe_expert_forward(const void* x, int x_dtype, const uint16_t* gate_up, const uint16_t* down,
                        const int32_t* expert_ids, const float* route_w, const int32_t* offsets,
@@ -155,10 +160,12 @@ int moe_expert_forward(const void* x, int x_dtype, const uint16_t* gate_up, cons
  * replayed, an allocator hook that must not re-enter the allocator, a
  * runtime with a fixed memory budget).  The pages have no counterpart: this
  * is an interface convenience, not part of the method.
- * Same arguments and results as moe_expert_forward, minus the workspace:
- * the scratch (h [R,I] and o [R,H], fp32) lives in one static device array
- * of MOE_NOALLOC_SCRATCH_BYTES inside the library, held on every GPU that
- * loads the library until the process exits.  Problems needing more than
+ * Same arguments and results as moe_expert_forward, minus the workspace,
+ * except that every expert runs on the CUDA-core GEMV kernels (the tensor-
+ * core path needs operand buffers of its own): MOE_F_FORCE_TC returns
+ * MOE_ERR_UNSUPPORTED.  The scratch (h [R,I] and o [R,H], fp32) lives in
+ * one static device array of MOE_NOALLOC_SCRATCH_BYTES inside the library,
+ * held on every GPU that loads the library until the process exits.  Problems needing more than
  * that (4*R*(I+H) bytes plus alignment, R = B*top_k) return
  * MOE_ERR_WORKSPACE before anything is enqueued.  Nothing is allocated or
  * freed.  The first call on a device looks up the array's device address
@@ -211,6 +218,23 @@ int moe_stack_forward(int L, const uint16_t* const* w_router, const float* const
                       int32_t* dev_status, void* stream);
 
 /*
+ * moe_workspace_grouping -- where a workspace holds the grouped route list
+ * of the last layer a forward call computed in it (moe_layer_forward, and
+ * the last layer of moe_stack_forward), in the layout of
+ * moe_group_by_expert: offsets [E+1], route_idx [B*top_k], unique_experts
+ * [E] (first *num_unique valid), num_unique [1].  Host-only pointer
+ * arithmetic: the four outputs receive DEVICE addresses inside `workspace`
+ * (same shape arguments as the forward call), valid after that call has
+ * completed on its stream (unspecified with MOE_F_NO_DEDUP).  Exposes the
+ * grouping the layer itself used, so that it can be checked against
+ * moe_group_by_expert's definition ("perf(cpu-moe): dedup experts across
+ * the batch in pass 1 - #46", commit message: the counting sort).
+ */
+int moe_workspace_grouping(void* workspace, size_t workspace_bytes, int B, int H, int I, int E, int top_k,
+                           int32_t** offsets, int32_t** route_idx, int32_t** unique_experts,
+                           int32_t** num_unique);
+
+/*
  * moe_set_trace_buffer -- profiling aid.  While set, every launch of the
  * persistent decode kernel records, per CTA, per layer and per phase
  * boundary, a pair of 64-bit words (globaltimer ns, SM clock) into the device
@@ -241,6 +265,14 @@ int moe_set_trace_buffer(unsigned long long* trace, int words);
  * outside [0, 1024].  Host-only setting, not thread-safe.
  */
 int moe_inject_barrier_stall(int extra_arrivals);
+
+/*
+ * moe_launch_count -- how many CUDA kernels the library has launched in this
+ * process so far (all devices, all entry points; a relaxed atomic counter).
+ * For measurement: the difference around a timed region is the number of
+ * the library's kernel launches in it.  Host-only; never fails.
+ */
+unsigned long long moe_launch_count(void);
 
 /* moe_status_string -- static text for a moe_status code or MOE_DEV_* bit. */
 const char* moe_status_string(int code);

@@ -37,6 +37,10 @@ _lib.moe_expert_forward_noalloc.argtypes = [_P, _I, _P, _P, _P, _P, _P, _P, _P, 
 _lib.moe_layer_forward.argtypes = [_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _U,
                                    _P, _S, _P, _P]
 _lib.moe_stack_forward.argtypes = [_I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _U, _P, _S, _P, _P]
+_lib.moe_workspace_grouping.argtypes = [_P, _S, _I, _I, _I, _I, _I, ctypes.POINTER(_P), ctypes.POINTER(_P),
+                                        ctypes.POINTER(_P), ctypes.POINTER(_P)]
+_lib.moe_launch_count.argtypes = []
+_lib.moe_launch_count.restype = ctypes.c_ulonglong
 _lib.moe_set_trace_buffer.argtypes = [_P, _I]
 _lib.moe_set_trace_buffer.restype = ctypes.c_int
 _lib.moe_inject_barrier_stall.argtypes = [_I]
@@ -44,11 +48,12 @@ _lib.moe_inject_barrier_stall.restype = ctypes.c_int
 _lib.moe_status_string.argtypes = [_I]
 _lib.moe_status_string.restype = ctypes.c_char_p
 for _f in ("moe_workspace_bytes", "moe_route", "moe_group_by_expert", "moe_expert_forward",
-           "moe_expert_forward_noalloc", "moe_layer_forward", "moe_stack_forward"):
+           "moe_expert_forward_noalloc", "moe_layer_forward", "moe_stack_forward", "moe_workspace_grouping"):
     getattr(_lib, _f).restype = ctypes.c_int
 
 EXPORTED = ("moe_workspace_bytes", "moe_route", "moe_group_by_expert", "moe_expert_forward",
-            "moe_expert_forward_noalloc", "moe_layer_forward", "moe_stack_forward", "moe_set_trace_buffer",
+            "moe_expert_forward_noalloc", "moe_layer_forward", "moe_stack_forward", "moe_workspace_grouping",
+            "moe_launch_count", "moe_set_trace_buffer",
             "moe_inject_barrier_stall", "moe_status_string")
 
 MOE_OK = 0
@@ -125,8 +130,38 @@ def _opt(t, dtype, name, device):
 
 def _need_x(x):
     _x_dtype(x)
+    if x.dim() != 2:
+        raise ValueError(f"x has shape {tuple(x.shape)}, expected [B, H]")
     if not x.is_cuda or not x.is_contiguous():
         raise ValueError("x must be a contiguous CUDA tensor")
+
+
+def _shape(t, shape, name):
+    """t (when given) must have exactly this shape; None entries match any size.
+    Checked before any pointer reaches the library: a short buffer would be
+    read or written out of bounds on the device."""
+    if t is None:
+        return
+    if t.dim() != len(shape) or any(s is not None and d != s for d, s in zip(t.shape, shape)):
+        want = "[" + ", ".join("*" if s is None else str(s) for s in shape) + "]"
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {want}")
+
+
+def _at_least(t, n, name):
+    if t.dim() != 1 or t.numel() < n:
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected 1-D with at least {n} entries")
+
+
+def _expert_shapes(x, gate_up, down):
+    """-> (B, H, I, E) from x [B,H], gate_up [E,2I,H] and down [E,H,I]."""
+    if x.dim() != 2:
+        raise ValueError(f"x has shape {tuple(x.shape)}, expected [B, H]")
+    B, H = x.shape
+    if gate_up.dim() != 3 or gate_up.shape[1] % 2 or gate_up.shape[2] != H:
+        raise ValueError(f"gate_up has shape {tuple(gate_up.shape)}, expected [E, 2I, {H}]")
+    E, I = gate_up.shape[0], gate_up.shape[1] // 2
+    _shape(down, (E, H, I), "down")
+    return B, H, I, E
 
 
 def set_trace_buffer(buf):
@@ -157,12 +192,38 @@ def new_workspace(B, H, I, E, top_k, device=None) -> torch.Tensor:
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
 
 
+def workspace_grouping(workspace, B, H, I, E, top_k):
+    """The grouped route list that the last forward call left in `workspace`
+    -> (offsets [E+1], route_idx [B*k], unique [E], num_unique [1]) int32
+    views into it (read them after that call has completed)."""
+    _need(workspace, torch.uint8, "workspace")
+    outs = [_P() for _ in range(4)]
+    _check(_lib.moe_workspace_grouping(_ptr(workspace), workspace.numel(), B, H, I, E, top_k,
+                                       *[ctypes.byref(o) for o in outs]), "moe_workspace_grouping")
+    base = workspace.data_ptr()
+    views = []
+    for o, n in zip(outs, (E + 1, B * top_k, E, 1)):
+        off = o.value - base
+        views.append(workspace[off:off + 4 * n].view(torch.int32))
+    return tuple(views)
+
+
+def launch_count() -> int:
+    """Kernels the library has launched in this process so far."""
+    return int(_lib.moe_launch_count())
+
+
 def new_status(device=None) -> torch.Tensor:
     return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
 
 
 def route(x, w_router, top_k, bias=None, stream=None, status=None):
     """-> (expert_ids [B,k] int32, route_w [B,k] fp32, logits [B,E] fp32)."""
+    if x.dim() != 2 or w_router.dim() != 2:
+        raise ValueError(f"x {tuple(x.shape)} and w_router {tuple(w_router.shape)} must be [B, H] and [E, H]")
+    _shape(w_router, (None, x.shape[1]), "w_router")
+    _shape(bias, (w_router.shape[0],), "bias")
+    _shape(status, (1,), "status")
     _need_x(x)
     _need(w_router, torch.bfloat16, "w_router")
     _opt(bias, torch.float32, "bias", x.device)
@@ -179,6 +240,9 @@ def route(x, w_router, top_k, bias=None, stream=None, status=None):
 
 def group_by_expert(expert_ids, E, stream=None, status=None):
     """-> (offsets [E+1], route_idx [R], unique [E] (first num_unique valid), num_unique [1])."""
+    if expert_ids.dim() != 2:
+        raise ValueError(f"expert_ids has shape {tuple(expert_ids.shape)}, expected [B, top_k]")
+    _shape(status, (1,), "status")
     _need(expert_ids, torch.int32, "expert_ids")
     B, k = expert_ids.shape
     dev = expert_ids.device
@@ -193,6 +257,22 @@ def group_by_expert(expert_ids, E, stream=None, status=None):
 
 
 def _check_expert_args(x, gate_up, down, expert_ids, route_w, grouping, residual, out, status):
+    B, H, I, E = _expert_shapes(x, gate_up, down)
+    if expert_ids is None or route_w is None:
+        raise ValueError("expert_ids and route_w are required")
+    if expert_ids.dim() != 2 or expert_ids.shape[0] != B:
+        raise ValueError(f"expert_ids has shape {tuple(expert_ids.shape)}, expected [{B}, top_k]")
+    k = expert_ids.shape[1]
+    _shape(route_w, (B, k), "route_w")
+    if grouping is None or len(grouping) != 4 or any(t is None for t in grouping):
+        raise ValueError("grouping must be (offsets, route_idx, unique_experts, num_unique)")
+    R = B * k
+    for t, n, need in zip(grouping, ("offsets", "route_idx", "unique_experts", "num_unique"),
+                          (E + 1, R, min(R, E), 1)):
+        _at_least(t, need, n)
+    _shape(residual, (B, H), "residual")
+    _shape(out, (B, H), "out")
+    _shape(status, (1,), "status")
     _need_x(x)
     _need(gate_up, torch.bfloat16, "gate_up")
     _need(down, torch.bfloat16, "down")
@@ -248,6 +328,12 @@ def expert_forward_noalloc(x, gate_up, down, expert_ids, route_w, grouping, resi
 def layer_forward(x, w_router, gate_up, down, top_k, bias=None, residual=None, flags=0, out=None,
                   ids_out=None, w_out=None, workspace=None, status=None, stream=None):
     """Whole layer -> (y [B,H] fp32, expert_ids [B,k], route_w [B,k])."""
+    B, H, I, E = _expert_shapes(x, gate_up, down)
+    _shape(w_router, (E, H), "w_router")
+    _shape(bias, (E,), "bias")
+    for t, shp, n in ((residual, (B, H), "residual"), (out, (B, H), "out"), (ids_out, (B, top_k), "ids_out"),
+                      (w_out, (B, top_k), "w_out"), (status, (1,), "status")):
+        _shape(t, shp, n)
     _need_x(x)
     for t, n in ((w_router, "w_router"), (gate_up, "gate_up"), (down, "down")):
         _need(t, torch.bfloat16, n)
@@ -285,9 +371,15 @@ class StackWeights:
         self.bias = ((ctypes.c_void_p * L)(*[(l["bias"].data_ptr() if l.get("bias") is not None else None)
                                              for l in layers]) if has_bias else None)
         g = layers[0]["gate_up"]
+        if g.dim() != 3 or g.shape[1] % 2:
+            raise ValueError(f"gate_up has shape {tuple(g.shape)}, expected [E, 2I, H]")
         self.E, twoI, self.H = g.shape
         self.I = twoI // 2
         for l in layers:
+            _shape(l["w_router"], (self.E, self.H), "w_router")
+            _shape(l["gate_up"], (self.E, 2 * self.I, self.H), "gate_up")
+            _shape(l["down"], (self.E, self.H, self.I), "down")
+            _shape(l.get("bias"), (self.E,), "bias")
             for n in ("w_router", "gate_up", "down"):
                 _need(l[n], torch.bfloat16, n)
             if l.get("bias") is not None:
@@ -297,6 +389,10 @@ class StackWeights:
 def stack_forward_(x, stack: StackWeights, top_k, flags=0, ids_out=None, workspace=None, status=None,
                    stream=None):
     """In place: x [B,H] fp32 <- x + layer_l(x) for every layer.  Returns x."""
+    if x.dim() != 2 or stack is None or x.shape[1] != stack.H:
+        raise ValueError(f"x has shape {tuple(x.shape)}, expected [B, H] with H of the stack's weights")
+    _shape(ids_out, (stack.L, x.shape[0], top_k), "ids_out")
+    _shape(status, (1,), "status")
     _need(x, torch.float32, "x")
     for t, dt, n in ((ids_out, torch.int32, "ids_out"), (workspace, torch.uint8, "workspace"),
                      (status, torch.int32, "status")):

@@ -10,6 +10,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "moe.h"
@@ -240,7 +241,20 @@ static int to_status(cudaError_t e) {
     return MOE_ERR_CUDA;
 }
 
-static int launch_check() { return to_status(cudaGetLastError()); }
+// Kernels this library has launched in the process (every launch site goes
+// through launch_check or launch_ex), for measurement: moe_launch_count().
+static std::atomic<unsigned long long> g_launches{0};
+
+static int launch_check() {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return to_status(cudaGetLastError());
+}
+
+template <typename K, typename... Args>
+static int launch_ex(const cudaLaunchConfig_t& cfg, K kernel, Args... args) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return to_status(cudaLaunchKernelEx(&cfg, kernel, args...));
+}
 
 // dynamic shared memory above 48 KB needs an opt-in per kernel and device
 template <typename K>
@@ -531,7 +545,7 @@ static int launch_fused(const Ctx& c, const StackArgs& sa, unsigned* bar, cudaSt
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return to_status(cudaLaunchKernelEx(&cfg, fused_kernel, c, sa, bar));
+    return launch_ex(cfg, fused_kernel, c, sa, bar);
 }
 
 
@@ -608,6 +622,10 @@ static int launch_decode(DkParams& p, size_t smem, int sms, char* ws, const WsLa
     }
     p.acc = reinterpret_cast<unsigned long long*>(ws + L.acc);
     p.bar = reinterpret_cast<unsigned*>(ws + L.bar);
+    p.g_offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+    p.g_route_idx = reinterpret_cast<int32_t*>(ws + L.route_idx);
+    p.g_unique = reinterpret_cast<int32_t*>(ws + L.unique);
+    p.g_num_unique = reinterpret_cast<int32_t*>(ws + L.num_unique);
     if ((rc = to_status(cudaMemsetAsync(ws + L.bar, 0, L.acc_end - L.bar, st)))) return rc;
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
@@ -620,7 +638,7 @@ static int launch_decode(DkParams& p, size_t smem, int sms, char* ws, const WsLa
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return to_status(cudaLaunchKernelEx(&cfg, kernel, p));
+    return launch_ex(cfg, kernel, p);
 }
 
 static unsigned long long* g_trace = nullptr;
@@ -873,6 +891,24 @@ int moe_stack_forward(int Lc, const uint16_t* const* w_router, const float* cons
     return launch_fused(c, sa, reinterpret_cast<unsigned*>(ws + L.bar), st);
 }
 
+int moe_workspace_grouping(void* workspace, size_t workspace_bytes, int B, int H, int I, int E, int top_k,
+                           int32_t** offsets, int32_t** route_idx, int32_t** unique_experts,
+                           int32_t** num_unique) {
+    const int rc = check_dims(B, H, I, E, top_k, true);
+    if (rc) return rc;
+    if (!workspace || !offsets || !route_idx || !unique_experts || !num_unique) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(B, H, I, E, top_k);
+    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+    char* ws = static_cast<char*>(workspace);
+    *offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+    *route_idx = reinterpret_cast<int32_t*>(ws + L.route_idx);
+    *unique_experts = reinterpret_cast<int32_t*>(ws + L.unique);
+    *num_unique = reinterpret_cast<int32_t*>(ws + L.num_unique);
+    return MOE_OK;
+}
+
+unsigned long long moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
 int moe_inject_barrier_stall(int extra_arrivals) {
     if (extra_arrivals < 0 || extra_arrivals > 1024) return MOE_ERR_INVALID_ARG;
     g_bar_extra = (unsigned)extra_arrivals;
@@ -897,6 +933,7 @@ const char* moe_status_string(int code) {
         case MOE_DEV_BAD_EXPERT_ID: return "device: expert id outside [0, E)";
         case MOE_DEV_DUP_EXPERT: return "device: a token lists the same expert twice";
         case MOE_DEV_NONFINITE: return "device: non-finite router logit";
+        case MOE_DEV_BAD_ROUTE: return "device: route index outside [0, B*top_k)";
         default: return "unknown status";
     }
 }
@@ -952,6 +989,7 @@ extern "C" int moe_expert_forward_noalloc(const void* x, int x_dtype, const uint
     if (rc) return rc;
     if (x_dtype != MOE_DT_F32 && x_dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
     if (flags & ~(MOE_F_NO_DEDUP | MOE_F_UNFUSED | MOE_F_FORCE_TC | MOE_F_NO_TC)) return MOE_ERR_INVALID_ARG;
+    if (flags & MOE_F_FORCE_TC) return MOE_ERR_UNSUPPORTED;  // no operand buffers for the tensor cores here
     const size_t R = (size_t)B * top_k;
     const size_t h_bytes = align_up(sizeof(float) * R * I, 256);
     if (h_bytes + sizeof(float) * R * H > MOE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;

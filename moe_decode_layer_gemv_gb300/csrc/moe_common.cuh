@@ -130,7 +130,9 @@ __device__ __forceinline__ bool get_seg(const Ctx& c, int s, Seg& sg) {
         sg.p0 = s;
         sg.p1 = s + 1;
     } else {
-        if (s >= ld_act_i(c.num_unique)) return false;
+        // a caller-supplied count is trusted only up to the segment capacity
+        const int nu = ld_act_i(c.num_unique);
+        if (s >= nu || s >= max_segments(c)) return false;
         sg.e = ld_act_i(c.unique + s);
         sg.p0 = ld_act_i(c.offsets + sg.e);
         sg.p1 = ld_act_i(c.offsets + sg.e + 1);
@@ -139,9 +141,19 @@ __device__ __forceinline__ bool get_seg(const Ctx& c, int s, Seg& sg) {
     return sg.e >= 0 && sg.e < c.E && sg.p0 >= 0 && sg.p1 > sg.p0 && sg.p1 <= c.B * c.k;
 }
 
-// flat route index r stored at position p of the (grouped) route list
+// flat route index r stored at position p of the (grouped) route list.  A
+// caller-supplied entry outside [0, B*k) would index x and the per-route
+// outputs out of bounds: it is flagged (MOE_DEV_BAD_ROUTE) and replaced by
+// route 0, so every access stays inside the buffers (the result is then
+// not valid, as the status word says).
 __device__ __forceinline__ int route_at(const Ctx& c, int p) {
-    return no_dedup(c) ? p : ld_act_i(c.route_idx + p);
+    if (no_dedup(c)) return p;
+    const int r = ld_act_i(c.route_idx + p);
+    if (r < 0 || r >= c.B * c.k) {
+        set_status(c.status, MOE_DEV_BAD_ROUTE);
+        return 0;
+    }
+    return r;
 }
 
 }  // namespace moe

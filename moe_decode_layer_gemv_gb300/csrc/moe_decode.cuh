@@ -48,6 +48,9 @@ struct DkParams {
     LayerWeights layer[MOE_MAX_LAYERS];
     int32_t* ids_out;  // [L, B, k] or nullptr
     float* w_out;      // [B, k] (single layer) or nullptr
+    // the grouped route list of the layer, as moe_group_by_expert lays it
+    // out (written by CTA 0; a stack leaves its last layer's)
+    int32_t *g_offsets, *g_route_idx, *g_unique, *g_num_unique;
     float* h;          // [R, I] exchange buffer
     unsigned long long* acc;  // [2][kDkShadows][B][E] fixed-point logits
     float* alog;              // [B][E] next layer's logits predicted from this layer's input
@@ -351,6 +354,23 @@ __device__ void dk_group(DkMisc* m, int R, int E, bool no_dedup) {
         m->seg_p[U] = R;
     }
     __syncwarp();
+}
+
+// The CTA's grouping in the layout of moe_group_by_expert (one warp):
+// offsets[e] = routes whose expert id is below e, route_idx = the routes in
+// grouped order, unique = the segments' experts, num_unique = U.
+__device__ __forceinline__ void dk_store_grouping(const DkParams& p, const DkMisc* m, int R, int E) {
+    const int lane = threadIdx.x & 31;
+    const int U = m->U;
+    for (int e = lane; e <= E; e += 32) {
+        int off = 0;
+        for (int u = 0; u < U; ++u)
+            if (m->seg_e[u] < e) off += m->seg_p[u + 1] - m->seg_p[u];
+        p.g_offsets[e] = off;
+    }
+    if (lane < R) p.g_route_idx[lane] = m->rat[lane];
+    if (lane < U) p.g_unique[lane] = m->seg_e[lane];
+    if (lane == 0) *p.g_num_unique = U;
 }
 
 // Sum of N values held by every lane over the 32 lanes of a warp; the N
@@ -761,6 +781,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
             if (blockIdx.x == 0) {
                 if (p.ids_out && lane < R) p.ids_out[(size_t)l * R + lane] = m->ids[lane];
                 if (p.w_out && lane < R) p.w_out[lane] = m->w[lane];
+                if (p.g_offsets && !no_dedup) dk_store_grouping(p, m, R, E);
             }
             if (tid == 0) dk_trace<kTrace>(p, l, 9);
             named_arrive(4, kDkThreads);

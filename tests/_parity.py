@@ -89,8 +89,28 @@ def layer_weights_np(lw):
             "bias": None if lw.get("bias") is None else lw["bias"].detach().cpu().numpy()}
 
 
+def oracle_weights_for(logits_o, ids_use):
+    """The oracle's routing weights for a given choice of experts: oracle.topk
+    on the oracle's logits with every expert outside the choice masked to
+    -inf (its softmax term is then exactly 0, so the renormalised weights are
+    those of the chosen experts), returned in the order of ids_use."""
+    lo = np.asarray(logits_o, np.float32)
+    ids_use = np.asarray(ids_use)
+    B, k = ids_use.shape
+    rows = np.arange(B)[:, None]
+    masked = np.full_like(lo, -np.inf)
+    masked[rows, ids_use] = lo[rows, ids_use]
+    ids_m, w_m = oracle.topk(masked, k)
+    w = np.empty((B, k), np.float32)
+    for t in range(B):
+        pos = {int(e): j for j, e in enumerate(ids_m[t])}
+        w[t] = [w_m[t, pos[int(e)]] for e in ids_use[t]]
+    return w
+
+
 def oracle_layer_following(x, lw_np, k, ids_gpu, residual=None):
-    """Oracle layer using the GPU's ids where they differ only on near ties."""
+    """Oracle layer using the GPU's ids where they differ only on near ties
+    (their weights from the oracle as well, for the GPU's choice)."""
     xn = np_x(x)
     lo = oracle.router(xn, lw_np["w_router"], lw_np["bias"])
     ids_o, w_o = oracle.topk(lo, k)
@@ -99,14 +119,42 @@ def oracle_layer_following(x, lw_np, k, ids_gpu, residual=None):
     if ex.any():
         ig = ids_gpu.cpu().numpy()
         ids[ex] = ig[ex]
-        # weights for the GPU's choice: softmax of the chosen logits, renormalised
-        for t in np.nonzero(ex)[0]:
-            l = lo[t]
-            m = np.max(l)
-            p = np.exp((l - m).astype(np.float32)).astype(np.float32)
-            p = p / p.sum(dtype=np.float32)
-            sel = p[ids[t]]
-            w_o[t] = sel / sel.sum(dtype=np.float32)
+        w_o[ex] = oracle_weights_for(lo[ex], ids[ex])
     E = lw_np["w_router"].shape[0]
     y = oracle.experts(xn, lw_np["gate_up"], lw_np["down"], ids, w_o, E, residual=residual)
     return y, ids, int(ex.sum())
+
+
+def check_layer_routing(x, wr, bias, k, ids_g, w_g, logits_o=None):
+    """The ids and routing weights a forward call itself returned, against the
+    oracle: ids in order (as a set where two selected logits are within
+    NEAR_TIE; exempt where the k-th/(k+1)-th margin is), and the weights of
+    the GPU's choice within W_TOL of the oracle's weights for that choice.
+    Returns the number of exempt (near-tie) tokens."""
+    xn = np_x(x)
+    lo = logits_o if logits_o is not None else oracle.router(
+        xn, synth.bf16_bits(wr), None if bias is None else bias.detach().cpu().numpy())
+    ids_o, _ = oracle.topk(lo, k)
+    ex = margins(lo, k) < NEAR_TIE
+    srt = -np.sort(-lo.astype(np.float64), axis=1)[:, :k]
+    inner = np.any(np.diff(srt, axis=1) > -NEAR_TIE, axis=1) if k > 1 else np.zeros(len(lo), bool)
+    ig = ids_g.cpu().numpy()
+    strict = ~ex & ~inner
+    assert np.array_equal(ig[strict], ids_o[strict])
+    assert np.array_equal(np.sort(ig[~ex], axis=1), np.sort(ids_o[~ex], axis=1))
+    wg = w_g.cpu().numpy()
+    w_for = oracle_weights_for(lo, ig)
+    assert np.max(np.abs(wg - w_for), initial=0.0) <= W_TOL, float(np.max(np.abs(wg - w_for)))
+    return int(ex.sum())
+
+
+def check_grouping(api, ws, ids_g, B, H, I, E, k):
+    """The grouped route list the layer left in its workspace, bit-exact
+    against the oracle's counting sort of the layer's own ids."""
+    off, ridx, uniq, nu = api.workspace_grouping(ws, B, H, I, E, k)
+    off_o, ridx_o, uniq_o = oracle.group(ids_g.cpu().numpy(), E)
+    assert np.array_equal(off.cpu().numpy(), off_o)
+    assert np.array_equal(ridx.cpu().numpy(), ridx_o)
+    n = int(nu.item())
+    assert n == len(uniq_o)
+    assert np.array_equal(uniq.cpu().numpy()[:n], uniq_o)

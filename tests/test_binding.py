@@ -21,7 +21,7 @@ def api():
 def test_binding_names_every_declared_entry_point(api):
     src = open(os.path.join(ROOT, "include", "moe.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    declared = set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(moe_\w+)\s*\(", src, flags=re.M))
+    declared = set(re.findall(r"^\s*(?:const\s+)?(?:\w+\s+)*\w+\s*\*?\s*(moe_\w+)\s*\(", src, flags=re.M))
     assert declared == set(api.EXPORTED)
 
 
@@ -79,3 +79,42 @@ def test_workspace_grows_with_the_batch(api):
 def test_status_strings_name_the_device_bits(api):
     assert "timed out" in api.status_string(api.MOE_DEV_TIMEOUT)
     assert api.status_string(api.MOE_OK)
+
+
+def test_mismatched_shapes_are_refused_before_any_launch(api):
+    """A buffer shorter than the problem needs would be read or written out
+    of bounds on the device: every shape is checked in the binding first."""
+    B, H, I, E, k = 3, 64, 32, 8, 2
+    x = torch.zeros(B, H)
+    wr = torch.zeros(E, H, dtype=torch.bfloat16)
+    gu = torch.zeros(E, 2 * I, H, dtype=torch.bfloat16)
+    dn = torch.zeros(E, H, I, dtype=torch.bfloat16)
+    ids = torch.zeros(B, k, dtype=torch.int32)
+    rw = torch.zeros(B, k)
+    grouping = tuple(torch.zeros(n, dtype=torch.int32) for n in (E + 1, B * k, E, 1))
+    shape = "shape"
+    with pytest.raises(ValueError, match=shape):  # gate_up's H disagrees with x
+        api.layer_forward(x, wr, gu[:, :, :32], dn, k)
+    with pytest.raises(ValueError, match=shape):  # down's I disagrees with gate_up
+        api.layer_forward(x, wr, gu, dn[:, :, :16], k)
+    with pytest.raises(ValueError, match=shape):  # router rows != E
+        api.layer_forward(x, wr[:4], gu, dn, k)
+    with pytest.raises(ValueError, match=shape):  # out too small
+        api.layer_forward(x, wr, gu, dn, k, out=torch.zeros(B - 1, H))
+    with pytest.raises(ValueError, match=shape):  # ids_out of the wrong top_k
+        api.layer_forward(x, wr, gu, dn, k, ids_out=torch.zeros(B, k + 1, dtype=torch.int32))
+    with pytest.raises(ValueError, match=shape):  # bias of the wrong length
+        api.route(x, wr, k, bias=torch.zeros(E - 1))
+    for bad in ((torch.zeros(E, dtype=torch.int32),) + grouping[1:],          # offsets [E] < E+1
+                grouping[:1] + (torch.zeros(B * k - 1, dtype=torch.int32),) + grouping[2:],  # route_idx
+                grouping[:3] + (torch.zeros(0, dtype=torch.int32),)):         # num_unique
+        with pytest.raises(ValueError, match=shape):
+            api.expert_forward(x, gu, dn, ids, rw, bad)
+        with pytest.raises(ValueError, match=shape):
+            api.expert_forward_noalloc(x, gu, dn, ids, rw, bad)
+    with pytest.raises(ValueError, match=shape):  # route_w of the wrong shape
+        api.expert_forward(x, gu, dn, ids, rw[:, :1], grouping)
+    with pytest.raises(ValueError, match="required"):
+        api.expert_forward_noalloc(x, gu, dn, None, rw, grouping)
+    with pytest.raises(ValueError, match=shape):  # residual too small
+        api.expert_forward(x, gu, dn, ids, rw, grouping, residual=torch.zeros(B, H // 2))

@@ -9,7 +9,8 @@ import torch
 
 import oracle
 from moe_decode_layer_gemv_gb300 import synth
-from _parity import (check_route, check_y, layer_weights_np, np_x, oracle_layer_following)
+from _parity import (check_grouping, check_layer_routing, check_route, check_y, layer_weights_np, np_x,
+                     oracle_layer_following)
 
 pytestmark = pytest.mark.gpu
 
@@ -92,13 +93,18 @@ def test_group_flags_bad_and_duplicate_ids(cuda_lib):
 def test_layer_parity(cuda_lib, B, H, I, E, k, flags):
     _, lw, x = make_case(B, H, I, E, k, seed=3 * B + I)
     st = cuda_lib.new_status()
+    ws = cuda_lib.new_workspace(B, H, I, E, k)
     y, ids, w = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k, flags=flags,
-                                       status=st)
+                                       workspace=ws, status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     lnp = layer_weights_np(lw)
     y_o, _, _ = oracle_layer_following(x, lnp, k, ids)
     check_y(y, y_o)
+    # the routing and grouping this layer call itself used
+    check_layer_routing(x, lw["w_router"], None, k, ids, w)
+    if not flags & cuda_lib.MOE_F_NO_DEDUP:
+        check_grouping(cuda_lib, ws, ids, B, H, I, E, k)
     ids_g, w_g, logits_g = cuda_lib.route(x, lw["w_router"], k)
     check_route(x, lw["w_router"], None, k, ids_g, w_g, logits_g)
     assert torch.equal(ids_g, ids)
@@ -113,6 +119,7 @@ def test_layer_with_bias_and_residual(cuda_lib):
     torch.cuda.synchronize()
     y_o, _, _ = oracle_layer_following(x, layer_weights_np(lw), k, ids, residual=res.cpu().numpy())
     check_y(y, y_o)
+    check_layer_routing(x, lw["w_router"], lw["bias"], k, ids, w)
 
 
 def test_bf16_activations(cuda_lib):

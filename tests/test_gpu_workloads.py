@@ -12,7 +12,8 @@ import torch
 
 import oracle
 from moe_decode_layer_gemv_gb300 import accounting, synth
-from _parity import (NEAR_TIE, check_route, check_y, margins, np_x, oracle_layer_following)
+from _parity import (NEAR_TIE, check_grouping, check_layer_routing, check_route, check_y, margins, np_x,
+                     oracle_layer_following)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -58,11 +59,17 @@ def oracle_layer_lazy(x, lw, k, ids_gpu, residual=None, tokens=None):
 
 
 def run_layer(cuda_lib, w, lw, x):
+    """The layer in the benchmark's launch configuration; also checks the
+    routing weights it returned and the grouping it left in its workspace."""
     st = cuda_lib.new_status()
+    B = x.shape[0]
+    ws = cuda_lib.new_workspace(B, w.H, w.I, w.E, w.top_k)
     y, ids, rw = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], w.top_k,
-                                        bias=lw.get("bias"), status=st)
+                                        bias=lw.get("bias"), workspace=ws, status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
+    check_layer_routing(x, lw["w_router"], lw.get("bias"), w.top_k, ids, rw)
+    check_grouping(cuda_lib, ws, ids, B, w.H, w.I, w.E, w.top_k)
     return y, ids, rw
 
 
@@ -114,7 +121,9 @@ def test_skewed_routing_layer(cuda_lib, skewed_layer, B):
     assert np.array_equal(uniq.cpu().numpy()[:int(nu.item())], uniq_o)
 
 
-def test_prefill_sized_layer_sampled(cuda_lib):
+def test_prefill_sized_layer_every_row(cuda_lib):
+    """All 512 tokens of the prefill-sized layer (every expert's tensor-core
+    tiles) against the oracle, which evaluates the whole layer here."""
     w = synth.PREFILL
     lw = synth.make_layer(w, 0, seed=0, device=DEV)
     x = synth.make_x(w, 0, seed=0, device=DEV)
@@ -122,11 +131,8 @@ def test_prefill_sized_layer_sampled(cuda_lib):
     ids_r, w_r, lg = cuda_lib.route(x, lw["w_router"], w.top_k)
     torch.cuda.synchronize()
     check_route(x, lw["w_router"], None, w.top_k, ids_r, w_r, lg)
-    rng = np.random.default_rng(0)
-    tok = np.sort(np.concatenate([[0, w.B - 1], rng.choice(np.arange(1, w.B - 1), 10, replace=False)]))
-    y_o, _, _ = oracle_layer_lazy(x, lw, w.top_k, ids, tokens=tok)
-    yg = y[torch.as_tensor(tok, device=DEV)]
-    check_y(yg, y_o)
+    y_o, _, _ = oracle_layer_lazy(x, lw, w.top_k, ids)
+    check_y(y, y_o)
     del lw
     torch.cuda.empty_cache()
 
@@ -147,6 +153,13 @@ def test_stack_of_30_layers_end_to_end(cuda_lib):
         y_o, ids_o, ex = oracle_layer_lazy(x, lw, w.top_k, ids[l], residual=x.cpu().numpy())
         n_ties += int(ex.sum())
         ig = ids[l].cpu().numpy()
+        # in order (descending logit), unless the two selected logits are
+        # within the near-tie margin of each other
+        lo = oracle.router(np_x(x), synth.bf16_bits(lw["w_router"]))
+        srt = -np.sort(-lo.astype(np.float64), axis=1)[:, :w.top_k]
+        inner = np.any(np.diff(srt, axis=1) > -NEAR_TIE, axis=1)
+        strict = ~ex & ~inner
+        assert np.array_equal(ig[strict], ids_o[strict]), l
         assert np.array_equal(np.sort(ig[~ex], 1), np.sort(ids_o[~ex], 1)), l
         x = torch.from_numpy(y_o).to(DEV)
     check_y(x_out, x.cpu().numpy())
