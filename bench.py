@@ -18,7 +18,9 @@ and combine, with the residual add), one fused persistent kernel launch.
             (tiny layer, uniform-routing sweep B = 1..64, skewed-routing
             sweep B = 1..128, prefill-sized layer): ms, tokens/s, algorithmic
             bytes, GB/s and fraction of the peak, unique experts, reuse,
-            near-tie tokens and kernel launches per step.
+            near-tie tokens and kernel launches per step; and the dense
+            counterpart of the stack (E=1, top-1, I=1536: the same active
+            bytes per layer), with moe_over_dense_time beside the headline.
 
 --impl reference times the CPU oracle itself on this workload (rank 0 only).
 --workload {uniform,skewed,prefill,tiny} times one layer of that workload.
@@ -57,8 +59,10 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=30,
                     help="layers in the stack (30 = the workload; fewer only for profiling captures)")
-    ap.add_argument("--workload", default="stack", choices=["stack", "uniform", "skewed", "prefill", "tiny"],
-                    help="stack = the 30-layer decode stack (the headline); the others time one layer")
+    ap.add_argument("--workload", default="stack",
+                    choices=["stack", "uniform", "skewed", "prefill", "tiny", "dense"],
+                    help="stack = the 30-layer decode stack (the headline); dense = its dense SwiGLU "
+                         "counterpart (E=1, top-1, I=1536); the others time one layer")
     ap.add_argument("--batch", type=int, default=None, help="tokens per step for a single-layer workload")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the sub-records of the other workloads in the default run")
@@ -376,7 +380,8 @@ def measure_layer(api, accounting, synth, w, dev, steps, warmup, flags=0, seed=0
 
 
 def run_layer_workload(args):
-    """One MoE layer per step (uniform / skewed / prefill-sized / tiny)."""
+    """One MoE layer per step (uniform / skewed / prefill-sized / tiny), or
+    the dense stack."""
     rank, world, local = dist_env()
     import torch
     torch.cuda.set_device(local)
@@ -384,6 +389,25 @@ def run_layer_workload(args):
     from moe_decode_layer_gemv_gb300 import accounting, build, synth
     build.build()
     from moe_decode_layer_gemv_gb300 import api
+    if args.workload == "dense":
+        flags = api.MOE_F_UNFUSED if args.mode == "unfused" else 0
+        with ClockSampler(local) as clk:
+            rec = measure_stack(api, accounting, synth, synth.DENSE, dev, args.steps, args.warmup, flags, args.seed)
+        peak, peak_src = hbm_peak()
+        w = synth.DENSE
+        line = {"metric": METRIC, "value": rec["tokens_per_s"], "unit": "tokens/s", "n_gpus": 1,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": rec["ms"], "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "weights_dtype": "bf16",
+                "data": "synthetic", "mode": args.mode, "l2_flush": "256 MiB memset before every timed step",
+                "config": {"workload": w.name, "layers": w.layers, "B": w.B, "H": w.H, "I": w.I, "E": w.E,
+                           "top_k": w.top_k},
+                "us_per_layer": rec["us_per_layer"], "hbm_gbs": rec["hbm_gbs"],
+                "roofline": {"bound": "hbm", "achieved": rec["hbm_gbs"], "peak": peak, "unit": "GB/s",
+                             "frac": rec["frac"], "peak_source": peak_src, "traffic": None,
+                             "bytes_per_launch": rec["bytes_per_step"]},
+                "gpu_launches": int(round(rec["launches_per_step"] * args.steps)), "clocks": clk.summary()}
+        print(json.dumps(line), flush=True)
+        return
     base = {"uniform": synth.UNIFORM, "skewed": synth.SKEWED, "prefill": synth.PREFILL,
             "tiny": synth.TINY}[args.workload]
     w = base.with_batch(args.batch) if args.batch else base
@@ -407,6 +431,55 @@ def run_layer_workload(args):
     print(json.dumps(line), flush=True)
 
 
+def measure_stack(api, accounting, synth, w, dev, steps, warmup, flags=0, seed=0, flush=None):
+    """One token through an L-layer stack per step (L2 flushed before each
+    timed step, CUDA events on the launching stream).  Returns the sub-record."""
+    import numpy as np
+    import torch
+    layers = [synth.make_layer(w, l, seed=seed, device=dev) for l in range(w.layers)]
+    sw = api.StackWeights(layers)
+    xs = [synth.make_x(w, s, seed=seed, device=dev) for s in range(warmup + steps)]
+    xbuf = torch.empty_like(xs[0])
+    ids = torch.empty((w.layers, w.B, w.top_k), dtype=torch.int32, device=dev)
+    ws = api.new_workspace(w.B, w.H, w.I, w.E, w.top_k, dev)
+    status = api.new_status(dev)
+    flush = flush if flush is not None else torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for i in range(warmup):
+        flush.zero_()
+        xbuf.copy_(xs[i])
+        api.stack_forward_(xbuf, sw, w.top_k, flags=flags, ids_out=ids, workspace=ws, status=status, stream=stream)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    uniq, launches = [], 0
+    for s in range(steps):
+        flush.zero_()
+        xbuf.copy_(xs[warmup + s])
+        n0 = api.launch_count()
+        ev[s][0].record(stream)
+        api.stack_forward_(xbuf, sw, w.top_k, flags=flags, ids_out=ids, workspace=ws, status=status, stream=stream)
+        ev[s][1].record(stream)
+        launches += api.launch_count() - n0
+        uniq.append(ids.clone())
+    torch.cuda.synchronize()
+    st = int(status.item())
+    if st != 0:
+        raise SystemExit(f"{w.name}: device status {st}: {api.status_string(st)}")
+    mean_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    u_layers = [len(np.unique(u.cpu().numpy()[l])) for u in uniq for l in range(w.layers)]
+    bytes_step = statistics.mean(
+        sum(accounting.layer_bytes(w.H, w.I, w.E, len(np.unique(u.cpu().numpy()[l]))) for l in range(w.layers))
+        for u in uniq)
+    achieved = bytes_step / (mean_ms / 1e3) / 1e9
+    peak, _ = hbm_peak()
+    del layers, sw
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "B": w.B, "H": w.H, "I": w.I, "E": w.E, "top_k": w.top_k, "layers": w.layers,
+            "ms": mean_ms, "tokens_per_s": w.B / (mean_ms / 1e3), "us_per_layer": 1000.0 * mean_ms / w.layers,
+            "bytes_per_step": bytes_step, "hbm_gbs": achieved, "frac": achieved / peak,
+            "unique_experts": statistics.mean(u_layers), "launches_per_step": launches / steps, "steps": steps}
+
+
 def config_records(api, accounting, synth, dev, steps, warmup, seed=0):
     """Sub-records for every workload besides the stack: the tiny layer, the
     uniform-routing sweep, the skewed-routing sweep and the prefill-sized
@@ -425,6 +498,9 @@ def config_records(api, accounting, synth, dev, steps, warmup, seed=0):
         torch.cuda.empty_cache()
     out["prefill"] = measure_layer(api, accounting, synth, synth.PREFILL, dev, steps, warmup, 0, seed, flush)
     torch.cuda.empty_cache()
+    # the dense counterpart of the stack (one expert, top-1, same active bytes
+    # per layer): the dense-vs-MoE comparison of the first page
+    out["dense_stack"] = measure_stack(api, accounting, synth, synth.DENSE, dev, steps, warmup, 0, seed, flush)
     return out
 
 
@@ -606,6 +682,9 @@ def run_ours(args):
         del layers, sw
         torch.cuda.empty_cache()
         line["configs"] = config_records(api, accounting, synth, dev, args.config_steps, 3, args.seed)
+        dense = line["configs"].get("dense_stack")
+        if dense:  # per-token time of the MoE stack over its dense counterpart (same active bytes)
+            line["moe_over_dense_time"] = mean_ms / dense["ms"]
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg:

@@ -85,6 +85,9 @@ typedef enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 } moe_dtype;
 #define MOE_F_FORCE_TC 4u   /* every expert with any route uses the tensor-core
                                GEMMs (testing; needs H % 128 == 0, I % 64 == 0) */
 #define MOE_F_NO_TC 8u      /* never use the tensor-core GEMMs */
+#define MOE_F_NO_PREFETCH 16u /* stack: no speculative L2 prefetch of the next layer's
+                               predicted experts (results are unchanged; the prefetch
+                               only moves bytes earlier) */
 #define MOE_TC_MIN_ROUTES 8 /* by default an expert chosen by at least this many
                                routes runs on the tensor cores */
 
@@ -273,6 +276,23 @@ int moe_inject_barrier_stall(int extra_arrivals);
  * the library's kernel launches in it.  Host-only; never fails.
  */
 unsigned long long moe_launch_count(void);
+
+/*
+ * moe_forward_path -- which kernels moe_layer_forward (L = 1) or
+ * moe_stack_forward (L layers) runs for this shape and these flags on the
+ * current device (host-only; the same decision the forward call makes):
+ *   MOE_PATH_DECODE   one cooperative launch of the persistent decode kernel
+ *                     (batches of up to 4 tokens and 32 routes)
+ *   MOE_PATH_FUSED    one cooperative launch of the general fused kernel
+ *   MOE_PATH_PHASES   the phases as separate kernels (per layer)
+ *   0                 nothing (B == 0)
+ * *grid (may be NULL) receives the persistent kernel's grid (0 for
+ * MOE_PATH_PHASES).
+ */
+#define MOE_PATH_DECODE 2
+#define MOE_PATH_FUSED 3
+#define MOE_PATH_PHASES 4
+int moe_forward_path(int B, int H, int I, int E, int top_k, int L, uint32_t flags, int* path, int* grid);
 
 /* moe_status_string -- static text for a moe_status code or MOE_DEV_* bit. */
 const char* moe_status_string(int code);

@@ -39,6 +39,8 @@ _lib.moe_layer_forward.argtypes = [_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _
 _lib.moe_stack_forward.argtypes = [_I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _U, _P, _S, _P, _P]
 _lib.moe_workspace_grouping.argtypes = [_P, _S, _I, _I, _I, _I, _I, ctypes.POINTER(_P), ctypes.POINTER(_P),
                                         ctypes.POINTER(_P), ctypes.POINTER(_P)]
+_lib.moe_forward_path.argtypes = [_I, _I, _I, _I, _I, _I, _U, ctypes.POINTER(_I), ctypes.POINTER(_I)]
+_lib.moe_forward_path.restype = ctypes.c_int
 _lib.moe_launch_count.argtypes = []
 _lib.moe_launch_count.restype = ctypes.c_ulonglong
 _lib.moe_set_trace_buffer.argtypes = [_P, _I]
@@ -53,7 +55,7 @@ for _f in ("moe_workspace_bytes", "moe_route", "moe_group_by_expert", "moe_exper
 
 EXPORTED = ("moe_workspace_bytes", "moe_route", "moe_group_by_expert", "moe_expert_forward",
             "moe_expert_forward_noalloc", "moe_layer_forward", "moe_stack_forward", "moe_workspace_grouping",
-            "moe_launch_count", "moe_set_trace_buffer",
+            "moe_launch_count", "moe_forward_path", "moe_set_trace_buffer",
             "moe_inject_barrier_stall", "moe_status_string")
 
 MOE_OK = 0
@@ -71,6 +73,7 @@ MOE_F_NO_DEDUP = 1
 MOE_F_UNFUSED = 2
 MOE_F_FORCE_TC = 4
 MOE_F_NO_TC = 8
+MOE_F_NO_PREFETCH = 16
 TC_MIN_ROUTES = 8
 MAX_E, MAX_TOPK, MAX_B, MAX_DIM, MAX_LAYERS = 256, 8, 1024, 16384, 64
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -206,6 +209,19 @@ def workspace_grouping(workspace, B, H, I, E, top_k):
         off = o.value - base
         views.append(workspace[off:off + 4 * n].view(torch.int32))
     return tuple(views)
+
+
+PATH_DECODE, PATH_FUSED, PATH_PHASES = 2, 3, 4
+PATH_NAMES = {0: "none", 2: "decode kernel", 3: "fused kernel", 4: "phase kernels"}
+
+
+def forward_path(B, H, I, E, top_k, L=1, flags=0):
+    """-> (path, grid): the kernels a layer (L=1) or stack forward runs for
+    this shape on the current device (MOE_PATH_*), and its persistent grid."""
+    path, grid = _I(0), _I(0)
+    _check(_lib.moe_forward_path(B, H, I, E, top_k, L, flags, ctypes.byref(path), ctypes.byref(grid)),
+           "moe_forward_path")
+    return path.value, grid.value
 
 
 def launch_count() -> int:

@@ -158,6 +158,8 @@ __global__ void __launch_bounds__(kThreads) fused_kernel(Ctx c, StackArgs sa, un
 // -------------------------------------------------------------- host side
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+constexpr unsigned kAllFlags = MOE_F_NO_DEDUP | MOE_F_UNFUSED | MOE_F_FORCE_TC | MOE_F_NO_TC | MOE_F_NO_PREFETCH;
+
 struct WsLayout {
     size_t logits, ids, rw, offsets, route_idx, unique, num_unique, status, bar, acc, acc_end, h, o;
     size_t x_hi, x_lo, h_hi, h_lo, seg_list, seg_count, alog, total;
@@ -558,7 +560,7 @@ static bool decode_plan(int B, int H, int I, int E, int k, int sms, DkParams& p,
     if (B < 1 || B > kDkMaxB || R > kDkMaxR || sms < 1 || sms > 1024) return false;
     const int ng = H >> 3;
     const int maxrows = 8 * ((ng + sms - 1) / sms);
-    size_t off = 1024;  // ring barriers (2 x kDkMaxStages) and the two direct-mode barriers
+    size_t off = 1024;  // ring barriers (2 x kDkMaxStages) and the direct-mode barriers
     p.off_misc = (int)off;
     off = align_up(off + sizeof(DkMisc) + sizeof(float) * (size_t)B * ((E + 7) & ~7), 128);
     p.off_x = (int)off;
@@ -615,7 +617,7 @@ static int launch_decode(DkParams& p, size_t smem, int sms, char* ws, const WsLa
     // only: L > 1).  (Measured on the 30-layer stack: top k beats top k+1,
     // whose extra expert costs more HBM time than its hits save.)
     p.prefetch_k = 0;
-    if (p.B == 1 && p.L > 1) {
+    if (p.B == 1 && p.L > 1 && !(p.flags & MOE_F_NO_PREFETCH)) {
         const unsigned long long per_e = 6ull * p.I * p.H;
         const int kp = p.k;
         if (per_e * kp <= (64ull << 20) && kp <= 32) p.prefetch_k = kp;
@@ -726,7 +728,7 @@ int moe_expert_forward(const void* x, int x_dtype, const uint16_t* gate_up, cons
     int rc = check_dims(B, H, I, E, top_k, true);
     if (rc) return rc;
     if (x_dtype != MOE_DT_F32 && x_dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
-    if (flags & ~(MOE_F_NO_DEDUP | MOE_F_UNFUSED | MOE_F_FORCE_TC | MOE_F_NO_TC)) return MOE_ERR_INVALID_ARG;
+    if (flags & ~kAllFlags) return MOE_ERR_INVALID_ARG;
     if (B == 0) return MOE_OK;
     MOE_REQ(x);
     MOE_REQ(gate_up);
@@ -764,7 +766,7 @@ int moe_layer_forward(const void* x, int x_dtype, const uint16_t* w_router, cons
     int rc = check_dims(B, H, I, E, top_k, true);
     if (rc) return rc;
     if (x_dtype != MOE_DT_F32 && x_dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
-    if (flags & ~(MOE_F_NO_DEDUP | MOE_F_UNFUSED | MOE_F_FORCE_TC | MOE_F_NO_TC)) return MOE_ERR_INVALID_ARG;
+    if (flags & ~kAllFlags) return MOE_ERR_INVALID_ARG;
     if (B == 0) return MOE_OK;
     MOE_REQ(x);
     MOE_REQ(w_router);
@@ -824,7 +826,7 @@ int moe_stack_forward(int Lc, const uint16_t* const* w_router, const float* cons
     int rc = check_dims(B, H, I, E, top_k, true);
     if (rc) return rc;
     if (Lc < 1 || Lc > MOE_MAX_LAYERS) return MOE_ERR_INVALID_ARG;
-    if (flags & ~(MOE_F_NO_DEDUP | MOE_F_UNFUSED | MOE_F_FORCE_TC | MOE_F_NO_TC)) return MOE_ERR_INVALID_ARG;
+    if (flags & ~kAllFlags) return MOE_ERR_INVALID_ARG;
     if (B == 0) return MOE_OK;
     if (!w_router || !gate_up || !down) return MOE_ERR_INVALID_ARG;
     for (int l = 0; l < Lc; ++l) {
@@ -909,6 +911,32 @@ int moe_workspace_grouping(void* workspace, size_t workspace_bytes, int B, int H
 
 unsigned long long moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+int moe_forward_path(int B, int H, int I, int E, int top_k, int L, uint32_t flags, int* path, int* grid) {
+    int rc = check_dims(B, H, I, E, top_k, true);
+    if (rc) return rc;
+    if (!path || L < 1 || L > MOE_MAX_LAYERS || (flags & ~kAllFlags)) return MOE_ERR_INVALID_ARG;
+    int g = 0;
+    if (B == 0) {
+        *path = 0;
+    } else if (flags & MOE_F_UNFUSED) {
+        *path = MOE_PATH_PHASES;
+    } else {
+        DkParams dp;
+        size_t dsm = 0;
+        const int sms = sm_count();
+        if (decode_plan(B, H, I, E, top_k, sms, dp, dsm)) {
+            *path = MOE_PATH_DECODE;
+            g = sms;
+        } else if (tc_threshold_for(flags, H, I) > 0) {
+            *path = MOE_PATH_PHASES;
+        } else {
+            *path = MOE_PATH_FUSED;
+        }
+    }
+    if (grid) *grid = g;
+    return MOE_OK;
+}
+
 int moe_inject_barrier_stall(int extra_arrivals) {
     if (extra_arrivals < 0 || extra_arrivals > 1024) return MOE_ERR_INVALID_ARG;
     g_bar_extra = (unsigned)extra_arrivals;
@@ -988,7 +1016,7 @@ extern "C" int moe_expert_forward_noalloc(const void* x, int x_dtype, const uint
     int rc = check_dims(B, H, I, E, top_k, true);
     if (rc) return rc;
     if (x_dtype != MOE_DT_F32 && x_dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
-    if (flags & ~(MOE_F_NO_DEDUP | MOE_F_UNFUSED | MOE_F_FORCE_TC | MOE_F_NO_TC)) return MOE_ERR_INVALID_ARG;
+    if (flags & ~kAllFlags) return MOE_ERR_INVALID_ARG;
     if (flags & MOE_F_FORCE_TC) return MOE_ERR_UNSUPPORTED;  // no operand buffers for the tensor cores here
     const size_t R = (size_t)B * top_k;
     const size_t h_bytes = align_up(sizeof(float) * R * I, 256);

@@ -37,6 +37,7 @@ constexpr uint32_t kDkWaitLimit = 1u << 22;
 constexpr unsigned long long kDkSpinLimit = 1ull << 22;
 constexpr float kFixScale = 4294967296.0f;  // 2^32
 constexpr int kDkSmemMax = 227 * 1024;
+constexpr int kDkGChunks = 8;  // direct mode: gate/up rows land on this many barriers (in issue order)
 
 struct DkParams {
     int B, H, I, E, k, L;
@@ -236,20 +237,19 @@ __device__ __forceinline__ float key_value(unsigned k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// Top-k of token t's logits in shared memory (lg[e], e < E) by one warp:
-// lane L holds experts L + 32 s (s < 8) as order-preserving keys; k rounds
-// of a max reduction (and a min reduction over the ids holding it: ties to
-// the lower id), then the weights.
-__device__ __forceinline__ void dk_topk_smem(const float* lg, int E, int k, int t, DkMisc* m, int32_t* status) {
+// Top-k of token t by one warp from values in registers: lane L holds the
+// logit of expert L + 32 s in v[s] (s < 8; entries for e >= E are ignored)
+// as order-preserving keys; k rounds of a max reduction (and a min reduction
+// over the ids holding it: ties to the lower id), then the weights.
+__device__ __forceinline__ void dk_topk_vals(const float (&v)[8], int E, int k, int t, DkMisc* m, int32_t* status) {
     const int lane = threadIdx.x & 31;
     unsigned key[8];
     bool bad = false;
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
         const int e = lane + 32 * s;
-        const float v = e < E ? lg[e] : 0.f;
-        if (e < E && !isfinite(v)) bad = true;
-        key[s] = e < E ? order_key(v) : 0u;
+        if (e < E && !isfinite(v[s])) bad = true;
+        key[s] = e < E ? order_key(v[s]) : 0u;
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(status, MOE_DEV_NONFINITE);
     unsigned taken = 0;
@@ -284,6 +284,18 @@ __device__ __forceinline__ void dk_topk_smem(const float* lg, int E, int k, int 
         m->w[t * k + lane] = ex / den;
     }
     __syncwarp();
+}
+
+// The same from token t's logits in shared memory (lg[e], e < E).
+__device__ __forceinline__ void dk_topk_smem(const float* lg, int E, int k, int t, DkMisc* m, int32_t* status) {
+    const int lane = threadIdx.x & 31;
+    float v[8];
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+        const int e = lane + 32 * s;
+        v[s] = e < E ? lg[e] : 0.f;
+    }
+    dk_topk_vals(v, E, k, t, m, status);
 }
 
 // Router partial sums of this CTA's hidden rows [h0, h0+nrows) for every
@@ -660,7 +672,8 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + kDkMaxStages;
-    uint64_t* dbar = empty + kDkMaxStages;  // direct mode: [0] gate/up rows landed, [1] down rows landed
+    uint64_t* dbar = empty + kDkMaxStages;  // direct mode: [0] unused, [1] down rows landed
+    uint64_t* gch = dbar + 2;               // direct mode: [kDkGChunks] a chunk of gate/up pairs landed
     DkMisc* m = reinterpret_cast<DkMisc*>(smem + p.off_misc);
     float* xs = reinterpret_cast<float*>(smem + p.off_x);   // [B][H]
     float* xq = reinterpret_cast<float*>(smem + p.off_xq);  // [B][dk_hq(H)] lane-blocked copy of xs
@@ -693,6 +706,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
         }
         mbar_init(&dbar[0], 1);
         mbar_init(&dbar[1], 1);
+        for (int c = 0; c < kDkGChunks; ++c) mbar_init(&gch[c], 1);
         m->abort_flag = 0;
         m->mid_epoch = 0;
         for (int q = 0; q < kDkMaxStages; ++q) m->last_pos[q] = -1;
@@ -837,14 +851,27 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
         if (warp == 0 && direct) {
             // ================= producer, direct mode
             if (lane == 0 && d_gate) {
-                mbar_arrive_expect_tx(&dbar[0], d_gate_bytes);
-                dk_gate_runs(lw.gate_up, m->seg_e, wk.ga, wk.gb, H, I, d_g, d_u, &dbar[0]);
+                // the CTA's pairs in up to kDkGChunks chunks, each on its own
+                // barrier, so that the consumers start on the first chunk while
+                // the others are still on their way (every chunk barrier
+                // completes one phase per layer: unused ones with no bytes)
+                const int csz = max(4, (wk.ng + kDkGChunks - 1) / kDkGChunks);
+                for (int ch = 0; ch < kDkGChunks; ++ch) {
+                    const int ca = min(wk.ng, ch * csz), cb = min(wk.ng, ca + csz);
+                    mbar_arrive_expect_tx(&gch[ch], (uint32_t)(cb - ca) * 4u * (uint32_t)H);
+                    if (cb > ca)
+                        dk_gate_runs(lw.gate_up, m->seg_e, wk.ga + ca, wk.ga + cb, H, I, d_g + (size_t)ca * 2 * H,
+                                     d_u + (size_t)ca * 2 * H, &gch[ch]);
+                }
             }
             __syncwarp();
             if (lane == 1 && d_down) {
                 // the gate/up rows first: the down rows are needed only after
                 // the mid-layer barrier, so they do not share the bandwidth
-                if (d_gate) dk_wait(&dbar[0], (uint32_t)(dg_count & 1), m, p);
+                if (d_gate) {
+                    const int csz = max(4, (wk.ng + kDkGChunks - 1) / kDkGChunks);
+                    dk_wait(&gch[(wk.ng - 1) / csz], (uint32_t)(dg_count & 1), m, p);
+                }
                 mbar_arrive_expect_tx(&dbar[1], d_down_bytes);
                 for (int u = 0; u < U; ++u)
                     bulk_g2s(d_d + (size_t)u * nrows * 2 * I, lw.down + (size_t)m->seg_e[u] * H * I + (size_t)h0 * I,
@@ -936,11 +963,12 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
             const bool predicting = p.prefetch_k > 0 && has_next && cw == kDkConsumers - 1;
             if (predicting) dk_predict_logits(p.layer[l + 1], xq, H, E, p.alog);
             if (d_gate) {
-                bool landed = false;
+                const int csz = max(4, (wk.ng + kDkGChunks - 1) / kDkGChunks);
+                int landed = -1;
                 for (int c = cw; c < wk.ng; c += kDkConsumers) {
-                    if (!landed) {
-                        if (!dk_wait(&dbar[0], (uint32_t)(dg_count & 1), m, p)) break;
-                        landed = true;
+                    if (c / csz != landed) {
+                        if (!dk_wait(&gch[c / csz], (uint32_t)(dg_count & 1), m, p)) break;
+                        landed = c / csz;
                         if (tid == kDkLeader) dk_trace<kTrace>(p, l, 12);
                     }
                     const int q = wk.ga + c;
@@ -1072,7 +1100,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
             const int n = m->last_pos[st];
             if (n >= 0) mbar_wait(&full[st], (uint32_t)((n / p.S) & 1), kDkWaitLimit);
         }
-        if (lane == 0 && dg_count > 0) mbar_wait(&dbar[0], (uint32_t)((dg_count - 1) & 1), kDkWaitLimit);
+        if (lane < kDkGChunks && dg_count > 0) mbar_wait(&gch[lane], (uint32_t)((dg_count - 1) & 1), kDkWaitLimit);
         if (lane == 1 && dd_count > 0) mbar_wait(&dbar[1], (uint32_t)((dd_count - 1) & 1), kDkWaitLimit);
     }
     __syncthreads();

@@ -62,8 +62,17 @@ SKEWED = Workload("skewed_zipf_e256_k6_h2048_i768", B=128, H=2048, I=768, E=256,
                   sigma_router=2048 ** -0.5, zipf_bias=True, batches=(1, 16, 64, 128))
 PREFILL = Workload("prefill_b512_e256_k8_h4096_i1536", B=512, H=4096, I=1536, E=256, top_k=8,
                    x_bf16=True)
+# The dense counterpart of the stack: one expert, top-1 (a plain SwiGLU MLP per
+# layer, routing weight 1), with I = 2 x 768 so that a layer streams the same
+# active weight bytes as a top-2 layer of the MoE stack.  The layer output
+# scales as sigma^3 * sqrt(I) (times sqrt(sum w^2) for the MoE: about 0.71
+# for two experts); sigma = 0.016 gives the dense layer the MoE layer's
+# output scale (0.02^3 * sqrt(768) * 0.71 = 0.016^3 * sqrt(1536)), so that
+# the 30-layer residual stream stays O(1) as it does for the MoE stack.
+DENSE = Workload("dense_stack30_b1_h2048_i1536", B=1, H=2048, I=1536, E=1, top_k=1, layers=30,
+                 sigma_expert=0.016, residual=True)
 
-WORKLOADS = {w.name: w for w in (TINY, STACK, UNIFORM, SKEWED, PREFILL)}
+WORKLOADS = {w.name: w for w in (TINY, STACK, UNIFORM, SKEWED, PREFILL, DENSE)}
 
 
 def _gen(seed: int, tensor_id: int, sub: int, device) -> torch.Generator:

@@ -165,3 +165,24 @@ def test_stack_of_30_layers_end_to_end(cuda_lib):
     check_y(x_out, x.cpu().numpy())
     del layers
     torch.cuda.empty_cache()
+
+
+def test_dense_stack_of_30_layers_end_to_end(cuda_lib):
+    """The dense counterpart of the stack (one expert, top-1: a SwiGLU MLP
+    per layer with routing weight 1) through the same stack entry point,
+    layer by layer against the oracle and end to end."""
+    w = synth.DENSE
+    layers = [synth.make_layer(w, l, seed=0, device=DEV) for l in range(w.layers)]
+    x0 = synth.make_x(w, 0, seed=0, device=DEV)
+    st = cuda_lib.new_status()
+    x_out, ids = cuda_lib.stack_forward(x0, cuda_lib.StackWeights(layers), w.top_k, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert int(ids.abs().sum()) == 0  # the only expert, every layer
+    lnp = [{"w_router": synth.bf16_bits(lw["w_router"]), "gate_up": synth.bf16_bits(lw["gate_up"]),
+            "down": synth.bf16_bits(lw["down"])} for lw in layers]
+    x_o, ids_o = oracle.stack(x0.cpu().numpy(), lnp, w.top_k)
+    assert np.array_equal(ids.cpu().numpy(), ids_o)
+    check_y(x_out, x_o)
+    del layers
+    torch.cuda.empty_cache()
