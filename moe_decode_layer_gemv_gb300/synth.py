@@ -17,6 +17,8 @@ Recipe (every tensor has its own generator stream, seeded from
 * down[l]:      [E, H, I], N(0, 0.02) -> bf16; tensor_id 12 + 3l.
 * bias (skewed routing only): b_e = 2 * log(1 / rank_e ** 1.1) with rank a
                 seeded random permutation of 1..E (tensor_id 1).
+* norm[l] (pre-norm stacks only): RMSNorm weights 1 + 0.1 * N(0, 1), fp32;
+                tensor_id 5000 + l.
 
 Small cases are generated on the CPU and copied to the device; the
 full-size workloads are generated directly on the GPU by torch's own
@@ -100,6 +102,12 @@ def make_layer(w: Workload, layer: int = 0, seed: int = 0, device="cpu"):
         down[e] = normal_bf16((H, I), w.sigma_expert, seed, 12 + 3 * layer, e, device)
     bias = zipf_bias(E, seed).to(device) if w.zipf_bias else None
     return {"w_router": wr, "gate_up": gate_up, "down": down, "bias": bias}
+
+
+def norm_weights(H: int, layer: int = 0, seed: int = 0, device="cpu") -> torch.Tensor:
+    """RMSNorm weights of layer l: 1 + 0.1 * N(0, 1), fp32 (tensor_id 5000 + l)."""
+    g = _gen(seed, 5000 + layer, 0, device)
+    return 1.0 + 0.1 * torch.randn(H, generator=g, device=device, dtype=torch.float32)
 
 
 def zipf_bias(E: int, seed: int = 0) -> torch.Tensor:

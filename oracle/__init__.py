@@ -59,8 +59,10 @@ def _load():
             lib.oracle_experts.argtypes = [P, i, P, P, P, P, i, i, i, i, i, i, P, P, P, P]
             lib.oracle_layer.argtypes = [P, i, P, P, P, P, i, i, i, i, i, i, P, P, P, P, P]
             lib.oracle_stack.argtypes = [i, P, P, P, P, i, i, i, i, i, i, P, P]
+            lib.oracle_rmsnorm.argtypes = [P, P, i, i, ctypes.c_float, P]
+            lib.oracle_stack_norm.argtypes = [i, P, P, P, P, P, ctypes.c_float, i, i, i, i, i, i, P, P]
             for f in ("oracle_router", "oracle_topk", "oracle_group", "oracle_experts",
-                      "oracle_layer", "oracle_stack"):
+                      "oracle_layer", "oracle_stack", "oracle_rmsnorm", "oracle_stack_norm"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -181,6 +183,67 @@ def stack(x, layers, k, mode=DEDUP):
         xa = y
         all_ids.append(ids)
     return xa, np.stack(all_ids) if all_ids else np.zeros((0,) + xa.shape[:1] + (k,), np.int32)
+
+
+def rmsnorm(x, g, eps):
+    """a[B,H] = x * (1/sqrt(mean_h x^2 + eps)) * g, fp32, sum of squares in h order."""
+    xa = np.ascontiguousarray(x, dtype=np.float32)
+    ga = np.ascontiguousarray(g, dtype=np.float32)
+    B, H = xa.shape
+    a = np.empty((B, H), np.float32)
+    _check(_load().oracle_rmsnorm(_ptr(xa), _ptr(ga), B, H, float(eps), _ptr(a)), "rmsnorm")
+    return a
+
+
+def stack_norm(x, layers, k, eps, mode=DEDUP):
+    """Pre-norm stack: x <- x + layer_l(rmsnorm_l(x)) for each layer dict
+    {w_router, gate_up, down, bias, norm}.  Returns (x_out, ids[L,B,k])."""
+    xa = np.array(x, dtype=np.float32, copy=True)
+    all_ids = []
+    for lw in layers:
+        a = rmsnorm(xa, lw["norm"], eps)
+        y, ids, _, _ = layer(a, lw["w_router"], lw["gate_up"], lw["down"], k,
+                             bias=lw.get("bias"), mode=mode, residual=xa)
+        xa = y
+        all_ids.append(ids)
+    return xa, np.stack(all_ids) if all_ids else np.zeros((0,) + xa.shape[:1] + (k,), np.int32)
+
+
+def stack_norm_c(x, layers, k, eps, mode=DEDUP):
+    """The same pre-norm stack driven by the C loop (oracle_stack_norm)."""
+    xa = np.array(x, dtype=np.float32, copy=True)
+    L = len(layers)
+    B, H = xa.shape
+    E = layers[0]["w_router"].shape[0]
+    I = layers[0]["gate_up"].shape[1] // 2
+    wr = (ctypes.c_void_p * L)()
+    bs = (ctypes.c_void_p * L)()
+    nw = (ctypes.c_void_p * L)()
+    gp = (ctypes.c_void_p * (L * E))()
+    dp = (ctypes.c_void_p * (L * E))()
+    keep = []
+    for l, lw in enumerate(layers):
+        a = np.ascontiguousarray(lw["w_router"], dtype=np.uint16)
+        n = np.ascontiguousarray(lw["norm"], dtype=np.float32)
+        keep += [a, n]
+        wr[l] = a.ctypes.data
+        nw[l] = n.ctypes.data
+        if lw.get("bias") is not None:
+            b = np.ascontiguousarray(lw["bias"], dtype=np.float32)
+            keep.append(b)
+            bs[l] = b.ctypes.data
+        g = np.ascontiguousarray(lw["gate_up"], dtype=np.uint16)
+        d = np.ascontiguousarray(lw["down"], dtype=np.uint16)
+        keep += [g, d]
+        for e in range(E):
+            gp[l * E + e] = g[e].ctypes.data
+            dp[l * E + e] = d[e].ctypes.data
+    ids = np.empty((L, B, k), np.int32)
+    _check(_load().oracle_stack_norm(L, ctypes.addressof(wr), ctypes.addressof(bs), ctypes.addressof(gp),
+                                     ctypes.addressof(dp), ctypes.addressof(nw), float(eps), B, H, I, E, k, mode,
+                                     _ptr(xa), _ptr(ids)), "stack_norm")
+    del keep
+    return xa, ids
 
 
 def stack_c(x, layers, k, mode=DEDUP):

@@ -267,6 +267,27 @@ int oracle_experts(const void* x, int x_dtype, const uint16_t* const* gate_up_pt
     return OR_OK;
 }
 
+/* RMSNorm of every token's row, the norm half of the fused "norm + residual
+ * add" operation ("TEXT Generation Optimization Report", Fused Operations:
+ * fused_rms_norm_residual; the formula is not on the pages: the standard
+ * RMSNorm is taken):
+ *   ms = (sum_h x[t,h]^2) / H        fp32, h ascending
+ *   a[t,h] = (x[t,h] * (1 / sqrtf(ms + eps))) * g[h]
+ * In a stack the residual add is x_{l+1} = x_l + layer_l(a_l) (see
+ * oracle_stack_norm). */
+int oracle_rmsnorm(const float* x, const float* g, int B, int H, float eps, float* a) {
+    if (B < 0 || H <= 0 || !x || !g || !a) return OR_BAD_ARG;
+    for (int t = 0; t < B; ++t) {
+        const float* xr = x + (size_t)t * H;
+        float ss = 0.0f;
+        for (int h = 0; h < H; ++h) ss += xr[h] * xr[h];
+        const float ms = ss / (float)H;
+        const float r = 1.0f / sqrtf(ms + eps);
+        for (int h = 0; h < H; ++h) a[(size_t)t * H + h] = (xr[h] * r) * g[h];
+    }
+    return OR_OK;
+}
+
 /* Whole layer: router -> top-k -> experts -> combine.  ids/w/logits are
  * outputs ([B,k], [B,k], [B,E]); gate_up_ptrs/down_ptrs as above. */
 int oracle_layer(const void* x, int x_dtype, const uint16_t* wr, const float* bias,
@@ -279,6 +300,38 @@ int oracle_layer(const void* x, int x_dtype, const uint16_t* wr, const float* bi
     if (rc) return rc;
     return oracle_experts(x, x_dtype, gate_up_ptrs, down_ptrs, ids, w, B, H, I, E, k, mode,
                           residual, y, NULL, NULL);
+}
+
+/* Pre-norm stack: x <- x + layer_l(rmsnorm_l(x)) for l = 0..L-1; norm_w[l]
+ * [H] fp32 holds layer l's norm weights, the other arguments are those of
+ * oracle_stack. */
+int oracle_stack_norm(int L, const uint16_t* const* wr, const float* const* bias,
+                      const uint16_t* const* gate_up_ptrs, const uint16_t* const* down_ptrs,
+                      const float* const* norm_w, float eps, int B, int H, int I, int E, int k,
+                      int mode, float* x, int32_t* ids_out) {
+    if (L <= 0 || B < 0 || !x || !norm_w) return OR_BAD_ARG;
+    float* a = (float*)malloc(sizeof(float) * (size_t)B * H + 1);
+    float* y = (float*)malloc(sizeof(float) * (size_t)B * H + 1);
+    float* lg = (float*)malloc(sizeof(float) * (size_t)B * E + 1);
+    int32_t* ids = (int32_t*)malloc(sizeof(int32_t) * (size_t)B * k + 4);
+    float* w = (float*)malloc(sizeof(float) * (size_t)B * k + 4);
+    int rc = OR_OK;
+    if (!a || !y || !lg || !ids || !w) rc = OR_BAD_ARG;
+    for (int l = 0; l < L && rc == OR_OK; ++l) {
+        rc = oracle_rmsnorm(x, norm_w[l], B, H, eps, a);
+        if (rc) break;
+        rc = oracle_layer(a, 0, wr[l], bias ? bias[l] : NULL, gate_up_ptrs + (size_t)l * E,
+                          down_ptrs + (size_t)l * E, B, H, I, E, k, mode, x, y, ids, w, lg);
+        if (rc) break;
+        memcpy(x, y, sizeof(float) * (size_t)B * H);
+        if (ids_out) memcpy(ids_out + (size_t)l * B * k, ids, sizeof(int32_t) * (size_t)B * k);
+    }
+    free(a);
+    free(y);
+    free(lg);
+    free(ids);
+    free(w);
+    return rc;
 }
 
 /* Stack of L layers with the residual: x <- x + layer_l(x), x fp32 [B,H]

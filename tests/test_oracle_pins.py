@@ -328,3 +328,61 @@ def test_stack_python_and_c_drivers_agree_and_add_the_residual():
 def test_oracle_rejects_out_of_range_ids():
     with pytest.raises(ValueError):
         oracle.group(np.array([[0, 9]], np.int32), 8)
+
+
+# -------------------------------------------------------------------- RMSNorm
+def _fp64_rmsnorm(x, g, eps):
+    xf = x.astype(np.float64)
+    return xf / np.sqrt(np.mean(xf * xf, axis=1, keepdims=True) + eps) * g.astype(np.float64)
+
+
+def test_rmsnorm_matches_fp64_within_fp32_rounding():
+    rng = np.random.default_rng(21)
+    for B, H in ((1, 64), (3, 2048), (5, 72)):
+        x = (rng.standard_normal((B, H)) * rng.uniform(0.1, 10.0)).astype(np.float32)
+        g = (1.0 + 0.1 * rng.standard_normal(H)).astype(np.float32)
+        a = oracle.rmsnorm(x, g, 1e-6)
+        ref = _fp64_rmsnorm(x, g, 1e-6)
+        assert np.max(np.abs(a - ref)) <= 1e-5 * np.max(np.abs(ref))
+
+
+def test_rmsnorm_with_unit_weights_gives_unit_rms_and_ignores_scale():
+    rng = np.random.default_rng(22)
+    x = rng.standard_normal((4, 256)).astype(np.float32)
+    ones = np.ones(256, np.float32)
+    a = oracle.rmsnorm(x, ones, 0.0)
+    assert np.allclose(np.sqrt(np.mean(a.astype(np.float64) ** 2, axis=1)), 1.0, atol=1e-6)
+    # scaling the input by a power of two changes nothing (eps = 0: every step
+    # is exact under the scaling)
+    assert np.array_equal(oracle.rmsnorm(x * 8.0, ones, 0.0), a)
+    # the weights multiply each column
+    g = np.linspace(0.5, 1.5, 256).astype(np.float32)
+    assert np.allclose(oracle.rmsnorm(x, g, 0.0), a * g, rtol=1e-6, atol=0)
+
+
+def test_prenorm_stack_adds_the_layer_of_the_normalised_input_to_the_raw_input():
+    """x1 = x0 + MoE(rmsnorm(x0)): checked against the fp64 brute-force layer
+    applied to the fp64 norm, and the C and Python drivers agree bitwise."""
+    rng = np.random.default_rng(23)
+    B, H, I, E, k, L, eps = 3, 64, 32, 8, 2, 3, 1e-6
+    layers = []
+    for _ in range(L):
+        layers.append({"w_router": rand_bf16(rng, (E, H), 0.1),
+                       "gate_up": rand_bf16(rng, (E, 2 * I, H), 0.05),
+                       "down": rand_bf16(rng, (E, H, I), 0.05),
+                       "norm": (1.0 + 0.1 * rng.standard_normal(H)).astype(np.float32)})
+    x = (3.0 * rng.standard_normal((B, H))).astype(np.float32)
+    xa, ida = oracle.stack_norm(x, layers, k, eps)
+    xb, idb = oracle.stack_norm_c(x, layers, k, eps)
+    assert np.array_equal(xa, xb) and np.array_equal(ida, idb)
+    x1, id1 = oracle.stack_norm(x, layers[:1], k, eps)
+    a64 = _fp64_rmsnorm(x, layers[0]["norm"], eps)
+    yref, idref, margins = _fp64_bruteforce_layer(a64, layers[0]["w_router"], layers[0]["gate_up"],
+                                                  layers[0]["down"], k)
+    ok = margins > 1e-5
+    assert np.array_equal(id1[0][ok], idref[ok])
+    ref = x.astype(np.float64) + yref
+    assert np.max(np.abs(x1[ok] - ref[ok])) <= 2e-5 * np.max(np.abs(yref))
+    # without the norm the layer sees a different input: the norm is applied
+    xs, _ = oracle.stack(x, layers[:1], k)
+    assert not np.allclose(xs, x1)
