@@ -104,6 +104,36 @@ def make_layer(w: Workload, layer: int = 0, seed: int = 0, device="cpu"):
     return {"w_router": wr, "gate_up": gate_up, "down": down, "bias": bias}
 
 
+def quantize_fp8_block(w: torch.Tensor, block: int = 128):
+    """Block-scaled FP8 copy of a weight matrix [..., R, C] (input
+    preparation, not the layer's arithmetic): per block of block x block
+    elements the fp32 scale amax / 448 (448 = the largest E4M3 value; a zero
+    block gets scale 1), the codes round(w / scale) to float8_e4m3fn by
+    torch.  Returns (codes uint8 [..., R, C], scales fp32 [..., ceil(R/b),
+    ceil(C/b)])."""
+    wf = w.to(torch.float32)
+    *lead, R, C = wf.shape
+    nbr, nbc = (R + block - 1) // block, (C + block - 1) // block
+    pad = torch.zeros(*lead, nbr * block, nbc * block, dtype=torch.float32, device=w.device)
+    pad[..., :R, :C] = wf
+    blocks = pad.reshape(*lead, nbr, block, nbc, block)
+    amax = blocks.abs().amax(dim=(-3, -1))
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    q = (blocks / scale[..., :, None, :, None]).reshape(*lead, nbr * block, nbc * block)[..., :R, :C]
+    codes = q.contiguous().to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes, scale.contiguous()
+
+
+def make_layer_fp8(w: Workload, layer: int = 0, seed: int = 0, device="cpu"):
+    """A layer of the recipe with its expert weights in block-scaled FP8:
+    the bf16 weights of make_layer, quantised per 128 x 128 block."""
+    lw = make_layer(w, layer, seed=seed, device=device)
+    gq, gs = quantize_fp8_block(lw["gate_up"])
+    dq, ds = quantize_fp8_block(lw["down"])
+    lw.update({"gate_up_q": gq, "gate_up_scale": gs, "down_q": dq, "down_scale": ds})
+    return lw
+
+
 def norm_weights(H: int, layer: int = 0, seed: int = 0, device="cpu") -> torch.Tensor:
     """RMSNorm weights of layer l: 1 + 0.1 * N(0, 1), fp32 (tensor_id 5000 + l)."""
     g = _gen(seed, 5000 + layer, 0, device)

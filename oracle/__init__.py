@@ -60,9 +60,12 @@ def _load():
             lib.oracle_layer.argtypes = [P, i, P, P, P, P, i, i, i, i, i, i, P, P, P, P, P]
             lib.oracle_stack.argtypes = [i, P, P, P, P, i, i, i, i, i, i, P, P]
             lib.oracle_rmsnorm.argtypes = [P, P, i, i, ctypes.c_float, P]
+            lib.oracle_experts_w.argtypes = [P, i, P, P, i, P, P, i, i, i, i, i, i, P, P, P, P]
+            lib.oracle_dequant_fp8_block.argtypes = [P, P, i, i, P]
             lib.oracle_stack_norm.argtypes = [i, P, P, P, P, P, ctypes.c_float, i, i, i, i, i, i, P, P]
             for f in ("oracle_router", "oracle_topk", "oracle_group", "oracle_experts",
-                      "oracle_layer", "oracle_stack", "oracle_rmsnorm", "oracle_stack_norm"):
+                      "oracle_layer", "oracle_stack", "oracle_rmsnorm", "oracle_stack_norm",
+                      "oracle_experts_w", "oracle_dequant_fp8_block"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -120,11 +123,13 @@ def group(ids, E):
 
 
 def _expert_ptrs(gate_up, down, E):
-    """Per-expert host pointer tables.  gate_up/down may be full [E,...]
-    arrays or dicts {e: array} holding only the experts that are needed."""
+    """Per-expert host pointer tables and the weight type (0: bf16 bit
+    patterns in uint16, 1: fp32).  gate_up/down may be full [E,...] arrays or
+    dicts {e: array} holding only the experts that are needed."""
     gp = (ctypes.c_void_p * E)()
     dp = (ctypes.c_void_p * E)()
     keep = []
+    wtype = None
     for e in range(E):
         if isinstance(gate_up, dict):
             g = gate_up.get(e)
@@ -132,12 +137,17 @@ def _expert_ptrs(gate_up, down, E):
         else:
             g, d = gate_up[e], down[e]
         if g is not None:
-            g = np.ascontiguousarray(g, dtype=np.uint16)
-            d = np.ascontiguousarray(d, dtype=np.uint16)
+            t = 1 if np.asarray(g).dtype == np.float32 else 0
+            wtype = t if wtype is None else wtype
+            if t != wtype:
+                raise ValueError("expert weights of one call must share a type")
+            dt = np.float32 if t == 1 else np.uint16
+            g = np.ascontiguousarray(g, dtype=dt)
+            d = np.ascontiguousarray(d, dtype=dt)
             keep += [g, d]
             gp[e] = g.ctypes.data
             dp[e] = d.ctypes.data
-    return gp, dp, keep
+    return gp, dp, keep, (wtype or 0)
 
 
 def experts(x, gate_up, down, ids, w, E, mode=DEDUP, residual=None, return_parts=False):
@@ -149,18 +159,31 @@ def experts(x, gate_up, down, ids, w, E, mode=DEDUP, residual=None, return_parts
     k = ia.shape[1]
     g0 = gate_up[int(ia.flat[0])] if isinstance(gate_up, dict) and B > 0 else gate_up[0]
     I = g0.shape[0] // 2
-    gp, dp, keep = _expert_ptrs(gate_up, down, E)
+    gp, dp, keep, wtype = _expert_ptrs(gate_up, down, E)
     res = None if residual is None else np.ascontiguousarray(residual, dtype=np.float32)
     y = np.empty((B, H), np.float32)
     hr = np.empty((max(B * k, 1), I), np.float32)
     orr = np.empty((max(B * k, 1), H), np.float32)
-    _check(_load().oracle_experts(_ptr(xa), xd, ctypes.addressof(gp), ctypes.addressof(dp),
-                                  _ptr(ia), _ptr(wa), B, H, I, E, k, mode, _ptr(res), _ptr(y),
-                                  _ptr(hr), _ptr(orr)), "experts")
+    _check(_load().oracle_experts_w(_ptr(xa), xd, ctypes.addressof(gp), ctypes.addressof(dp), wtype,
+                                    _ptr(ia), _ptr(wa), B, H, I, E, k, mode, _ptr(res), _ptr(y),
+                                    _ptr(hr), _ptr(orr)), "experts")
     del keep
     if return_parts:
         return y, hr[:B * k], orr[:B * k]
     return y
+
+
+def dequant_fp8_block(q, scale):
+    """Block-scaled FP8 (E4M3 codes [R, C] uint8, fp32 scales [ceil(R/128),
+    ceil(C/128)]) -> fp32 [R, C]: decode(q) * scale of the code's block."""
+    qa = np.ascontiguousarray(q, dtype=np.uint8)
+    sa = np.ascontiguousarray(scale, dtype=np.float32)
+    R, C = qa.shape
+    if sa.shape != ((R + 127) // 128, (C + 127) // 128):
+        raise ValueError(f"scale shape {sa.shape} for codes {qa.shape}")
+    out = np.empty((R, C), np.float32)
+    _check(_load().oracle_dequant_fp8_block(_ptr(qa), _ptr(sa), R, C, _ptr(out)), "dequant_fp8_block")
+    return out
 
 
 def layer(x, w_router, gate_up, down, k, bias=None, mode=DEDUP, residual=None):

@@ -52,6 +52,34 @@ static float bf16_to_f32(uint16_t b) {
     return f;
 }
 
+/* One FP8 E4M3 code as fp32 (the OCP 8-bit floating point format, "E4M3":
+ * sign, 4 exponent bits with bias 7, 3 mantissa bits; exponent 0 holds the
+ * subnormals m/8 * 2^-6; S.1111.111 is NaN; there are no infinities).  The
+ * format is not on the pages, which name "fp8_block" expert weights only. */
+static float fp8e4m3_to_f32(uint8_t b) {
+    const int sgn = b >> 7, e = (b >> 3) & 15, m = b & 7;
+    float v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexpf((float)m / 8.0f, -6);
+    else
+        v = ldexpf(1.0f + (float)m / 8.0f, e - 7);
+    return sgn ? -v : v;
+}
+
+/* Block-scaled FP8 weights ("fp8_block"): a [R, C] matrix of E4M3 codes with
+ * one fp32 scale per 128 x 128 block (row-major over the blocks, ceil(C/128)
+ * per block row):  w[r,c] = decode(q[r,c]) * scale[r/128][c/128], an fp32
+ * product. */
+int oracle_dequant_fp8_block(const uint8_t* q, const float* scale, int R, int C, float* out) {
+    if (R <= 0 || C <= 0 || !q || !scale || !out) return OR_BAD_ARG;
+    const int nbc = (C + 127) / 128;
+    for (int r = 0; r < R; ++r)
+        for (int c = 0; c < C; ++c)
+            out[(size_t)r * C + c] = fp8e4m3_to_f32(q[(size_t)r * C + c]) * scale[(size_t)(r / 128) * nbc + c / 128];
+    return OR_OK;
+}
+
 /* x_dtype: 0 = fp32, 1 = bf16 (raw 16-bit patterns). */
 static float load_x(const void* x, int x_dtype, size_t idx) {
     if (x_dtype == 1) return bf16_to_f32(((const uint16_t*)x)[idx]);
@@ -140,19 +168,26 @@ int oracle_group(const int32_t* ids, int B, int k, int E, int32_t* offsets,
     return OR_OK;
 }
 
+/* An expert weight as fp32: wtype 0 = bf16 bit patterns (widened exactly),
+ * 1 = fp32 (e.g. dequantised block-scaled FP8 weights). */
+static float load_w(const void* w, int wtype, size_t idx) {
+    if (wtype == 1) return ((const float*)w)[idx];
+    return bf16_to_f32(((const uint16_t*)w)[idx]);
+}
+
 /* Pass 1 of one expert on one token, gate/up rows [i0, i1):
  * h[i] = SiLU(G_i . x) * (U_i . x), each dot product in h order.
  * gate_up_e: [2I, H] bf16 (rows [0,I) gate, [I,2I) up). */
-static void expert_gate_rows(const void* x, int x_dtype, size_t x_off, const uint16_t* gate_up_e,
+static void expert_gate_rows(const void* x, int x_dtype, size_t x_off, const void* gate_up_e, int wtype,
                              int H, int I, int i0, int i1, float* hbuf) {
     for (int i = i0; i < i1; ++i) {
         float g = 0.0f, u = 0.0f;
-        const uint16_t* grow = gate_up_e + (size_t)i * H;
-        const uint16_t* urow = gate_up_e + (size_t)(I + i) * H;
+        const size_t grow = (size_t)i * H;
+        const size_t urow = (size_t)(I + i) * H;
         for (int h = 0; h < H; ++h) {
             float xv = load_x(x, x_dtype, x_off + h);
-            g += bf16_to_f32(grow[h]) * xv;
-            u += bf16_to_f32(urow[h]) * xv;
+            g += load_w(gate_up_e, wtype, grow + h) * xv;
+            u += load_w(gate_up_e, wtype, urow + h) * xv;
         }
         float silu = g / (1.0f + expf(-g));
         hbuf[i] = silu * u;
@@ -161,21 +196,21 @@ static void expert_gate_rows(const void* x, int x_dtype, size_t x_off, const uin
 
 /* Pass 2 of one expert on one token, down rows [r0, r1): o[r] = D_r . h,
  * each dot product in i order.  down_e: [H, I] bf16. */
-static void expert_down_rows(const uint16_t* down_e, int I, int r0, int r1, const float* hbuf,
+static void expert_down_rows(const void* down_e, int wtype, int I, int r0, int r1, const float* hbuf,
                              float* o) {
     for (int r = r0; r < r1; ++r) {
         float acc = 0.0f;
-        const uint16_t* drow = down_e + (size_t)r * I;
-        for (int i = 0; i < I; ++i) acc += bf16_to_f32(drow[i]) * hbuf[i];
+        const size_t drow = (size_t)r * I;
+        for (int i = 0; i < I; ++i) acc += load_w(down_e, wtype, drow + i) * hbuf[i];
         o[r] = acc;
     }
 }
 
 /* One expert on one token: h = SiLU(G x) * (U x), o = D h. */
-static void expert_one(const void* x, int x_dtype, size_t x_off, const uint16_t* gate_up_e,
-                       const uint16_t* down_e, int H, int I, float* hbuf, float* o) {
-    expert_gate_rows(x, x_dtype, x_off, gate_up_e, H, I, 0, I, hbuf);
-    expert_down_rows(down_e, I, 0, H, hbuf, o);
+static void expert_one(const void* x, int x_dtype, size_t x_off, const void* gate_up_e, const void* down_e,
+                       int wtype, int H, int I, float* hbuf, float* o) {
+    expert_gate_rows(x, x_dtype, x_off, gate_up_e, wtype, H, I, 0, I, hbuf);
+    expert_down_rows(down_e, wtype, I, 0, H, hbuf, o);
 }
 
 /* rows per work item of the dedup passes */
@@ -190,10 +225,10 @@ static void expert_one(const void* x, int x_dtype, size_t x_off, const uint16_t*
  *            order); every route's arithmetic is the same as in mode 0, so
  *            the two modes are bit-identical.
  * y[t] = sum_j w[t,j] * o[t*k+j], j ascending, then + residual[t] if given. */
-int oracle_experts(const void* x, int x_dtype, const uint16_t* const* gate_up_ptrs,
-                   const uint16_t* const* down_ptrs, const int32_t* ids, const float* w,
-                   int B, int H, int I, int E, int k, int mode, const float* residual,
-                   float* y, float* h_routes, float* o_routes) {
+int oracle_experts_w(const void* x, int x_dtype, const void* const* gate_up_ptrs,
+                     const void* const* down_ptrs, int wtype, const int32_t* ids, const float* w,
+                     int B, int H, int I, int E, int k, int mode, const float* residual,
+                     float* y, float* h_routes, float* o_routes) {
     if (B < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0 || !x || !gate_up_ptrs || !down_ptrs ||
         !ids || !w || !y)
         return OR_BAD_ARG;
@@ -209,7 +244,7 @@ int oracle_experts(const void* x, int x_dtype, const uint16_t* const* gate_up_pt
         for (int t = 0; t < B; ++t)
             for (int j = 0; j < k; ++j) {
                 int r = t * k + j, e = ids[r];
-                expert_one(x, x_dtype, (size_t)t * H, gate_up_ptrs[e], down_ptrs[e], H, I,
+                expert_one(x, x_dtype, (size_t)t * H, gate_up_ptrs[e], down_ptrs[e], wtype, H, I,
                            hb + (size_t)r * I, o + (size_t)r * H);
             }
     } else {
@@ -233,7 +268,7 @@ int oracle_experts(const void* x, int x_dtype, const uint16_t* const* gate_up_pt
                 int i1 = i0 + ORACLE_ROW_BLOCK < I ? i0 + ORACLE_ROW_BLOCK : I;
                 for (int q = offsets[e]; q < offsets[e + 1]; ++q) {
                     int r = ridx[q], t = r / k;
-                    expert_gate_rows(x, x_dtype, (size_t)t * H, gate_up_ptrs[e], H, I, i0, i1,
+                    expert_gate_rows(x, x_dtype, (size_t)t * H, gate_up_ptrs[e], wtype, H, I, i0, i1,
                                      hb + (size_t)r * I);
                 }
             }
@@ -246,7 +281,7 @@ int oracle_experts(const void* x, int x_dtype, const uint16_t* const* gate_up_pt
                 int r1 = r0 + ORACLE_ROW_BLOCK < H ? r0 + ORACLE_ROW_BLOCK : H;
                 for (int q = offsets[e]; q < offsets[e + 1]; ++q) {
                     int r = ridx[q];
-                    expert_down_rows(down_ptrs[e], I, r0, r1, hb + (size_t)r * I,
+                    expert_down_rows(down_ptrs[e], wtype, I, r0, r1, hb + (size_t)r * I,
                                      o + (size_t)r * H);
                 }
             }
@@ -265,6 +300,15 @@ int oracle_experts(const void* x, int x_dtype, const uint16_t* const* gate_up_pt
     if (!o_routes) free(o);
     if (!h_routes) free(hb);
     return OR_OK;
+}
+
+/* The expert pass with bf16 expert weights. */
+int oracle_experts(const void* x, int x_dtype, const uint16_t* const* gate_up_ptrs,
+                   const uint16_t* const* down_ptrs, const int32_t* ids, const float* w,
+                   int B, int H, int I, int E, int k, int mode, const float* residual,
+                   float* y, float* h_routes, float* o_routes) {
+    return oracle_experts_w(x, x_dtype, (const void* const*)gate_up_ptrs, (const void* const*)down_ptrs, 0, ids,
+                            w, B, H, I, E, k, mode, residual, y, h_routes, o_routes);
 }
 
 /* RMSNorm of every token's row, the norm half of the fused "norm + residual

@@ -386,3 +386,68 @@ def test_prenorm_stack_adds_the_layer_of_the_normalised_input_to_the_raw_input()
     # without the norm the layer sees a different input: the norm is applied
     xs, _ = oracle.stack(x, layers[:1], k)
     assert not np.allclose(xs, x1)
+
+
+# ------------------------------------------------------- block-scaled FP8
+def test_fp8_e4m3_decode_matches_torch_on_every_code():
+    codes = np.arange(256, dtype=np.uint8).reshape(1, 256)
+    # one 1 x 256 matrix, two blocks of columns, unit scales
+    dq = oracle.dequant_fp8_block(codes, np.ones((1, 2), np.float32))
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(dq), nan) and nan.sum() == 2  # S.1111.111
+    assert np.array_equal(dq[~nan], ref[~nan])
+    assert float(np.nanmax(dq)) == 448.0 and float(dq[0, 1]) == 2.0 ** -9  # largest; smallest subnormal
+
+
+def test_fp8_block_scales_apply_per_128_block():
+    rng = np.random.default_rng(31)
+    R, C = 200, 300  # ragged blocks at both edges
+    codes = rng.integers(0, 126, size=(R, C)).astype(np.uint8)  # finite positive codes
+    scale = rng.uniform(0.5, 2.0, size=(2, 3)).astype(np.float32)
+    dq = oracle.dequant_fp8_block(codes, scale)
+    base = oracle.dequant_fp8_block(codes, np.ones((2, 3), np.float32))
+    for br in range(2):
+        for bc in range(3):
+            blk = np.s_[128 * br:128 * (br + 1), 128 * bc:128 * (bc + 1)]
+            assert np.array_equal(dq[blk], (base[blk] * scale[br, bc]).astype(np.float32))
+
+
+def test_fp8_block_round_trip_error_is_within_the_format_bound():
+    w = synth.normal_bf16((2, 384, 256), 0.02, 0, 99, 0, "cpu")
+    q, s = synth.quantize_fp8_block(w)
+    wf = w.to(torch.float32).numpy()
+    for e in range(2):
+        dq = oracle.dequant_fp8_block(q[e].numpy(), s[e].numpy())
+        # 3 mantissa bits: a normal code is within 2^-4 of its value; the
+        # subnormals (below 2^-6 of the block's scale) within 2^-10 * scale
+        sc = np.repeat(np.repeat(s[e].numpy(), 128, 0), 128, 1)[:384, :256]
+        assert np.all(np.abs(dq - wf[e]) <= np.maximum(2.0 ** -4 * np.abs(wf[e]), 2.0 ** -10 * sc) + 1e-12)
+
+
+def test_fp8_layer_is_the_bf16_layer_on_the_dequantised_weights():
+    """The expert pass on fp32 weights (the FP8 path's dequantised weights)
+    against the fp64 brute force on the same weights, and close to the bf16
+    layer it was quantised from."""
+    w = synth.TINY
+    lw = synth.make_layer_fp8(w, 0, seed=0)
+    x = synth.make_x(w, 0, seed=0).numpy()
+    wr = synth.bf16_bits(lw["w_router"])
+    gq = {e: oracle.dequant_fp8_block(lw["gate_up_q"][e].numpy(), lw["gate_up_scale"][e].numpy()) for e in range(w.E)}
+    dq = {e: oracle.dequant_fp8_block(lw["down_q"][e].numpy(), lw["down_scale"][e].numpy()) for e in range(w.E)}
+    lo = oracle.router(x, wr)
+    ids, wts = oracle.topk(lo, w.top_k)
+    y8 = oracle.experts(x, gq, dq, ids, wts, w.E)
+    # fp64 brute force over the dequantised weights (routing fixed by the router)
+    y64 = np.zeros_like(x, dtype=np.float64)
+    for t in range(w.B):
+        for j in range(w.top_k):
+            e = ids[t, j]
+            G = gq[e].astype(np.float64)
+            g = G[:w.I] @ x[t]
+            u = G[w.I:] @ x[t]
+            h = g / (1.0 + np.exp(-g)) * u
+            y64[t] += wts[t, j] * (dq[e].astype(np.float64) @ h)
+    assert np.max(np.abs(y8 - y64)) <= 2e-5 * np.max(np.abs(y64))
+    ybf = oracle.experts(x, synth.bf16_bits(lw["gate_up"]), synth.bf16_bits(lw["down"]), ids, wts, w.E)
+    assert np.max(np.abs(y8 - ybf)) <= 0.1 * np.max(np.abs(ybf))  # quantisation noise, not a different layer
