@@ -20,7 +20,8 @@ and combine, with the residual add), one fused persistent kernel launch.
             bytes, GB/s and fraction of the peak, unique experts, reuse,
             near-tie tokens and kernel launches per step; and the dense
             counterpart of the stack (E=1, top-1, I=1536: the same active
-            bytes per layer), with moe_over_dense_time beside the headline.
+            bytes per layer), with moe_over_dense_time beside the headline;
+            and the stack as a pre-norm stack (RMSNorm fused).
 
 --impl reference times the CPU oracle itself on this workload (rank 0 only).
 --workload {uniform,skewed,prefill,tiny} times one layer of that workload.
@@ -431,13 +432,31 @@ def run_layer_workload(args):
     print(json.dumps(line), flush=True)
 
 
-def measure_stack(api, accounting, synth, w, dev, steps, warmup, flags=0, seed=0, flush=None):
+def measure_stack(api, accounting, synth, w, dev, steps, warmup, flags=0, seed=0, flush=None, norm=False,
+                  fp8=False):
     """One token through an L-layer stack per step (L2 flushed before each
-    timed step, CUDA events on the launching stream).  Returns the sub-record."""
+    timed step, CUDA events on the launching stream); norm=True makes it a
+    pre-norm stack (RMSNorm fused into the router and residual add), fp8=True
+    gives it block-scaled FP8 expert weights. Returns the sub-record."""
     import numpy as np
     import torch
-    layers = [synth.make_layer(w, l, seed=seed, device=dev) for l in range(w.layers)]
-    sw = api.StackWeights(layers)
+    if fp8:
+        layers = [synth.make_layer_fp8(w, l, seed=seed, device=dev) for l in range(w.layers)]
+        for lw in layers:  # only the codes and scales stay resident
+            lw.pop("gate_up", None)
+            lw.pop("down", None)
+        sw = api.StackWeightsFP8(layers)
+        fwd = lambda xb, **kw: api.stack_forward_fp8_(xb, sw, w.top_k, **kw)
+        lbytes = accounting.layer_bytes_fp8
+    else:
+        layers = [synth.make_layer(w, l, seed=seed, device=dev) for l in range(w.layers)]
+        if norm:
+            for l, lw in enumerate(layers):
+                lw["norm"] = synth.norm_weights(w.H, l, seed=seed, device=dev)
+        sw = api.StackWeights(layers)
+        fwd = ((lambda xb, **kw: api.stack_forward_norm_(xb, sw, w.top_k, eps=1e-6, **kw)) if norm else
+               (lambda xb, **kw: api.stack_forward_(xb, sw, w.top_k, **kw)))
+        lbytes = accounting.layer_bytes
     xs = [synth.make_x(w, s, seed=seed, device=dev) for s in range(warmup + steps)]
     xbuf = torch.empty_like(xs[0])
     ids = torch.empty((w.layers, w.B, w.top_k), dtype=torch.int32, device=dev)
@@ -448,7 +467,7 @@ def measure_stack(api, accounting, synth, w, dev, steps, warmup, flags=0, seed=0
     for i in range(warmup):
         flush.zero_()
         xbuf.copy_(xs[i])
-        api.stack_forward_(xbuf, sw, w.top_k, flags=flags, ids_out=ids, workspace=ws, status=status, stream=stream)
+        fwd(xbuf, flags=flags, ids_out=ids, workspace=ws, status=status, stream=stream)
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     uniq, launches = [], 0
@@ -457,7 +476,7 @@ def measure_stack(api, accounting, synth, w, dev, steps, warmup, flags=0, seed=0
         xbuf.copy_(xs[warmup + s])
         n0 = api.launch_count()
         ev[s][0].record(stream)
-        api.stack_forward_(xbuf, sw, w.top_k, flags=flags, ids_out=ids, workspace=ws, status=status, stream=stream)
+        fwd(xbuf, flags=flags, ids_out=ids, workspace=ws, status=status, stream=stream)
         ev[s][1].record(stream)
         launches += api.launch_count() - n0
         uniq.append(ids.clone())
@@ -468,13 +487,14 @@ def measure_stack(api, accounting, synth, w, dev, steps, warmup, flags=0, seed=0
     mean_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     u_layers = [len(np.unique(u.cpu().numpy()[l])) for u in uniq for l in range(w.layers)]
     bytes_step = statistics.mean(
-        sum(accounting.layer_bytes(w.H, w.I, w.E, len(np.unique(u.cpu().numpy()[l]))) for l in range(w.layers))
+        sum(lbytes(w.H, w.I, w.E, len(np.unique(u.cpu().numpy()[l]))) for l in range(w.layers))
         for u in uniq)
     achieved = bytes_step / (mean_ms / 1e3) / 1e9
     peak, _ = hbm_peak()
     del layers, sw
     torch.cuda.empty_cache()
-    return {"workload": w.name, "B": w.B, "H": w.H, "I": w.I, "E": w.E, "top_k": w.top_k, "layers": w.layers,
+    return {"workload": w.name + ("_rmsnorm" if norm else "") + ("_fp8_block128" if fp8 else ""), "B": w.B, "H": w.H, "I": w.I, "E": w.E,
+            "top_k": w.top_k, "layers": w.layers,
             "ms": mean_ms, "tokens_per_s": w.B / (mean_ms / 1e3), "us_per_layer": 1000.0 * mean_ms / w.layers,
             "bytes_per_step": bytes_step, "hbm_gbs": achieved, "frac": achieved / peak,
             "unique_experts": statistics.mean(u_layers), "launches_per_step": launches / steps, "steps": steps}
@@ -494,6 +514,11 @@ def config_records(api, accounting, synth, dev, steps, warmup, seed=0):
             key = f"{'uniform' if base is synth.UNIFORM else 'skewed'}_B{B}"
             out[key] = measure_layer(api, accounting, synth, base.with_batch(B), dev, steps, warmup, 0, seed,
                                      flush, lw=lw)
+            if base is synth.SKEWED and B > 4:
+                # the step's most chosen experts kept in L2 across steps (an L2
+                # policy on the weight copies; the same flush between steps)
+                out[key + "_hot_l2"] = measure_layer(api, accounting, synth, base.with_batch(B), dev, steps, warmup,
+                                                     api.MOE_F_HOT_L2, seed, flush, lw=lw)
         del lw
         torch.cuda.empty_cache()
     out["prefill"] = measure_layer(api, accounting, synth, synth.PREFILL, dev, steps, warmup, 0, seed, flush)
@@ -501,6 +526,12 @@ def config_records(api, accounting, synth, dev, steps, warmup, seed=0):
     # the dense counterpart of the stack (one expert, top-1, same active bytes
     # per layer): the dense-vs-MoE comparison of the first page
     out["dense_stack"] = measure_stack(api, accounting, synth, synth.DENSE, dev, steps, warmup, 0, seed, flush)
+    # the stack as a pre-norm stack: RMSNorm fused into the router and residual add
+    out["stack_rmsnorm"] = measure_stack(api, accounting, synth, synth.STACK, dev, steps, warmup, 0, seed, flush,
+                                         norm=True)
+    # the stack with block-scaled FP8 experts (E4M3 codes, fp32 scale per 128x128 block)
+    out["stack_fp8"] = measure_stack(api, accounting, synth, synth.STACK, dev, steps, warmup, 0, seed, flush,
+                                     fp8=True)
     return out
 
 

@@ -88,6 +88,13 @@ typedef enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 } moe_dtype;
 #define MOE_F_NO_PREFETCH 16u /* stack: no speculative L2 prefetch of the next layer's
                                predicted experts (results are unchanged; the prefetch
                                only moves bytes earlier) */
+#define MOE_F_HOT_L2 32u    /* layer/stack, batches beyond the decode kernel: keep
+                               the step's most chosen experts in L2 for the next
+                               steps -- the experts with at least MOE_TC_MIN_ROUTES
+                               routes load their weights with an evict_last L2
+                               policy, the others stream with evict_first ("MoE
+                               Performance Optimization Analysis", Option 3:
+                               expert caching; results are unchanged) */
 #define MOE_TC_MIN_ROUTES 8 /* by default an expert chosen by at least this many
                                routes runs on the tensor cores */
 
@@ -219,6 +226,49 @@ int moe_stack_forward(int L, const uint16_t* const* w_router, const float* const
                       int I, int E, int top_k, float* x_inout, int32_t* expert_ids_out,
                       uint32_t flags, void* workspace, size_t workspace_bytes,
                       int32_t* dev_status, void* stream);
+
+/*
+ * moe_stack_forward_norm -- a pre-norm stack: L MoE layers, each applied to
+ * the RMSNorm of its input, with the residual add between them,
+ *   x <- x + layer_l(RMSNorm_l(x)),
+ *   RMSNorm_l(x)[t,h] = (x[t,h] / sqrt(mean_h x[t,h]^2 + eps)) * norm_w[l][h],
+ * entirely on the device ("TEXT Generation Optimization Report", Fused
+ * Operations: fused_rms_norm_residual, norm + residual add; the RMSNorm
+ * formula is the standard one, the page gives none).  For batches the
+ * persistent decode kernel takes (up to 4 tokens, 32 routes) the norm is
+ * fused into the router and the residual add: the next layer's logits are
+ * formed from the CTAs' partial sums over g * x and x^2, so it costs no
+ * extra pass or barrier.  Larger batches run a norm kernel per layer.
+ * norm_w is a HOST array of L device pointers to [H] fp32 weights; eps in
+ * [0, 1].  The other arguments are those of moe_stack_forward.
+ */
+int moe_stack_forward_norm(int L, const uint16_t* const* w_router, const float* const* logit_bias,
+                           const uint16_t* const* gate_up, const uint16_t* const* down, const float* const* norm_w,
+                           float eps, int B, int H, int I, int E, int top_k, float* x_inout,
+                           int32_t* expert_ids_out, uint32_t flags, void* workspace, size_t workspace_bytes,
+                           int32_t* dev_status, void* stream);
+
+/*
+ * moe_stack_forward_fp8 -- moe_stack_forward with block-scaled FP8 expert
+ * weights ("fp8_block", one of the expert formats of "perf(cpu-moe): dedup
+ * experts across the batch in pass 1 - #46", commit message; the encoding is
+ * not on the pages: the OCP FP8 E4M3 format is taken).  Expert e's gate_up
+ * [2I, H] and down [H, I] are E4M3 codes (one byte each, row-major), and
+ *   w[r, c] = decode(q[r, c]) * scale[r / 128][c / 128]   (an fp32 product)
+ * with the fp32 block scales gate_up_scale [E][ceil(2I/128)][ceil(H/128)] and
+ * down_scale [E][ceil(H/128)][ceil(I/128)].  The router stays bf16.  The
+ * experts stream half the bytes of bf16 weights; every sum stays fp32.
+ * gate_up_q, gate_up_scale, down_q and down_scale are HOST arrays of L
+ * device pointers.  Requires H and I multiples of 16 and a batch the
+ * persistent decode kernel takes (up to 4 tokens and 32 routes), else
+ * MOE_ERR_UNSUPPORTED; flags: MOE_F_NO_DEDUP, MOE_F_NO_PREFETCH.  The other
+ * arguments are those of moe_stack_forward.
+ */
+int moe_stack_forward_fp8(int L, const uint16_t* const* w_router, const float* const* logit_bias,
+                          const uint8_t* const* gate_up_q, const float* const* gate_up_scale,
+                          const uint8_t* const* down_q, const float* const* down_scale, int B, int H, int I, int E,
+                          int top_k, float* x_inout, int32_t* expert_ids_out, uint32_t flags, void* workspace,
+                          size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /*
  * moe_workspace_grouping -- where a workspace holds the grouped route list

@@ -28,3 +28,12 @@ def traffic_model_speedup(reuse: float) -> float:
 
 def sigma_logit(w) -> float:
     return w.sigma_router * math.sqrt(w.H)
+
+
+def layer_bytes_fp8(H: int, I: int, E: int, unique: int) -> int:
+    """The same for block-scaled FP8 experts: the bf16 router plus each unique
+    selected expert's E4M3 codes (3I*H bytes) and fp32 block scales (one per
+    128 x 128 block of gate_up [2I, H] and down [H, I])."""
+    nb = lambda n: (n + 127) // 128
+    scales = 4 * (nb(2 * I) * nb(H) + nb(H) * nb(I))
+    return 2 * E * H + unique * (3 * I * H + scales)

@@ -37,6 +37,10 @@ _lib.moe_expert_forward_noalloc.argtypes = [_P, _I, _P, _P, _P, _P, _P, _P, _P, 
 _lib.moe_layer_forward.argtypes = [_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _U,
                                    _P, _S, _P, _P]
 _lib.moe_stack_forward.argtypes = [_I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _U, _P, _S, _P, _P]
+_lib.moe_stack_forward_fp8.argtypes = [_I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _U, _P, _S, _P,
+                                       _P]
+_lib.moe_stack_forward_norm.argtypes = [_I, _P, _P, _P, _P, _P, ctypes.c_float, _I, _I, _I, _I, _I, _P, _P, _U,
+                                        _P, _S, _P, _P]
 _lib.moe_workspace_grouping.argtypes = [_P, _S, _I, _I, _I, _I, _I, ctypes.POINTER(_P), ctypes.POINTER(_P),
                                         ctypes.POINTER(_P), ctypes.POINTER(_P)]
 _lib.moe_forward_path.argtypes = [_I, _I, _I, _I, _I, _I, _U, ctypes.POINTER(_I), ctypes.POINTER(_I)]
@@ -50,11 +54,13 @@ _lib.moe_inject_barrier_stall.restype = ctypes.c_int
 _lib.moe_status_string.argtypes = [_I]
 _lib.moe_status_string.restype = ctypes.c_char_p
 for _f in ("moe_workspace_bytes", "moe_route", "moe_group_by_expert", "moe_expert_forward",
-           "moe_expert_forward_noalloc", "moe_layer_forward", "moe_stack_forward", "moe_workspace_grouping"):
+           "moe_expert_forward_noalloc", "moe_layer_forward", "moe_stack_forward", "moe_stack_forward_norm",
+           "moe_stack_forward_fp8", "moe_workspace_grouping"):
     getattr(_lib, _f).restype = ctypes.c_int
 
 EXPORTED = ("moe_workspace_bytes", "moe_route", "moe_group_by_expert", "moe_expert_forward",
-            "moe_expert_forward_noalloc", "moe_layer_forward", "moe_stack_forward", "moe_workspace_grouping",
+            "moe_expert_forward_noalloc", "moe_layer_forward", "moe_stack_forward", "moe_stack_forward_norm",
+            "moe_stack_forward_fp8", "moe_workspace_grouping",
             "moe_launch_count", "moe_forward_path", "moe_set_trace_buffer",
             "moe_inject_barrier_stall", "moe_status_string")
 
@@ -74,6 +80,7 @@ MOE_F_UNFUSED = 2
 MOE_F_FORCE_TC = 4
 MOE_F_NO_TC = 8
 MOE_F_NO_PREFETCH = 16
+MOE_F_HOT_L2 = 32
 TC_MIN_ROUTES = 8
 MAX_E, MAX_TOPK, MAX_B, MAX_DIM, MAX_LAYERS = 256, 8, 1024, 16384, 64
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -373,6 +380,63 @@ def layer_forward(x, w_router, gate_up, down, top_k, bias=None, residual=None, f
     return y, ids, w
 
 
+class StackWeightsFP8:
+    """Host pointer tables for moe_stack_forward_fp8: each layer dict holds
+    w_router [E,H] bf16, gate_up_q [E,2I,H] / down_q [E,H,I] uint8 E4M3 codes,
+    gate_up_scale [E,ceil(2I/128),ceil(H/128)] / down_scale
+    [E,ceil(H/128),ceil(I/128)] fp32, and optionally bias [E]."""
+
+    def __init__(self, layers):
+        self.layers = layers
+        L = self.L = len(layers)
+        g = layers[0]["gate_up_q"]
+        if g.dim() != 3 or g.shape[1] % 2:
+            raise ValueError(f"gate_up_q has shape {tuple(g.shape)}, expected [E, 2I, H]")
+        self.E, twoI, self.H = g.shape
+        self.I = twoI // 2
+        nb = lambda n: (n + 127) // 128
+        for l in layers:
+            _shape(l["w_router"], (self.E, self.H), "w_router")
+            _shape(l["gate_up_q"], (self.E, 2 * self.I, self.H), "gate_up_q")
+            _shape(l["down_q"], (self.E, self.H, self.I), "down_q")
+            _shape(l["gate_up_scale"], (self.E, nb(2 * self.I), nb(self.H)), "gate_up_scale")
+            _shape(l["down_scale"], (self.E, nb(self.H), nb(self.I)), "down_scale")
+            _shape(l.get("bias"), (self.E,), "bias")
+            _need(l["w_router"], torch.bfloat16, "w_router")
+            for n in ("gate_up_q", "down_q"):
+                _need(l[n], torch.uint8, n)
+            for n in ("gate_up_scale", "down_scale"):
+                _need(l[n], torch.float32, n)
+        P = lambda name: (ctypes.c_void_p * L)(*[l[name].data_ptr() for l in layers])
+        self.wr, self.gq, self.gs, self.dq, self.ds = (P(n) for n in ("w_router", "gate_up_q", "gate_up_scale",
+                                                                       "down_q", "down_scale"))
+        has_bias = any(l.get("bias") is not None for l in layers)
+        self.bias = ((ctypes.c_void_p * L)(*[(l["bias"].data_ptr() if l.get("bias") is not None else None)
+                                             for l in layers]) if has_bias else None)
+
+
+def stack_forward_fp8_(x, stack: StackWeightsFP8, top_k, flags=0, ids_out=None, workspace=None, status=None,
+                       stream=None):
+    """In place, block-scaled FP8 experts: x [B,H] fp32 <- x + layer_l(x)."""
+    if x.dim() != 2 or stack is None or x.shape[1] != stack.H:
+        raise ValueError(f"x has shape {tuple(x.shape)}, expected [B, H] with H of the stack's weights")
+    _shape(ids_out, (stack.L, x.shape[0], top_k), "ids_out")
+    _shape(status, (1,), "status")
+    _need(x, torch.float32, "x")
+    for t, dt, n in ((ids_out, torch.int32, "ids_out"), (workspace, torch.uint8, "workspace"),
+                     (status, torch.int32, "status")):
+        _opt(t, dt, n, x.device)
+    B, H = x.shape
+    ws = workspace if workspace is not None else new_workspace(B, H, stack.I, stack.E, top_k, x.device)
+    _check(_lib.moe_stack_forward_fp8(stack.L, ctypes.addressof(stack.wr),
+                                      ctypes.addressof(stack.bias) if stack.bias is not None else None,
+                                      ctypes.addressof(stack.gq), ctypes.addressof(stack.gs),
+                                      ctypes.addressof(stack.dq), ctypes.addressof(stack.ds), B, H, stack.I, stack.E,
+                                      top_k, _ptr(x), _ptr(ids_out), flags, _ptr(ws), ws.numel(), _ptr(status),
+                                      _stream(stream)), "moe_stack_forward_fp8")
+    return x
+
+
 class StackWeights:
     """Host pointer tables for moe_stack_forward (built once, reused)."""
 
@@ -383,6 +447,8 @@ class StackWeights:
         self.wr = (ctypes.c_void_p * L)(*[l["w_router"].data_ptr() for l in layers])
         self.gu = (ctypes.c_void_p * L)(*[l["gate_up"].data_ptr() for l in layers])
         self.dn = (ctypes.c_void_p * L)(*[l["down"].data_ptr() for l in layers])
+        has_norm = all(l.get("norm") is not None for l in layers)
+        self.norm = ((ctypes.c_void_p * L)(*[l["norm"].data_ptr() for l in layers]) if has_norm else None)
         has_bias = any(l.get("bias") is not None for l in layers)
         self.bias = ((ctypes.c_void_p * L)(*[(l["bias"].data_ptr() if l.get("bias") is not None else None)
                                              for l in layers]) if has_bias else None)
@@ -396,6 +462,9 @@ class StackWeights:
             _shape(l["gate_up"], (self.E, 2 * self.I, self.H), "gate_up")
             _shape(l["down"], (self.E, self.H, self.I), "down")
             _shape(l.get("bias"), (self.E,), "bias")
+            _shape(l.get("norm"), (self.H,), "norm")
+            if l.get("norm") is not None:
+                _need(l["norm"], torch.float32, "norm")
             for n in ("w_router", "gate_up", "down"):
                 _need(l[n], torch.bfloat16, n)
             if l.get("bias") is not None:
@@ -420,6 +489,31 @@ def stack_forward_(x, stack: StackWeights, top_k, flags=0, ids_out=None, workspa
                                   ctypes.addressof(stack.gu), ctypes.addressof(stack.dn), B, H, stack.I,
                                   stack.E, top_k, _ptr(x), _ptr(ids_out), flags, _ptr(ws), ws.numel(),
                                   _ptr(status), _stream(stream)), "moe_stack_forward")
+    return x
+
+
+def stack_forward_norm_(x, stack: StackWeights, top_k, eps=1e-6, flags=0, ids_out=None, workspace=None,
+                        status=None, stream=None):
+    """Pre-norm stack, in place: x <- x + layer_l(RMSNorm_l(x)) for every
+    layer (each layer dict carries its "norm" weights [H] fp32).  Returns x."""
+    if x.dim() != 2 or stack is None or x.shape[1] != stack.H:
+        raise ValueError(f"x has shape {tuple(x.shape)}, expected [B, H] with H of the stack's weights")
+    if stack.norm is None:
+        raise ValueError("every layer needs its 'norm' weights for a pre-norm stack")
+    _shape(ids_out, (stack.L, x.shape[0], top_k), "ids_out")
+    _shape(status, (1,), "status")
+    _need(x, torch.float32, "x")
+    for t, dt, n in ((ids_out, torch.int32, "ids_out"), (workspace, torch.uint8, "workspace"),
+                     (status, torch.int32, "status")):
+        _opt(t, dt, n, x.device)
+    B, H = x.shape
+    ws = workspace if workspace is not None else new_workspace(B, H, stack.I, stack.E, top_k, x.device)
+    _check(_lib.moe_stack_forward_norm(stack.L, ctypes.addressof(stack.wr),
+                                       ctypes.addressof(stack.bias) if stack.bias is not None else None,
+                                       ctypes.addressof(stack.gu), ctypes.addressof(stack.dn),
+                                       ctypes.addressof(stack.norm), float(eps), B, H, stack.I, stack.E, top_k,
+                                       _ptr(x), _ptr(ids_out), flags, _ptr(ws), ws.numel(), _ptr(status),
+                                       _stream(stream)), "moe_stack_forward_norm")
     return x
 
 

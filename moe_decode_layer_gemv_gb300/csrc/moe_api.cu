@@ -158,11 +158,12 @@ __global__ void __launch_bounds__(kThreads) fused_kernel(Ctx c, StackArgs sa, un
 // -------------------------------------------------------------- host side
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-constexpr unsigned kAllFlags = MOE_F_NO_DEDUP | MOE_F_UNFUSED | MOE_F_FORCE_TC | MOE_F_NO_TC | MOE_F_NO_PREFETCH;
+constexpr unsigned kAllFlags =
+    MOE_F_NO_DEDUP | MOE_F_UNFUSED | MOE_F_FORCE_TC | MOE_F_NO_TC | MOE_F_NO_PREFETCH | MOE_F_HOT_L2;
 
 struct WsLayout {
     size_t logits, ids, rw, offsets, route_idx, unique, num_unique, status, bar, acc, acc_end, h, o;
-    size_t x_hi, x_lo, h_hi, h_lo, seg_list, seg_count, alog, total;
+    size_t x_hi, x_lo, h_hi, h_lo, seg_list, seg_count, alog, xn, total;
 };
 
 static WsLayout ws_layout(int B, int H, int I, int E, int k) {
@@ -194,6 +195,7 @@ static WsLayout ws_layout(int B, int H, int I, int E, int k) {
     L.seg_list = take(sizeof(int32_t) * 2 * (R > (size_t)E ? R : (size_t)E));
     L.seg_count = take(sizeof(int32_t) * 2);
     L.alog = take(sizeof(float) * (size_t)B * E);
+    L.xn = take(sizeof(float) * (size_t)B * H);  // pre-norm stacks: the normalised layer input
     L.total = off;
     return L;
 }
@@ -555,7 +557,8 @@ static int launch_fused(const Ctx& c, const StackArgs& sa, unsigned* bar, cudaSt
 // The decode kernel keeps x [B,H], h [R,I], the combine outputs and the next
 // router's column slice in shared memory and gives the rest to the weight
 // ring; it applies when B <= 4, B*k <= 32 and the ring gets >= 4 stages.
-static bool decode_plan(int B, int H, int I, int E, int k, int sms, DkParams& p, size_t& smem) {
+static bool decode_plan(int B, int H, int I, int E, int k, int sms, DkParams& p, size_t& smem, bool norm = false,
+                        int wb = 2) {
     const int R = B * k;
     if (B < 1 || B > kDkMaxB || R > kDkMaxR || sms < 1 || sms > 1024) return false;
     const int ng = H >> 3;
@@ -573,8 +576,11 @@ static bool decode_plan(int B, int H, int I, int E, int k, int sms, DkParams& p,
     off = align_up(off + sizeof(float) * (size_t)R * maxrows, 128);
     p.off_wr = (int)off;
     off = align_up(off + sizeof(uint16_t) * (size_t)E * maxrows, 128);
+    p.off_gq = (int)off;  // pre-norm stacks: two layers' norm weights
+    if (norm) off = align_up(off + 2 * sizeof(float) * (size_t)H, 128);
     p.off_ring = (int)off;
-    const size_t stage = align_up((size_t)(4 * H > 2 * I ? 4 * H : 2 * I), 128);
+    // a stage holds one gate/up row pair or a block of down rows (wb bytes an element)
+    const size_t stage = align_up((size_t)(2 * H > I ? 2 * wb * H : wb * I), 128);
     if (off >= (size_t)kDkSmemMax) return false;
     size_t S = ((size_t)kDkSmemMax - off) / stage;
     if (S > (size_t)kDkMaxStages) S = kDkMaxStages;
@@ -590,15 +596,24 @@ static bool decode_plan(int B, int H, int I, int E, int k, int sms, DkParams& p,
     return true;
 }
 
-static int launch_decode(DkParams& p, size_t smem, int sms, char* ws, const WsLayout& L, cudaStream_t st) {
+static int launch_decode(DkParams& p, size_t smem, int sms, char* ws, const WsLayout& L, cudaStream_t st,
+                         bool fp8 = false) {
     // direct mode for every layer: a CTA's largest share -- ceil(U*I/G) gate/up
     // pairs and maxrows down rows of U experts, U <= R -- fits in the ring area
+    const size_t wb = fp8 ? 1 : 2;
     const size_t Ru = (size_t)p.B * p.k;
-    const size_t g_max = ((Ru * p.I + sms - 1) / sms) * 4 * (size_t)p.H;
-    const size_t d_max = Ru * p.maxrows * 2 * (size_t)p.I;
+    const size_t g_max = ((Ru * p.I + sms - 1) / sms) * 2 * wb * (size_t)p.H;
+    const size_t d_max = Ru * p.maxrows * wb * (size_t)p.I;
     const bool all_direct = g_max + d_max <= (size_t)p.S * p.stage_bytes && g_max < (1u << 20) && d_max < (1u << 20);
     void (*kernel)(DkParams);
-    if (p.B == 1 && all_direct)
+    if (fp8) {  // block-scaled FP8 experts (no traced variant)
+        if (p.B == 1 && all_direct)
+            kernel = decode_kernel<false, 1, true, true>;
+        else if (p.B == 1)
+            kernel = decode_kernel<false, 1, false, true>;
+        else
+            kernel = decode_kernel<false, 4, false, true>;
+    } else if (p.B == 1 && all_direct)
         kernel = p.trace ? decode_kernel<true, 1, true> : decode_kernel<false, 1, true>;
     else if (p.B == 1)
         kernel = p.trace ? decode_kernel<true, 1, false> : decode_kernel<false, 1, false>;
@@ -618,7 +633,7 @@ static int launch_decode(DkParams& p, size_t smem, int sms, char* ws, const WsLa
     // whose extra expert costs more HBM time than its hits save.)
     p.prefetch_k = 0;
     if (p.B == 1 && p.L > 1 && !(p.flags & MOE_F_NO_PREFETCH)) {
-        const unsigned long long per_e = 6ull * p.I * p.H;
+        const unsigned long long per_e = 3ull * wb * p.I * p.H;
         const int kp = p.k;
         if (per_e * kp <= (64ull << 20) && kp <= 32) p.prefetch_k = kp;
     }
@@ -891,6 +906,140 @@ int moe_stack_forward(int Lc, const uint16_t* const* w_router, const float* cons
         return MOE_OK;
     }
     return launch_fused(c, sa, reinterpret_cast<unsigned*>(ws + L.bar), st);
+}
+
+int moe_stack_forward_norm(int Lc, const uint16_t* const* w_router, const float* const* logit_bias,
+                           const uint16_t* const* gate_up, const uint16_t* const* down, const float* const* norm_w,
+                           float eps, int B, int H, int I, int E, int top_k, float* x_inout,
+                           int32_t* expert_ids_out, uint32_t flags, void* workspace, size_t workspace_bytes,
+                           int32_t* dev_status, void* stream) {
+    int rc = check_dims(B, H, I, E, top_k, true);
+    if (rc) return rc;
+    if (Lc < 1 || Lc > MOE_MAX_LAYERS) return MOE_ERR_INVALID_ARG;
+    if (flags & ~kAllFlags) return MOE_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || eps > 1.f) return MOE_ERR_INVALID_ARG;  // rejects NaN too
+    if (B == 0) return MOE_OK;
+    if (!w_router || !gate_up || !down || !norm_w) return MOE_ERR_INVALID_ARG;
+    for (int l = 0; l < Lc; ++l) {
+        MOE_REQ(w_router[l]);
+        MOE_REQ(gate_up[l]);
+        MOE_REQ(down[l]);
+        MOE_REQ(norm_w[l]);
+        if (logit_bias) MOE_OPT(logit_bias[l]);
+    }
+    MOE_REQ(x_inout);
+    MOE_OPT(expert_ids_out);
+    MOE_REQ(workspace);
+    MOE_OPT(dev_status);
+    const WsLayout L = ws_layout(B, H, I, E, top_k);
+    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+    char* ws = static_cast<char*>(workspace);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    LayerWeights lws[MOE_MAX_LAYERS];
+    for (int l = 0; l < Lc; ++l) {
+        lws[l].w_router = w_router[l];
+        lws[l].bias = logit_bias ? logit_bias[l] : nullptr;
+        lws[l].gate_up = gate_up[l];
+        lws[l].down = down[l];
+        lws[l].norm = norm_w[l];
+    }
+    if (!(flags & MOE_F_UNFUSED)) {
+        // small batches: the norm fused into the decode kernel's router and
+        // residual add (one launch for the whole stack)
+        DkParams dp;
+        memset(&dp, 0, sizeof dp);
+        size_t dsm = 0;
+        const int sms = sm_count();
+        if (decode_plan(B, H, I, E, top_k, sms, dp, dsm, true)) {
+            decode_common(dp, B, H, I, E, top_k, Lc, flags, dev_status ? dev_status
+                                                                       : reinterpret_cast<int32_t*>(ws + L.status));
+            dp.x_bf16 = 0;
+            dp.x_in = x_inout;
+            dp.residual = x_inout;
+            dp.y = x_inout;
+            for (int l = 0; l < Lc; ++l) dp.layer[l] = lws[l];
+            dp.ids_out = expert_ids_out;
+            dp.w_out = nullptr;
+            dp.has_norm = 1;
+            dp.eps = eps;
+            return launch_decode(dp, dsm, sms, ws, L, st);
+        }
+    }
+    // otherwise layer by layer: the norm into the workspace, then the layer on
+    // it with the raw input as the residual (y aliases the residual)
+    float* xn = reinterpret_cast<float*>(ws + L.xn);
+    Ctx c = make_ctx(xn, MOE_DT_F32, x_inout, x_inout, B, H, I, E, top_k, flags, ws, L, dev_status);
+    int32_t* ids_ws = c.ids;
+    for (int l = 0; l < Lc; ++l) {
+        rmsnorm_kernel<<<B, kThreads, 0, st>>>(x_inout, norm_w[l], H, eps, xn);
+        if ((rc = launch_check())) return rc;
+        c.w = lws[l];
+        c.ids = expert_ids_out ? expert_ids_out + (size_t)l * B * top_k : ids_ws;
+        if ((flags & MOE_F_UNFUSED) || c.tc_threshold > 0) {
+            if ((rc = launch_unfused_layer(c, st, ws, L))) return rc;
+        } else {
+            StackArgs sa;
+            memset(&sa, 0, sizeof sa);
+            sa.L = 1;
+            sa.bar_extra = g_bar_extra;
+            sa.layer[0] = c.w;
+            sa.ids_out = c.ids;
+            if ((rc = launch_fused(c, sa, reinterpret_cast<unsigned*>(ws + L.bar), st))) return rc;
+        }
+    }
+    return MOE_OK;
+}
+
+int moe_stack_forward_fp8(int Lc, const uint16_t* const* w_router, const float* const* logit_bias,
+                          const uint8_t* const* gate_up_q, const float* const* gate_up_scale,
+                          const uint8_t* const* down_q, const float* const* down_scale, int B, int H, int I, int E,
+                          int top_k, float* x_inout, int32_t* expert_ids_out, uint32_t flags, void* workspace,
+                          size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    int rc = check_dims(B, H, I, E, top_k, true);
+    if (rc) return rc;
+    if (Lc < 1 || Lc > MOE_MAX_LAYERS) return MOE_ERR_INVALID_ARG;
+    if ((H & 15) || (I & 15)) return MOE_ERR_INVALID_ARG;  // rows of codes in whole 16-byte pieces
+    if (flags & ~(MOE_F_NO_DEDUP | MOE_F_NO_PREFETCH)) return MOE_ERR_INVALID_ARG;
+    if (B == 0) return MOE_OK;
+    if (!w_router || !gate_up_q || !gate_up_scale || !down_q || !down_scale) return MOE_ERR_INVALID_ARG;
+    for (int l = 0; l < Lc; ++l) {
+        MOE_REQ(w_router[l]);
+        MOE_REQ(gate_up_q[l]);
+        MOE_REQ(down_q[l]);
+        if (!gate_up_scale[l] || !down_scale[l]) return MOE_ERR_INVALID_ARG;
+        if (logit_bias) MOE_OPT(logit_bias[l]);
+    }
+    MOE_REQ(x_inout);
+    MOE_OPT(expert_ids_out);
+    MOE_REQ(workspace);
+    MOE_OPT(dev_status);
+    const WsLayout L = ws_layout(B, H, I, E, top_k);
+    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+    char* ws = static_cast<char*>(workspace);
+    DkParams dp;
+    memset(&dp, 0, sizeof dp);
+    size_t dsm = 0;
+    const int sms = sm_count();
+    if (!decode_plan(B, H, I, E, top_k, sms, dp, dsm, false, 1)) return MOE_ERR_UNSUPPORTED;
+    decode_common(dp, B, H, I, E, top_k, Lc, flags,
+                  dev_status ? dev_status : reinterpret_cast<int32_t*>(ws + L.status));
+    dp.trace = nullptr;
+    dp.trace_words = 0;
+    dp.x_bf16 = 0;
+    dp.x_in = x_inout;
+    dp.residual = x_inout;
+    dp.y = x_inout;
+    for (int l = 0; l < Lc; ++l) {
+        dp.layer[l].w_router = w_router[l];
+        dp.layer[l].bias = logit_bias ? logit_bias[l] : nullptr;
+        dp.layer[l].gate_up = reinterpret_cast<const uint16_t*>(gate_up_q[l]);
+        dp.layer[l].down = reinterpret_cast<const uint16_t*>(down_q[l]);
+        dp.layer[l].gate_up_scale = gate_up_scale[l];
+        dp.layer[l].down_scale = down_scale[l];
+    }
+    dp.ids_out = expert_ids_out;
+    dp.w_out = nullptr;
+    return launch_decode(dp, dsm, sms, ws, L, static_cast<cudaStream_t>(stream), true);
 }
 
 int moe_workspace_grouping(void* workspace, size_t workspace_bytes, int B, int H, int I, int E, int top_k,

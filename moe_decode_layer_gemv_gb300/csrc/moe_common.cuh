@@ -77,6 +77,12 @@ struct LayerWeights {
     const float* bias;         // [E] or nullptr
     const uint16_t* gate_up;   // [E, 2I, H]
     const uint16_t* down;      // [E, H, I]
+    const float* norm;         // [H] RMSNorm weights of the layer input (pre-norm stacks), or nullptr
+    // block-scaled FP8 experts (gate_up / down then hold E4M3 codes, one byte
+    // each): fp32 scales per 128 x 128 block, [E][ceil(2I/128)][ceil(H/128)]
+    // and [E][ceil(H/128)][ceil(I/128)]; nullptr for bf16 experts
+    const float* gate_up_scale;
+    const float* down_scale;
 };
 
 // Everything one layer step needs.  Built on the host, passed by value.

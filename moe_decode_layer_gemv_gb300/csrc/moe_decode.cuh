@@ -23,6 +23,9 @@
 // read once, split by (expert, row block).)
 #pragma once
 
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "moe_common.cuh"
 #include "moe_ptx.cuh"
 
@@ -64,6 +67,11 @@ struct DkParams {
     unsigned long long* trace;  // optional phase timestamps (see dk_trace), or nullptr
     int trace_words;
     int off_misc, off_x, off_xq, off_h, off_o, off_wr, off_ring;
+    int off_gq;  // pre-norm stacks: [2][H] fp32, layer m's norm weights in buffer m & 1
+    // pre-norm stacks: layer l's input is RMSNorm_l(x_l) = x_l * rn * norm_l
+    // with rn = 1/sqrt(mean(x_l^2) + eps); the residual is x_l itself
+    int has_norm;
+    float eps;
 };
 
 struct __align__(16) DkMisc {
@@ -79,6 +87,7 @@ struct __align__(16) DkMisc {
     int seg_p[kDkMaxR + 1];
     int last_pos[kDkMaxStages];  // latest ring position armed in each stage (-1: none)
     int mid_epoch;               // layers whose mid-layer barrier has completed (for the producer warp)
+    float rn[kDkMaxB];           // pre-norm stacks: 1/sqrt(mean(x^2) + eps) of each token's layer input
     int ga_tab[kDkMaxR + 1];     // this CTA's gate/up pair range [ga_tab[U], gb_tab[U]) for U segments
     int gb_tab[kDkMaxR + 1];
 };
@@ -133,7 +142,20 @@ __device__ __forceinline__ DkWork dk_work(const DkWork& base, int U, const DkMis
 // p.bar[0] = counter, p.bar[1] = abort word.  Bounded: after kDkSpinLimit
 // polls the CTA sets MOE_DEV_TIMEOUT and the abort word and reports failure.
 constexpr int kDkLeader = 32;  // first consumer thread
-constexpr int kDkShadows = 2;  // copies of the logit accumulator (spread the atomics; 2 measured best of 1, 2, 4, 8)
+#ifndef MOE_DK_SHADOWS
+#define MOE_DK_SHADOWS 2
+#endif
+#ifndef MOE_DK_THREAD_FENCE
+#define MOE_DK_THREAD_FENCE 1
+#endif
+constexpr int kDkShadows = MOE_DK_SHADOWS;  // copies of the logit accumulator (spread the atomics; 2 measured best of 1, 2, 4, 8)
+
+// Pre-norm stacks: the fixed-point sums of x^2 of layer l's input,
+// [kDkShadows][B], behind the two logit accumulators.
+__device__ __forceinline__ unsigned long long* dk_nacc(const DkParams& p, int l) {
+    return p.acc + (size_t)2 * kDkShadows * p.B * p.E + (size_t)(l & 1) * kDkShadows * p.B;
+}
+
 
 __device__ __forceinline__ unsigned atom_add_release_gpu(unsigned* p, unsigned v) {
     unsigned old;
@@ -302,9 +324,17 @@ __device__ __forceinline__ void dk_topk_smem(const float* lg, int E, int k, int 
 // (token, expert): one thread per pair, rows in 8-wide vectors from shared
 // memory, the result added to shadow copy (CTA mod kDkShadows) of the
 // fixed-point accumulator.
+//
+// Pre-norm stacks (g = the layer's norm weights): the logits of RMSNorm(x)
+// are rn * sum_h W[e,h] g[h] x[h] with rn = 1/sqrt(mean(x^2) + eps), one
+// scalar per token, so the partial sums take g in and leave rn out, and the
+// partial sums of x^2 go into a second fixed-point accumulator (nacc[t]);
+// rn is applied where the logits are read.  The router stays fused into the
+// residual add that forms x (the norm + residual fusion).
 __device__ __forceinline__ void dk_router_partials(const uint16_t* wrs, int maxrows, const float* xs, int H,
                                                    int h0, int nrows, int B, int E,
-                                                   unsigned long long* acc, int t0, int nth) {
+                                                   unsigned long long* acc, int t0, int nth,
+                                                   const float* g = nullptr, unsigned long long* nacc = nullptr) {
     unsigned long long* sh = acc + (size_t)(blockIdx.x % kDkShadows) * B * E;
     for (int v = t0; v < B * E; v += nth) {
         const int t = v / E, e = v - t * E;
@@ -313,8 +343,14 @@ __device__ __forceinline__ void dk_router_partials(const uint16_t* wrs, int maxr
         float2 a = make_float2(0.f, 0.f);
         for (int r = 0; r < nrows; r += 8) {
             const uint4 wv = *reinterpret_cast<const uint4*>(wrow + r);
-            const float4 xa = *reinterpret_cast<const float4*>(xr + r);
-            const float4 xb = *reinterpret_cast<const float4*>(xr + r + 4);
+            float4 xa = *reinterpret_cast<const float4*>(xr + r);
+            float4 xb = *reinterpret_cast<const float4*>(xr + r + 4);
+            if (g) {
+                const float4 ga = *reinterpret_cast<const float4*>(g + h0 + r);
+                const float4 gb = *reinterpret_cast<const float4*>(g + h0 + r + 4);
+                xa = make_float4(xa.x * ga.x, xa.y * ga.y, xa.z * ga.z, xa.w * ga.w);
+                xb = make_float4(xb.x * gb.x, xb.y * gb.y, xb.z * gb.z, xb.w * gb.w);
+            }
             a = ffma2(bf16x2_to_f2(wv.x), make_float2(xa.x, xa.y), a);
             a = ffma2(bf16x2_to_f2(wv.y), make_float2(xa.z, xa.w), a);
             a = ffma2(bf16x2_to_f2(wv.z), make_float2(xb.x, xb.y), a);
@@ -322,7 +358,17 @@ __device__ __forceinline__ void dk_router_partials(const uint16_t* wrs, int maxr
         }
         red_add_u64(sh + v, float_to_fix(a.x + a.y));
     }
+    if (nacc) {  // sum of squares of this CTA's rows, one thread per token
+        for (int t = t0; t < B; t += nth) {
+            const float* xr = xs + (size_t)t * H + h0;
+            float ss = 0.f;
+            for (int r = 0; r < nrows; ++r) ss = fmaf(xr[r], xr[r], ss);
+            red_add_u64(nacc + (size_t)(blockIdx.x % kDkShadows) * B + t, float_to_fix(ss));
+        }
+    }
+#if MOE_DK_THREAD_FENCE
     __threadfence();  // the reductions are performed before this thread reaches the next barrier
+#endif
 }
 
 // Stable grouping of R <= 32 routes by expert in one warp: the position of
@@ -401,10 +447,19 @@ __device__ __forceinline__ void warp_sum_n(float (&v)[N]) {
 __host__ __device__ __forceinline__ int dk_hq(int H) { return lb_stride(H); }
 __device__ __forceinline__ int dk_xq_index(int c) { return lb_index(c); }
 
-// Four x values at flat index f = t*H + c (c a multiple of 4) into both copies.
-__device__ __forceinline__ void dk_store_x(float* xs, float* xq, int H, int f, float4 v) {
+// Four x values at flat index f = t*H + c (c a multiple of 4) into both
+// copies: xs keeps x (the residual), xq the layer input -- x itself, or for
+// a pre-norm stack RMSNorm(x) = (x * rn[t]) * g (g != nullptr: the norm
+// weights in shared memory).
+__device__ __forceinline__ void dk_store_x(float* xs, float* xq, int H, int f, float4 v, const float* g = nullptr,
+                                           const DkMisc* m = nullptr) {
     *reinterpret_cast<float4*>(xs + f) = v;
     const int t = f / H, c = f - t * H;
+    if (g) {
+        const float r = m->rn[t];
+        const float4 gv = *reinterpret_cast<const float4*>(g + c);
+        v = make_float4((v.x * r) * gv.x, (v.y * r) * gv.y, (v.z * r) * gv.z, (v.w * r) * gv.w);
+    }
     *reinterpret_cast<float4*>(xq + (size_t)t * dk_hq(H) + dk_xq_index(c)) = v;
 }
 
@@ -512,11 +567,128 @@ __device__ __forceinline__ void dk_down_rows(const unsigned char* st, int nrc, i
     }
 }
 
+// ---------------------------------------------------- block-scaled FP8
+// Two E4M3 codes (low byte first) as fp32: the hardware conversion to f16 is
+// exact for every E4M3 value, and so is the widening to f32.
+__device__ __forceinline__ float2 f8x2_to_f2(unsigned v) {
+    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(v & 0xffffu), __NV_E4M3);
+    __half2 h;
+    memcpy(&h, &hr, sizeof h);
+    return __half22float2(h);
+}
+
+// The FP8 form of dk_gate_pair: rows of H E4M3 codes (gate row at grow, up
+// row at urow) with their block scales along the row (gsr, usr: the scale
+// rows of the 128-row blocks the two rows lie in).  Lane L takes the 8-code
+// groups v = L + 32j (one 8-byte load each, a warp reads 256 contiguous
+// bytes); a group lies in one 128-column block, so its 8 products are summed
+// first and scaled once: sum_v s_v * sum_8 decode(q) x.
+template <int NQ>
+__device__ __forceinline__ void dk_gate_pair_f8(const unsigned char* grow, const unsigned char* urow,
+                                                const float* gsr, const float* usr, const float* xq,
+                                                const int (&tok)[4], int H, float (&gu)[2 * NQ]) {
+    const int lane = threadIdx.x & 31;
+    float ag[NQ], au[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) ag[q] = au[q] = 0.f;
+    const int nv = H >> 3, hq = dk_hq(H);
+    for (int v = lane; v < nv; v += 32) {
+        const uint2 gw = *reinterpret_cast<const uint2*>(grow + 8 * v);
+        const uint2 uw = *reinterpret_cast<const uint2*>(urow + 8 * v);
+        const float sg = __ldg(gsr + (v >> 4)), su = __ldg(usr + (v >> 4));
+        const float2 g0 = f8x2_to_f2(gw.x), g1 = f8x2_to_f2(gw.x >> 16);
+        const float2 g2 = f8x2_to_f2(gw.y), g3 = f8x2_to_f2(gw.y >> 16);
+        const float2 u0 = f8x2_to_f2(uw.x), u1 = f8x2_to_f2(uw.x >> 16);
+        const float2 u2 = f8x2_to_f2(uw.y), u3 = f8x2_to_f2(uw.y >> 16);
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            const float* xp = xq + (size_t)tok[q] * hq + ((v >> 5) << 8) + ((v & 31) << 2);
+            const float4 xa = *reinterpret_cast<const float4*>(xp);
+            const float4 xb = *reinterpret_cast<const float4*>(xp + 128);
+            float2 pg = ffma2(g0, make_float2(xa.x, xa.y), make_float2(0.f, 0.f));
+            float2 pu = ffma2(u0, make_float2(xa.x, xa.y), make_float2(0.f, 0.f));
+            pg = ffma2(g1, make_float2(xa.z, xa.w), pg);
+            pu = ffma2(u1, make_float2(xa.z, xa.w), pu);
+            pg = ffma2(g2, make_float2(xb.x, xb.y), pg);
+            pu = ffma2(u2, make_float2(xb.x, xb.y), pu);
+            pg = ffma2(g3, make_float2(xb.z, xb.w), pg);
+            pu = ffma2(u3, make_float2(xb.z, xb.w), pu);
+            ag[q] = fmaf(sg, pg.x + pg.y, ag[q]);
+            au[q] = fmaf(su, pu.x + pu.y, au[q]);
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+        gu[2 * q] = ag[q];
+        gu[2 * q + 1] = au[q];
+    }
+    warp_sum_n<2 * NQ>(gu);
+}
+
+// The FP8 form of dk_down_rows: rows of I codes, four at a time; row r's
+// scales are row (row_abs0 + r) / 128 of the expert's block scales dsr.
+template <int NQ>
+__device__ __forceinline__ void dk_down_rows_f8(const unsigned char* st, int nrc, int I, const float* dsr,
+                                                int dsr_ld, int row_abs0, const float* hrow, float* os, int ld,
+                                                int orow0) {
+    const int lane = threadIdx.x & 31;
+    const int nv = I >> 3;
+    for (int rb = 0; rb < nrc; rb += 4) {
+        const int n4 = min(4, nrc - rb);
+        const float* sr[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sr[j] = dsr + (size_t)((row_abs0 + rb + min(j, n4 - 1)) >> 7) * dsr_ld;
+        float acc[4][NQ];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) acc[j][q] = 0.f;
+        for (int v = lane; v < nv; v += 32) {
+            float s[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) s[j] = __ldg(sr[j] + (v >> 4));
+            uint2 wv[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                wv[j] = j < n4 ? *reinterpret_cast<const uint2*>(st + (size_t)(rb + j) * I + 8 * v) : make_uint2(0u, 0u);
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                const float4* hp = reinterpret_cast<const float4*>(hrow + (size_t)q * I + 8 * v);
+                const float4 ha = hp[0], hb = hp[1];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float2 a = ffma2(f8x2_to_f2(wv[j].x), make_float2(ha.x, ha.y), make_float2(0.f, 0.f));
+                    a = ffma2(f8x2_to_f2(wv[j].x >> 16), make_float2(ha.z, ha.w), a);
+                    a = ffma2(f8x2_to_f2(wv[j].y), make_float2(hb.x, hb.y), a);
+                    a = ffma2(f8x2_to_f2(wv[j].y >> 16), make_float2(hb.z, hb.w), a);
+                    acc[j][q] = fmaf(s[j], a.x + a.y, acc[j][q]);
+                }
+            }
+        }
+        float red[4 * NQ];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) red[j * NQ + q] = acc[j][q];
+        warp_sum_n<4 * NQ>(red);
+        if (lane == 0) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (j < n4)
+#pragma unroll
+                    for (int q = 0; q < NQ; ++q) os[(size_t)q * ld + orow0 + rb + j] = red[j * NQ + q];
+        }
+    }
+}
+
 // Gate/up pair q of the layer (segment u, row i) from shared-memory rows:
-// h[p, i] = SiLU(g) * u for every route p of the segment.
-template <int kNQ>
+// h[p, i] = SiLU(g) * u for every route p of the segment.  kF8: the rows
+// hold E4M3 codes and gsr/usr are the scale rows of gate row i and up row
+// I + i.
+template <int kNQ, bool kF8 = false>
 __device__ __forceinline__ void dk_pair_compute(const DkMisc* m, const unsigned char* grow, const unsigned char* urow,
-                                                const float* xq, int H, int I, int k, int u, int i, float* h) {
+                                                const float* xq, int H, int I, int k, int u, int i, float* h,
+                                                const float* gsr = nullptr, const float* usr = nullptr) {
     const int lane = threadIdx.x & 31;
     const int p0 = m->seg_p[u], p1 = m->seg_p[u + 1];
     int tok[kDkMaxB];
@@ -524,15 +696,28 @@ __device__ __forceinline__ void dk_pair_compute(const DkMisc* m, const unsigned 
     for (int qq = 0; qq < kDkMaxB; ++qq) tok[qq] = p0 + qq < p1 ? m->rat[p0 + qq] / k : 0;
     const int nq = kNQ == 1 ? 1 : p1 - p0;
     float gu[2 * kDkMaxB];
-    switch (kNQ == 1 ? 1 : nq) {
-        case 1: { float r[2]; dk_gate_pair<1>(grow, urow, xq, tok, H, r); gu[0] = r[0]; gu[1] = r[1]; } break;
-        case 2: { float r[4]; dk_gate_pair<2>(grow, urow, xq, tok, H, r);
+    if constexpr (kF8) {
+        switch (kNQ == 1 ? 1 : nq) {
+            case 1: { float r[2]; dk_gate_pair_f8<1>(grow, urow, gsr, usr, xq, tok, H, r); gu[0] = r[0]; gu[1] = r[1]; } break;
+            case 2: { float r[4]; dk_gate_pair_f8<2>(grow, urow, gsr, usr, xq, tok, H, r);
 #pragma unroll
-                  for (int j = 0; j < 4; ++j) gu[j] = r[j]; } break;
-        case 3: { float r[6]; dk_gate_pair<3>(grow, urow, xq, tok, H, r);
+                      for (int j = 0; j < 4; ++j) gu[j] = r[j]; } break;
+            case 3: { float r[6]; dk_gate_pair_f8<3>(grow, urow, gsr, usr, xq, tok, H, r);
 #pragma unroll
-                  for (int j = 0; j < 6; ++j) gu[j] = r[j]; } break;
-        default: dk_gate_pair<4>(grow, urow, xq, tok, H, gu); break;
+                      for (int j = 0; j < 6; ++j) gu[j] = r[j]; } break;
+            default: dk_gate_pair_f8<4>(grow, urow, gsr, usr, xq, tok, H, gu); break;
+        }
+    } else {
+        switch (kNQ == 1 ? 1 : nq) {
+            case 1: { float r[2]; dk_gate_pair<1>(grow, urow, xq, tok, H, r); gu[0] = r[0]; gu[1] = r[1]; } break;
+            case 2: { float r[4]; dk_gate_pair<2>(grow, urow, xq, tok, H, r);
+#pragma unroll
+                      for (int j = 0; j < 4; ++j) gu[j] = r[j]; } break;
+            case 3: { float r[6]; dk_gate_pair<3>(grow, urow, xq, tok, H, r);
+#pragma unroll
+                      for (int j = 0; j < 6; ++j) gu[j] = r[j]; } break;
+            default: dk_gate_pair<4>(grow, urow, xq, tok, H, gu); break;
+        }
     }
     if (lane < nq) {
         float g = gu[0], uu = gu[1];
@@ -547,13 +732,24 @@ __device__ __forceinline__ void dk_pair_compute(const DkMisc* m, const unsigned 
 }
 
 // Down rows [r0, r1) of segment u from shared memory (row r at base + (r -
-// r0) * 2I) into os (j-th route of the segment at row p0 + j).
-template <int kNQ>
+// r0) * row bytes) into os (j-th route of the segment at row p0 + j).  kF8:
+// E4M3 codes with the expert's block scales dsc ([ceil(H/128)][dsc_ld]).
+template <int kNQ, bool kF8 = false>
 __device__ __forceinline__ void dk_down_compute(const DkMisc* m, const unsigned char* base, int r0, int r1, int I,
-                                                const float* hs, float* os, int maxrows, int h0, int u) {
+                                                const float* hs, float* os, int maxrows, int h0, int u,
+                                                const float* dsc = nullptr, int dsc_ld = 0) {
     const int p0 = m->seg_p[u], p1 = m->seg_p[u + 1];
     const float* hrow = hs + (size_t)p0 * I;
     float* orow = os + (size_t)p0 * maxrows;
+    if constexpr (kF8) {
+        switch (kNQ == 1 ? 1 : p1 - p0) {
+            case 1: dk_down_rows_f8<1>(base, r1 - r0, I, dsc, dsc_ld, r0, hrow, orow, maxrows, r0 - h0); break;
+            case 2: dk_down_rows_f8<2>(base, r1 - r0, I, dsc, dsc_ld, r0, hrow, orow, maxrows, r0 - h0); break;
+            case 3: dk_down_rows_f8<3>(base, r1 - r0, I, dsc, dsc_ld, r0, hrow, orow, maxrows, r0 - h0); break;
+            default: dk_down_rows_f8<4>(base, r1 - r0, I, dsc, dsc_ld, r0, hrow, orow, maxrows, r0 - h0); break;
+        }
+        return;
+    }
     switch (kNQ == 1 ? 1 : p1 - p0) {
         case 1: dk_down_rows<1>(base, r1 - r0, I, hrow, orow, maxrows, r0 - h0); break;
         case 2: dk_down_rows<2>(base, r1 - r0, I, hrow, orow, maxrows, r0 - h0); break;
@@ -626,16 +822,16 @@ __device__ __forceinline__ int dk_predict_top(const float* alog, int E, int kp) 
 // L2: lane j < kp takes expert j (my_e) and issues two bulk prefetches, its
 // piece of the gate_up block and its piece of the down block (pieces of
 // equal 16-byte-aligned size, the last CTA taking the remainder).
-__device__ __forceinline__ void dk_prefetch_l2(const LayerWeights& wn, int my_e, int H, int I, int kp) {
+__device__ __forceinline__ void dk_prefetch_l2(const LayerWeights& wn, int my_e, int H, int I, int kp, int wb = 2) {
     const int lane = threadIdx.x & 31;
     if (lane < kp && my_e >= 0) {
         const unsigned G = gridDim.x, c = blockIdx.x;
-        const unsigned gsz = 4u * (unsigned)I * (unsigned)H, dsz = 2u * (unsigned)I * (unsigned)H;
+        const unsigned gsz = 2u * (unsigned)wb * (unsigned)I * (unsigned)H, dsz = (unsigned)wb * (unsigned)I * (unsigned)H;
         const unsigned gp = (gsz / G) & ~15u, dp = (dsz / G) & ~15u;
         const unsigned g0 = c * gp, d0 = c * dp;
         const unsigned gn = c + 1 == G ? gsz - g0 : gp, dn = c + 1 == G ? dsz - d0 : dp;
-        const char* ge = reinterpret_cast<const char*>(wn.gate_up + (size_t)my_e * 2 * I * H);
-        const char* de = reinterpret_cast<const char*>(wn.down + (size_t)my_e * H * I);
+        const char* ge = reinterpret_cast<const char*>(wn.gate_up) + (size_t)my_e * gsz;
+        const char* de = reinterpret_cast<const char*>(wn.down) + (size_t)my_e * dsz;
         if (gn > 0) bulk_prefetch_l2(ge + g0, gn);
         if (dn > 0) bulk_prefetch_l2(de + d0, dn);
     }
@@ -646,14 +842,15 @@ __device__ __forceinline__ void dk_prefetch_l2(const LayerWeights& wn, int my_e,
 // (gb - ga) * 4H bytes): per run of one segment, the gate rows to
 // dg + (q - ga)*2H and the up rows to du + (q - ga)*2H.
 __device__ __forceinline__ void dk_gate_runs(const uint16_t* gate_up, const int* seg_e, int ga, int gb, int H, int I,
-                                             unsigned char* dg, unsigned char* du, uint64_t* bar) {
+                                             unsigned char* dg, unsigned char* du, uint64_t* bar, int wb = 2) {
+    const size_t row = (size_t)wb * H;  // bytes of one row
     for (int q = ga; q < gb;) {
         const int u = q / I, i = q - u * I;
         const int qe = min(gb, (u + 1) * I);
-        const uint32_t bytes = (uint32_t)(qe - q) * 2u * H;
-        const uint16_t* G = gate_up + (size_t)seg_e[u] * 2 * I * H;
-        bulk_g2s(dg + (size_t)(q - ga) * 2 * H, G + (size_t)i * H, bytes, bar);
-        bulk_g2s(du + (size_t)(q - ga) * 2 * H, G + (size_t)(I + i) * H, bytes, bar);
+        const uint32_t bytes = (uint32_t)((qe - q) * row);
+        const unsigned char* G = reinterpret_cast<const unsigned char*>(gate_up) + (size_t)seg_e[u] * 2 * I * row;
+        bulk_g2s(dg + (size_t)(q - ga) * row, G + (size_t)i * row, bytes, bar);
+        bulk_g2s(du + (size_t)(q - ga) * row, G + (size_t)(I + i) * row, bytes, bar);
         q = qe;
     }
 }
@@ -667,7 +864,7 @@ __device__ __forceinline__ void dk_gate_runs(const uint16_t* gate_up, const int*
 // instruction stream: the kernel runs every phase of a layer once per
 // layer, so its speed depends on how much code it streams through the
 // instruction caches.
-template <bool kTrace, int kNQ, bool kDirect>
+template <bool kTrace, int kNQ, bool kDirect, bool kF8 = false>
 __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -681,12 +878,19 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
     float* os = reinterpret_cast<float*>(smem + p.off_o);   // [R][maxrows]
     uint16_t* wrs = reinterpret_cast<uint16_t*>(smem + p.off_wr);  // [E][maxrows]
     unsigned char* ring = smem + p.off_ring;
+    float* gq = reinterpret_cast<float*>(smem + p.off_gq);  // [2][H] (pre-norm stacks only)
     float* lg = reinterpret_cast<float*>(smem + p.off_misc + sizeof(DkMisc));  // [B][Ep] logits
     const int Ep = (p.E + 7) & ~7;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = kNQ == 1 ? 1 : p.B;  // a compile-time constant for one token
     const int H = p.H, I = p.I, E = p.E, k = p.k, R = B * k;
+    // bytes of a gate/up row and of a down row (bf16, or one-byte E4M3 codes)
+    constexpr int kWb = kF8 ? 1 : 2;
+    const int rowg = kWb * H, rowd = kWb * I;
+    // block-scale row lengths of gate_up [2I, H] and down [H, I] (FP8 only)
+    const int sg_ld = (H + 127) >> 7, sd_ld = (I + 127) >> 7;
+    const int sg_e = ((2 * I + 127) >> 7) * sg_ld, sd_e = ((H + 127) >> 7) * sd_ld;
     const bool no_dedup = (p.flags & MOE_F_NO_DEDUP) != 0;
     int h0, h1;
     dk_rows(blockIdx.x, gridDim.x, H, h0, h1);
@@ -694,7 +898,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
     DkWork wbase;
     wbase.h0 = h0;
     wbase.h1 = h1;
-    wbase.nr = max(1, p.stage_bytes / (2 * I));
+    wbase.nr = max(1, p.stage_bytes / rowd);
     if (wbase.nr >= 4) wbase.nr &= ~3;  // whole 4-row groups in the down compute
     wbase.nd_per_u = nrows > 0 ? (nrows + wbase.nr - 1) / wbase.nr : 0;
     wbase.ga = wbase.gb = wbase.ng = wbase.n = 0;
@@ -737,6 +941,8 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
             const int e = v / (nrows >> 3), c8 = (v - e * (nrows >> 3)) << 3;
             cp_async16(wrs + e * p.maxrows + c8, w0.w_router + (size_t)e * H + h0 + c8);
         }
+        if (p.has_norm)
+            for (int v = tid; v < (H >> 2); v += blockDim.x) cp_async16(gq + 4 * v, w0.norm + 4 * v);
         cp_async_commit();
         for (int v = tid; v < B * nrows; v += blockDim.x) {
             const int t = v / nrows, r = v - t * nrows;
@@ -746,7 +952,9 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
         }
         cp_async_wait_all();
         __syncthreads();
-        if (nrows > 0) dk_router_partials(wrs, p.maxrows, xs, H, h0, nrows, B, E, p.acc, tid, blockDim.x);
+        if (nrows > 0)
+            dk_router_partials(wrs, p.maxrows, xs, H, h0, nrows, B, E, p.acc, tid, blockDim.x,
+                               p.has_norm ? gq : nullptr, p.has_norm ? dk_nacc(p, 0) : nullptr);
     }
     if (tid == kDkLeader) dk_trace<kTrace>(p, -1, 1);
     dk_grid_sync(p, epoch, m, 0, kDkThreads);
@@ -766,14 +974,23 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
             // consumers: every (token, expert) logit from the shadow
             // accumulators (an integer sum: exact in any order) into lg
             const int ct = tid - 32, nct = 32 * kDkConsumers;
+            const unsigned long long* nacc_now = p.has_norm ? dk_nacc(p, l) : nullptr;
             for (int v = ct; v < B * Ep; v += nct) {
                 const int t = v / Ep, e = v - t * Ep;
                 float val = -INFINITY;
+                float rn = 1.f;
+                if (nacc_now) {  // pre-norm: 1/sqrt(mean(x^2) + eps) of token t's input
+                    unsigned long long ss = 0ull;
+#pragma unroll
+                    for (int sh = 0; sh < kDkShadows; ++sh) ss += __ldcg(nacc_now + (size_t)sh * B + t);
+                    rn = 1.0f / sqrtf(fix_to_float(ss) / (float)H + p.eps);
+                    if (e == 0) m->rn[t] = rn;
+                }
                 if (e < E) {
                     unsigned long long sum = 0ull;
 #pragma unroll
                     for (int sh = 0; sh < kDkShadows; ++sh) sum += __ldcg(acc_now + ((size_t)sh * B + t) * E + e);
-                    val = fix_to_float(sum);
+                    val = rn * fix_to_float(sum);
                     if (lw.bias) val += __ldg(lw.bias + e);
                 }
                 lg[v] = val;
@@ -805,19 +1022,21 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                 // both loads of a thread in flight before either store
                 const float* xsrc = (l > 0) ? p.y : static_cast<const float*>(p.x_in);
                 const int nv4 = (B * H) >> 2;
+                const float* gn = p.has_norm ? gq + (size_t)(l & 1) * H : nullptr;
                 for (int v0 = ct; v0 < nv4; v0 += 2 * nct) {
                     const int v1 = v0 + nct;
                     const float4 a = ld_act_f4(xsrc + 4 * (size_t)v0);
                     const float4 b = v1 < nv4 ? ld_act_f4(xsrc + 4 * (size_t)v1) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    dk_store_x(xs, xq, H, 4 * v0, a);
-                    if (v1 < nv4) dk_store_x(xs, xq, H, 4 * v1, b);
+                    dk_store_x(xs, xq, H, 4 * v0, a, gn, m);
+                    if (v1 < nv4) dk_store_x(xs, xq, H, 4 * v1, b, gn, m);
                 }
             } else {
                 const uint16_t* xb = static_cast<const uint16_t*>(p.x_in);
                 for (int v = ct; v < (B * H) >> 2; v += nct) {
                     const uint2 w = *reinterpret_cast<const uint2*>(xb + 4 * (size_t)v);
                     const float2 lo = bf16x2_to_f2(w.x), hi = bf16x2_to_f2(w.y);
-                    dk_store_x(xs, xq, H, 4 * v, make_float4(lo.x, lo.y, hi.x, hi.y));
+                    dk_store_x(xs, xq, H, 4 * v, make_float4(lo.x, lo.y, hi.x, hi.y),
+                               p.has_norm ? gq + (size_t)(l & 1) * H : nullptr, m);
                 }
             }
             if (has_next) {
@@ -825,6 +1044,11 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                 for (int v = ct; v < E * (nrows >> 3); v += nct) {
                     const int e = v / (nrows >> 3), c8 = (v - e * (nrows >> 3)) << 3;
                     cp_async16(wrs + e * p.maxrows + c8, wn.w_router + (size_t)e * H + h0 + c8);
+                }
+                // the next layer's norm weights into the buffer that layer l-1 used
+                if (p.has_norm) {
+                    float* gd = gq + (size_t)((l + 1) & 1) * H;
+                    for (int v = ct; v < (H >> 2); v += nct) cp_async16(gd + 4 * v, wn.norm + 4 * v);
                 }
                 cp_async_commit();
             }
@@ -838,15 +1062,15 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
         // fit in the ring area together, they are fetched by a handful of
         // large bulk copies (rows of one expert are contiguous) onto two
         // barriers instead of chunk by chunk through the ring.
-        const uint32_t d_gate_bytes = (uint32_t)wk.ng * 4u * (uint32_t)H;
-        const uint32_t d_down_bytes = (uint32_t)U * (uint32_t)nrows * 2u * (uint32_t)I;
+        const uint32_t d_gate_bytes = (uint32_t)wk.ng * 2u * (uint32_t)rowg;
+        const uint32_t d_down_bytes = (uint32_t)U * (uint32_t)nrows * (uint32_t)rowd;
         // (kDirect: the host has checked that every CTA's share fits for any routing)
         const bool direct = kDirect || (size_t)d_gate_bytes + d_down_bytes <= (size_t)p.S * p.stage_bytes &&
                             d_gate_bytes < (1u << 20) && d_down_bytes < (1u << 20);
         const bool d_gate = direct && wk.ng > 0, d_down = direct && d_down_bytes > 0;
-        unsigned char* d_g = ring;                                       // [ng][2H] gate rows
-        unsigned char* d_u = ring + (size_t)wk.ng * 2 * H;               // [ng][2H] up rows
-        unsigned char* d_d = ring + (size_t)wk.ng * 4 * H;               // [U][nrows][2I] down rows
+        unsigned char* d_g = ring;                                       // [ng][rowg] gate rows
+        unsigned char* d_u = ring + (size_t)wk.ng * rowg;                // [ng][rowg] up rows
+        unsigned char* d_d = ring + (size_t)wk.ng * 2 * rowg;            // [U][nrows][rowd] down rows
 
         if (warp == 0 && direct) {
             // ================= producer, direct mode
@@ -858,10 +1082,10 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                 const int csz = max(4, (wk.ng + kDkGChunks - 1) / kDkGChunks);
                 for (int ch = 0; ch < kDkGChunks; ++ch) {
                     const int ca = min(wk.ng, ch * csz), cb = min(wk.ng, ca + csz);
-                    mbar_arrive_expect_tx(&gch[ch], (uint32_t)(cb - ca) * 4u * (uint32_t)H);
+                    mbar_arrive_expect_tx(&gch[ch], (uint32_t)(cb - ca) * 2u * (uint32_t)rowg);
                     if (cb > ca)
-                        dk_gate_runs(lw.gate_up, m->seg_e, wk.ga + ca, wk.ga + cb, H, I, d_g + (size_t)ca * 2 * H,
-                                     d_u + (size_t)ca * 2 * H, &gch[ch]);
+                        dk_gate_runs(lw.gate_up, m->seg_e, wk.ga + ca, wk.ga + cb, H, I, d_g + (size_t)ca * rowg,
+                                     d_u + (size_t)ca * rowg, &gch[ch], kWb);
                 }
             }
             __syncwarp();
@@ -874,8 +1098,9 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                 }
                 mbar_arrive_expect_tx(&dbar[1], d_down_bytes);
                 for (int u = 0; u < U; ++u)
-                    bulk_g2s(d_d + (size_t)u * nrows * 2 * I, lw.down + (size_t)m->seg_e[u] * H * I + (size_t)h0 * I,
-                             (uint32_t)nrows * 2u * I, &dbar[1]);
+                    bulk_g2s(d_d + (size_t)u * nrows * rowd,
+                             reinterpret_cast<const unsigned char*>(lw.down) + ((size_t)m->seg_e[u] * H + h0) * rowd,
+                             (uint32_t)nrows * (uint32_t)rowd, &dbar[1]);
             }
             __syncwarp();
         } else if (warp == 0) {
@@ -898,19 +1123,20 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                 if (c < wk.ng) {
                     const int pq = wk.ga + c;
                     const int u = pq / I, i = pq - u * I;
-                    const uint16_t* G = lw.gate_up + (size_t)m->seg_e[u] * 2 * I * H;
-                    mbar_arrive_expect_tx(&full[s], 4u * H);
-                    bulk_g2s(dst, G + (size_t)i * H, 2u * H, &full[s]);
-                    bulk_g2s(dst + 2 * H, G + (size_t)(I + i) * H, 2u * H, &full[s]);
+                    const unsigned char* G =
+                        reinterpret_cast<const unsigned char*>(lw.gate_up) + (size_t)m->seg_e[u] * 2 * I * rowg;
+                    mbar_arrive_expect_tx(&full[s], 2u * (uint32_t)rowg);
+                    bulk_g2s(dst, G + (size_t)i * rowg, (uint32_t)rowg, &full[s]);
+                    bulk_g2s(dst + rowg, G + (size_t)(I + i) * rowg, (uint32_t)rowg, &full[s]);
                 } else {
                     const int mm = c - wk.ng;
                     const int u = mm / wk.nd_per_u, sub = mm - u * wk.nd_per_u;
                     const int r0 = wk.h0 + sub * wk.nr;
                     const int r1 = min(wk.h1, r0 + wk.nr);
-                    const uint16_t* D = lw.down + (size_t)m->seg_e[u] * H * I;
-                    const uint32_t bytes = 2u * (r1 - r0) * I;
+                    const unsigned char* D = reinterpret_cast<const unsigned char*>(lw.down) + (size_t)m->seg_e[u] * H * rowd;
+                    const uint32_t bytes = (uint32_t)(r1 - r0) * (uint32_t)rowd;
                     mbar_arrive_expect_tx(&full[s], bytes);
-                    bulk_g2s(dst, D + (size_t)r0 * I, bytes, &full[s]);
+                    bulk_g2s(dst, D + (size_t)r0 * rowd, bytes, &full[s]);
                 }
                 m->last_pos[s] = n;
             }
@@ -942,7 +1168,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
             }
             if (__all_sync(0xffffffffu, seen)) {
                 const int my_e = dk_predict_top(p.alog, E, p.prefetch_k);
-                dk_prefetch_l2(p.layer[l + 1], my_e, H, I, p.prefetch_k);
+                dk_prefetch_l2(p.layer[l + 1], my_e, H, I, p.prefetch_k, kWb);
             }
         }
         if (warp != 0) {
@@ -973,7 +1199,10 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                     }
                     const int q = wk.ga + c;
                     const int u = q / I, i = q - u * I;
-                    dk_pair_compute<kNQ>(m, d_g + (size_t)c * 2 * H, d_u + (size_t)c * 2 * H, xq, H, I, k, u, i, p.h);
+                    const float* gsr = kF8 ? lw.gate_up_scale + (size_t)m->seg_e[u] * sg_e + (size_t)(i >> 7) * sg_ld : nullptr;
+                    const float* usr = kF8 ? lw.gate_up_scale + (size_t)m->seg_e[u] * sg_e + (size_t)((I + i) >> 7) * sg_ld : nullptr;
+                    dk_pair_compute<kNQ, kF8>(m, d_g + (size_t)c * rowg, d_u + (size_t)c * rowg, xq, H, I, k, u, i, p.h,
+                                              gsr, usr);
                 }
             }
             for (int c = c0; !direct && consumes && c < wk.ng; c += p.W) {
@@ -983,7 +1212,9 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                 const int q = wk.ga + c;
                 const int u = q / I, i = q - u * I;
                 const unsigned char* st = ring + (size_t)s * p.stage_bytes;
-                dk_pair_compute<kNQ>(m, st, st + 2 * H, xq, H, I, k, u, i, p.h);
+                const float* gsr = kF8 ? lw.gate_up_scale + (size_t)m->seg_e[u] * sg_e + (size_t)(i >> 7) * sg_ld : nullptr;
+                const float* usr = kF8 ? lw.gate_up_scale + (size_t)m->seg_e[u] * sg_e + (size_t)((I + i) >> 7) * sg_ld : nullptr;
+                dk_pair_compute<kNQ, kF8>(m, st, st + rowg, xq, H, I, k, u, i, p.h, gsr, usr);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
                 s += p.W;
@@ -1015,7 +1246,8 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                     }
                     const int u = j / ng4, rg = j - u * ng4;
                     const int r0 = h0 + 4 * rg, r1 = min(h1, r0 + 4);
-                    dk_down_compute<kNQ>(m, d_d + ((size_t)u * nrows + 4 * rg) * 2 * I, r0, r1, I, hs, os, p.maxrows, h0, u);
+                    dk_down_compute<kNQ, kF8>(m, d_d + ((size_t)u * nrows + 4 * rg) * rowd, r0, r1, I, hs, os, p.maxrows,
+                                              h0, u, kF8 ? lw.down_scale + (size_t)m->seg_e[u] * sd_e : nullptr, sd_ld);
                 }
             }
             c0 = wk.ng + ((cw - (rs + wk.ng) % p.W) % p.W + p.W) % p.W;
@@ -1031,7 +1263,8 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                 const int r0 = wk.h0 + sub * wk.nr;
                 const int r1 = min(wk.h1, r0 + wk.nr);
                 const unsigned char* st = ring + (size_t)s * p.stage_bytes;
-                dk_down_compute<kNQ>(m, st, r0, r1, I, hs, os, p.maxrows, h0, u);
+                dk_down_compute<kNQ, kF8>(m, st, r0, r1, I, hs, os, p.maxrows, h0, u,
+                                          kF8 ? lw.down_scale + (size_t)m->seg_e[u] * sd_e : nullptr, sd_ld);
                 __syncwarp();
                 if (c == c0 && cw == 0 && lane == 0) dk_trace<kTrace>(p, l, 13);
                 if (lane == 0) mbar_arrive(&empty[s]);
@@ -1061,6 +1294,8 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
             }
             if (blockIdx.x == 0) {  // acc_now was read by every CTA before the last barrier
                 for (int v = tid - 32; v < kDkShadows * B * E; v += 32 * kDkConsumers) acc_now[v] = 0ull;
+                if (p.has_norm)
+                    for (int v = tid - 32; v < kDkShadows * B; v += 32 * kDkConsumers) dk_nacc(p, l)[v] = 0ull;
                 __threadfence();  // performed before this CTA reaches the end-of-layer barrier
             }
             if (tid == kDkLeader) dk_trace<kTrace>(p, l, 10);
@@ -1070,7 +1305,8 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
             // ---- router of layer l+1: partial dot products over this CTA's rows
             if (has_next && nrows > 0)
                 dk_router_partials(wrs, p.maxrows, xs, H, h0, nrows, B, E, acc_next, tid - 32,
-                                   32 * kDkConsumers);
+                                   32 * kDkConsumers, p.has_norm ? gq + (size_t)((l + 1) & 1) * H : nullptr,
+                                   p.has_norm ? dk_nacc(p, l + 1) : nullptr);
             }  // ok
             if (has_next) cp_async_wait_all();
         }

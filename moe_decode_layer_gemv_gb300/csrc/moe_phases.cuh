@@ -534,4 +534,26 @@ __device__ void combine_item(const Ctx& c, int item) {
     }
 }
 
+// ================================================================ RMSNorm
+// a[t,:] = (x[t,:] * rn) * g, rn = 1/sqrt(mean(x[t,:]^2) + eps), fp32; one
+// CTA per token.  ("TEXT Generation Optimization Report", Fused Operations:
+// norm + residual add -- the norm of a pre-norm layer's input; the residual
+// add happens in the layer's combine.)
+__global__ void __launch_bounds__(kThreads) rmsnorm_kernel(const float* x, const float* g, int H, float eps,
+                                                           float* a) {
+    __shared__ float part[kWarps];
+    const int t = blockIdx.x;
+    const float* xr = x + (size_t)t * H;
+    float ss = 0.f;
+    for (int h = threadIdx.x; h < H; h += blockDim.x) ss = fmaf(xr[h], xr[h], ss);
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) tot += part[w];
+    const float rn = 1.0f / sqrtf(tot / (float)H + eps);
+    for (int h = threadIdx.x; h < H; h += blockDim.x) a[(size_t)t * H + h] = (xr[h] * rn) * g[h];
+}
+
 }  // namespace moe

@@ -188,6 +188,11 @@ __global__ void __launch_bounds__(kSgThreads, 1) stream_gemv_kernel(const SgPara
 
     if (warp == 0) {
         // ================= producer: lane s issues the items of stage s in order
+        // (MOE_F_HOT_L2: these experts have few routes this step; their
+        // weights are streamed with evict_first so that they do not push the
+        // tensor-core experts' weights out of L2)
+        const bool cold = (c.flags & MOE_F_HOT_L2) != 0;
+        const uint64_t pol = cold ? l2_policy_evict_first() : 0ull;
         const int s = lane;
         int cur = -1;
         Seg sg;
@@ -207,13 +212,22 @@ __global__ void __launch_bounds__(kSgThreads, 1) stream_gemv_kernel(const SgPara
                 const uint16_t* Gm = c.w.gate_up + (size_t)sg.e * 2 * c.I * c.H;
                 const uint32_t bytes = (uint32_t)np * 2u * c.H;
                 mbar_arrive_expect_tx(&m->full[s], 2u * bytes);
-                bulk_g2s(dst, Gm + (size_t)i0 * c.H, bytes, &m->full[s]);
-                bulk_g2s(dst + bytes, Gm + (size_t)(c.I + i0) * c.H, bytes, &m->full[s]);
+                if (cold) {
+                    bulk_g2s_hint(dst, Gm + (size_t)i0 * c.H, bytes, &m->full[s], pol);
+                    bulk_g2s_hint(dst + bytes, Gm + (size_t)(c.I + i0) * c.H, bytes, &m->full[s], pol);
+                } else {
+                    bulk_g2s(dst, Gm + (size_t)i0 * c.H, bytes, &m->full[s]);
+                    bulk_g2s(dst + bytes, Gm + (size_t)(c.I + i0) * c.H, bytes, &m->full[s]);
+                }
             } else {
                 const int r0 = b * P.rpi, nr = min(P.rpi, c.H - r0);
                 const uint32_t bytes = (uint32_t)nr * 2u * c.I;
                 mbar_arrive_expect_tx(&m->full[s], bytes);
-                bulk_g2s(dst, c.w.down + (size_t)sg.e * c.H * c.I + (size_t)r0 * c.I, bytes, &m->full[s]);
+                const uint16_t* src = c.w.down + (size_t)sg.e * c.H * c.I + (size_t)r0 * c.I;
+                if (cold)
+                    bulk_g2s_hint(dst, src, bytes, &m->full[s], pol);
+                else
+                    bulk_g2s(dst, src, bytes, &m->full[s]);
             }
         }
         // before leaving: the last phase armed in this lane's stage has landed

@@ -63,6 +63,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
+// the same with an L2 cache policy (createpolicy)
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar,
+                                                 uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
 // 1024 bytes apart (start address and strides in 16-byte units).
 __device__ __forceinline__ uint64_t umma_sdesc(uint32_t saddr) {
@@ -216,6 +226,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
 
         if (warp == 0 && lane == 0) {
             // ---------------- TMA producer
+            // MOE_F_HOT_L2: the tensor-core experts are the step's most chosen
+            // ones (>= threshold routes); their weights are loaded with
+            // evict_last so that they stay in L2 for the next steps
+            const bool hot = (c.flags & MOE_F_HOT_L2) != 0;
+            const uint64_t pol = hot ? l2_policy_evict_last() : 0ull;
             const uint32_t bytes = kTcATile + (uint32_t)n_pad * 128u * (p.with_lo ? 2u : 1u);
             int arow0, arow1 = 0;
             if (p.gate) {
@@ -234,7 +249,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
                 }
                 unsigned char* st = smem + (size_t)s * kTcStageBytes;
                 mbar_arrive_expect_tx(&full[s], bytes);
-                if (p.gate) {
+                if (hot) {  // the expert's weights stay in L2 for the next steps
+                    tma_load_2d_hint(st, &p.ta, kc * kTcBK, arow0, &full[s], pol);
+                    if (p.gate) tma_load_2d_hint(st + 8192, &p.ta, kc * kTcBK, arow1, &full[s], pol);
+                } else if (p.gate) {
                     tma_load_2d(st, &p.ta, kc * kTcBK, arow0, &full[s]);
                     tma_load_2d(st + 8192, &p.ta, kc * kTcBK, arow1, &full[s]);
                 } else {

@@ -66,3 +66,18 @@ def test_tensor_core_and_gemv_paths_agree(cuda_lib):
     torch.cuda.synchronize()
     assert torch.equal(ia, ib)
     assert float((ya - yb).abs().max()) <= 1e-4 * float(yb.abs().max())
+
+
+def test_hot_expert_l2_policy_leaves_results_unchanged(cuda_lib):
+    """MOE_F_HOT_L2 only changes the L2 eviction priority of the weight
+    copies (evict_last for the tensor-core experts, evict_first for the
+    rest): the layer's outputs are bit-identical with and without it."""
+    B, H, I, E, k = 96, 1024, 256, 32, 4
+    lw, x = _case(B, H, I, E, k, seed=6, skew=True)
+    y0, i0, _ = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k, bias=lw["bias"])
+    y1, i1, _ = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k, bias=lw["bias"],
+                                       flags=cuda_lib.MOE_F_HOT_L2)
+    torch.cuda.synchronize()
+    assert torch.equal(i0, i1) and torch.equal(y0, y1)
+    y_o, _, _ = oracle_layer_following(x, layer_weights_np(lw), k, i1)
+    check_y(y1, y_o)
