@@ -65,6 +65,9 @@ typedef enum {
 #define MOE_DEV_DUP_EXPERT 4     /* one token lists the same expert twice    */
 #define MOE_DEV_NONFINITE 8      /* a router logit was NaN or infinite       */
 #define MOE_DEV_BAD_ROUTE 16     /* a route_idx entry outside [0, B*top_k)    */
+#define MOE_DEV_RANGE 32         /* a router partial sum of the persistent     */
+                                 /* decode kernel beyond +-2^21 (clamped: that */
+                                 /* token's routing is not exact)              */
 
 /* activation dtypes */
 typedef enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 } moe_dtype;

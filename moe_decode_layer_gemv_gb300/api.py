@@ -73,6 +73,8 @@ MOE_DEV_TIMEOUT = 1
 MOE_DEV_BAD_EXPERT_ID = 2
 MOE_DEV_DUP_EXPERT = 4
 MOE_DEV_NONFINITE = 8
+MOE_DEV_BAD_ROUTE = 16
+MOE_DEV_RANGE = 32
 MOE_DT_F32 = 0
 MOE_DT_BF16 = 1
 MOE_F_NO_DEDUP = 1

@@ -162,7 +162,7 @@ constexpr unsigned kAllFlags =
     MOE_F_NO_DEDUP | MOE_F_UNFUSED | MOE_F_FORCE_TC | MOE_F_NO_TC | MOE_F_NO_PREFETCH | MOE_F_HOT_L2;
 
 struct WsLayout {
-    size_t logits, ids, rw, offsets, route_idx, unique, num_unique, status, bar, acc, acc_end, h, o;
+    size_t logits, ids, rw, offsets, route_idx, unique, num_unique, status, bar, acc, xt, acc_end, h, o;
     size_t x_hi, x_lo, h_hi, h_lo, seg_list, seg_count, alog, xn, total;
 };
 
@@ -184,9 +184,14 @@ static WsLayout ws_layout(int B, int H, int I, int E, int k) {
     L.num_unique = take(sizeof(int32_t));
     L.status = take(sizeof(int32_t));
     L.bar = take(sizeof(unsigned) * 1056);  // abort/counter words + one barrier flag per CTA (<= 1024)
-    L.acc = take(sizeof(unsigned long long) * 2 * 8 * (size_t)B * E);  // right after bar: one memset clears both
-    L.acc_end = L.acc + sizeof(unsigned long long) * 2 * 8 * (size_t)B * E;
-    L.h = take(sizeof(float) * R * I);
+    // decode kernel: three sets of counted logit words [2][B][E] and of sums
+    // of squares [2][B], and the tagged copy of x [B][H] u64 after them,
+    // right after bar: one memset clears all
+    const size_t acc_bytes = sizeof(unsigned long long) * 3 * 2 * (size_t)B * (E + 1);
+    L.acc = take(acc_bytes);
+    L.xt = take(sizeof(unsigned long long) * 2 * (size_t)B * H);
+    L.acc_end = L.xt + sizeof(unsigned long long) * 2 * (size_t)B * H;
+    L.h = take(sizeof(float) * 2 * R * I);  // two by layer parity (decode kernel)
     L.o = take(sizeof(float) * R * H);
     L.x_hi = take(sizeof(uint16_t) * R * H);  // tensor-core activation operands (bf16 hi/lo)
     L.x_lo = take(sizeof(uint16_t) * R * H);
@@ -194,7 +199,7 @@ static WsLayout ws_layout(int B, int H, int I, int E, int k) {
     L.h_lo = take(sizeof(uint16_t) * R * I);
     L.seg_list = take(sizeof(int32_t) * 2 * (R > (size_t)E ? R : (size_t)E));
     L.seg_count = take(sizeof(int32_t) * 2);
-    L.alog = take(sizeof(float) * (size_t)B * E);
+    L.alog = take(sizeof(float) * 2 * (size_t)B * E);  // [2][E]: predicted logits, by layer parity
     L.xn = take(sizeof(float) * (size_t)B * H);  // pre-norm stacks: the normalised layer input
     L.total = off;
     return L;
@@ -626,6 +631,7 @@ static int launch_decode(DkParams& p, size_t smem, int sms, char* ws, const WsLa
         return MOE_ERR_CUDA;
     if (per_sm < 1) return MOE_ERR_UNSUPPORTED;
     p.h = reinterpret_cast<float*>(ws + L.h);
+    p.xt = reinterpret_cast<unsigned long long*>(ws + L.xt);
     p.alog = reinterpret_cast<float*>(ws + L.alog);
     // next-layer L2 prefetch: single-token decode, the top k experts of the
     // predicted logits while that stays within 64 MB of weights (a stack
@@ -643,6 +649,9 @@ static int launch_decode(DkParams& p, size_t smem, int sms, char* ws, const WsLa
     p.g_route_idx = reinterpret_cast<int32_t*>(ws + L.route_idx);
     p.g_unique = reinterpret_cast<int32_t*>(ws + L.unique);
     p.g_num_unique = reinterpret_cast<int32_t*>(ws + L.num_unique);
+    // the count field of a logit word holds at most 127 contributions
+    static_assert(kDkShadows == 2, "workspace accumulator sets are sized for two shadow copies");
+    if (sms > 127 * kDkShadows) return MOE_ERR_UNSUPPORTED;
     if ((rc = to_status(cudaMemsetAsync(ws + L.bar, 0, L.acc_end - L.bar, st)))) return rc;
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
@@ -1111,6 +1120,7 @@ const char* moe_status_string(int code) {
         case MOE_DEV_DUP_EXPERT: return "device: a token lists the same expert twice";
         case MOE_DEV_NONFINITE: return "device: non-finite router logit";
         case MOE_DEV_BAD_ROUTE: return "device: route index outside [0, B*top_k)";
+        case MOE_DEV_RANGE: return "device: router partial sum beyond the fixed-point range (+-2^21)";
         default: return "unknown status";
     }
 }

@@ -38,7 +38,16 @@ constexpr int kDkMaxR = 32;
 constexpr int kDkMaxStages = 32;
 constexpr uint32_t kDkWaitLimit = 1u << 22;
 constexpr unsigned long long kDkSpinLimit = 1ull << 22;
-constexpr float kFixScale = 4294967296.0f;  // 2^32
+// Counted fixed-point words (see dk_router_partials): a CTA's value v adds
+// q + kFixBias + kFixCount to a word, q = round(v * scale) with |q| <
+// kFixBias = 2^49.  The low 57 bits hold the sum of up to 127 such terms
+// (each below 2^50) without overflow, bits 57..63 count them; a word whose
+// count reaches the number of contributing CTAs holds the exact sum of
+// every q, whatever order the terms arrived in.
+constexpr unsigned long long kFixCount = 1ull << 57;
+constexpr long long kFixBias = 1ll << 49;
+constexpr float kFixScale = 268435456.0f;  // 2^28 for logits: |v| < 2^21, steps of 2^-28
+constexpr float kFixScaleSq = 65536.0f;    // 2^16 for sums of x^2: |v| < 2^33
 constexpr int kDkSmemMax = 227 * 1024;
 constexpr int kDkGChunks = 8;  // direct mode: gate/up rows land on this many barriers (in issue order)
 
@@ -55,7 +64,8 @@ struct DkParams {
     // the grouped route list of the layer, as moe_group_by_expert lays it
     // out (written by CTA 0; a stack leaves its last layer's)
     int32_t *g_offsets, *g_route_idx, *g_unique, *g_num_unique;
-    float* h;          // [R, I] exchange buffer
+    float* h;          // [2][R, I] exchange buffer, by layer parity
+    unsigned long long* xt;   // [2][B][H] tagged x: (layer << 32) | bits of x_layer[t][h], layers >= 1, by parity
     unsigned long long* acc;  // [2][kDkShadows][B][E] fixed-point logits
     float* alog;              // [B][E] next layer's logits predicted from this layer's input
     int prefetch_k;           // experts per token to prefetch into L2 for the next layer (0: off)
@@ -136,24 +146,31 @@ __device__ __forceinline__ DkWork dk_work(const DkWork& base, int U, const DkMis
 // thread adds 1 to a shared arrival counter with a release atomic and polls
 // it until it reaches epoch * G, then an acquire fence.  (Measured on GB300
 // with 152 CTAs: ~1.15 us; a flag per CTA polled by every CTA, a master-
-// released flag array and a two-level counter tree were all slower.)  Every
-// thread that wrote global memory with relaxed reductions fences before
-// entering, since the release orders only the leader's own accesses.
+// released flag array and a two-level counter tree were all slower.)  The
+// release is cumulative: it orders every access of the CTA that precedes
+// the CTA-wide barrier, whichever thread made it.
 // p.bar[0] = counter, p.bar[1] = abort word.  Bounded: after kDkSpinLimit
 // polls the CTA sets MOE_DEV_TIMEOUT and the abort word and reports failure.
 constexpr int kDkLeader = 32;  // first consumer thread
-#ifndef MOE_DK_SHADOWS
-#define MOE_DK_SHADOWS 2
-#endif
-#ifndef MOE_DK_THREAD_FENCE
-#define MOE_DK_THREAD_FENCE 1
-#endif
-constexpr int kDkShadows = MOE_DK_SHADOWS;  // copies of the logit accumulator (spread the atomics; 2 measured best of 1, 2, 4, 8)
+constexpr int kDkShadows = 2;  // copies of the logit accumulator (CTA c adds into copy c mod 2)
 
-// Pre-norm stacks: the fixed-point sums of x^2 of layer l's input,
-// [kDkShadows][B], behind the two logit accumulators.
+// The logit accumulators of layer l: [kDkShadows][B][E] counted fixed-point
+// words, three sets in rotation (set l mod 3 is read by layer l, set l+1 is
+// filled during layer l, set l+2 -- read by layer l-1 -- is cleared during
+// layer l, between that layer's mid barrier and the next one).
+__device__ __forceinline__ unsigned long long* dk_acc(const DkParams& p, int l) {
+    return p.acc + (size_t)(l % 3) * kDkShadows * p.B * p.E;
+}
+
+// Pre-norm stacks: the counted fixed-point sums of x^2 of layer l's input,
+// [kDkShadows][B], three sets behind the logit accumulators.
 __device__ __forceinline__ unsigned long long* dk_nacc(const DkParams& p, int l) {
-    return p.acc + (size_t)2 * kDkShadows * p.B * p.E + (size_t)(l & 1) * kDkShadows * p.B;
+    return p.acc + (size_t)3 * kDkShadows * p.B * p.E + (size_t)(l % 3) * kDkShadows * p.B;
+}
+
+// CTAs that add into shadow copy sh (those with blockIdx.x mod kDkShadows == sh).
+__device__ __forceinline__ unsigned dk_shadow_ctas(int sh) {
+    return (gridDim.x - (unsigned)sh + kDkShadows - 1) / kDkShadows;
 }
 
 
@@ -170,6 +187,17 @@ __device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned* p) {
 }
 
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void ld_relaxed_gpu_u64x2(const unsigned long long* p, unsigned long long& a,
+                                                     unsigned long long& b) {
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
 
 __device__ __forceinline__ bool dk_grid_sync(const DkParams& p, unsigned& epoch, DkMisc* m, int bar_id,
                                              int nthreads) {
@@ -234,12 +262,39 @@ __device__ __forceinline__ void dk_trace(const DkParams& p, int l, int ev) {
 }
 
 // ----------------------------------------------------------- small steps
-__device__ __forceinline__ float fix_to_float(unsigned long long v) {
-    return __ll2float_rn((long long)v) * (1.0f / kFixScale);
+// One CTA's contribution of v at `scale` into the counted word w.
+// |v * scale| must stay below 2^49: a larger value is clamped
+// (MOE_DEV_RANGE), a non-finite one counts as 0 (MOE_DEV_NONFINITE).
+__device__ __forceinline__ void fix_add(unsigned long long* w, float v, float scale, int32_t* status) {
+    const float lim = 562949953421312.0f;  // 2^49
+    float z = v * scale;
+    if (!(fabsf(z) < lim)) {
+        const bool fin = isfinite(z);
+        set_status(status, fin ? MOE_DEV_RANGE : MOE_DEV_NONFINITE);
+        z = fin ? copysignf(0.5f * lim, z) : 0.f;
+    }
+    red_add_u64(w, (unsigned long long)(__float2ll_rn(z) + kFixBias) + kFixCount);
 }
 
-__device__ __forceinline__ unsigned long long float_to_fix(float v) {
-    return (unsigned long long)__float2ll_rn(v * kFixScale);
+// The sum of the n contributions of a complete counted word (exact).
+__device__ __forceinline__ long long fix_sum(unsigned long long w, unsigned n) {
+    return (long long)(w & (kFixCount - 1ull)) - (long long)n * kFixBias;
+}
+
+// Waits (bounded) until the counted word at w holds n contributions; false
+// when the launch is being aborted (this CTA timed out, or another one did).
+__device__ __forceinline__ bool dk_poll(const unsigned long long* w, unsigned n, unsigned long long& out,
+                                        const DkParams& p, DkMisc* m) {
+    for (unsigned long long it = 0;; ++it) {
+        out = ld_relaxed_gpu_u64(w);
+        if ((unsigned)(out >> 57) >= n) return true;
+        if ((it & 63ull) == 63ull && (ld_relaxed_gpu(p.bar + 1) != 0u || *(volatile int*)&m->abort_flag)) return false;
+        if (it > kDkSpinLimit) {
+            set_status(p.status, MOE_DEV_TIMEOUT);
+            atomicExch(p.bar + 1, 1u);
+            return false;
+        }
+    }
 }
 
 // Top-k of one token (one warp; lane l holds experts l, l+32, ...; E <= 256).
@@ -321,9 +376,53 @@ __device__ __forceinline__ void dk_topk_smem(const float* lg, int E, int k, int 
 }
 
 // Router partial sums of this CTA's hidden rows [h0, h0+nrows) for every
+__device__ __forceinline__ void st_relaxed_gpu_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+struct Tagged4 {
+    unsigned long long a, b, c, d;
+};
+
+__device__ __forceinline__ void dk_ld_tagged4(const unsigned long long* w, Tagged4& t) {
+    ld_relaxed_gpu_u64x2(w, t.a, t.b);
+    ld_relaxed_gpu_u64x2(w + 2, t.c, t.d);
+}
+
+__device__ __forceinline__ bool dk_tags_are(const Tagged4& t, unsigned tag) {
+    return (unsigned)(t.a >> 32) == tag && (unsigned)(t.b >> 32) == tag && (unsigned)(t.c >> 32) == tag &&
+           (unsigned)(t.d >> 32) == tag;
+}
+
+// Four consecutive tagged elements of x (two 16-byte loads, already issued
+// into t), waited for until each carries tag `tag` (bounded like dk_poll);
+// false when aborting.
+__device__ __forceinline__ bool dk_load_tagged4(const unsigned long long* w, unsigned tag, Tagged4& t, float4& out,
+                                                const DkParams& p, DkMisc* m) {
+    for (unsigned long long it = 0;; ++it) {
+        if (dk_tags_are(t, tag)) break;
+        if ((it & 63ull) == 63ull && (ld_relaxed_gpu(p.bar + 1) != 0u || *(volatile int*)&m->abort_flag)) return false;
+        if (it > kDkSpinLimit) {
+            set_status(p.status, MOE_DEV_TIMEOUT);
+            atomicExch(p.bar + 1, 1u);
+            return false;
+        }
+        dk_ld_tagged4(w, t);
+    }
+    out = make_float4(__uint_as_float((unsigned)t.a), __uint_as_float((unsigned)t.b), __uint_as_float((unsigned)t.c),
+                      __uint_as_float((unsigned)t.d));
+    return true;
+}
+
 // (token, expert): one thread per pair, rows in 8-wide vectors from shared
 // memory, the result added to shadow copy (CTA mod kDkShadows) of the
-// fixed-point accumulator.
+// fixed-point accumulator as a counted contribution.  Every CTA adds to
+// every word of its copy (a CTA without rows adds zero), so a word is
+// complete -- and its reader needs no barrier -- once its count reaches the
+// number of CTAs of that copy.  The words carry only themselves: the rows of
+// x travel with their own tags (DkParams::xt), and the buffers a CTA reads
+// after the mid barrier (h, the predicted logits) alternate by layer, so no
+// fence orders anything before the reductions.
 //
 // Pre-norm stacks (g = the layer's norm weights): the logits of RMSNorm(x)
 // are rn * sum_h W[e,h] g[h] x[h] with rn = 1/sqrt(mean(x^2) + eps), one
@@ -334,7 +433,8 @@ __device__ __forceinline__ void dk_topk_smem(const float* lg, int E, int k, int 
 __device__ __forceinline__ void dk_router_partials(const uint16_t* wrs, int maxrows, const float* xs, int H,
                                                    int h0, int nrows, int B, int E,
                                                    unsigned long long* acc, int t0, int nth,
-                                                   const float* g = nullptr, unsigned long long* nacc = nullptr) {
+                                                   int32_t* status, const float* g = nullptr,
+                                                   unsigned long long* nacc = nullptr) {
     unsigned long long* sh = acc + (size_t)(blockIdx.x % kDkShadows) * B * E;
     for (int v = t0; v < B * E; v += nth) {
         const int t = v / E, e = v - t * E;
@@ -356,19 +456,16 @@ __device__ __forceinline__ void dk_router_partials(const uint16_t* wrs, int maxr
             a = ffma2(bf16x2_to_f2(wv.z), make_float2(xb.x, xb.y), a);
             a = ffma2(bf16x2_to_f2(wv.w), make_float2(xb.z, xb.w), a);
         }
-        red_add_u64(sh + v, float_to_fix(a.x + a.y));
+        fix_add(sh + v, a.x + a.y, kFixScale, status);
     }
     if (nacc) {  // sum of squares of this CTA's rows, one thread per token
         for (int t = t0; t < B; t += nth) {
             const float* xr = xs + (size_t)t * H + h0;
             float ss = 0.f;
             for (int r = 0; r < nrows; ++r) ss = fmaf(xr[r], xr[r], ss);
-            red_add_u64(nacc + (size_t)(blockIdx.x % kDkShadows) * B + t, float_to_fix(ss));
+            fix_add(nacc + (size_t)(blockIdx.x % kDkShadows) * B + t, ss, kFixScaleSq, status);
         }
     }
-#if MOE_DK_THREAD_FENCE
-    __threadfence();  // the reductions are performed before this thread reaches the next barrier
-#endif
 }
 
 // Stable grouping of R <= 32 routes by expert in one warp: the position of
@@ -769,6 +866,8 @@ __device__ __forceinline__ void dk_down_compute(const DkMisc* m, const unsigned 
 // Predicted logits of this CTA's experts (e = blockIdx.x, + G, ...) for
 // token 0 (one warp).
 __device__ __forceinline__ void dk_predict_logits(const LayerWeights& wn, const float* xq, int H, int E, float* alog) {
+    // (alog: this layer's half of the [2][E] buffer -- layers alternate, so a
+    // CTA still reading layer l's predictions is never overwritten by layer l+1)
     const int lane = threadIdx.x & 31;
     for (int e = blockIdx.x; e < E; e += gridDim.x) {
         const uint16_t* wrow = wn.w_router + (size_t)e * H;
@@ -952,51 +1051,65 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
         }
         cp_async_wait_all();
         __syncthreads();
-        if (nrows > 0)
-            dk_router_partials(wrs, p.maxrows, xs, H, h0, nrows, B, E, p.acc, tid, blockDim.x,
-                               p.has_norm ? gq : nullptr, p.has_norm ? dk_nacc(p, 0) : nullptr);
+        dk_router_partials(wrs, p.maxrows, xs, H, h0, nrows, B, E, dk_acc(p, 0), tid, blockDim.x, p.status,
+                           p.has_norm ? gq : nullptr, p.has_norm ? dk_nacc(p, 0) : nullptr);
     }
     if (tid == kDkLeader) dk_trace<kTrace>(p, -1, 1);
-    dk_grid_sync(p, epoch, m, 0, kDkThreads);
+    // (no barrier: each layer waits on its own logit words)
 
     for (int l = 0; l < p.L && !*(volatile int*)&m->abort_flag; ++l) {
         const LayerWeights& lw = p.layer[l];
         const bool has_next = l + 1 < p.L;
-        unsigned long long* acc_now = p.acc + (size_t)(l & 1) * kDkShadows * B * E;
-        unsigned long long* acc_next = p.acc + (size_t)((l + 1) & 1) * kDkShadows * B * E;
-        // ---- A0: the consumers sum the logit accumulators into lg; the
-        // router warps (token t: warp t) take the top-k while the consumers
-        // stage x and the next router slice; the producer warp then groups,
-        // hands the routing over (named barrier 4: it arrives, the consumers
-        // wait) and goes on to issue the copies at once
+        const unsigned long long* acc_now = dk_acc(p, l);
+        unsigned long long* acc_next = dk_acc(p, l + 1);
+        float* hb = p.h + (size_t)(l & 1) * R * I;  // this layer's h exchange buffer
+        // ---- A0: the consumers wait for the logit words of this layer
+        // (complete once every CTA has added its rows of x_l) and sum their
+        // shadow copies into lg; the router warps (token t: warp t) take the
+        // top-k while the consumers stage x and the next router slice; the
+        // producer warp then groups, hands the routing over (named barrier 4:
+        // it arrives, the consumers wait) and goes on to issue the copies at once
         if (tid == kDkLeader) dk_trace<kTrace>(p, l, 0);
+        bool polled = true;
         if (warp >= 1) {
             // consumers: every (token, expert) logit from the shadow
             // accumulators (an integer sum: exact in any order) into lg
             const int ct = tid - 32, nct = 32 * kDkConsumers;
             const unsigned long long* nacc_now = p.has_norm ? dk_nacc(p, l) : nullptr;
-            for (int v = ct; v < B * Ep; v += nct) {
+            for (int v = ct; v < B * Ep && polled; v += nct) {
                 const int t = v / Ep, e = v - t * Ep;
                 float val = -INFINITY;
                 float rn = 1.f;
                 if (nacc_now) {  // pre-norm: 1/sqrt(mean(x^2) + eps) of token t's input
-                    unsigned long long ss = 0ull;
+                    long long ss = 0;
 #pragma unroll
-                    for (int sh = 0; sh < kDkShadows; ++sh) ss += __ldcg(nacc_now + (size_t)sh * B + t);
-                    rn = 1.0f / sqrtf(fix_to_float(ss) / (float)H + p.eps);
+                    for (int sh = 0; sh < kDkShadows; ++sh) {
+                        unsigned long long w = 0ull;
+                        polled = polled && dk_poll(nacc_now + (size_t)sh * B + t, dk_shadow_ctas(sh), w, p, m);
+                        ss += fix_sum(w, dk_shadow_ctas(sh));
+                    }
+                    rn = 1.0f / sqrtf(__ll2float_rn(ss) * (1.0f / kFixScaleSq) / (float)H + p.eps);
                     if (e == 0) m->rn[t] = rn;
                 }
                 if (e < E) {
-                    unsigned long long sum = 0ull;
+                    long long sum = 0;  // the shadow copies' integer sums, exact, then one rounding
 #pragma unroll
-                    for (int sh = 0; sh < kDkShadows; ++sh) sum += __ldcg(acc_now + ((size_t)sh * B + t) * E + e);
-                    val = rn * fix_to_float(sum);
+                    for (int sh = 0; sh < kDkShadows; ++sh) {
+                        unsigned long long w = 0ull;
+                        polled = polled && dk_poll(acc_now + ((size_t)sh * B + t) * E + e, dk_shadow_ctas(sh), w, p, m);
+                        sum += fix_sum(w, dk_shadow_ctas(sh));
+                    }
+                    val = rn * (__ll2float_rn(sum) * (1.0f / kFixScale));
                     if (lw.bias) val += __ldg(lw.bias + e);
                 }
                 lg[v] = val;
             }
         }
-        __syncthreads();
+        if (__syncthreads_or(!polled)) {
+            if (tid == 0) *(volatile int*)&m->abort_flag = 1;
+            break;
+        }
+        if (tid == kDkLeader) dk_trace<kTrace>(p, l, 14);
         if (warp < B) {
             dk_topk_smem(lg + warp * Ep, E, k, warp, m, p.status);
             if (tid == 0) dk_trace<kTrace>(p, l, 7);
@@ -1018,9 +1131,34 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
             named_arrive(4, kDkThreads);
         } else {
             const int ct = tid - 32, nct = 32 * kDkConsumers;
-            if (l > 0 || !p.x_bf16) {
+            if (l > 0) {
+                // x_l from the tagged copy: every element carries the layer it
+                // belongs to, so an element not yet visible is waited for on
+                // its own (bounded), with no fence or barrier
+                const int nv4 = (B * H) >> 2;
+                const float* gn = p.has_norm ? gq + (size_t)(l & 1) * H : nullptr;
+                const unsigned long long* xt = p.xt + (size_t)(l & 1) * B * H;
+                for (int v0 = ct; v0 < nv4; v0 += 2 * nct) {
+                    // both groups' loads in flight before either is checked
+                    const int v1 = v0 + nct;
+                    Tagged4 t0, t1;
+                    dk_ld_tagged4(xt + 4 * (size_t)v0, t0);
+                    if (v1 < nv4) dk_ld_tagged4(xt + 4 * (size_t)v1, t1);
+                    float4 a;
+                    bool ok = dk_load_tagged4(xt + 4 * (size_t)v0, (unsigned)l, t0, a, p, m);
+                    if (ok) dk_store_x(xs, xq, H, 4 * v0, a, gn, m);
+                    if (ok && v1 < nv4) {
+                        ok = dk_load_tagged4(xt + 4 * (size_t)v1, (unsigned)l, t1, a, p, m);
+                        if (ok) dk_store_x(xs, xq, H, 4 * v1, a, gn, m);
+                    }
+                    if (!ok) {
+                        *(volatile int*)&m->abort_flag = 1;
+                        break;
+                    }
+                }
+            } else if (!p.x_bf16) {
                 // both loads of a thread in flight before either store
-                const float* xsrc = (l > 0) ? p.y : static_cast<const float*>(p.x_in);
+                const float* xsrc = static_cast<const float*>(p.x_in);
                 const int nv4 = (B * H) >> 2;
                 const float* gn = p.has_norm ? gq + (size_t)(l & 1) * H : nullptr;
                 for (int v0 = ct; v0 < nv4; v0 += 2 * nct) {
@@ -1167,7 +1305,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                 __nanosleep(64);
             }
             if (__all_sync(0xffffffffu, seen)) {
-                const int my_e = dk_predict_top(p.alog, E, p.prefetch_k);
+                const int my_e = dk_predict_top(p.alog + (size_t)(l & 1) * E, E, p.prefetch_k);
                 dk_prefetch_l2(p.layer[l + 1], my_e, H, I, p.prefetch_k, kWb);
             }
         }
@@ -1187,7 +1325,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
             s = rs + c0 - q0 * p.S;
             ph = rph ^ (uint32_t)(q0 & 1);
             const bool predicting = p.prefetch_k > 0 && has_next && cw == kDkConsumers - 1;
-            if (predicting) dk_predict_logits(p.layer[l + 1], xq, H, E, p.alog);
+            if (predicting) dk_predict_logits(p.layer[l + 1], xq, H, E, p.alog + (size_t)(l & 1) * E);
             if (d_gate) {
                 const int csz = max(4, (wk.ng + kDkGChunks - 1) / kDkGChunks);
                 int landed = -1;
@@ -1201,7 +1339,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                     const int u = q / I, i = q - u * I;
                     const float* gsr = kF8 ? lw.gate_up_scale + (size_t)m->seg_e[u] * sg_e + (size_t)(i >> 7) * sg_ld : nullptr;
                     const float* usr = kF8 ? lw.gate_up_scale + (size_t)m->seg_e[u] * sg_e + (size_t)((I + i) >> 7) * sg_ld : nullptr;
-                    dk_pair_compute<kNQ, kF8>(m, d_g + (size_t)c * rowg, d_u + (size_t)c * rowg, xq, H, I, k, u, i, p.h,
+                    dk_pair_compute<kNQ, kF8>(m, d_g + (size_t)c * rowg, d_u + (size_t)c * rowg, xq, H, I, k, u, i, hb,
                                               gsr, usr);
                 }
             }
@@ -1214,7 +1352,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                 const unsigned char* st = ring + (size_t)s * p.stage_bytes;
                 const float* gsr = kF8 ? lw.gate_up_scale + (size_t)m->seg_e[u] * sg_e + (size_t)(i >> 7) * sg_ld : nullptr;
                 const float* usr = kF8 ? lw.gate_up_scale + (size_t)m->seg_e[u] * sg_e + (size_t)((I + i) >> 7) * sg_ld : nullptr;
-                dk_pair_compute<kNQ, kF8>(m, st, st + rowg, xq, H, I, k, u, i, p.h, gsr, usr);
+                dk_pair_compute<kNQ, kF8>(m, st, st + rowg, xq, H, I, k, u, i, hb, gsr, usr);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
                 s += p.W;
@@ -1229,7 +1367,13 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
             // ---- B: down rows of every selected expert for this CTA's rows
             if (ok) {
             for (int v = tid - 32; v < (R * I) >> 2; v += 32 * kDkConsumers)
-                reinterpret_cast<float4*>(hs)[v] = ld_act_f4(p.h + 4 * (size_t)v);
+                reinterpret_cast<float4*>(hs)[v] = ld_act_f4(hb + 4 * (size_t)v);
+            if (blockIdx.x == 0) {  // clear the accumulator set that layer l-1 read (layer l+1 fills it)
+                unsigned long long* a2 = dk_acc(p, l + 2);
+                for (int v = tid - 32; v < kDkShadows * B * E; v += 32 * kDkConsumers) a2[v] = 0ull;
+                if (p.has_norm)
+                    for (int v = tid - 32; v < kDkShadows * B; v += 32 * kDkConsumers) dk_nacc(p, l + 2)[v] = 0ull;
+            }
             named_sync(1, 32 * kDkConsumers);
             if (tid == kDkLeader) dk_trace<kTrace>(p, l, 3);
             if (tid == kDkLeader) {  // tell the producer warp that every CTA's predicted logits are visible
@@ -1289,23 +1433,21 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                     a = xs[t * H + h0 + r] + a;
                 else if (p.residual)
                     a = ld_act_f(p.residual + gi) + a;
-                p.y[gi] = a;
+                if (has_next)  // x_{l+1} for every CTA, tagged with its layer (buffers alternate by layer)
+                    st_relaxed_gpu_u64(p.xt + (size_t)((l + 1) & 1) * B * H + gi,
+                                       ((unsigned long long)(l + 1) << 32) | __float_as_uint(a));
+                else
+                    p.y[gi] = a;
                 xs[t * H + h0 + r] = a;  // x_{l+1} rows for the next router
-            }
-            if (blockIdx.x == 0) {  // acc_now was read by every CTA before the last barrier
-                for (int v = tid - 32; v < kDkShadows * B * E; v += 32 * kDkConsumers) acc_now[v] = 0ull;
-                if (p.has_norm)
-                    for (int v = tid - 32; v < kDkShadows * B; v += 32 * kDkConsumers) dk_nacc(p, l)[v] = 0ull;
-                __threadfence();  // performed before this CTA reaches the end-of-layer barrier
             }
             if (tid == kDkLeader) dk_trace<kTrace>(p, l, 10);
             if (has_next) cp_async_wait_all();
             named_sync(1, 32 * kDkConsumers);
             if (tid == kDkLeader) dk_trace<kTrace>(p, l, 11);
             // ---- router of layer l+1: partial dot products over this CTA's rows
-            if (has_next && nrows > 0)
+            if (has_next)
                 dk_router_partials(wrs, p.maxrows, xs, H, h0, nrows, B, E, acc_next, tid - 32,
-                                   32 * kDkConsumers, p.has_norm ? gq + (size_t)((l + 1) & 1) * H : nullptr,
+                                   32 * kDkConsumers, p.status, p.has_norm ? gq + (size_t)((l + 1) & 1) * H : nullptr,
                                    p.has_norm ? dk_nacc(p, l + 1) : nullptr);
             }  // ok
             if (has_next) cp_async_wait_all();
@@ -1319,13 +1461,9 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
         dg_count += d_gate ? 1 : 0;
         dd_count += d_down ? 1 : 0;
         if (tid == kDkLeader) dk_trace<kTrace>(p, l, 5);
+        // no device-wide barrier here: the next layer waits on its logit words
         __syncthreads();
-        // every thread reads the same flag: nobody writes it between the two
-        // barriers around this read
-        const bool aborted = *(volatile int*)&m->abort_flag != 0;
-        if (has_next && !aborted) dk_grid_sync(p, epoch, m, 0, kDkThreads);
         if (tid == kDkLeader) dk_trace<kTrace>(p, l, 6);
-        __syncthreads();
     }
     // leave only after this CTA's own copies in flight have landed: the latest
     // phase armed in each stage is the only one that can still be in flight

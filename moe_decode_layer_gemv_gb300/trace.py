@@ -3,12 +3,15 @@
 trace_stack() runs one stack forward with the trace buffer set and returns,
 per layer, the duration of each phase (median and max over CTAs, in us):
   route   layer start -> routing done (logits, top-k, grouping)
+  poll    layer start -> every logit word of the layer complete (the wait
+          for the other CTAs' router contributions; there is no
+          end-of-layer barrier)
   gate    routing done -> this CTA's gate/up pairs done
   mid     wait in the barrier after the gate/up pass
   down    down rows done (weights mostly already in shared memory)
   tail    combine, residual, next router partial sums
-  end     wait in the end-of-layer barrier
-and the layer's wall time (first start to last barrier exit).
+  end     the CTA-wide barrier closing the layer
+and the layer's wall time (first start to last layer exit).
 """
 from __future__ import annotations
 
@@ -40,7 +43,7 @@ def trace_stack(api, x, stack, top_k, sms=None, flags=0):
         d = lambda a, b: (ev[:, b] - ev[:, a]).tolist()
         row = {}
         for name, a, b in (("route", 0, 1), ("gate", 1, 2), ("mid", 2, 3), ("down", 3, 4),
-                           ("tail", 4, 5), ("end", 5, 6), ("topk", 0, 7), ("xload", 0, 8), ("group", 7, 9),
+                           ("tail", 4, 5), ("end", 5, 6), ("poll", 0, 14), ("topk", 0, 7), ("xload", 0, 8), ("group", 7, 9),
                            ("handoff", 9, 1), ("combine", 4, 10), ("cpwait", 10, 11), ("partial", 11, 5),
                            ("gate1st", 1, 12), ("issued", 1, 18), ("land0", 1, 19), ("gate_land", 1, 16), ("all_land", 1, 17)):
             v = d(a, b)
@@ -51,7 +54,8 @@ def trace_stack(api, x, stack, top_k, sms=None, flags=0):
         # SM-clock intervals (same SM, any warps): exact where globaltimer is coarse
         for name, a, b in (("cy_land", 1, 16), ("cy_after_land", 16, 2), ("cy_lead_wait", 1, 12),
                            ("cy_lead_compute", 12, 2), ("cy_mid", 2, 3), ("cy_down", 3, 4),
-                           ("cy_combine", 4, 10), ("cy_partial", 11, 5), ("cy_end", 5, 6), ("cy_topk", 0, 7),
+                           ("cy_combine", 4, 10), ("cy_partial", 11, 5), ("cy_end", 5, 6), ("cy_poll", 0, 14),
+                           ("cy_topk", 0, 7),
                            ("cy_group", 7, 9), ("cy_xload", 0, 8), ("cy_route", 0, 1)):
             v = (c[:, b] - c[:, a]).tolist()
             row[name] = (statistics.median(v), max(v))
@@ -61,7 +65,7 @@ def trace_stack(api, x, stack, top_k, sms=None, flags=0):
 
 
 def format_detail(res) -> str:
-    names = ("topk", "xload", "group", "handoff", "combine", "partial", "issued", "gate_land", "all_land")
+    names = ("poll", "topk", "xload", "group", "handoff", "combine", "partial", "issued", "gate_land", "all_land")
     lines = ["layer  " + "  ".join(f"{n:>11s}" for n in names) + "  route_cycles"]
     for l, r in enumerate(res["layers"]):
         lines.append(f"{l:5d}  " + "  ".join(f"{r[n][0]:5.2f}/{r[n][1]:5.2f}" for n in names)
@@ -70,7 +74,7 @@ def format_detail(res) -> str:
 
 
 def format_cycles(res) -> str:
-    names = ("cy_topk", "cy_group", "cy_xload", "cy_route", "cy_land", "cy_after_land", "cy_lead_wait", "cy_lead_compute", "cy_mid", "cy_down",
+    names = ("cy_poll", "cy_topk", "cy_group", "cy_xload", "cy_route", "cy_land", "cy_after_land", "cy_lead_wait", "cy_lead_compute", "cy_mid", "cy_down",
              "cy_combine", "cy_partial", "cy_end")
     lines = ["layer " + " ".join(f"{n[3:]:>15s}" for n in names) + "   (SM cycles, median/max)"]
     for l, r in enumerate(res["layers"]):

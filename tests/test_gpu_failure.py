@@ -71,3 +71,26 @@ def test_stack_barrier_timeout_reports_and_recovers(cuda_lib):
     torch.cuda.synchronize()
     assert torch.equal(ia, ib)
     assert float((xa - xb).abs().max()) <= 1e-5 * float(xb.abs().max())
+
+
+def test_stack_flags_router_values_beyond_the_fixed_point_range(cuda_lib):
+    """The decode kernel sums the router's per-CTA partial logits in counted
+    fixed-point words; a partial beyond their range is clamped and reported
+    (MOE_DEV_RANGE), never a wait that runs out, and the next call is clean."""
+    w = synth.Workload("stack2", B=1, H=512, I=128, E=32, top_k=2, layers=2, residual=True,
+                       sigma_router=512 ** -0.5, sigma_expert=0.05)
+    layers = [synth.make_layer(w, l, seed=2, device=DEV) for l in range(2)]
+    sw = cuda_lib.StackWeights(layers)
+    x = synth.make_x(w, 0, seed=2, device=DEV)
+    st = cuda_lib.new_status()
+    t0 = time.perf_counter()
+    cuda_lib.stack_forward(x * 1e8, sw, w.top_k, status=st)
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 < 30.0
+    v = int(st.item())
+    assert v & cuda_lib.MOE_DEV_RANGE, v
+    assert v & ~(cuda_lib.MOE_DEV_RANGE | cuda_lib.MOE_DEV_NONFINITE) == 0, v
+    st2 = cuda_lib.new_status()
+    cuda_lib.stack_forward(x, sw, w.top_k, status=st2)
+    torch.cuda.synchronize()
+    assert int(st2.item()) == 0
