@@ -65,6 +65,8 @@ def parse():
                     help="stack = the 30-layer decode stack (the headline); dense = its dense SwiGLU "
                          "counterpart (E=1, top-1, I=1536); the others time one layer")
     ap.add_argument("--batch", type=int, default=None, help="tokens per step for a single-layer workload")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="experts of a single-layer workload (fewer only for scaled profiling captures)")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the sub-records of the other workloads in the default run")
     ap.add_argument("--config-steps", type=int, default=10, help="timed steps per sub-record")
@@ -426,6 +428,9 @@ def run_layer_workload(args):
     base = {"uniform": synth.UNIFORM, "skewed": synth.SKEWED, "prefill": synth.PREFILL,
             "tiny": synth.TINY}[args.workload]
     w = base.with_batch(args.batch) if args.batch else base
+    if args.experts:
+        import dataclasses
+        w = dataclasses.replace(w, E=args.experts, name=f"{w.name}_e{args.experts}")
     flags = api.MOE_F_UNFUSED if args.mode == "unfused" else 0
     with ClockSampler(local) as clk:
         rec = measure_layer(api, accounting, synth, w, dev, args.steps, args.warmup, flags, args.seed)

@@ -198,7 +198,7 @@ static WsLayout ws_layout(int B, int H, int I, int E, int k) {
     L.h_hi = take(sizeof(uint16_t) * R * I);
     L.h_lo = take(sizeof(uint16_t) * R * I);
     L.seg_list = take(sizeof(int32_t) * 2 * (R > (size_t)E ? R : (size_t)E));
-    L.seg_count = take(sizeof(int32_t) * 2);
+    L.seg_count = take(sizeof(int32_t) * 4);  // CUDA-core and tensor-core segments, largest tensor-core segment
     L.alog = take(sizeof(float) * 2 * (size_t)B * E);  // [2][E]: predicted logits, by layer parity
     L.xn = take(sizeof(float) * (size_t)B * H);  // pre-norm stacks: the normalised layer input
     L.total = off;

@@ -99,7 +99,8 @@ struct Ctx {
     // Work lists built on the device by classify_kernel (nullptr: iterate over
     // every segment directly): seg_list[0 .. seg_count[0]) are the segments
     // for the CUDA-core GEMV, seg_list[max_segments .. + seg_count[1]) those
-    // for the tensor-core GEMMs.
+    // for the tensor-core GEMMs; seg_count[2] = routes of the largest
+    // tensor-core segment.
     int32_t* seg_list;
     int32_t* seg_count;
     // routing (device)

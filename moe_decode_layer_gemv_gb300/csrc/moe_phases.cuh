@@ -273,7 +273,7 @@ __device__ void classify_warp(const Ctx& c) {
     const int lane = threadIdx.x & 31;
     const int nseg = no_dedup(c) ? c.B * c.k : ld_act_i(c.num_unique);
     const int maxseg = max_segments(c);
-    int ng = 0, nt = 0;
+    int ng = 0, nt = 0, nmax = 0;
     for (int base = 0; base < nseg; base += 32) {
         const int s = base + lane;
         bool valid = false, tc = false;
@@ -281,6 +281,7 @@ __device__ void classify_warp(const Ctx& c) {
             Seg sg;
             valid = get_seg(c, s, sg);
             tc = valid && c.tc_threshold > 0 && sg.p1 - sg.p0 >= c.tc_threshold;
+            if (tc) nmax = max(nmax, sg.p1 - sg.p0);
         }
         const unsigned bt = __ballot_sync(0xffffffffu, tc);
         const unsigned bg = __ballot_sync(0xffffffffu, valid && !tc);
@@ -290,9 +291,11 @@ __device__ void classify_warp(const Ctx& c) {
         nt += __popc(bt);
         ng += __popc(bg);
     }
+    nmax = __reduce_max_sync(0xffffffffu, nmax);
     if (lane == 0) {
         c.seg_count[0] = ng;
         c.seg_count[1] = nt;
+        c.seg_count[2] = nmax;  // routes of the largest tensor-core segment
     }
 }
 

@@ -122,6 +122,21 @@ __device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Named barrier that also ORs a predicate over its threads: every thread
+// gets the same answer (a uniform decision among the barrier's threads).
+__device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "barrier.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
 // Arrive at named barrier `id` without waiting (the producer side of a
 // hand-off: the consumers wait with named_sync on the same id and count).
 __device__ __forceinline__ void named_arrive(uint32_t id, uint32_t nthreads) {

@@ -5,9 +5,13 @@
 // Swap-AB: the weight rows are the MMA's M side (128 rows per tile), the
 // expert's tokens its N side (up to 128), K runs over H (gate/up) or I
 // (down) in 64-element steps.  Weight tiles and activation tiles are moved
-// by the TMA engine with the 128-byte swizzle into a 4-stage shared-memory
-// ring; one thread issues the MMAs; the accumulator tile lives in tensor
-// memory and four warps read it back for the epilogue.
+// by the TMA engine with the 128-byte swizzle into a shared-memory ring
+// whose depth follows the launch's largest token count (stages hold one
+// weight tile and that many activation rows, so small N buys more weight
+// bytes in flight); one warp issues the copies, one thread the MMAs into one
+// of two tensor-memory accumulators, and four warps read the other one back
+// for the epilogue, so copies, MMAs and the epilogue of consecutive tiles
+// overlap.
 //
 // Precision: the MMA takes bf16 operands.  Weights are bf16 already; fp32
 // activations are split into hi = bf16(a) and lo = bf16(a - hi) and the MMA
@@ -29,18 +33,31 @@
 
 namespace moe {
 
-constexpr int kTcThreads = 128;
+constexpr int kTcThreads = 192;  // warps 0-3 epilogue, warp 4 TMA producer, warp 5 MMA issuer
 constexpr int kTcBK = 64;        // K elements per stage (one 128-byte swizzle row)
 constexpr int kTcMaxN = 128;     // tokens per tile
 constexpr int kTcBoxN = 32;      // rows per activation TMA box
-constexpr int kTcStages = 4;
+constexpr int kTcMaxStages = 16;
 constexpr int kTcATile = 128 * 128;      // 128 rows x 128 B
-constexpr int kTcBTile = kTcMaxN * 128;  // per activation operand
-constexpr int kTcStageBytes = kTcATile + 2 * kTcBTile;
-constexpr int kTcEpiLd = kTcMaxN + 1;    // fp32 row stride of the epilogue tile
-constexpr int kTcSmem = 1024 + kTcStages * kTcStageBytes + 256;
+constexpr int kTcEpiCols = 32;           // accumulator columns per epilogue pass
+constexpr int kTcEpiLd = kTcEpiCols + 1; // fp32 row stride of the epilogue tile
+constexpr int kTcEpiBytes = 17 * 1024;   // >= 128 * kTcEpiLd * 4, a multiple of 1024
+constexpr int kTcSmem = 227 * 1024;
 constexpr uint32_t kTcWaitLimit = 1u << 24;
-constexpr uint32_t kTcTmemCols = 128;
+constexpr uint32_t kTcTmemCols = 256;    // two accumulators of 128 columns
+static_assert(128 * kTcEpiLd * 4 <= kTcEpiBytes, "epilogue tile");
+
+// Barriers and flags at the start of the kernel's shared memory.
+struct TcBars {
+    uint64_t full[kTcMaxStages];   // a stage's tiles landed (TMA transaction count)
+    uint64_t empty[kTcMaxStages];  // a stage's MMAs are done with it (tcgen05.commit)
+    uint64_t acc_full[2];          // an accumulator's MMAs are complete
+    uint64_t acc_empty[2];         // the epilogue has read an accumulator (4 warps arrive)
+    uint64_t mma_done;             // every MMA issued has completed (teardown)
+    uint32_t tmem_slot;
+    int abort;                     // a bounded wait ran out: every role stops
+};
+static_assert(sizeof(TcBars) <= 1024, "barrier block");
 
 struct TcParams {
     CUtensorMap ta;      // weights [rows, K] bf16, box {64, 64 (gate) or 128 (down)}
@@ -149,6 +166,16 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity) {
     return false;
 }
 
+// The same, also giving up once another role has raised the abort flag.
+__device__ __forceinline__ bool tc_wait_ab(uint64_t* bar, uint32_t parity, TcBars* b) {
+    for (uint32_t i = 0; i < kTcWaitLimit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 63u && *(volatile int*)&b->abort) return false;
+    }
+    *(volatile int*)&b->abort = 1;
+    return false;
+}
+
 // ------------------------------------------------------------ activations
 // Split the activation rows of every route position p into bf16 hi and lo:
 // x_hi[p] = bf16(x[t]), x_lo[p] = bf16(x[t] - x_hi[p]), t = route_at(p) / k.
@@ -169,17 +196,21 @@ __global__ void __launch_bounds__(kThreads) tc_split_x_kernel(Ctx c, uint16_t* x
 // ------------------------------------------------------------ the GEMM
 // Persistent: one CTA per SM walks the items of the tensor-core segment
 // list; an item is (segment, M tile of 64 gate/up row pairs or 128 down rows,
-// 128-token chunk).  The ring position and the accumulator phase carry over
-// from item to item; TMEM and the barriers are set up once.
+// 128-token chunk).  Three roles run through the same item sequence:
+//   warp 4 (one lane)  TMA producer: k-steps into the ring, waits only for a
+//                      stage to be released, so it runs ahead across items;
+//   warp 5 (one lane)  MMA issuer: item d accumulates into tensor-memory
+//                      buffer d mod 2 once the epilogue has read that
+//                      buffer's previous item;
+//   warps 0-3          epilogue: accumulator lanes 32w..32w+31, 32 columns
+//                      per pass through shared memory to coalesced stores.
 __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ __align__(1024) unsigned char tc_smem_raw[];
-    unsigned char* smem = reinterpret_cast<unsigned char*>(
+    unsigned char* base = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTcStages * kTcStageBytes);
-    uint64_t* empty = full + kTcStages;
-    uint64_t* accum = empty + kTcStages;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
-    int* ok_flag = reinterpret_cast<int*>(tmem_slot + 1);
+    TcBars* b = reinterpret_cast<TcBars*>(base);
+    float* epi = reinterpret_cast<float*>(base + 1024);  // [128][kTcEpiLd]
+    unsigned char* ring = base + 1024 + kTcEpiBytes;
 
     const Ctx& c = p.c;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -191,24 +222,45 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     const int n_items = ld_act_i(c.seg_count + 1) * mtiles * nchunk;
     if ((int)blockIdx.x >= n_items) return;  // uniform: nothing for this CTA
 
+    // Ring geometry from the launch's largest tensor-core token count.  A
+    // stage holds ksub consecutive 64-wide k-steps (weight tile, then the
+    // activation tiles): tensor-copy streams run far below the copy bandwidth
+    // when each stage (one mbarrier phase) carries only 16 KB, and near it
+    // from about 32 KB up, so small token counts take two k-steps a stage.
+    const int nmax = min(kTcMaxN, max(1, ld_act_i(c.seg_count + 2)));
+    const uint32_t bbytes = (uint32_t)((nmax + kTcBoxN - 1) / kTcBoxN * kTcBoxN) * 128u;  // one activation operand
+    const uint32_t nb = p.with_lo ? 2u : 1u;
+    const uint32_t ring_bytes = (uint32_t)kTcSmem - 1023u - (uint32_t)(ring - base);
+    auto stage_of = [&](int ks) { return ((uint32_t)ks * (kTcATile + nb * bbytes) + 1023u) & ~1023u; };
+    int ksub = 1;
+    while (ksub < 4 && stage_of(ksub) < 32768u && ring_bytes / stage_of(2 * ksub) >= 3u) ksub *= 2;
+    const uint32_t stage_bytes = stage_of(ksub);
+    const uint32_t b_off = (uint32_t)ksub * kTcATile;   // activation tiles after the ksub weight tiles
+    const int S = min(kTcMaxStages, (int)(ring_bytes / stage_bytes));
+    const int nst = (nk + ksub - 1) / ksub;             // stages per item
+
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kTcStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+        for (int s = 0; s < kTcMaxStages; ++s) {
+            mbar_init(&b->full[s], 1);
+            mbar_init(&b->empty[s], 1);
         }
-        mbar_init(accum, 1);
-        *ok_flag = 1;
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&b->acc_full[a], 1);
+            mbar_init(&b->acc_empty[a], 4);
+        }
+        mbar_init(&b->mma_done, 1);
+        b->abort = 0;
         fence_mbar_init();
     }
-    if (warp == 0) tmem_alloc(tmem_slot, kTcTmemCols);
+    if (warp == 5) tmem_alloc(&b->tmem_slot, kTcTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    float* epi = reinterpret_cast<float*>(smem);  // [128][kTcEpiLd]: stage memory, idle during the epilogue
+    const uint32_t tmem = b->tmem_slot;
 
-    int g = 0;     // k-steps through the ring so far (same in every thread)
-    int done = 0;  // items finished (accumulator phases)
+    uint32_t g = 0;         // stages through the ring so far (same in every role)
+    uint32_t g_armed = 0;   // stages whose copies the producer armed (producer lane only)
+    int d = 0;              // items processed (same in every role)
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
         // the token chunk varies slowest: items of later chunks (which exist
         // only for segments with more than 128 routes) come after every
@@ -223,128 +275,149 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         if (q0 >= sg.p1) continue;
         const int n = min(kTcMaxN, sg.p1 - q0);
         const int n_pad = (n + kTcBoxN - 1) / kTcBoxN * kTcBoxN;
+        const int buf = d & 1, use = d >> 1;
 
-        if (warp == 0 && lane == 0) {
-            // ---------------- TMA producer
-            // MOE_F_HOT_L2: the tensor-core experts are the step's most chosen
-            // ones (>= threshold routes); their weights are loaded with
-            // evict_last so that they stay in L2 for the next steps
-            const bool hot = (c.flags & MOE_F_HOT_L2) != 0;
-            const uint64_t pol = hot ? l2_policy_evict_last() : 0ull;
-            const uint32_t bytes = kTcATile + (uint32_t)n_pad * 128u * (p.with_lo ? 2u : 1u);
-            int arow0, arow1 = 0;
-            if (p.gate) {
-                arow0 = sg.e * 2 * c.I + mt * 64;
-                arow1 = arow0 + c.I;
-            } else {
-                arow0 = sg.e * c.H + mt * 128;
-            }
-            for (int kc = 0; kc < nk; ++kc) {
-                const int gk = g + kc;
-                const int s = gk % kTcStages;
-                const uint32_t ph = (uint32_t)((gk / kTcStages) & 1);
-                if (gk >= kTcStages && !tc_wait(&empty[s], ph ^ 1u)) {
-                    *(volatile int*)ok_flag = 0;
-                    break;
-                }
-                unsigned char* st = smem + (size_t)s * kTcStageBytes;
-                mbar_arrive_expect_tx(&full[s], bytes);
-                if (hot) {  // the expert's weights stay in L2 for the next steps
-                    tma_load_2d_hint(st, &p.ta, kc * kTcBK, arow0, &full[s], pol);
-                    if (p.gate) tma_load_2d_hint(st + 8192, &p.ta, kc * kTcBK, arow1, &full[s], pol);
-                } else if (p.gate) {
-                    tma_load_2d(st, &p.ta, kc * kTcBK, arow0, &full[s]);
-                    tma_load_2d(st + 8192, &p.ta, kc * kTcBK, arow1, &full[s]);
+        if (warp == 4) {
+            if (lane == 0) {
+                // ---------------- TMA producer
+                // MOE_F_HOT_L2: the tensor-core experts are the step's most
+                // chosen ones; their weights are loaded with evict_last so that
+                // they stay in L2 for the next steps
+                const bool hot = (c.flags & MOE_F_HOT_L2) != 0;
+                const uint64_t pol = hot ? l2_policy_evict_last() : 0ull;
+                const uint32_t bytes = kTcATile + (uint32_t)n_pad * 128u * (p.with_lo ? 2u : 1u);
+                int arow0, arow1 = 0;
+                if (p.gate) {
+                    arow0 = sg.e * 2 * c.I + mt * 64;
+                    arow1 = arow0 + c.I;
                 } else {
-                    tma_load_2d(st, &p.ta, kc * kTcBK, arow0, &full[s]);
+                    arow0 = sg.e * c.H + mt * 128;
                 }
-                for (int r = 0; r < n_pad; r += kTcBoxN) {
-                    tma_load_2d(st + kTcATile + r * 128, &p.tb_hi, kc * kTcBK, q0 + r, &full[s]);
-                    if (p.with_lo)
-                        tma_load_2d(st + kTcATile + kTcBTile + r * 128, &p.tb_lo, kc * kTcBK, q0 + r, &full[s]);
+                for (int j = 0; j < nst; ++j) {
+                    const uint32_t gs = g + (uint32_t)j;
+                    const int s = (int)(gs % (uint32_t)S);
+                    const uint32_t ph = (gs / (uint32_t)S) & 1u;
+                    if (gs >= (uint32_t)S && !tc_wait_ab(&b->empty[s], ph ^ 1u, b)) break;
+                    unsigned char* st = ring + (size_t)s * stage_bytes;
+                    const int k0 = j * ksub, ke = min(ksub, nk - k0);  // k-steps k0 .. k0+ke-1
+                    mbar_arrive_expect_tx(&b->full[s], (uint32_t)ke * bytes);
+                    g_armed = gs + 1u;
+                    for (int u = 0; u < ke; ++u) {
+                        const int kx = (k0 + u) * kTcBK;
+                        unsigned char* sa = st + (size_t)u * kTcATile;
+                        unsigned char* sb = st + b_off + (size_t)u * bbytes;
+                        if (hot) {
+                            tma_load_2d_hint(sa, &p.ta, kx, arow0, &b->full[s], pol);
+                            if (p.gate) tma_load_2d_hint(sa + 8192, &p.ta, kx, arow1, &b->full[s], pol);
+                        } else {
+                            tma_load_2d(sa, &p.ta, kx, arow0, &b->full[s]);
+                            if (p.gate) tma_load_2d(sa + 8192, &p.ta, kx, arow1, &b->full[s]);
+                        }
+                        for (int r = 0; r < n_pad; r += kTcBoxN) {
+                            tma_load_2d(sb + r * 128, &p.tb_hi, kx, q0 + r, &b->full[s]);
+                            if (p.with_lo)
+                                tma_load_2d(sb + (size_t)ksub * bbytes + r * 128, &p.tb_lo, kx, q0 + r, &b->full[s]);
+                        }
+                    }
                 }
             }
-        } else if (warp == 1 && lane == 0) {
-            // ---------------- MMA issuer (one thread)
-            const uint32_t idesc = umma_idesc_bf16(128, n_pad);
-            for (int kc = 0; kc < nk; ++kc) {
-                const int gk = g + kc;
-                const int s = gk % kTcStages;
-                const uint32_t ph = (uint32_t)((gk / kTcStages) & 1);
-                if (!tc_wait(&full[s], ph)) {
-                    *(volatile int*)ok_flag = 0;
-                    break;
-                }
+            __syncwarp();
+        } else if (warp == 5) {
+            if (lane == 0) {
+                // ---------------- MMA issuer (one thread)
+                bool ok = use == 0 || tc_wait_ab(&b->acc_empty[buf], (uint32_t)((use - 1) & 1), b);
                 tc_fence_after();
-                const uint32_t a_addr = smem_u32(smem + (size_t)s * kTcStageBytes);
-                const uint32_t bh_addr = a_addr + kTcATile;
-                const uint32_t bl_addr = bh_addr + kTcBTile;
+                const uint32_t tacc = tmem + (uint32_t)(buf * 128);
+                const uint32_t idesc = umma_idesc_bf16(128, n_pad);
+                for (int j = 0; ok && j < nst; ++j) {
+                    const uint32_t gs = g + (uint32_t)j;
+                    const int s = (int)(gs % (uint32_t)S);
+                    const uint32_t ph = (gs / (uint32_t)S) & 1u;
+                    if (!tc_wait_ab(&b->full[s], ph, b)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int ke = min(ksub, nk - j * ksub);
+                    const uint32_t st_addr = smem_u32(ring + (size_t)s * stage_bytes);
+                    for (int u = 0; u < ke; ++u) {
+                        const uint32_t a_addr = st_addr + (uint32_t)u * kTcATile;
+                        const uint32_t bh_addr = st_addr + b_off + (uint32_t)u * bbytes;
+                        const uint32_t bl_addr = bh_addr + (uint32_t)ksub * bbytes;
 #pragma unroll
-                for (int kk = 0; kk < kTcBK / 16; ++kk) {
-                    const uint64_t ad = umma_sdesc(a_addr + kk * 32);
-                    umma_bf16(tmem, ad, umma_sdesc(bh_addr + kk * 32), idesc, (kc > 0 || kk > 0) ? 1u : 0u);
-                    if (p.with_lo) umma_bf16(tmem, ad, umma_sdesc(bl_addr + kk * 32), idesc, 1u);
+                        for (int kk = 0; kk < kTcBK / 16; ++kk) {
+                            const uint64_t ad = umma_sdesc(a_addr + kk * 32);
+                            umma_bf16(tacc, ad, umma_sdesc(bh_addr + kk * 32), idesc, (j > 0 || u > 0 || kk > 0) ? 1u : 0u);
+                            if (p.with_lo) umma_bf16(tacc, ad, umma_sdesc(bl_addr + kk * 32), idesc, 1u);
+                        }
+                    }
+                    umma_commit(&b->empty[s]);  // the stage is free once these MMAs have read it
                 }
-                umma_commit(&empty[s]);  // the stage is free once these MMAs have read it
+                if (ok) umma_commit(&b->acc_full[buf]);  // arrives when every MMA of the item is complete
             }
-            umma_commit(accum);  // every MMA issued so far is complete when this arrives
-        }
-        __syncwarp();
-
-        // ---------------- epilogue (all four warps)
-        if (!tc_wait(accum, (uint32_t)(done & 1))) *(volatile int*)ok_flag = 0;
-        tc_fence_after();
-        __syncthreads();
-        const bool good = *(volatile int*)ok_flag != 0;  // the same in every thread
-        if (good) {
-            const uint32_t row_addr = tmem + ((uint32_t)(warp * 32) << 16);
-            for (int col = 0; col < n_pad; col += 16) {
-                float v[16];
-                tmem_ld16(row_addr + col, v);
+            __syncwarp();
+        } else {
+            // ---------------- epilogue (warps 0-3: accumulator lanes 32w..32w+31)
+            // (one decision for all 128 threads: they meet at named barriers)
+            const bool ok = !named_sync_or(1, 128, !tc_wait_ab(&b->acc_full[buf], (uint32_t)(use & 1), b));
+            tc_fence_after();
+            const uint32_t row_addr = tmem + (uint32_t)(buf * 128) + ((uint32_t)(warp * 32) << 16);
+            for (int col0 = 0; ok && col0 < n_pad; col0 += kTcEpiCols) {
+                float v[kTcEpiCols];
+                tmem_ld16(row_addr + col0, *reinterpret_cast<float(*)[16]>(v));
+                tmem_ld16(row_addr + col0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+                if (col0 + kTcEpiCols >= n_pad) {  // the accumulator is read: the MMA warp may reuse it
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&b->acc_empty[buf]);
+                }
 #pragma unroll
-                for (int j = 0; j < 16; ++j) epi[threadIdx.x * kTcEpiLd + col + j] = v[j];
+                for (int j = 0; j < kTcEpiCols; ++j) epi[threadIdx.x * kTcEpiLd + j] = v[j];
+                named_sync(1, 128);
+                const int ncol = min(kTcEpiCols, n - col0);
+                if (p.gate) {
+                    const int i0 = mt * 64;
+                    for (int t = threadIdx.x; t < 64 * ncol; t += 128) {
+                        const int i = t & 63, jj = t >> 6;
+                        const float hv = silu_mul(epi[i * kTcEpiLd + jj], epi[(64 + i) * kTcEpiLd + jj]);
+                        const uint16_t hi = f2bf_bits(hv);
+                        const size_t at = (size_t)(q0 + col0 + jj) * c.I + i0 + i;
+                        p.h_hi[at] = hi;
+                        p.h_lo[at] = f2bf_bits(hv - bf_bits2f(hi));
+                    }
+                } else {
+                    const int r0 = mt * 128;
+                    for (int t = threadIdx.x; t < 128 * ncol; t += 128) {
+                        const int row = t & 127, jj = t >> 7;
+                        const int r = route_at(c, q0 + col0 + jj);
+                        c.o[(size_t)r * c.H + r0 + row] = epi[row * kTcEpiLd + jj];
+                    }
+                }
+                named_sync(1, 128);
             }
         }
-        tc_fence_before();
-        __syncthreads();
-        if (good) {
-            if (p.gate) {
-                const int i0 = mt * 64;
-                for (int v = threadIdx.x; v < 64 * n; v += kTcThreads) {
-                    const int i = v & 63, j = v >> 6;
-                    const float hv = silu_mul(epi[i * kTcEpiLd + j], epi[(64 + i) * kTcEpiLd + j]);
-                    const uint16_t hi = f2bf_bits(hv);
-                    const size_t at = (size_t)(q0 + j) * c.I + i0 + i;
-                    p.h_hi[at] = hi;
-                    p.h_lo[at] = f2bf_bits(hv - bf_bits2f(hi));
-                }
-            } else {
-                const int r0 = mt * 128;
-                for (int v = threadIdx.x; v < 128 * n; v += kTcThreads) {
-                    const int row = v & 127, j = v >> 7;
-                    const int r = route_at(c, q0 + j);
-                    c.o[(size_t)r * c.H + r0 + row] = epi[row * kTcEpiLd + j];
-                }
-            }
-        }
-        // the next item's loads and MMAs reuse the stages and TMEM only after
-        // every thread is done with this item's epilogue
-        __syncthreads();
-        g += nk;
-        ++done;
-        if (!good) {
-            if (threadIdx.x == 0) set_status(c.status, MOE_DEV_TIMEOUT);
-            break;
-        }
+        g += (uint32_t)nst;
+        ++d;
+        // stop on abort, with one decision per barrier group (the epilogue
+        // warps meet at named barriers, a warp's lanes at __syncwarp)
+        const bool stop = *(volatile int*)&b->abort != 0;
+        if (warp < 4 ? named_sync_or(1, 128, stop) : __any_sync(0xffffffffu, stop)) break;
     }
-    // leave with no copy in flight: the latest phase of every stage has landed
-    if (warp == 0 && lane == 0)
-        for (int s = 0; s < kTcStages; ++s) {
-            const int last = g - 1 - ((g - 1 - s) % kTcStages + kTcStages) % kTcStages;  // last k-step in stage s
-            if (last >= 0) tc_wait(&full[s], (uint32_t)((last / kTcStages) & 1));
+    // teardown: no MMA and no copy may still be in flight when the tensor
+    // memory is freed and the CTA exits
+    if (warp == 5 && lane == 0) {
+        umma_commit(&b->mma_done);
+        tc_wait(&b->mma_done, 0u);
+    }
+    if (warp == 4 && lane == 0)
+        for (int s = 0; s < S && (uint32_t)s < g_armed; ++s) {
+            // the latest armed use of stage s: its copies have landed once its phase completed
+            const uint32_t last = g_armed - 1u - ((g_armed - 1u - (uint32_t)s) % (uint32_t)S);
+            tc_wait(&b->full[s], (last / (uint32_t)S) & 1u);
         }
     __syncthreads();
-    if (warp == 0) {
+    if (*(volatile int*)&b->abort && threadIdx.x == 0) set_status(c.status, MOE_DEV_TIMEOUT);
+    if (warp == 5) {
         tc_fence_after();
         tmem_dealloc(tmem, kTcTmemCols);
     }
