@@ -42,6 +42,8 @@ constexpr int kTcATile = 128 * 128;      // 128 rows x 128 B
 constexpr int kTcEpiCols = 32;           // accumulator columns per epilogue pass
 constexpr int kTcEpiLd = kTcEpiCols + 1; // fp32 row stride of the epilogue tile
 constexpr int kTcEpiBytes = 17 * 1024;   // >= 128 * kTcEpiLd * 4, a multiple of 1024
+constexpr int kTcSegCache = 256;         // tensor-core segments whose (e, p0, p1) are kept in shared memory
+constexpr int kTcSegBytes = kTcSegCache * 16;
 constexpr int kTcSmem = 227 * 1024;
 constexpr uint32_t kTcWaitLimit = 1u << 24;
 constexpr uint32_t kTcTmemCols = 256;    // two accumulators of 128 columns
@@ -210,7 +212,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     TcBars* b = reinterpret_cast<TcBars*>(base);
     float* epi = reinterpret_cast<float*>(base + 1024);  // [128][kTcEpiLd]
-    unsigned char* ring = base + 1024 + kTcEpiBytes;
+    int4* segtab = reinterpret_cast<int4*>(base + 1024 + kTcEpiBytes);  // [kTcSegCache] (e, p0, p1, valid)
+    unsigned char* ring = base + 1024 + kTcEpiBytes + kTcSegBytes;
 
     const Ctx& c = p.c;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -253,6 +256,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         fence_mbar_init();
     }
     if (warp == 5) tmem_alloc(&b->tmem_slot, kTcTmemCols);
+    // the segments' descriptors once, so that decoding an item costs no
+    // dependent global loads in the producer's issue stream
+    const int nts = ld_act_i(c.seg_count + 1);
+    const bool cached = nts <= kTcSegCache;
+    if (cached)
+        for (int i = threadIdx.x; i < nts; i += blockDim.x) {
+            Seg sg;
+            const bool v = get_seg(c, ld_act_i(c.seg_list + maxseg + i), sg);
+            segtab[i] = make_int4(sg.e, sg.p0, sg.p1, v ? 1 : 0);
+        }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -270,7 +283,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         const int rem = item - nc * per_chunk;
         const int sl = rem / mtiles, mt = rem - sl * mtiles;
         Seg sg;
-        if (!get_seg(c, ld_act_i(c.seg_list + maxseg + sl), sg)) continue;  // uniform
+        if (cached) {
+            const int4 t = segtab[sl];
+            if (!t.w) continue;  // uniform
+            sg.e = t.x;
+            sg.p0 = t.y;
+            sg.p1 = t.z;
+        } else if (!get_seg(c, ld_act_i(c.seg_list + maxseg + sl), sg)) {
+            continue;  // uniform
+        }
         const int q0 = sg.p0 + nc * kTcMaxN;
         if (q0 >= sg.p1) continue;
         const int n = min(kTcMaxN, sg.p1 - q0);
