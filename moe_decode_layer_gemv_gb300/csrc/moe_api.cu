@@ -81,10 +81,12 @@ struct StackArgs {
 
 __global__ void __launch_bounds__(kThreads) router_kernel(Ctx c) {
     extern __shared__ __align__(128) unsigned char smem[];
+    grid_dep_wait();
     router_item(c, blockIdx.x, reinterpret_cast<float*>(smem));
 }
 
 __global__ void __launch_bounds__(kThreads) topk_kernel(Ctx c) {
+    grid_dep_wait();
     topk_item(c, blockIdx.x, c.ids, c.rw);
 }
 
@@ -93,6 +95,7 @@ __global__ void __launch_bounds__(kThreads) group_kernel(const int32_t* ids, int
                                                          int32_t* unique, int32_t* num_unique,
                                                          int32_t* status) {
     extern __shared__ __align__(128) unsigned char smem[];
+    grid_dep_wait();
     group_cta(ids, B, k, E, offsets, route_idx, unique, num_unique, status,
               reinterpret_cast<uint32_t*>(smem));
 }
@@ -108,6 +111,7 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(Ctx c) {
     float* xs;
     int* tok;
     split_smem(c, smem, xs, tok);
+    grid_dep_wait();
     const int n = c.seg_list ? ld_act_i(c.seg_count) * ceil_div(c.I, kWarps) : gateup_items(c);
     for (int it = blockIdx.x; it < n; it += gridDim.x) gateup_item(c, it, xs, tok);
 }
@@ -117,13 +121,20 @@ __global__ void __launch_bounds__(kThreads) down_kernel(Ctx c) {
     float* hs;
     int* rts;
     split_smem(c, smem, hs, rts);
+    grid_dep_wait();
     const int n = c.seg_list ? ld_act_i(c.seg_count) * ceil_div(c.H, kDownRows) : down_items(c);
     for (int it = blockIdx.x; it < n; it += gridDim.x) down_item(c, it, hs, rts);
 }
 
-__global__ void classify_kernel(Ctx c) { classify_warp(c); }
+__global__ void classify_kernel(Ctx c) {
+    grid_dep_wait();
+    classify_warp(c);
+}
 
-__global__ void __launch_bounds__(kThreads) combine_kernel(Ctx c) { combine_item(c, blockIdx.x); }
+__global__ void __launch_bounds__(kThreads) combine_kernel(Ctx c) {
+    grid_dep_wait();
+    combine_item(c, blockIdx.x);
+}
 
 // All phases of L layers in one launch.  For L > 1 (a stack) x, residual and
 // y all point at the fp32 residual stream, updated in place by the combine.
@@ -251,18 +262,33 @@ static int to_status(cudaError_t e) {
 }
 
 // Kernels this library has launched in the process (every launch site goes
-// through launch_check or launch_ex), for measurement: moe_launch_count().
+// through launch_ex or launch_pdl), for measurement: moe_launch_count().
 static std::atomic<unsigned long long> g_launches{0};
-
-static int launch_check() {
-    g_launches.fetch_add(1, std::memory_order_relaxed);
-    return to_status(cudaGetLastError());
-}
 
 template <typename K, typename... Args>
 static int launch_ex(const cudaLaunchConfig_t& cfg, K kernel, Args... args) {
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return to_status(cudaLaunchKernelEx(&cfg, kernel, args...));
+}
+
+// A launch that may start while the kernel ahead of it on the stream is
+// finishing (programmatic stream serialization): the kernel's setup overlaps
+// the previous kernel's tail; its first read of earlier results waits in
+// grid_dep_wait().  Used for the chain of phase kernels of one layer.
+template <typename K, typename... Args>
+static int launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return launch_ex(cfg, kernel, args...);
 }
 
 // dynamic shared memory above 48 KB needs an opt-in per kernel and device
@@ -311,10 +337,8 @@ static Ctx make_ctx(const void* x, int x_dtype, const float* residual, float* y,
 static int launch_route(const Ctx& c, cudaStream_t st) {
     int rc = allow_smem(router_kernel, kRouterSmem);
     if (rc) return rc;
-    router_kernel<<<router_items(c), kThreads, kRouterSmem, st>>>(c);
-    if ((rc = launch_check())) return rc;
-    topk_kernel<<<topk_items(c), kThreads, 0, st>>>(c);
-    return launch_check();
+    if ((rc = launch_pdl(router_kernel, router_items(c), kThreads, kRouterSmem, st, c))) return rc;
+    return launch_pdl(topk_kernel, topk_items(c), kThreads, 0, st, c);
 }
 
 static int launch_group(const int32_t* ids, int B, int k, int E, int32_t* offsets, int32_t* route_idx,
@@ -322,8 +346,8 @@ static int launch_group(const int32_t* ids, int B, int k, int E, int32_t* offset
     const size_t smem = group_smem_bytes(B, E);
     int rc = allow_smem(group_kernel, smem);
     if (rc) return rc;
-    group_kernel<<<1, kThreads, smem, st>>>(ids, B, k, E, offsets, route_idx, unique, num_unique, status);
-    return launch_check();
+    return launch_pdl(group_kernel, 1, kThreads, smem, st, ids, B, k, E, offsets, route_idx, unique, num_unique,
+                      status);
 }
 
 
@@ -384,8 +408,7 @@ static int launch_tc(const Ctx& c, char* ws, const WsLayout& L, cudaStream_t st)
     tp.h_hi = reinterpret_cast<uint16_t*>(ws + L.h_hi);
     tp.h_lo = reinterpret_cast<uint16_t*>(ws + L.h_lo);
     tp.with_lo = c.x_bf16 ? 0 : 1;
-    tc_split_x_kernel<<<R, kThreads, 0, st>>>(c, x_hi, x_lo);
-    if ((rc = launch_check())) return rc;
+    if ((rc = launch_pdl(tc_split_x_kernel, R, kThreads, 0, st, c, x_hi, x_lo))) return rc;
     const int nseg = max_segments(c);
     const int nchunk = (c.B + kTcMaxN - 1) / kTcMaxN;
     // gate/up: A = gate_up viewed as [E*2I, H], 64-row boxes
@@ -396,9 +419,7 @@ static int launch_tc(const Ctx& c, char* ws, const WsLayout& L, cudaStream_t st)
     const int grid = sm_count() > 0 ? sm_count() : 1;
     (void)nseg;
     (void)nchunk;
-    tc_gemm_kernel<<<grid, kTcThreads, kTcSmem, st>>>(tp);
-    if ((rc = launch_check())) return rc;
-    return MOE_OK;
+    return launch_pdl(tc_gemm_kernel, grid, kTcThreads, kTcSmem, st, tp);
 }
 
 static int launch_tc_down(const Ctx& c, char* ws, const WsLayout& L, cudaStream_t st) {
@@ -414,8 +435,7 @@ static int launch_tc_down(const Ctx& c, char* ws, const WsLayout& L, cudaStream_
         !encode_bf16_2d(&tp.tb_hi, h_hi, c.I, R, kTcBoxN) || !encode_bf16_2d(&tp.tb_lo, h_lo, c.I, R, kTcBoxN))
         return MOE_ERR_UNSUPPORTED;
     tp.gate = 0;
-    tc_gemm_kernel<<<sm_count() > 0 ? sm_count() : 1, kTcThreads, kTcSmem, st>>>(tp);
-    return launch_check();
+    return launch_pdl(tc_gemm_kernel, sm_count() > 0 ? sm_count() : 1, kTcThreads, kTcSmem, st, tp);
 }
 
 // Geometry of a streaming grouped-GEMV pass; false when it does not apply
@@ -459,8 +479,7 @@ static int launch_stream(const SgParams& P, size_t smem, cudaStream_t st) {
     int rc = allow_smem(stream_gemv_kernel, smem);
     if (rc) return rc;
     const int sms = sm_count();
-    stream_gemv_kernel<<<sms > 0 ? sms : 1, kSgThreads, smem, st>>>(P);
-    return launch_check();
+    return launch_pdl(stream_gemv_kernel, sms > 0 ? sms : 1, kSgThreads, smem, st, P);
 }
 
 // Resident CTAs of a kernel on the whole GPU (at least 1).
@@ -487,8 +506,7 @@ static int launch_experts(const Ctx& c0, cudaStream_t st, char* ws = nullptr, co
     if (ws) {
         c.seg_list = reinterpret_cast<int32_t*>(ws + L->seg_list);
         c.seg_count = reinterpret_cast<int32_t*>(ws + L->seg_count);
-        classify_kernel<<<1, 32, 0, st>>>(c);
-        if ((rc = launch_check())) return rc;
+        if ((rc = launch_pdl(classify_kernel, 1, 32, 0, st, c))) return rc;
         const int rg = resident_grid(gateup_kernel, kThreads, smem);
         const int rd = resident_grid(down_kernel, kThreads, smem);
         g_items = g_items < rg ? g_items : rg;
@@ -503,18 +521,15 @@ static int launch_experts(const Ctx& c0, cudaStream_t st, char* ws = nullptr, co
     if (streamed) {
         if ((rc = launch_stream(sg_gate, sg_gate_smem, st))) return rc;
     } else {
-        gateup_kernel<<<g_items, kThreads, smem, st>>>(c);
-        if ((rc = launch_check())) return rc;
+        if ((rc = launch_pdl(gateup_kernel, g_items, kThreads, smem, st, c))) return rc;
     }
     if (tc && (rc = launch_tc_down(c, ws, *L, st))) return rc;
     if (streamed) {
         if ((rc = launch_stream(sg_down, sg_down_smem, st))) return rc;
     } else {
-        down_kernel<<<d_items, kThreads, smem, st>>>(c);
-        if ((rc = launch_check())) return rc;
+        if ((rc = launch_pdl(down_kernel, d_items, kThreads, smem, st, c))) return rc;
     }
-    combine_kernel<<<combine_items(c), kThreads, 0, st>>>(c);
-    return launch_check();
+    return launch_pdl(combine_kernel, combine_items(c), kThreads, 0, st, c);
 }
 
 static int launch_unfused_layer(const Ctx& c, cudaStream_t st, char* ws, const WsLayout& L) {
@@ -980,8 +995,7 @@ int moe_stack_forward_norm(int Lc, const uint16_t* const* w_router, const float*
     Ctx c = make_ctx(xn, MOE_DT_F32, x_inout, x_inout, B, H, I, E, top_k, flags, ws, L, dev_status);
     int32_t* ids_ws = c.ids;
     for (int l = 0; l < Lc; ++l) {
-        rmsnorm_kernel<<<B, kThreads, 0, st>>>(x_inout, norm_w[l], H, eps, xn);
-        if ((rc = launch_check())) return rc;
+        if ((rc = launch_pdl(rmsnorm_kernel, B, kThreads, 0, st, (const float*)x_inout, norm_w[l], H, eps, xn))) return rc;
         c.w = lws[l];
         c.ids = expert_ids_out ? expert_ids_out + (size_t)l * B * top_k : ids_ws;
         if ((flags & MOE_F_UNFUSED) || c.tc_threshold > 0) {

@@ -6,6 +6,7 @@
 #pragma once
 
 #include "moe_common.cuh"
+#include "moe_ptx.cuh"
 
 namespace moe {
 
@@ -545,6 +546,7 @@ __device__ void combine_item(const Ctx& c, int item) {
 __global__ void __launch_bounds__(kThreads) rmsnorm_kernel(const float* x, const float* g, int H, float eps,
                                                            float* a) {
     __shared__ float part[kWarps];
+    grid_dep_wait();
     const int t = blockIdx.x;
     const float* xr = x + (size_t)t * H;
     float ss = 0.f;

@@ -114,6 +114,13 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// ---------------------------------------------- programmatic dependent launch
+// Kernels launched with programmatic stream serialization may be scheduled
+// before the kernel ahead of them on the stream has finished; this waits
+// until it has, with its memory visible (a no-op otherwise).  Every such
+// kernel calls it before it reads anything an earlier kernel wrote.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------- named barriers
 // The non-aligned form: threads of one warp may reach it at different times
 // (bar.sync is the .aligned form, which requires a converged warp -- a warp

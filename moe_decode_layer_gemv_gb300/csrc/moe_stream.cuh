@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(kSgThreads, 1) stream_gemv_kernel(const SgPara
     const Ctx& c = P.c;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, cta = blockIdx.x;
+    grid_dep_wait();
     const int nseg = ld_act_i(c.seg_count);  // CUDA-core segments
     const long long N = (long long)nseg * P.ips;
     const int ja = (int)(N * cta / G), jb = (int)(N * (cta + 1) / G);

@@ -182,6 +182,7 @@ __device__ __forceinline__ bool tc_wait_ab(uint64_t* bar, uint32_t parity, TcBar
 // Split the activation rows of every route position p into bf16 hi and lo:
 // x_hi[p] = bf16(x[t]), x_lo[p] = bf16(x[t] - x_hi[p]), t = route_at(p) / k.
 __global__ void __launch_bounds__(kThreads) tc_split_x_kernel(Ctx c, uint16_t* x_hi, uint16_t* x_lo) {
+    grid_dep_wait();
     const int p = blockIdx.x;
     if (p >= c.B * c.k) return;
     const int t = route_at(c, p) / c.k;
@@ -217,6 +218,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
 
     const Ctx& c = p.c;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    grid_dep_wait();
     const int K = p.gate ? c.H : c.I;
     const int nk = K / kTcBK;
     const int mtiles = p.gate ? c.I / 64 : c.H / 128;
