@@ -79,10 +79,11 @@ struct StackArgs {
     unsigned bar_extra;  // arrivals a barrier waits for beyond the grid (0; > 0 only to test the timeout)
 };
 
+template <int EPW>
 __global__ void __launch_bounds__(kThreads) router_kernel(Ctx c) {
     extern __shared__ __align__(128) unsigned char smem[];
     grid_dep_wait();
-    router_item(c, blockIdx.x, reinterpret_cast<float*>(smem));
+    router_item<EPW>(c, blockIdx.x, reinterpret_cast<float*>(smem));
 }
 
 __global__ void __launch_bounds__(kThreads) topk_kernel(Ctx c) {
@@ -334,10 +335,18 @@ static Ctx make_ctx(const void* x, int x_dtype, const float* residual, float* y,
     return c;
 }
 
+// The router with one expert per warp for small batches (more CTAs, each
+// weight row read by fewer of them), four per warp from 64 tokens on (the
+// staged x read once for four experts: a quarter of the shared-memory traffic).
 static int launch_route(const Ctx& c, cudaStream_t st) {
-    int rc = allow_smem(router_kernel, kRouterSmem);
-    if (rc) return rc;
-    if ((rc = launch_pdl(router_kernel, router_items(c), kThreads, kRouterSmem, st, c))) return rc;
+    int rc;
+    if (c.B >= 64) {
+        if ((rc = allow_smem(router_kernel<4>, kRouterSmem))) return rc;
+        if ((rc = launch_pdl(router_kernel<4>, router_items(c, 4), kThreads, kRouterSmem, st, c))) return rc;
+    } else {
+        if ((rc = allow_smem(router_kernel<1>, kRouterSmem))) return rc;
+        if ((rc = launch_pdl(router_kernel<1>, router_items(c), kThreads, kRouterSmem, st, c))) return rc;
+    }
     return launch_pdl(topk_kernel, topk_items(c), kThreads, 0, st, c);
 }
 

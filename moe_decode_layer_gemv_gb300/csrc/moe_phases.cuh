@@ -19,8 +19,11 @@ constexpr int kRouterTB = 8;
 constexpr int kRouterHC = 1024;
 constexpr size_t kRouterSmem = sizeof(float) * kRouterTB * kRouterHC;  // 32 KB
 
-__host__ __device__ __forceinline__ int router_items(const Ctx& c) {
-    return ceil_div(c.E, kWarps) * ceil_div(c.B, kRouterTB);
+// Work items of the router: blocks of kRouterTB tokens x (kWarps * EPW)
+// experts; a warp takes EPW experts (EPW > 1 for larger batches: the staged
+// x of a column block is then read once for EPW experts).
+__host__ __device__ __forceinline__ int router_items(const Ctx& c, int epw = 1) {
+    return ceil_div(c.E, kWarps * epw) * ceil_div(c.B, kRouterTB);
 }
 
 // Stage x[tok[q]][hc, hc+hn) (q < nq) into dst[q*ld + ...] as fp32; rows
@@ -52,45 +55,61 @@ __device__ __forceinline__ void stage_x(const Ctx& c, const int* tok, int t0, in
     }
 }
 
+template <int EPW = 1>
 __device__ void router_item(const Ctx& c, int item, float* smem) {
-    const int neb = ceil_div(c.E, kWarps);
+    const int neb = ceil_div(c.E, kWarps * EPW);
     const int eb = item % neb, tb = item / neb;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = eb * kWarps + warp;
+    const int e0 = (eb * kWarps + warp) * EPW;  // this warp's experts e0 .. e0 + EPW - 1
     const int t0 = tb * kRouterTB;
     const int nt = min(kRouterTB, c.B - t0);
-    float2 acc[kRouterTB];
+    float2 acc[EPW][kRouterTB];
 #pragma unroll
-    for (int q = 0; q < kRouterTB; ++q) acc[q] = make_float2(0.f, 0.f);
+    for (int j = 0; j < EPW; ++j)
+#pragma unroll
+        for (int q = 0; q < kRouterTB; ++q) acc[j][q] = make_float2(0.f, 0.f);
     for (int hc = 0; hc < c.H; hc += kRouterHC) {
         const int hn = min(kRouterHC, c.H - hc);
         __syncthreads();
         stage_x(c, nullptr, t0, nt, kRouterTB, hc, hn, smem, kRouterHC);
         __syncthreads();
-        if (e < c.E) {
-            const uint16_t* wrow = c.w.w_router + (size_t)e * c.H + hc;
+        if (e0 < c.E) {
             for (int i = lane * 8; i < hn; i += 256) {
-                const uint4 wv = ld_weight_v4(wrow + i);
-                const float2 w0 = bf16x2_to_f2(wv.x), w1 = bf16x2_to_f2(wv.y);
-                const float2 w2 = bf16x2_to_f2(wv.z), w3 = bf16x2_to_f2(wv.w);
+                float2 w[EPW][4];
+#pragma unroll
+                for (int j = 0; j < EPW; ++j) {
+                    const uint4 wv = e0 + j < c.E ? ld_weight_v4(c.w.w_router + (size_t)(e0 + j) * c.H + hc + i)
+                                                  : make_uint4(0u, 0u, 0u, 0u);
+                    w[j][0] = bf16x2_to_f2(wv.x);
+                    w[j][1] = bf16x2_to_f2(wv.y);
+                    w[j][2] = bf16x2_to_f2(wv.z);
+                    w[j][3] = bf16x2_to_f2(wv.w);
+                }
 #pragma unroll
                 for (int q = 0; q < kRouterTB; ++q) {
                     const float4* xp = reinterpret_cast<const float4*>(smem + q * kRouterHC + i);
                     const float4 xa = xp[0], xb = xp[1];
-                    acc[q] = ffma2(w0, make_float2(xa.x, xa.y), acc[q]);
-                    acc[q] = ffma2(w1, make_float2(xa.z, xa.w), acc[q]);
-                    acc[q] = ffma2(w2, make_float2(xb.x, xb.y), acc[q]);
-                    acc[q] = ffma2(w3, make_float2(xb.z, xb.w), acc[q]);
+#pragma unroll
+                    for (int j = 0; j < EPW; ++j) {
+                        acc[j][q] = ffma2(w[j][0], make_float2(xa.x, xa.y), acc[j][q]);
+                        acc[j][q] = ffma2(w[j][1], make_float2(xa.z, xa.w), acc[j][q]);
+                        acc[j][q] = ffma2(w[j][2], make_float2(xb.x, xb.y), acc[j][q]);
+                        acc[j][q] = ffma2(w[j][3], make_float2(xb.z, xb.w), acc[j][q]);
+                    }
                 }
             }
         }
     }
-    if (e < c.E) {
-        const float b = c.w.bias ? c.w.bias[e] : 0.f;
 #pragma unroll
-        for (int q = 0; q < kRouterTB; ++q) {
-            const float v = warp_sum(acc[q].x + acc[q].y);
-            if (lane == q && q < nt) c.logits[(size_t)(t0 + q) * c.E + e] = v + b;
+    for (int j = 0; j < EPW; ++j) {
+        const int e = e0 + j;
+        if (e < c.E) {
+            const float b = c.w.bias ? c.w.bias[e] : 0.f;
+#pragma unroll
+            for (int q = 0; q < kRouterTB; ++q) {
+                const float v = warp_sum(acc[j][q].x + acc[j][q].y);
+                if (lane == q && q < nt) c.logits[(size_t)(t0 + q) * c.E + e] = v + b;
+            }
         }
     }
 }
