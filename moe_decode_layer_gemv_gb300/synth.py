@@ -134,6 +134,55 @@ def make_layer_fp8(w: Workload, layer: int = 0, seed: int = 0, device="cpu"):
     return lw
 
 
+# E2M1 magnitudes by code (bits: exponent, mantissa) and the midpoints between
+# neighbours, for round-to-nearest (a value on a midpoint takes the smaller code)
+_E2M1 = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+_E2M1_MID = (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0)
+
+
+def quantize_nvfp4(w: torch.Tensor):
+    """[E, R, C] weights -> NVFP4: E2M1 codes packed two a byte [E, R, C/2]
+    uint8 (element 2i of a row in the low nibble), E4M3 scales of 16-element
+    row blocks [E, R, C/16] uint8, one fp32 scale per matrix [E]:
+    gs = amax / (448 * 6), block scale = e4m3(block amax / 6 / gs), code =
+    nearest E2M1 of w / (block scale * gs), clamped to +-6."""
+    E, R, C = w.shape
+    if C % 16:
+        raise ValueError("NVFP4 rows need a multiple of 16 elements")
+    dev = w.device
+    mid = torch.tensor(_E2M1_MID, dtype=torch.float32, device=dev)
+    q = torch.empty((E, R, C // 2), dtype=torch.uint8, device=dev)
+    bs = torch.empty((E, R, C // 16), dtype=torch.uint8, device=dev)
+    gs = torch.empty(E, dtype=torch.float32)
+    for e in range(E):  # one matrix at a time: bounded temporaries
+        wf = w[e].to(torch.float32)
+        g = float(wf.abs().amax()) / (448.0 * 6.0)
+        g = g if g > 0.0 else 1.0
+        blk = wf.view(R, C // 16, 16)
+        s = (blk.abs().amax(-1) / 6.0 / g).clamp(max=448.0)
+        s8 = s.to(torch.float8_e4m3fn)
+        sf = s8.to(torch.float32)
+        v = blk / torch.where(sf > 0, sf, torch.ones_like(sf)).unsqueeze(-1) / g
+        mag = torch.bucketize(v.abs().clamp(max=6.0), mid).to(torch.uint8)  # 0..7
+        code = mag | ((v < 0) & (mag > 0)).to(torch.uint8) << 3
+        code = code.view(R, C)
+        q[e] = code[:, 0::2] | (code[:, 1::2] << 4)
+        bs[e] = s8.view(torch.uint8)
+        gs[e] = g
+    return q, bs, gs.to(dev)
+
+
+def make_layer_nvfp4(w: Workload, layer: int = 0, seed: int = 0, device="cpu"):
+    """A layer of the recipe with its expert weights in NVFP4: the bf16 weights
+    of make_layer, quantised per 16-element row block."""
+    lw = make_layer(w, layer, seed=seed, device=device)
+    gq, gb, gg = quantize_nvfp4(lw["gate_up"])
+    dq, db, dg = quantize_nvfp4(lw["down"])
+    lw.update({"gate_up_q4": gq, "gate_up_bs": gb, "gate_up_gs": gg,
+               "down_q4": dq, "down_bs": db, "down_gs": dg})
+    return lw
+
+
 def norm_weights(H: int, layer: int = 0, seed: int = 0, device="cpu") -> torch.Tensor:
     """RMSNorm weights of layer l: 1 + 0.1 * N(0, 1), fp32 (tensor_id 5000 + l)."""
     g = _gen(seed, 5000 + layer, 0, device)

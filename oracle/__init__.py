@@ -62,10 +62,11 @@ def _load():
             lib.oracle_rmsnorm.argtypes = [P, P, i, i, ctypes.c_float, P]
             lib.oracle_experts_w.argtypes = [P, i, P, P, i, P, P, i, i, i, i, i, i, P, P, P, P]
             lib.oracle_dequant_fp8_block.argtypes = [P, P, i, i, P]
+            lib.oracle_dequant_nvfp4.argtypes = [P, P, ctypes.c_float, i, i, P]
             lib.oracle_stack_norm.argtypes = [i, P, P, P, P, P, ctypes.c_float, i, i, i, i, i, i, P, P]
             for f in ("oracle_router", "oracle_topk", "oracle_group", "oracle_experts",
                       "oracle_layer", "oracle_stack", "oracle_rmsnorm", "oracle_stack_norm",
-                      "oracle_experts_w", "oracle_dequant_fp8_block"):
+                      "oracle_experts_w", "oracle_dequant_fp8_block", "oracle_dequant_nvfp4"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -183,6 +184,22 @@ def dequant_fp8_block(q, scale):
         raise ValueError(f"scale shape {sa.shape} for codes {qa.shape}")
     out = np.empty((R, C), np.float32)
     _check(_load().oracle_dequant_fp8_block(_ptr(qa), _ptr(sa), R, C, _ptr(out)), "dequant_fp8_block")
+    return out
+
+
+def dequant_nvfp4(q, bscale, gscale):
+    """NVFP4 (E2M1 codes packed two a byte [R, C/2] uint8, element 2i in the
+    low nibble; E4M3 scales of 16-element row blocks [R, C/16] uint8; one
+    fp32 scale) -> fp32 [R, C]: e2m1(q) * e4m3(bscale) * gscale."""
+    qa = np.ascontiguousarray(q, dtype=np.uint8)
+    ba = np.ascontiguousarray(bscale, dtype=np.uint8)
+    R, C2 = qa.shape
+    C = 2 * C2
+    if C % 16 or ba.shape != (R, C // 16):
+        raise ValueError(f"block scales {ba.shape} for codes {qa.shape}")
+    out = np.empty((R, C), np.float32)
+    _check(_load().oracle_dequant_nvfp4(_ptr(qa), _ptr(ba), ctypes.c_float(float(gscale)), R, C, _ptr(out)),
+           "dequant_nvfp4")
     return out
 
 

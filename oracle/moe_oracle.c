@@ -80,6 +80,29 @@ int oracle_dequant_fp8_block(const uint8_t* q, const float* scale, int R, int C,
     return OR_OK;
 }
 
+/* NVFP4 element: E2M1 (sign, 2 exponent bits biased by 1, 1 mantissa bit):
+ * 0, 0.5 (the one subnormal), 1, 1.5, 2, 3, 4, 6 and their negatives. */
+static float fp4e2m1_to_f32(uint8_t c) {
+    const int sgn = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+    const float v = (e == 0) ? 0.5f * (float)m : ldexpf(1.0f + 0.5f * (float)m, e - 1);
+    return sgn ? -v : v;
+}
+
+/* NVFP4 weights: a [R, C] matrix of E2M1 codes packed two to a byte (element
+ * 2i of a row in the low nibble of byte i), one E4M3 scale per 16
+ * consecutive elements of a row ([R][C/16] bytes) and one fp32 scale for the
+ * whole matrix:  w[r,c] = (e2m1(q[r,c]) * e4m3(bs[r][c/16])) * gs, fp32. */
+int oracle_dequant_nvfp4(const uint8_t* q, const uint8_t* bs, float gs, int R, int C, float* out) {
+    if (R <= 0 || C <= 0 || (C % 16) != 0 || !q || !bs || !out) return OR_BAD_ARG;
+    for (int r = 0; r < R; ++r)
+        for (int c = 0; c < C; ++c) {
+            const uint8_t byte = q[(size_t)r * (C / 2) + c / 2];
+            const uint8_t code = (c & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+            out[(size_t)r * C + c] = (fp4e2m1_to_f32(code) * fp8e4m3_to_f32(bs[(size_t)r * (C / 16) + c / 16])) * gs;
+        }
+    return OR_OK;
+}
+
 /* x_dtype: 0 = fp32, 1 = bf16 (raw 16-bit patterns). */
 static float load_x(const void* x, int x_dtype, size_t idx) {
     if (x_dtype == 1) return bf16_to_f32(((const uint16_t*)x)[idx]);

@@ -451,3 +451,77 @@ def test_fp8_layer_is_the_bf16_layer_on_the_dequantised_weights():
     assert np.max(np.abs(y8 - y64)) <= 2e-5 * np.max(np.abs(y64))
     ybf = oracle.experts(x, synth.bf16_bits(lw["gate_up"]), synth.bf16_bits(lw["down"]), ids, wts, w.E)
     assert np.max(np.abs(y8 - ybf)) <= 0.1 * np.max(np.abs(ybf))  # quantisation noise, not a different layer
+
+
+# ---------------------------------------------------------------- NVFP4
+# E2M1 by its definition: sign, 2 exponent bits biased by 1, 1 mantissa bit;
+# exponent 0 is the subnormal 0.m (so 0 and 0.5)
+def _e2m1_by_definition(code):
+    s, e, m = (code >> 3) & 1, (code >> 1) & 3, code & 1
+    v = 0.5 * m if e == 0 else (1.0 + 0.5 * m) * 2.0 ** (e - 1)
+    return -v if s else v
+
+
+def test_nvfp4_decodes_every_code_and_its_nibble():
+    codes = np.arange(16, dtype=np.uint8)
+    # two elements a byte: element 2i in the low nibble of byte i
+    packed = (codes[0::2] | (codes[1::2] << 4)).reshape(1, 8)
+    one = np.array([[0x38]], np.uint8)  # E4M3 1.0: exponent 7 (the bias), mantissa 0
+    dq = oracle.dequant_nvfp4(packed, one, 1.0)
+    expect = np.array([_e2m1_by_definition(int(c)) for c in codes], np.float32).reshape(1, 16)
+    assert np.array_equal(dq, expect)
+    assert dq[0, :8].tolist() == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_nvfp4_block_and_matrix_scales_apply_per_16_elements():
+    rng = np.random.default_rng(41)
+    R, C = 5, 96
+    codes = rng.integers(0, 16, size=(R, C)).astype(np.uint8)
+    packed = codes[:, 0::2] | (codes[:, 1::2] << 4)
+    bs = rng.integers(0x08, 0x77, size=(R, C // 16)).astype(np.uint8)  # finite E4M3 codes
+    gs = 0.3125
+    dq = oracle.dequant_nvfp4(packed, bs, gs)
+    bsf = torch.from_numpy(bs.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    el = np.vectorize(_e2m1_by_definition)(codes.astype(np.int64))
+    ref = (el * np.repeat(bsf, 16, axis=1) * gs).astype(np.float32)  # exact up to one rounding
+    assert np.array_equal(dq, ref)
+
+
+def test_nvfp4_round_trip_is_within_half_a_code_step():
+    w = synth.normal_bf16((2, 96, 256), 0.02, 0, 98, 0, "cpu")
+    q, bs, gs = synth.quantize_nvfp4(w)
+    wf = w.to(torch.float32).numpy()
+    for e in range(2):
+        dq = oracle.dequant_nvfp4(q[e].numpy(), bs[e].numpy(), float(gs[e]))
+        unit = np.repeat(torch.from_numpy(bs[e].numpy().copy()).view(torch.float8_e4m3fn)
+                         .to(torch.float32).numpy(), 16, axis=1) * float(gs[e])
+        v = np.abs(wf[e]) / unit
+        # half the gap to the neighbouring E2M1 magnitude, or the excess over 6
+        half_gap = np.where(v < 2.0, 0.25, np.where(v < 4.0, 0.5, 1.0))
+        bound = np.maximum(half_gap, v - 6.0) * unit
+        assert np.all(np.abs(dq - wf[e]) <= bound * (1 + 1e-6) + 1e-12)
+
+
+def test_nvfp4_layer_on_the_dequantised_weights():
+    """The expert pass on the NVFP4 path's dequantised fp32 weights against
+    the fp64 brute force on the same weights."""
+    w = synth.TINY
+    lw = synth.make_layer_nvfp4(w, 0, seed=0)
+    x = synth.make_x(w, 0, seed=0).numpy()
+    wr = synth.bf16_bits(lw["w_router"])
+    gq = {e: oracle.dequant_nvfp4(lw["gate_up_q4"][e].numpy(), lw["gate_up_bs"][e].numpy(),
+                                  float(lw["gate_up_gs"][e])) for e in range(w.E)}
+    dq = {e: oracle.dequant_nvfp4(lw["down_q4"][e].numpy(), lw["down_bs"][e].numpy(),
+                                  float(lw["down_gs"][e])) for e in range(w.E)}
+    lo = oracle.router(x, wr)
+    ids, wts = oracle.topk(lo, w.top_k)
+    y4 = oracle.experts(x, gq, dq, ids, wts, w.E)
+    y64 = np.zeros_like(x, dtype=np.float64)
+    for t in range(w.B):
+        for j in range(w.top_k):
+            e = ids[t, j]
+            G = gq[e].astype(np.float64)
+            g = G[:w.I] @ x[t]
+            u = G[w.I:] @ x[t]
+            y64[t] += wts[t, j] * (dq[e].astype(np.float64) @ (g / (1.0 + np.exp(-g)) * u))
+    assert np.max(np.abs(y4 - y64)) <= 2e-5 * np.max(np.abs(y64))
