@@ -452,14 +452,25 @@ def run_layer_workload(args):
 
 
 def measure_stack(api, accounting, synth, w, dev, steps, warmup, flags=0, seed=0, flush=None, norm=False,
-                  fp8=False):
+                  fp8=False, nvfp4=False):
     """One token through an L-layer stack per step (L2 flushed before each
     timed step, CUDA events on the launching stream); norm=True makes it a
     pre-norm stack (RMSNorm fused into the router and residual add), fp8=True
-    gives it block-scaled FP8 expert weights. Returns the sub-record."""
+    gives it block-scaled FP8 expert weights, nvfp4=True NVFP4 ones.
+    Returns the sub-record."""
     import numpy as np
     import torch
-    if fp8:
+    if nvfp4:
+        layers = []
+        for l in range(w.layers):
+            lw = synth.make_layer_nvfp4(w, l, seed=seed, device=dev)
+            lw.pop("gate_up")  # only the codes and scales stay resident
+            lw.pop("down")
+            layers.append(lw)
+        sw = api.StackWeightsNVFP4(layers)
+        fwd = lambda xb, **kw: api.stack_forward_nvfp4_(xb, sw, w.top_k, **kw)
+        lbytes = accounting.layer_bytes_nvfp4
+    elif fp8:
         layers = [synth.make_layer_fp8(w, l, seed=seed, device=dev) for l in range(w.layers)]
         for lw in layers:  # only the codes and scales stay resident
             lw.pop("gate_up", None)
@@ -511,7 +522,8 @@ def measure_stack(api, accounting, synth, w, dev, steps, warmup, flags=0, seed=0
     peak, _ = hbm_peak()
     del layers, sw
     torch.cuda.empty_cache()
-    return {"workload": w.name + ("_rmsnorm" if norm else "") + ("_fp8_block128" if fp8 else ""), "B": w.B, "H": w.H, "I": w.I, "E": w.E,
+    return {"workload": w.name + ("_rmsnorm" if norm else "") + ("_fp8_block128" if fp8 else "")
+            + ("_nvfp4" if nvfp4 else ""), "B": w.B, "H": w.H, "I": w.I, "E": w.E,
             "top_k": w.top_k, "layers": w.layers,
             "ms": mean_ms, "tokens_per_s": w.B / (mean_ms / 1e3), "us_per_layer": 1000.0 * mean_ms / w.layers,
             "bytes_per_step": bytes_step, "hbm_gbs": achieved, "frac": achieved / peak,
@@ -551,6 +563,9 @@ def config_records(api, accounting, synth, dev, steps, warmup, seed=0):
     # the stack with block-scaled FP8 experts (E4M3 codes, fp32 scale per 128x128 block)
     out["stack_fp8"] = measure_stack(api, accounting, synth, synth.STACK, dev, steps, warmup, 0, seed, flush,
                                      fp8=True)
+    # the stack with NVFP4 experts (E2M1 codes, E4M3 scale per 16 weights, fp32 per matrix)
+    out["stack_nvfp4"] = measure_stack(api, accounting, synth, synth.STACK, dev, steps, warmup, 0, seed, flush,
+                                       nvfp4=True)
     return out
 
 

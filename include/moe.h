@@ -274,6 +274,31 @@ int moe_stack_forward_fp8(int L, const uint16_t* const* w_router, const float* c
                           size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /*
+ * moe_stack_forward_nvfp4 -- moe_stack_forward with NVFP4 expert weights
+ * ("nvfp4", another of the expert formats the dedup page's commit message
+ * names; the encoding is not on the pages: the published NVFP4 layout is
+ * taken).  Expert e's gate_up [2I, H] and down [H, I] hold E2M1 codes (sign,
+ * 2 exponent bits biased by 1, 1 mantissa bit) two to a byte, element 2i of a
+ * row in the low nibble of byte i; each 16 consecutive elements of a row
+ * share one E4M3 scale, and each matrix one fp32 scale:
+ *   w[r, c] = e2m1(q[r, c]) * e4m3(bs[r][c / 16]) * gs
+ * gate_up_q [E][2I][H/2] and down_q [E][H][I/2] bytes, gate_up_bs
+ * [E][2I][H/16] and down_bs [E][H][I/16] bytes, gate_up_gs and down_gs [E]
+ * fp32.  The router stays bf16; the experts stream a quarter of the bytes of
+ * bf16 weights (plus one scale byte per 16 weights); every sum stays fp32.
+ * The six weight arguments are HOST arrays of L device pointers.  Requires H
+ * and I multiples of 32 and a batch the persistent decode kernel takes (up to
+ * 4 tokens and 32 routes), else MOE_ERR_UNSUPPORTED; flags: MOE_F_NO_DEDUP,
+ * MOE_F_NO_PREFETCH.  The other arguments are those of moe_stack_forward.
+ */
+int moe_stack_forward_nvfp4(int L, const uint16_t* const* w_router, const float* const* logit_bias,
+                            const uint8_t* const* gate_up_q, const uint8_t* const* gate_up_bs,
+                            const float* const* gate_up_gs, const uint8_t* const* down_q,
+                            const uint8_t* const* down_bs, const float* const* down_gs, int B, int H, int I, int E,
+                            int top_k, float* x_inout, int32_t* expert_ids_out, uint32_t flags, void* workspace,
+                            size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
  * moe_workspace_grouping -- where a workspace holds the grouped route list
  * of the last layer a forward call computed in it (moe_layer_forward, and
  * the last layer of moe_stack_forward), in the layout of

@@ -37,3 +37,10 @@ def layer_bytes_fp8(H: int, I: int, E: int, unique: int) -> int:
     nb = lambda n: (n + 127) // 128
     scales = 4 * (nb(2 * I) * nb(H) + nb(H) * nb(I))
     return 2 * E * H + unique * (3 * I * H + scales)
+
+
+def layer_bytes_nvfp4(H: int, I: int, E: int, unique: int) -> int:
+    """The same for NVFP4 experts: the bf16 router plus each unique selected
+    expert's E2M1 codes (3I*H / 2 bytes), E4M3 block scales (one byte per 16
+    weights) and two fp32 matrix scales."""
+    return 2 * E * H + unique * (3 * I * H // 2 + 3 * I * H // 16 + 8)

@@ -39,6 +39,8 @@ _lib.moe_layer_forward.argtypes = [_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _
 _lib.moe_stack_forward.argtypes = [_I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _U, _P, _S, _P, _P]
 _lib.moe_stack_forward_fp8.argtypes = [_I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _U, _P, _S, _P,
                                        _P]
+_lib.moe_stack_forward_nvfp4.argtypes = [_I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _U, _P,
+                                         _S, _P, _P]
 _lib.moe_stack_forward_norm.argtypes = [_I, _P, _P, _P, _P, _P, ctypes.c_float, _I, _I, _I, _I, _I, _P, _P, _U,
                                         _P, _S, _P, _P]
 _lib.moe_workspace_grouping.argtypes = [_P, _S, _I, _I, _I, _I, _I, ctypes.POINTER(_P), ctypes.POINTER(_P),
@@ -55,12 +57,12 @@ _lib.moe_status_string.argtypes = [_I]
 _lib.moe_status_string.restype = ctypes.c_char_p
 for _f in ("moe_workspace_bytes", "moe_route", "moe_group_by_expert", "moe_expert_forward",
            "moe_expert_forward_noalloc", "moe_layer_forward", "moe_stack_forward", "moe_stack_forward_norm",
-           "moe_stack_forward_fp8", "moe_workspace_grouping"):
+           "moe_stack_forward_fp8", "moe_stack_forward_nvfp4", "moe_workspace_grouping"):
     getattr(_lib, _f).restype = ctypes.c_int
 
 EXPORTED = ("moe_workspace_bytes", "moe_route", "moe_group_by_expert", "moe_expert_forward",
             "moe_expert_forward_noalloc", "moe_layer_forward", "moe_stack_forward", "moe_stack_forward_norm",
-            "moe_stack_forward_fp8", "moe_workspace_grouping",
+            "moe_stack_forward_fp8", "moe_stack_forward_nvfp4", "moe_workspace_grouping",
             "moe_launch_count", "moe_forward_path", "moe_set_trace_buffer",
             "moe_inject_barrier_stall", "moe_status_string")
 
@@ -436,6 +438,66 @@ def stack_forward_fp8_(x, stack: StackWeightsFP8, top_k, flags=0, ids_out=None, 
                                       ctypes.addressof(stack.dq), ctypes.addressof(stack.ds), B, H, stack.I, stack.E,
                                       top_k, _ptr(x), _ptr(ids_out), flags, _ptr(ws), ws.numel(), _ptr(status),
                                       _stream(stream)), "moe_stack_forward_fp8")
+    return x
+
+
+class StackWeightsNVFP4:
+    """Host pointer tables for moe_stack_forward_nvfp4: each layer dict holds
+    w_router [E,H] bf16, gate_up_q4 [E,2I,H/2] / down_q4 [E,H,I/2] uint8
+    (E2M1 codes two a byte, element 2i in the low nibble), gate_up_bs
+    [E,2I,H/16] / down_bs [E,H,I/16] uint8 E4M3 block scales, gate_up_gs /
+    down_gs [E] fp32 matrix scales, and optionally bias [E]."""
+
+    def __init__(self, layers):
+        self.layers = layers
+        L = self.L = len(layers)
+        g = layers[0]["gate_up_q4"]
+        if g.dim() != 3 or g.shape[1] % 2:
+            raise ValueError(f"gate_up_q4 has shape {tuple(g.shape)}, expected [E, 2I, H/2]")
+        self.E, twoI, h2 = g.shape
+        self.I, self.H = twoI // 2, 2 * h2
+        for l in layers:
+            _shape(l["w_router"], (self.E, self.H), "w_router")
+            _shape(l["gate_up_q4"], (self.E, 2 * self.I, self.H // 2), "gate_up_q4")
+            _shape(l["down_q4"], (self.E, self.H, self.I // 2), "down_q4")
+            _shape(l["gate_up_bs"], (self.E, 2 * self.I, self.H // 16), "gate_up_bs")
+            _shape(l["down_bs"], (self.E, self.H, self.I // 16), "down_bs")
+            _shape(l["gate_up_gs"], (self.E,), "gate_up_gs")
+            _shape(l["down_gs"], (self.E,), "down_gs")
+            _shape(l.get("bias"), (self.E,), "bias")
+            _need(l["w_router"], torch.bfloat16, "w_router")
+            for n in ("gate_up_q4", "down_q4", "gate_up_bs", "down_bs"):
+                _need(l[n], torch.uint8, n)
+            for n in ("gate_up_gs", "down_gs"):
+                _need(l[n], torch.float32, n)
+        P = lambda name: (ctypes.c_void_p * L)(*[l[name].data_ptr() for l in layers])
+        self.wr, self.gq, self.gb, self.gg, self.dq, self.db, self.dg = (
+            P(n) for n in ("w_router", "gate_up_q4", "gate_up_bs", "gate_up_gs", "down_q4", "down_bs", "down_gs"))
+        has_bias = any(l.get("bias") is not None for l in layers)
+        self.bias = ((ctypes.c_void_p * L)(*[(l["bias"].data_ptr() if l.get("bias") is not None else None)
+                                             for l in layers]) if has_bias else None)
+
+
+def stack_forward_nvfp4_(x, stack: StackWeightsNVFP4, top_k, flags=0, ids_out=None, workspace=None, status=None,
+                         stream=None):
+    """In place, NVFP4 experts: x [B,H] fp32 <- x + layer_l(x)."""
+    if x.dim() != 2 or stack is None or x.shape[1] != stack.H:
+        raise ValueError(f"x has shape {tuple(x.shape)}, expected [B, H] with H of the stack's weights")
+    _shape(ids_out, (stack.L, x.shape[0], top_k), "ids_out")
+    _shape(status, (1,), "status")
+    _need(x, torch.float32, "x")
+    for t, dt, n in ((ids_out, torch.int32, "ids_out"), (workspace, torch.uint8, "workspace"),
+                     (status, torch.int32, "status")):
+        _opt(t, dt, n, x.device)
+    B, H = x.shape
+    ws = workspace if workspace is not None else new_workspace(B, H, stack.I, stack.E, top_k, x.device)
+    _check(_lib.moe_stack_forward_nvfp4(stack.L, ctypes.addressof(stack.wr),
+                                        ctypes.addressof(stack.bias) if stack.bias is not None else None,
+                                        ctypes.addressof(stack.gq), ctypes.addressof(stack.gb),
+                                        ctypes.addressof(stack.gg), ctypes.addressof(stack.dq),
+                                        ctypes.addressof(stack.db), ctypes.addressof(stack.dg), B, H, stack.I,
+                                        stack.E, top_k, _ptr(x), _ptr(ids_out), flags, _ptr(ws), ws.numel(),
+                                        _ptr(status), _stream(stream)), "moe_stack_forward_nvfp4")
     return x
 
 

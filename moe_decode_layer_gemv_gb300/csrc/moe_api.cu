@@ -587,7 +587,7 @@ static int launch_fused(const Ctx& c, const StackArgs& sa, unsigned* bar, cudaSt
 // router's column slice in shared memory and gives the rest to the weight
 // ring; it applies when B <= 4, B*k <= 32 and the ring gets >= 4 stages.
 static bool decode_plan(int B, int H, int I, int E, int k, int sms, DkParams& p, size_t& smem, bool norm = false,
-                        int wb = 2) {
+                        int w2 = 4) {
     const int R = B * k;
     if (B < 1 || B > kDkMaxB || R > kDkMaxR || sms < 1 || sms > 1024) return false;
     const int ng = H >> 3;
@@ -608,8 +608,9 @@ static bool decode_plan(int B, int H, int I, int E, int k, int sms, DkParams& p,
     p.off_gq = (int)off;  // pre-norm stacks: two layers' norm weights
     if (norm) off = align_up(off + 2 * sizeof(float) * (size_t)H, 128);
     p.off_ring = (int)off;
-    // a stage holds one gate/up row pair or a block of down rows (wb bytes an element)
-    const size_t stage = align_up((size_t)(2 * H > I ? 2 * wb * H : wb * I), 128);
+    // a stage holds one gate/up row pair or a block of down rows (w2 bytes per
+    // two weights: 4 bf16, 2 E4M3, 1 E2M1)
+    const size_t stage = align_up((size_t)(2 * H > I ? (size_t)w2 * H : ((size_t)w2 * I) >> 1), 128);
     if (off >= (size_t)kDkSmemMax) return false;
     size_t S = ((size_t)kDkSmemMax - off) / stage;
     if (S > (size_t)kDkMaxStages) S = kDkMaxStages;
@@ -625,17 +626,27 @@ static bool decode_plan(int B, int H, int I, int E, int k, int sms, DkParams& p,
     return true;
 }
 
+// Expert weight formats of the decode kernel.
+enum DkFormat { kDkBf16 = 0, kDkFp8Block = 1, kDkNvfp4 = 2 };
+
 static int launch_decode(DkParams& p, size_t smem, int sms, char* ws, const WsLayout& L, cudaStream_t st,
-                         bool fp8 = false) {
+                         int fmt = kDkBf16) {
     // direct mode for every layer: a CTA's largest share -- ceil(U*I/G) gate/up
     // pairs and maxrows down rows of U experts, U <= R -- fits in the ring area
-    const size_t wb = fp8 ? 1 : 2;
+    const size_t w2 = fmt == kDkNvfp4 ? 1 : (fmt == kDkFp8Block ? 2 : 4);  // bytes of two weights
     const size_t Ru = (size_t)p.B * p.k;
-    const size_t g_max = ((Ru * p.I + sms - 1) / sms) * 2 * wb * (size_t)p.H;
-    const size_t d_max = Ru * p.maxrows * wb * (size_t)p.I;
+    const size_t g_max = ((Ru * p.I + sms - 1) / sms) * w2 * (size_t)p.H;
+    const size_t d_max = (Ru * p.maxrows * w2 * (size_t)p.I) >> 1;
     const bool all_direct = g_max + d_max <= (size_t)p.S * p.stage_bytes && g_max < (1u << 20) && d_max < (1u << 20);
     void (*kernel)(DkParams);
-    if (fp8) {  // block-scaled FP8 experts (no traced variant)
+    if (fmt == kDkNvfp4) {  // NVFP4 experts (no traced variant)
+        if (p.B == 1 && all_direct)
+            kernel = decode_kernel<false, 1, true, false, true>;
+        else if (p.B == 1)
+            kernel = decode_kernel<false, 1, false, false, true>;
+        else
+            kernel = decode_kernel<false, 4, false, false, true>;
+    } else if (fmt == kDkFp8Block) {  // block-scaled FP8 experts (no traced variant)
         if (p.B == 1 && all_direct)
             kernel = decode_kernel<false, 1, true, true>;
         else if (p.B == 1)
@@ -663,7 +674,7 @@ static int launch_decode(DkParams& p, size_t smem, int sms, char* ws, const WsLa
     // whose extra expert costs more HBM time than its hits save.)
     p.prefetch_k = 0;
     if (p.B == 1 && p.L > 1 && !(p.flags & MOE_F_NO_PREFETCH)) {
-        const unsigned long long per_e = 3ull * wb * p.I * p.H;
+        const unsigned long long per_e = (3ull * w2 * p.I * p.H) >> 1;
         const int kp = p.k;
         if (per_e * kp <= (64ull << 20) && kp <= 32) p.prefetch_k = kp;
     }
@@ -1052,7 +1063,7 @@ int moe_stack_forward_fp8(int Lc, const uint16_t* const* w_router, const float* 
     memset(&dp, 0, sizeof dp);
     size_t dsm = 0;
     const int sms = sm_count();
-    if (!decode_plan(B, H, I, E, top_k, sms, dp, dsm, false, 1)) return MOE_ERR_UNSUPPORTED;
+    if (!decode_plan(B, H, I, E, top_k, sms, dp, dsm, false, 2)) return MOE_ERR_UNSUPPORTED;
     decode_common(dp, B, H, I, E, top_k, Lc, flags,
                   dev_status ? dev_status : reinterpret_cast<int32_t*>(ws + L.status));
     dp.trace = nullptr;
@@ -1071,7 +1082,63 @@ int moe_stack_forward_fp8(int Lc, const uint16_t* const* w_router, const float* 
     }
     dp.ids_out = expert_ids_out;
     dp.w_out = nullptr;
-    return launch_decode(dp, dsm, sms, ws, L, static_cast<cudaStream_t>(stream), true);
+    return launch_decode(dp, dsm, sms, ws, L, static_cast<cudaStream_t>(stream), kDkFp8Block);
+}
+
+int moe_stack_forward_nvfp4(int Lc, const uint16_t* const* w_router, const float* const* logit_bias,
+                            const uint8_t* const* gate_up_q, const uint8_t* const* gate_up_bs,
+                            const float* const* gate_up_gs, const uint8_t* const* down_q,
+                            const uint8_t* const* down_bs, const float* const* down_gs, int B, int H, int I, int E,
+                            int top_k, float* x_inout, int32_t* expert_ids_out, uint32_t flags, void* workspace,
+                            size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    int rc = check_dims(B, H, I, E, top_k, true);
+    if (rc) return rc;
+    if (Lc < 1 || Lc > MOE_MAX_LAYERS) return MOE_ERR_INVALID_ARG;
+    if ((H & 31) || (I & 31)) return MOE_ERR_INVALID_ARG;  // rows of codes in whole 16-byte pieces
+    if (flags & ~(MOE_F_NO_DEDUP | MOE_F_NO_PREFETCH)) return MOE_ERR_INVALID_ARG;
+    if (B == 0) return MOE_OK;
+    if (!w_router || !gate_up_q || !gate_up_bs || !gate_up_gs || !down_q || !down_bs || !down_gs)
+        return MOE_ERR_INVALID_ARG;
+    for (int l = 0; l < Lc; ++l) {
+        MOE_REQ(w_router[l]);
+        MOE_REQ(gate_up_q[l]);
+        MOE_REQ(down_q[l]);
+        if (!gate_up_bs[l] || !down_bs[l] || !gate_up_gs[l] || !down_gs[l]) return MOE_ERR_INVALID_ARG;
+        if (logit_bias) MOE_OPT(logit_bias[l]);
+    }
+    MOE_REQ(x_inout);
+    MOE_OPT(expert_ids_out);
+    MOE_REQ(workspace);
+    MOE_OPT(dev_status);
+    const WsLayout L = ws_layout(B, H, I, E, top_k);
+    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+    char* ws = static_cast<char*>(workspace);
+    DkParams dp;
+    memset(&dp, 0, sizeof dp);
+    size_t dsm = 0;
+    const int sms = sm_count();
+    if (!decode_plan(B, H, I, E, top_k, sms, dp, dsm, false, 1)) return MOE_ERR_UNSUPPORTED;
+    decode_common(dp, B, H, I, E, top_k, Lc, flags,
+                  dev_status ? dev_status : reinterpret_cast<int32_t*>(ws + L.status));
+    dp.trace = nullptr;
+    dp.trace_words = 0;
+    dp.x_bf16 = 0;
+    dp.x_in = x_inout;
+    dp.residual = x_inout;
+    dp.y = x_inout;
+    for (int l = 0; l < Lc; ++l) {
+        dp.layer[l].w_router = w_router[l];
+        dp.layer[l].bias = logit_bias ? logit_bias[l] : nullptr;
+        dp.layer[l].gate_up = reinterpret_cast<const uint16_t*>(gate_up_q[l]);
+        dp.layer[l].down = reinterpret_cast<const uint16_t*>(down_q[l]);
+        dp.layer[l].gate_up_bs = gate_up_bs[l];
+        dp.layer[l].down_bs = down_bs[l];
+        dp.layer[l].gate_up_gs = gate_up_gs[l];
+        dp.layer[l].down_gs = down_gs[l];
+    }
+    dp.ids_out = expert_ids_out;
+    dp.w_out = nullptr;
+    return launch_decode(dp, dsm, sms, ws, L, static_cast<cudaStream_t>(stream), kDkNvfp4);
 }
 
 int moe_workspace_grouping(void* workspace, size_t workspace_bytes, int B, int H, int I, int E, int top_k,

@@ -83,6 +83,12 @@ struct LayerWeights {
     // and [E][ceil(H/128)][ceil(I/128)]; nullptr for bf16 experts
     const float* gate_up_scale;
     const float* down_scale;
+    // NVFP4 experts: E4M3 scales of 16-element row blocks ([E][rows][cols/16]
+    // bytes) and one fp32 scale per expert matrix ([E])
+    const unsigned char* gate_up_bs;
+    const unsigned char* down_bs;
+    const float* gate_up_gs;
+    const float* down_gs;
 };
 
 // Everything one layer step needs.  Built on the host, passed by value.

@@ -25,6 +25,7 @@
 
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
+#include <cuda_fp4.h>
 
 #include "moe_common.cuh"
 #include "moe_ptx.cuh"
@@ -778,14 +779,134 @@ __device__ __forceinline__ void dk_down_rows_f8(const unsigned char* st, int nrc
     }
 }
 
+// ---------------------------------------------------------------- NVFP4
+// Two E2M1 codes (low nibble first) as fp32, and one E4M3 code as fp32: the
+// hardware conversions to f16 are exact for every code, and so is the
+// widening to f32.
+__device__ __forceinline__ float2 f4x2_to_f2(unsigned v) {
+    const __half2_raw hr = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)(v & 0xffu), __NV_E2M1);
+    __half2 h;
+    memcpy(&h, &hr, sizeof h);
+    return __half22float2(h);
+}
+
+__device__ __forceinline__ float f8_to_f(unsigned v) {
+    const __half_raw hr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)(v & 0xffu), __NV_E4M3);
+    __half h;
+    memcpy(&h, &hr, sizeof h);
+    return __half2float(h);
+}
+
+// The NVFP4 form of dk_gate_pair: rows of H E2M1 codes two to a byte (gate
+// row at grow, up row at urow), the rows' E4M3 block scales (gbs, ubs: one
+// byte per 16 elements) and the matrix scale gsc.  Lane L takes the 8-code
+// groups v = L + 32j (one 4-byte load each, a warp reads 128 contiguous
+// bytes); a group lies in one 16-element block, so its 8 products are summed
+// first and scaled once.
+template <int NQ>
+__device__ __forceinline__ void dk_gate_pair_f4(const unsigned char* grow, const unsigned char* urow,
+                                                const unsigned char* gbs, const unsigned char* ubs, float gsc,
+                                                const float* xq, const int (&tok)[4], int H, float (&gu)[2 * NQ]) {
+    const int lane = threadIdx.x & 31;
+    float ag[NQ], au[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) ag[q] = au[q] = 0.f;
+    const int nv = H >> 3, hq = dk_hq(H);
+    for (int v = lane; v < nv; v += 32) {
+        const unsigned gw = *reinterpret_cast<const unsigned*>(grow + 4 * v);
+        const unsigned uw = *reinterpret_cast<const unsigned*>(urow + 4 * v);
+        const float sg = f8_to_f(__ldg(gbs + (v >> 1))) * gsc, su = f8_to_f(__ldg(ubs + (v >> 1))) * gsc;
+        const float2 g0 = f4x2_to_f2(gw), g1 = f4x2_to_f2(gw >> 8), g2 = f4x2_to_f2(gw >> 16), g3 = f4x2_to_f2(gw >> 24);
+        const float2 u0 = f4x2_to_f2(uw), u1 = f4x2_to_f2(uw >> 8), u2 = f4x2_to_f2(uw >> 16), u3 = f4x2_to_f2(uw >> 24);
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            const float* xp = xq + (size_t)tok[q] * hq + ((v >> 5) << 8) + ((v & 31) << 2);
+            const float4 xa = *reinterpret_cast<const float4*>(xp);
+            const float4 xb = *reinterpret_cast<const float4*>(xp + 128);
+            float2 pg = ffma2(g0, make_float2(xa.x, xa.y), make_float2(0.f, 0.f));
+            float2 pu = ffma2(u0, make_float2(xa.x, xa.y), make_float2(0.f, 0.f));
+            pg = ffma2(g1, make_float2(xa.z, xa.w), pg);
+            pu = ffma2(u1, make_float2(xa.z, xa.w), pu);
+            pg = ffma2(g2, make_float2(xb.x, xb.y), pg);
+            pu = ffma2(u2, make_float2(xb.x, xb.y), pu);
+            pg = ffma2(g3, make_float2(xb.z, xb.w), pg);
+            pu = ffma2(u3, make_float2(xb.z, xb.w), pu);
+            ag[q] = fmaf(sg, pg.x + pg.y, ag[q]);
+            au[q] = fmaf(su, pu.x + pu.y, au[q]);
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+        gu[2 * q] = ag[q];
+        gu[2 * q + 1] = au[q];
+    }
+    warp_sum_n<2 * NQ>(gu);
+}
+
+// The NVFP4 form of dk_down_rows: rows of I codes two to a byte, four rows at
+// a time; row r's block scales at dbs + r * I/16 (dbs: the scales of the
+// first row), matrix scale dgs.
+template <int NQ>
+__device__ __forceinline__ void dk_down_rows_f4(const unsigned char* st, int nrc, int I, const unsigned char* dbs,
+                                                float dgs, const float* hrow, float* os, int ld, int orow0) {
+    const int lane = threadIdx.x & 31;
+    const int nv = I >> 3, rb_bytes = I >> 1, sb = I >> 4;
+    for (int rb = 0; rb < nrc; rb += 4) {
+        const int n4 = min(4, nrc - rb);
+        float acc[4][NQ];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) acc[j][q] = 0.f;
+        for (int v = lane; v < nv; v += 32) {
+            float s[4];
+            unsigned wv[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int r = rb + min(j, n4 - 1);
+                s[j] = f8_to_f(__ldg(dbs + (size_t)r * sb + (v >> 1))) * dgs;
+                wv[j] = j < n4 ? *reinterpret_cast<const unsigned*>(st + (size_t)(rb + j) * rb_bytes + 4 * v) : 0u;
+            }
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                const float4* hp = reinterpret_cast<const float4*>(hrow + (size_t)q * I + 8 * v);
+                const float4 ha = hp[0], hb = hp[1];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float2 a = ffma2(f4x2_to_f2(wv[j]), make_float2(ha.x, ha.y), make_float2(0.f, 0.f));
+                    a = ffma2(f4x2_to_f2(wv[j] >> 8), make_float2(ha.z, ha.w), a);
+                    a = ffma2(f4x2_to_f2(wv[j] >> 16), make_float2(hb.x, hb.y), a);
+                    a = ffma2(f4x2_to_f2(wv[j] >> 24), make_float2(hb.z, hb.w), a);
+                    acc[j][q] = fmaf(s[j], a.x + a.y, acc[j][q]);
+                }
+            }
+        }
+        float red[4 * NQ];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) red[j * NQ + q] = acc[j][q];
+        warp_sum_n<4 * NQ>(red);
+        if (lane == 0) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (j < n4)
+#pragma unroll
+                    for (int q = 0; q < NQ; ++q) os[(size_t)q * ld + orow0 + rb + j] = red[j * NQ + q];
+        }
+    }
+}
+
 // Gate/up pair q of the layer (segment u, row i) from shared-memory rows:
 // h[p, i] = SiLU(g) * u for every route p of the segment.  kF8: the rows
 // hold E4M3 codes and gsr/usr are the scale rows of gate row i and up row
 // I + i.
-template <int kNQ, bool kF8 = false>
+template <int kNQ, bool kF8 = false, bool kF4 = false>
 __device__ __forceinline__ void dk_pair_compute(const DkMisc* m, const unsigned char* grow, const unsigned char* urow,
                                                 const float* xq, int H, int I, int k, int u, int i, float* h,
-                                                const float* gsr = nullptr, const float* usr = nullptr) {
+                                                const float* gsr = nullptr, const float* usr = nullptr,
+                                                const unsigned char* gbs = nullptr, const unsigned char* ubs = nullptr,
+                                                float gsc = 1.f) {
     const int lane = threadIdx.x & 31;
     const int p0 = m->seg_p[u], p1 = m->seg_p[u + 1];
     int tok[kDkMaxB];
@@ -793,7 +914,18 @@ __device__ __forceinline__ void dk_pair_compute(const DkMisc* m, const unsigned 
     for (int qq = 0; qq < kDkMaxB; ++qq) tok[qq] = p0 + qq < p1 ? m->rat[p0 + qq] / k : 0;
     const int nq = kNQ == 1 ? 1 : p1 - p0;
     float gu[2 * kDkMaxB];
-    if constexpr (kF8) {
+    if constexpr (kF4) {
+        switch (kNQ == 1 ? 1 : nq) {
+            case 1: { float r[2]; dk_gate_pair_f4<1>(grow, urow, gbs, ubs, gsc, xq, tok, H, r); gu[0] = r[0]; gu[1] = r[1]; } break;
+            case 2: { float r[4]; dk_gate_pair_f4<2>(grow, urow, gbs, ubs, gsc, xq, tok, H, r);
+#pragma unroll
+                      for (int j = 0; j < 4; ++j) gu[j] = r[j]; } break;
+            case 3: { float r[6]; dk_gate_pair_f4<3>(grow, urow, gbs, ubs, gsc, xq, tok, H, r);
+#pragma unroll
+                      for (int j = 0; j < 6; ++j) gu[j] = r[j]; } break;
+            default: dk_gate_pair_f4<4>(grow, urow, gbs, ubs, gsc, xq, tok, H, gu); break;
+        }
+    } else if constexpr (kF8) {
         switch (kNQ == 1 ? 1 : nq) {
             case 1: { float r[2]; dk_gate_pair_f8<1>(grow, urow, gsr, usr, xq, tok, H, r); gu[0] = r[0]; gu[1] = r[1]; } break;
             case 2: { float r[4]; dk_gate_pair_f8<2>(grow, urow, gsr, usr, xq, tok, H, r);
@@ -831,13 +963,24 @@ __device__ __forceinline__ void dk_pair_compute(const DkMisc* m, const unsigned 
 // Down rows [r0, r1) of segment u from shared memory (row r at base + (r -
 // r0) * row bytes) into os (j-th route of the segment at row p0 + j).  kF8:
 // E4M3 codes with the expert's block scales dsc ([ceil(H/128)][dsc_ld]).
-template <int kNQ, bool kF8 = false>
+template <int kNQ, bool kF8 = false, bool kF4 = false>
 __device__ __forceinline__ void dk_down_compute(const DkMisc* m, const unsigned char* base, int r0, int r1, int I,
                                                 const float* hs, float* os, int maxrows, int h0, int u,
-                                                const float* dsc = nullptr, int dsc_ld = 0) {
+                                                const float* dsc = nullptr, int dsc_ld = 0,
+                                                const unsigned char* dbs = nullptr, float dgs = 1.f) {
     const int p0 = m->seg_p[u], p1 = m->seg_p[u + 1];
     const float* hrow = hs + (size_t)p0 * I;
     float* orow = os + (size_t)p0 * maxrows;
+    if constexpr (kF4) {  // dbs: the expert's block scales; row r0's row of them first
+        const unsigned char* sr = dbs + (size_t)r0 * (I >> 4);
+        switch (kNQ == 1 ? 1 : p1 - p0) {
+            case 1: dk_down_rows_f4<1>(base, r1 - r0, I, sr, dgs, hrow, orow, maxrows, r0 - h0); break;
+            case 2: dk_down_rows_f4<2>(base, r1 - r0, I, sr, dgs, hrow, orow, maxrows, r0 - h0); break;
+            case 3: dk_down_rows_f4<3>(base, r1 - r0, I, sr, dgs, hrow, orow, maxrows, r0 - h0); break;
+            default: dk_down_rows_f4<4>(base, r1 - r0, I, sr, dgs, hrow, orow, maxrows, r0 - h0); break;
+        }
+        return;
+    }
     if constexpr (kF8) {
         switch (kNQ == 1 ? 1 : p1 - p0) {
             case 1: dk_down_rows_f8<1>(base, r1 - r0, I, dsc, dsc_ld, r0, hrow, orow, maxrows, r0 - h0); break;
@@ -921,11 +1064,12 @@ __device__ __forceinline__ int dk_predict_top(const float* alog, int E, int kp) 
 // L2: lane j < kp takes expert j (my_e) and issues two bulk prefetches, its
 // piece of the gate_up block and its piece of the down block (pieces of
 // equal 16-byte-aligned size, the last CTA taking the remainder).
-__device__ __forceinline__ void dk_prefetch_l2(const LayerWeights& wn, int my_e, int H, int I, int kp, int wb = 2) {
+__device__ __forceinline__ void dk_prefetch_l2(const LayerWeights& wn, int my_e, int H, int I, int kp, int w2 = 4) {
     const int lane = threadIdx.x & 31;
     if (lane < kp && my_e >= 0) {
+        // (w2: bytes of two weights -- 4 bf16, 2 E4M3, 1 E2M1)
         const unsigned G = gridDim.x, c = blockIdx.x;
-        const unsigned gsz = 2u * (unsigned)wb * (unsigned)I * (unsigned)H, dsz = (unsigned)wb * (unsigned)I * (unsigned)H;
+        const unsigned gsz = (unsigned)w2 * (unsigned)I * (unsigned)H, dsz = gsz >> 1;
         const unsigned gp = (gsz / G) & ~15u, dp = (dsz / G) & ~15u;
         const unsigned g0 = c * gp, d0 = c * dp;
         const unsigned gn = c + 1 == G ? gsz - g0 : gp, dn = c + 1 == G ? dsz - d0 : dp;
@@ -941,8 +1085,8 @@ __device__ __forceinline__ void dk_prefetch_l2(const LayerWeights& wn, int my_e,
 // (gb - ga) * 4H bytes): per run of one segment, the gate rows to
 // dg + (q - ga)*2H and the up rows to du + (q - ga)*2H.
 __device__ __forceinline__ void dk_gate_runs(const uint16_t* gate_up, const int* seg_e, int ga, int gb, int H, int I,
-                                             unsigned char* dg, unsigned char* du, uint64_t* bar, int wb = 2) {
-    const size_t row = (size_t)wb * H;  // bytes of one row
+                                             unsigned char* dg, unsigned char* du, uint64_t* bar, int w2 = 4) {
+    const size_t row = ((size_t)w2 * H) >> 1;  // bytes of one row (w2: bytes of two weights)
     for (int q = ga; q < gb;) {
         const int u = q / I, i = q - u * I;
         const int qe = min(gb, (u + 1) * I);
@@ -963,7 +1107,7 @@ __device__ __forceinline__ void dk_gate_runs(const uint16_t* gate_up, const int*
 // instruction stream: the kernel runs every phase of a layer once per
 // layer, so its speed depends on how much code it streams through the
 // instruction caches.
-template <bool kTrace, int kNQ, bool kDirect, bool kF8 = false>
+template <bool kTrace, int kNQ, bool kDirect, bool kF8 = false, bool kF4 = false>
 __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -985,8 +1129,9 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
     const int B = kNQ == 1 ? 1 : p.B;  // a compile-time constant for one token
     const int H = p.H, I = p.I, E = p.E, k = p.k, R = B * k;
     // bytes of a gate/up row and of a down row (bf16, or one-byte E4M3 codes)
-    constexpr int kWb = kF8 ? 1 : 2;
-    const int rowg = kWb * H, rowd = kWb * I;
+    // bytes of two weights: bf16, E4M3 or E2M1 (two codes a byte)
+    constexpr int kW2 = kF4 ? 1 : (kF8 ? 2 : 4);
+    const int rowg = (kW2 * H) >> 1, rowd = (kW2 * I) >> 1;
     // block-scale row lengths of gate_up [2I, H] and down [H, I] (FP8 only)
     const int sg_ld = (H + 127) >> 7, sd_ld = (I + 127) >> 7;
     const int sg_e = ((2 * I + 127) >> 7) * sg_ld, sd_e = ((H + 127) >> 7) * sd_ld;
@@ -1223,7 +1368,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                     mbar_arrive_expect_tx(&gch[ch], (uint32_t)(cb - ca) * 2u * (uint32_t)rowg);
                     if (cb > ca)
                         dk_gate_runs(lw.gate_up, m->seg_e, wk.ga + ca, wk.ga + cb, H, I, d_g + (size_t)ca * rowg,
-                                     d_u + (size_t)ca * rowg, &gch[ch], kWb);
+                                     d_u + (size_t)ca * rowg, &gch[ch], kW2);
                 }
             }
             __syncwarp();
@@ -1306,7 +1451,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
             }
             if (__all_sync(0xffffffffu, seen)) {
                 const int my_e = dk_predict_top(p.alog + (size_t)(l & 1) * E, E, p.prefetch_k);
-                dk_prefetch_l2(p.layer[l + 1], my_e, H, I, p.prefetch_k, kWb);
+                dk_prefetch_l2(p.layer[l + 1], my_e, H, I, p.prefetch_k, kW2);
             }
         }
         if (warp != 0) {
@@ -1339,8 +1484,10 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                     const int u = q / I, i = q - u * I;
                     const float* gsr = kF8 ? lw.gate_up_scale + (size_t)m->seg_e[u] * sg_e + (size_t)(i >> 7) * sg_ld : nullptr;
                     const float* usr = kF8 ? lw.gate_up_scale + (size_t)m->seg_e[u] * sg_e + (size_t)((I + i) >> 7) * sg_ld : nullptr;
-                    dk_pair_compute<kNQ, kF8>(m, d_g + (size_t)c * rowg, d_u + (size_t)c * rowg, xq, H, I, k, u, i, hb,
-                                              gsr, usr);
+                    const unsigned char* gbs = kF4 ? lw.gate_up_bs + ((size_t)m->seg_e[u] * 2 * I + i) * (H >> 4) : nullptr;
+                    dk_pair_compute<kNQ, kF8, kF4>(m, d_g + (size_t)c * rowg, d_u + (size_t)c * rowg, xq, H, I, k, u, i,
+                                                   hb, gsr, usr, gbs, kF4 ? gbs + (size_t)I * (H >> 4) : nullptr,
+                                                   kF4 ? __ldg(lw.gate_up_gs + m->seg_e[u]) : 1.f);
                 }
             }
             for (int c = c0; !direct && consumes && c < wk.ng; c += p.W) {
@@ -1352,7 +1499,10 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                 const unsigned char* st = ring + (size_t)s * p.stage_bytes;
                 const float* gsr = kF8 ? lw.gate_up_scale + (size_t)m->seg_e[u] * sg_e + (size_t)(i >> 7) * sg_ld : nullptr;
                 const float* usr = kF8 ? lw.gate_up_scale + (size_t)m->seg_e[u] * sg_e + (size_t)((I + i) >> 7) * sg_ld : nullptr;
-                dk_pair_compute<kNQ, kF8>(m, st, st + rowg, xq, H, I, k, u, i, hb, gsr, usr);
+                const unsigned char* gbs = kF4 ? lw.gate_up_bs + ((size_t)m->seg_e[u] * 2 * I + i) * (H >> 4) : nullptr;
+                dk_pair_compute<kNQ, kF8, kF4>(m, st, st + rowg, xq, H, I, k, u, i, hb, gsr, usr, gbs,
+                                               kF4 ? gbs + (size_t)I * (H >> 4) : nullptr,
+                                               kF4 ? __ldg(lw.gate_up_gs + m->seg_e[u]) : 1.f);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
                 s += p.W;
@@ -1390,8 +1540,11 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                     }
                     const int u = j / ng4, rg = j - u * ng4;
                     const int r0 = h0 + 4 * rg, r1 = min(h1, r0 + 4);
-                    dk_down_compute<kNQ, kF8>(m, d_d + ((size_t)u * nrows + 4 * rg) * rowd, r0, r1, I, hs, os, p.maxrows,
-                                              h0, u, kF8 ? lw.down_scale + (size_t)m->seg_e[u] * sd_e : nullptr, sd_ld);
+                    dk_down_compute<kNQ, kF8, kF4>(m, d_d + ((size_t)u * nrows + 4 * rg) * rowd, r0, r1, I, hs, os,
+                                                   p.maxrows, h0, u,
+                                                   kF8 ? lw.down_scale + (size_t)m->seg_e[u] * sd_e : nullptr, sd_ld,
+                                                   kF4 ? lw.down_bs + (size_t)m->seg_e[u] * H * (I >> 4) : nullptr,
+                                                   kF4 ? __ldg(lw.down_gs + m->seg_e[u]) : 1.f);
                 }
             }
             c0 = wk.ng + ((cw - (rs + wk.ng) % p.W) % p.W + p.W) % p.W;
@@ -1407,8 +1560,10 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                 const int r0 = wk.h0 + sub * wk.nr;
                 const int r1 = min(wk.h1, r0 + wk.nr);
                 const unsigned char* st = ring + (size_t)s * p.stage_bytes;
-                dk_down_compute<kNQ, kF8>(m, st, r0, r1, I, hs, os, p.maxrows, h0, u,
-                                          kF8 ? lw.down_scale + (size_t)m->seg_e[u] * sd_e : nullptr, sd_ld);
+                dk_down_compute<kNQ, kF8, kF4>(m, st, r0, r1, I, hs, os, p.maxrows, h0, u,
+                                               kF8 ? lw.down_scale + (size_t)m->seg_e[u] * sd_e : nullptr, sd_ld,
+                                               kF4 ? lw.down_bs + (size_t)m->seg_e[u] * H * (I >> 4) : nullptr,
+                                               kF4 ? __ldg(lw.down_gs + m->seg_e[u]) : 1.f);
                 __syncwarp();
                 if (c == c0 && cw == 0 && lane == 0) dk_trace<kTrace>(p, l, 13);
                 if (lane == 0) mbar_arrive(&empty[s]);
