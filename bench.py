@@ -545,6 +545,11 @@ def config_records(api, accounting, synth, dev, steps, warmup, seed=0):
             key = f"{'uniform' if base is synth.UNIFORM else 'skewed'}_B{B}"
             out[key] = measure_layer(api, accounting, synth, base.with_batch(B), dev, steps, warmup, 0, seed,
                                      flush, lw=lw)
+            if B > 4:
+                # the split dispatch: only the experts with >= 8 routes on the
+                # tensor cores, the rest on the CUDA-core streaming GEMV
+                out[key + "_split_tc"] = measure_layer(api, accounting, synth, base.with_batch(B), dev, steps,
+                                                       warmup, api.MOE_F_SPLIT_TC, seed, flush, lw=lw)
             if base is synth.SKEWED and B > 4:
                 # the step's most chosen experts kept in L2 across steps (an L2
                 # policy on the weight copies; the same flush between steps)

@@ -86,7 +86,8 @@ typedef enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 } moe_dtype;
 #define MOE_F_UNFUSED 2u    /* layer/stack: run the phases as separate kernels
                                instead of a persistent kernel */
 #define MOE_F_FORCE_TC 4u   /* every expert with any route uses the tensor-core
-                               GEMMs (testing; needs H % 128 == 0, I % 64 == 0) */
+                               GEMMs, even with MOE_F_SPLIT_TC (the default where
+                               H % 128 == 0 and I % 64 == 0 and a workspace is given) */
 #define MOE_F_NO_TC 8u      /* never use the tensor-core GEMMs */
 #define MOE_F_NO_PREFETCH 16u /* stack: no speculative L2 prefetch of the next layer's
                                predicted experts (results are unchanged; the prefetch
@@ -98,8 +99,13 @@ typedef enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 } moe_dtype;
                                policy, the others stream with evict_first ("MoE
                                Performance Optimization Analysis", Option 3:
                                expert caching; results are unchanged) */
-#define MOE_TC_MIN_ROUTES 8 /* by default an expert chosen by at least this many
-                               routes runs on the tensor cores */
+#define MOE_F_SPLIT_TC 64u  /* layer/stack, batches beyond the decode kernel: only
+                               the experts with at least MOE_TC_MIN_ROUTES routes
+                               use the tensor-core GEMMs, the others the CUDA-core
+                               streaming GEMV (two launches per projection; by
+                               default every chosen expert takes the tensor cores,
+                               one launch per projection) */
+#define MOE_TC_MIN_ROUTES 8 /* the split of MOE_F_SPLIT_TC and MOE_F_HOT_L2 */
 
 /*
  * moe_workspace_bytes -- size of the scratch buffer the forward entry points

@@ -85,6 +85,7 @@ MOE_F_FORCE_TC = 4
 MOE_F_NO_TC = 8
 MOE_F_NO_PREFETCH = 16
 MOE_F_HOT_L2 = 32
+MOE_F_SPLIT_TC = 64
 TC_MIN_ROUTES = 8
 MAX_E, MAX_TOPK, MAX_B, MAX_DIM, MAX_LAYERS = 256, 8, 1024, 16384, 64
 NOALLOC_SCRATCH_BYTES = 16 << 20

@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kThreads) fused_kernel(Ctx c, StackArgs sa, un
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 constexpr unsigned kAllFlags =
-    MOE_F_NO_DEDUP | MOE_F_UNFUSED | MOE_F_FORCE_TC | MOE_F_NO_TC | MOE_F_NO_PREFETCH | MOE_F_HOT_L2;
+    MOE_F_NO_DEDUP | MOE_F_UNFUSED | MOE_F_FORCE_TC | MOE_F_NO_TC | MOE_F_NO_PREFETCH | MOE_F_HOT_L2 | MOE_F_SPLIT_TC;
 
 struct WsLayout {
     size_t logits, ids, rw, offsets, route_idx, unique, num_unique, status, bar, acc, xt, acc_end, h, o;
@@ -398,10 +398,16 @@ static bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, u
 
 static bool tc_shape_ok(int H, int I) { return H >= 128 && (H % 128) == 0 && I >= 64 && (I % 64) == 0; }
 
+// Every chosen expert runs on the tensor cores, even one with a single
+// route: one GEMM launch per projection streams all the step's experts
+// through a deep TMA ring and keeps the whole GPU busy, where the split
+// between a tensor-core launch for the popular experts and a CUDA-core
+// streaming launch for the rest (MOE_F_SPLIT_TC) runs two launches that each
+// fill only part of it, and the GEMV's consumers are bound by their fp32 FMAs.
 static int tc_threshold_for(unsigned flags, int H, int I) {
     if ((flags & MOE_F_NO_TC) || !tc_shape_ok(H, I)) return 0;
-    if (flags & MOE_F_FORCE_TC) return 1;
-    return MOE_TC_MIN_ROUTES;
+    if ((flags & MOE_F_SPLIT_TC) && !(flags & MOE_F_FORCE_TC)) return MOE_TC_MIN_ROUTES;
+    return 1;
 }
 
 static int launch_tc(const Ctx& c, char* ws, const WsLayout& L, cudaStream_t st) {
@@ -450,7 +456,7 @@ static int launch_tc_down(const Ctx& c, char* ws, const WsLayout& L, cudaStream_
 // Geometry of a streaming grouped-GEMV pass; false when it does not apply
 // (segments may exceed kSgMaxTok routes, or the rows do not fit).
 static bool stream_plan(const Ctx& c, int gate, SgParams& P, size_t& smem) {
-    if (c.tc_threshold != MOE_TC_MIN_ROUTES || c.seg_list == nullptr) return false;
+    if (c.tc_threshold < 2 || c.tc_threshold > MOE_TC_MIN_ROUTES || c.seg_list == nullptr) return false;
     memset(&P, 0, sizeof P);
     P.c = c;
     P.gate = gate;
@@ -522,21 +528,22 @@ static int launch_experts(const Ctx& c0, cudaStream_t st, char* ws = nullptr, co
         d_items = d_items < rd ? d_items : rd;
     }
     const bool tc = c.tc_threshold > 0 && ws != nullptr;
+    const bool all_tc = tc && c.tc_threshold == 1;  // the CUDA-core list is empty
     SgParams sg_gate, sg_down;
     size_t sg_gate_smem = 0, sg_down_smem = 0;
     const bool streamed = ws != nullptr && stream_plan(c, 1, sg_gate, sg_gate_smem) &&
                           stream_plan(c, 0, sg_down, sg_down_smem);
     if (tc && (rc = launch_tc(c, ws, *L, st))) return rc;
-    if (streamed) {
-        if ((rc = launch_stream(sg_gate, sg_gate_smem, st))) return rc;
-    } else {
-        if ((rc = launch_pdl(gateup_kernel, g_items, kThreads, smem, st, c))) return rc;
+    if (!all_tc) {
+        rc = streamed ? launch_stream(sg_gate, sg_gate_smem, st)
+                      : launch_pdl(gateup_kernel, g_items, kThreads, smem, st, c);
+        if (rc) return rc;
     }
     if (tc && (rc = launch_tc_down(c, ws, *L, st))) return rc;
-    if (streamed) {
-        if ((rc = launch_stream(sg_down, sg_down_smem, st))) return rc;
-    } else {
-        if ((rc = launch_pdl(down_kernel, d_items, kThreads, smem, st, c))) return rc;
+    if (!all_tc) {
+        rc = streamed ? launch_stream(sg_down, sg_down_smem, st)
+                      : launch_pdl(down_kernel, d_items, kThreads, smem, st, c);
+        if (rc) return rc;
     }
     return launch_pdl(combine_kernel, combine_items(c), kThreads, 0, st, c);
 }

@@ -303,11 +303,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         if (warp == 4) {
             if (lane == 0) {
                 // ---------------- TMA producer
-                // MOE_F_HOT_L2: the tensor-core experts are the step's most
-                // chosen ones; their weights are loaded with evict_last so that
-                // they stay in L2 for the next steps
+                // MOE_F_HOT_L2: the experts with at least MOE_TC_MIN_ROUTES
+                // routes are the step's most chosen ones; their weights are
+                // loaded with evict_last so that they stay in L2 for the next
+                // steps, those of the others with evict_first
                 const bool hot = (c.flags & MOE_F_HOT_L2) != 0;
-                const uint64_t pol = hot ? l2_policy_evict_last() : 0ull;
+                const uint64_t pol = !hot                                   ? 0ull
+                                     : sg.p1 - sg.p0 >= MOE_TC_MIN_ROUTES ? l2_policy_evict_last()
+                                                                           : l2_policy_evict_first();
                 const uint32_t bytes = kTcATile + (uint32_t)n_pad * 128u * (p.with_lo ? 2u : 1u);
                 int arow0, arow1 = 0;
                 if (p.gate) {

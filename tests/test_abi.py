@@ -81,3 +81,18 @@ def test_status_strings(lib):
     assert b"invalid" in lib.moe_status_string(-1)
     assert b"workspace" in lib.moe_status_string(-4)
     assert b"timed out" in lib.moe_status_string(1)
+
+
+def test_binding_constants_match_the_header():
+    """Every integer constant of include/moe.h that the Python binding mirrors
+    (as MOE_X or as X) has the header's value."""
+    from moe_decode_layer_gemv_gb300 import api
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    checked = 0
+    for name, val in re.findall(r"^#define\s+(MOE_\w+)\s+(-?\d+)u?\b", src, flags=re.M):
+        for attr in (name, name[len("MOE_"):]):
+            if hasattr(api, attr):
+                assert getattr(api, attr) == int(val), name
+                checked += 1
+                break
+    assert checked >= 15 and api.MOE_F_SPLIT_TC == 64 and api.TC_MIN_ROUTES == 8

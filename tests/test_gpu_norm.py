@@ -56,8 +56,9 @@ def _oracle_walk(x0, layers, k, ids_gpu):
     (1, 256, 96, 16, 2, 3, 0),      # decode kernel, norm fused
     (4, 512, 128, 32, 4, 2, 0),     # decode kernel, four tokens
     (3, 72, 40, 5, 3, 2, 0),        # ragged H and I
-    (9, 256, 64, 12, 3, 2, 0),      # beyond the decode kernel: norm kernel + fused layer
-    (24, 256, 128, 8, 2, 2, 0),     # tensor-core experts (>= 8 routes): norm kernel + phases
+    (9, 256, 64, 12, 3, 2, 0),      # beyond the decode kernel: norm kernel + tensor-core phases
+    (9, 256, 64, 12, 3, 2, 8),      # MOE_F_NO_TC: norm kernel + fused CUDA-core layer
+    (24, 256, 128, 8, 2, 2, 64),    # MOE_F_SPLIT_TC: norm kernel + tensor cores + streaming GEMV
     (2, 256, 96, 16, 2, 2, 2),      # MOE_F_UNFUSED
 ])
 def test_prenorm_stack_matches_oracle(cuda_lib, B, H, I, E, k, L, flags):

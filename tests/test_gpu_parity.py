@@ -184,7 +184,8 @@ def test_persistent_decode_kernel_is_stable_over_repeated_runs(cuda_lib, B, k, E
     """The small-batch layer runs in one persistent kernel whose phases hand
     data over through device-wide barriers; a missing ordering would show up
     as an occasional wrong token.  Many seeds, compared with the phase-by-phase
-    kernels (each checked against the oracle above)."""
+    CUDA-core kernels (each checked against the oracle above; fp32 throughout,
+    like the persistent kernel, so the two agree to 1e-5)."""
     H, I = 2048, 768
     w = synth.Workload("rep", B=B, H=H, I=I, E=E, top_k=k, sigma_router=H ** -0.5)
     lw = synth.make_layer(w, 0, seed=7, device=DEV)
@@ -192,7 +193,7 @@ def test_persistent_decode_kernel_is_stable_over_repeated_runs(cuda_lib, B, k, E
         x = synth.make_x(w, step, seed=7, device=DEV)
         y0, i0, w0 = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k)
         y1, i1, w1 = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k,
-                                            flags=cuda_lib.MOE_F_UNFUSED)
+                                            flags=cuda_lib.MOE_F_UNFUSED | cuda_lib.MOE_F_NO_TC)
         torch.cuda.synchronize()
         assert torch.equal(i0, i1), step
         assert float((w0 - w1).abs().max()) <= 1e-6
@@ -207,7 +208,7 @@ def test_persistent_stack_is_stable_over_repeated_runs(cuda_lib):
     for step in range(30):
         x = synth.make_x(w, step, seed=3, device=DEV)
         xa, ia = cuda_lib.stack_forward(x, sw, k)
-        xb, ib = cuda_lib.stack_forward(x, sw, k, flags=cuda_lib.MOE_F_UNFUSED)
+        xb, ib = cuda_lib.stack_forward(x, sw, k, flags=cuda_lib.MOE_F_UNFUSED | cuda_lib.MOE_F_NO_TC)
         torch.cuda.synchronize()
         assert torch.equal(ia, ib), step
         assert float((xa - xb).abs().max()) <= 1e-5 * float(xb.abs().max()), step

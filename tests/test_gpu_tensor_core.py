@@ -1,7 +1,8 @@
 """The tensor-core (tcgen05) grouped GEMM path against the CPU oracle.
 
-Experts chosen by at least MOE_TC_MIN_ROUTES routes run as grouped GEMMs on
-the tensor cores; MOE_F_FORCE_TC sends every expert there.  Shapes cover
+By default every chosen expert runs as a grouped GEMM on the tensor cores;
+with MOE_F_SPLIT_TC only the experts chosen by at least MOE_TC_MIN_ROUTES
+routes do, the rest stream through the CUDA-core GEMV.  Shapes cover
 several M tiles, K steps, token tiles (more than 128 routes on one expert)
 and both activation dtypes.
 """
@@ -43,15 +44,34 @@ def test_forced_tensor_core_layer_matches_oracle(cuda_lib, B, H, I, E, k, x_bf16
     assert rel < 1e-4  # hi/lo split activations keep near-fp32 accuracy
 
 
-def test_mixed_dispatch_skewed_routing(cuda_lib):
-    """Skewed routing: popular experts (>= 8 routes) on the tensor cores, the
-    rest on the CUDA-core GEMV, in one layer."""
+def test_split_dispatch_skewed_routing(cuda_lib):
+    """MOE_F_SPLIT_TC with skewed routing: popular experts (>= 8 routes) on
+    the tensor cores, the rest on the CUDA-core streaming GEMV, in one layer."""
     B, H, I, E, k = 96, 1024, 256, 32, 4
     lw, x = _case(B, H, I, E, k, seed=4, skew=True)
-    y, ids, w = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k, bias=lw["bias"])
+    y, ids, w = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k, bias=lw["bias"],
+                                       flags=cuda_lib.MOE_F_SPLIT_TC)
     torch.cuda.synchronize()
     counts = np.bincount(ids.cpu().numpy().ravel(), minlength=E)
     assert counts.max() >= cuda_lib.TC_MIN_ROUTES and (counts[counts > 0] < cuda_lib.TC_MIN_ROUTES).any()
+    y_o, _, _ = oracle_layer_following(x, layer_weights_np(lw), k, ids)
+    check_y(y, y_o)
+
+
+@pytest.mark.parametrize("B,E,k", [(15, 16, 4), (96, 32, 4)])
+def test_default_runs_every_expert_on_the_tensor_cores(cuda_lib, B, E, k):
+    """By default every chosen expert -- popular or not -- takes the
+    tensor-core GEMM: the result is the forced one, bit for bit, and matches
+    the oracle."""
+    H, I = 1024, 256
+    lw, x = _case(B, H, I, E, k, seed=4, skew=True)
+    y, ids, w = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k, bias=lw["bias"])
+    yf, idsf, _ = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k, bias=lw["bias"],
+                                         flags=cuda_lib.MOE_F_FORCE_TC | cuda_lib.MOE_F_SPLIT_TC)
+    torch.cuda.synchronize()
+    counts = np.bincount(ids.cpu().numpy().ravel(), minlength=E)
+    assert counts.max() >= cuda_lib.TC_MIN_ROUTES and (counts[counts > 0] < cuda_lib.TC_MIN_ROUTES).any()
+    assert torch.equal(ids, idsf) and torch.equal(y, yf)
     y_o, _, _ = oracle_layer_following(x, layer_weights_np(lw), k, ids)
     check_y(y, y_o)
 
@@ -68,15 +88,19 @@ def test_tensor_core_and_gemv_paths_agree(cuda_lib):
     assert float((ya - yb).abs().max()) <= 1e-4 * float(yb.abs().max())
 
 
-def test_hot_expert_l2_policy_leaves_results_unchanged(cuda_lib):
+@pytest.mark.parametrize("split", [False, True])
+def test_hot_expert_l2_policy_leaves_results_unchanged(cuda_lib, split):
     """MOE_F_HOT_L2 only changes the L2 eviction priority of the weight
-    copies (evict_last for the tensor-core experts, evict_first for the
-    rest): the layer's outputs are bit-identical with and without it."""
+    copies (evict_last for the experts with >= 8 routes, evict_first for
+    the rest), on the tensor cores or the streaming GEMV: the layer's
+    outputs are bit-identical with and without it."""
     B, H, I, E, k = 96, 1024, 256, 32, 4
     lw, x = _case(B, H, I, E, k, seed=6, skew=True)
-    y0, i0, _ = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k, bias=lw["bias"])
+    base = cuda_lib.MOE_F_SPLIT_TC if split else 0
+    y0, i0, _ = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k, bias=lw["bias"],
+                                       flags=base)
     y1, i1, _ = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k, bias=lw["bias"],
-                                       flags=cuda_lib.MOE_F_HOT_L2)
+                                       flags=base | cuda_lib.MOE_F_HOT_L2)
     torch.cuda.synchronize()
     assert torch.equal(i0, i1) and torch.equal(y0, y1)
     y_o, _, _ = oracle_layer_following(x, layer_weights_np(lw), k, i1)

@@ -58,14 +58,14 @@ def oracle_layer_lazy(x, lw, k, ids_gpu, residual=None, tokens=None):
     return y, ids_o, ex
 
 
-def run_layer(cuda_lib, w, lw, x):
+def run_layer(cuda_lib, w, lw, x, flags=0):
     """The layer in the benchmark's launch configuration; also checks the
     routing weights it returned and the grouping it left in its workspace."""
     st = cuda_lib.new_status()
     B = x.shape[0]
     ws = cuda_lib.new_workspace(B, w.H, w.I, w.E, w.top_k)
     y, ids, rw = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], w.top_k,
-                                        bias=lw.get("bias"), workspace=ws, status=st)
+                                        bias=lw.get("bias"), workspace=ws, status=st, flags=flags)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     check_layer_routing(x, lw["w_router"], lw.get("bias"), w.top_k, ids, rw)
@@ -95,6 +95,18 @@ def test_uniform_routing_layer(cuda_lib, uniform_layer, B):
     U = len(np.unique(ids.cpu().numpy()))
     # unique count inside a generous band around the closed form
     assert abs(U - accounting.expected_unique(256, 8, B)) <= 6 * np.sqrt(max(B, 1)) + 2
+
+
+@pytest.mark.parametrize("B", [5, 16, 64])
+def test_uniform_layer_split_dispatch(cuda_lib, uniform_layer, B):
+    """MOE_F_SPLIT_TC: the experts with fewer than MOE_TC_MIN_ROUTES routes
+    stream through the CUDA-core grouped GEMV, the others (if any) take the
+    tensor cores."""
+    w, lw = uniform_layer
+    x = synth.make_x(w, 0, seed=B, device=DEV, B=B)
+    y, ids, rw = run_layer(cuda_lib, w, lw, x, flags=cuda_lib.MOE_F_SPLIT_TC)
+    y_o, _, ex = oracle_layer_lazy(x, lw, w.top_k, ids)
+    check_y(y, y_o)
 
 
 @pytest.fixture(scope="module")
