@@ -89,9 +89,9 @@ typedef enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 } moe_dtype;
                                GEMMs, even with MOE_F_SPLIT_TC (the default where
                                H % 128 == 0 and I % 64 == 0 and a workspace is given) */
 #define MOE_F_NO_TC 8u      /* never use the tensor-core GEMMs */
-#define MOE_F_NO_PREFETCH 16u /* stack: no speculative L2 prefetch of the next layer's
-                               predicted experts (results are unchanged; the prefetch
-                               only moves bytes earlier) */
+#define MOE_F_NO_PREFETCH 16u /* stack: no speculative L2 prefetch of the gate/up
+                               weights of the next layer's predicted experts (results
+                               are unchanged; the prefetch only moves bytes earlier) */
 #define MOE_F_HOT_L2 32u    /* layer/stack, batches beyond the decode kernel: keep
                                the step's most chosen experts in L2 for the next
                                steps -- the experts with at least MOE_TC_MIN_ROUTES
