@@ -121,10 +121,9 @@ __device__ void router_item(const Ctx& c, int item, float* smem) {
 // One warp per token; lane l holds experts l, l+32, ... (E <= 256).
 __host__ __device__ __forceinline__ int topk_items(const Ctx& c) { return ceil_div(c.B, kWarps); }
 
-__device__ void topk_item(const Ctx& c, int item, int32_t* ids_out, float* w_out) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = item * kWarps + warp;
-    if (t >= c.B) return;
+// Token t by the calling warp.
+__device__ void topk_token(const Ctx& c, int t, int32_t* ids_out, float* w_out) {
+    const int lane = threadIdx.x & 31;
     const float* l = c.logits + (size_t)t * c.E;
     float v[8];
     bool bad = false;
@@ -193,6 +192,11 @@ __device__ void topk_item(const Ctx& c, int item, int32_t* ids_out, float* w_out
             }
         }
     }
+}
+
+__device__ void topk_item(const Ctx& c, int item, int32_t* ids_out, float* w_out) {
+    const int t = item * kWarps + (threadIdx.x >> 5);
+    if (t < c.B) topk_token(c, t, ids_out, w_out);
 }
 
 // ================================================================= grouping
@@ -523,8 +527,10 @@ __device__ void down_item(const Ctx& c, int item, float* hs, int* rts) {
 // ================================================================== combine
 // y[t, :] = sum_j w[t,j] * o[t*k + j, :]  (j ascending)  (+ residual[t, :]).
 // ("MoE Performance Optimization Analysis", GPU Router Design: combination
-// on the GPU.)  Item = 1024 consecutive float4 of y.
-constexpr int kCombineVecs = kThreads * 4;
+// on the GPU.)  Item = 256 consecutive float4 of y, one per thread, so that
+// even a small batch spreads over many SMs and each thread's k loads are in
+// flight together.
+constexpr int kCombineVecs = kThreads;
 
 __host__ __device__ __forceinline__ int combine_items(const Ctx& c) {
     return ceil_div(c.B * (c.H >> 2), kCombineVecs);

@@ -59,7 +59,7 @@ struct TcBars {
     uint32_t tmem_slot;
     int abort;                     // a bounded wait ran out: every role stops
 };
-static_assert(sizeof(TcBars) <= 1024, "barrier block");
+static_assert(sizeof(TcBars) <= 512, "barrier block: the second half holds the route indices of an item");
 
 struct TcParams {
     CUtensorMap ta;      // weights [rows, K] bf16, box {64, 64 (gate) or 128 (down)}
@@ -186,13 +186,29 @@ __global__ void __launch_bounds__(kThreads) tc_split_x_kernel(Ctx c, uint16_t* x
     const int p = blockIdx.x;
     if (p >= c.B * c.k) return;
     const int t = route_at(c, p) / c.k;
-    for (int h = threadIdx.x; h < c.H; h += blockDim.x) {
-        float v;
-        if (c.x_bf16) v = bf_bits2f(static_cast<const uint16_t*>(c.x)[(size_t)t * c.H + h]);
-        else v = ld_act_f(static_cast<const float*>(c.x) + (size_t)t * c.H + h);
-        const uint16_t hi = f2bf_bits(v);
-        x_hi[(size_t)p * c.H + h] = hi;
-        x_lo[(size_t)p * c.H + h] = f2bf_bits(v - bf_bits2f(hi));
+    for (int h = 4 * threadIdx.x; h < c.H; h += 4 * blockDim.x) {  // four elements a thread (H % 8 == 0)
+        float v[4];
+        if (c.x_bf16) {
+            const uint2 u = __ldcg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(c.x) + (size_t)t * c.H + h));
+            v[0] = __uint_as_float(u.x << 16);
+            v[1] = __uint_as_float(u.x & 0xffff0000u);
+            v[2] = __uint_as_float(u.y << 16);
+            v[3] = __uint_as_float(u.y & 0xffff0000u);
+        } else {
+            const float4 f = ld_act_f4(static_cast<const float*>(c.x) + (size_t)t * c.H + h);
+            v[0] = f.x;
+            v[1] = f.y;
+            v[2] = f.z;
+            v[3] = f.w;
+        }
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            hi[j] = f2bf_bits(v[j]);
+            lo[j] = f2bf_bits(v[j] - bf_bits2f((uint16_t)hi[j]));
+        }
+        *reinterpret_cast<uint2*>(x_hi + (size_t)p * c.H + h) = make_uint2(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16));
+        *reinterpret_cast<uint2*>(x_lo + (size_t)p * c.H + h) = make_uint2(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
     }
 }
 
@@ -212,6 +228,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     unsigned char* base = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     TcBars* b = reinterpret_cast<TcBars*>(base);
+    int* rr = reinterpret_cast<int*>(base + 512);         // [kTcMaxN] flat routes of the item's tokens (down)
     float* epi = reinterpret_cast<float*>(base + 1024);  // [128][kTcEpiLd]
     int4* segtab = reinterpret_cast<int4*>(base + 1024 + kTcEpiBytes);  // [kTcSegCache] (e, p0, p1, valid)
     unsigned char* ring = base + 1024 + kTcEpiBytes + kTcSegBytes;
@@ -385,6 +402,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         } else {
             // ---------------- epilogue (warps 0-3: accumulator lanes 32w..32w+31)
             // (one decision for all 128 threads: they meet at named barriers)
+            // the down pass writes o by flat route: the item's route indices
+            // once into shared memory (ordered before their use by the first
+            // barrier below), not a dependent global load per column
+            if (!p.gate && (int)threadIdx.x < n) rr[threadIdx.x] = route_at(c, q0 + (int)threadIdx.x);
             const bool ok = !named_sync_or(1, 128, !tc_wait_ab(&b->acc_full[buf], (uint32_t)(use & 1), b));
             tc_fence_after();
             const uint32_t row_addr = tmem + (uint32_t)(buf * 128) + ((uint32_t)(warp * 32) << 16);
@@ -415,8 +436,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
                     const int r0 = mt * 128;
                     for (int t = threadIdx.x; t < 128 * ncol; t += 128) {
                         const int row = t & 127, jj = t >> 7;
-                        const int r = route_at(c, q0 + col0 + jj);
-                        c.o[(size_t)r * c.H + r0 + row] = epi[row * kTcEpiLd + jj];
+                        c.o[(size_t)rr[col0 + jj] * c.H + r0 + row] = epi[row * kTcEpiLd + jj];
                     }
                 }
                 named_sync(1, 128);
