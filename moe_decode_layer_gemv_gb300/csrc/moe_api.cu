@@ -153,6 +153,17 @@ __global__ void __launch_bounds__(kRouteTailThreads) route_tail_kernel(Ctx c) {
     if (warp == 0) classify_warp(c);
 }
 
+// Grouping and classification in one CTA, for batches beyond kRouteTailMaxB
+// (whose top-k runs on many CTAs): one launch fewer.
+__global__ void __launch_bounds__(kRouteTailThreads) group_classify_kernel(Ctx c) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    grid_dep_wait();
+    group_cta(c.ids, c.B, c.k, c.E, c.offsets, c.route_idx, c.unique, c.num_unique, c.status,
+              reinterpret_cast<uint32_t*>(smem));
+    __syncthreads();
+    if (threadIdx.x < 32) classify_warp(c);
+}
+
 __global__ void __launch_bounds__(kThreads) combine_kernel(Ctx c) {
     grid_dep_wait();
     combine_item(c, blockIdx.x);
@@ -576,14 +587,22 @@ static int launch_experts(const Ctx& c0, cudaStream_t st, char* ws = nullptr, co
 
 static int launch_unfused_layer(const Ctx& c, cudaStream_t st, char* ws, const WsLayout& L) {
     int rc;
-    if (ws && c.B <= kRouteTailMaxB) {  // router, then top-k + grouping + classification in one CTA
-        if ((rc = launch_router(c, st))) return rc;
+    if (ws) {
+        // router; then top-k + grouping + classification in one CTA, or for
+        // larger batches the top-k on its own and grouping + classification
         Ctx cc = c;
         cc.seg_list = reinterpret_cast<int32_t*>(ws + L.seg_list);
         cc.seg_count = reinterpret_cast<int32_t*>(ws + L.seg_count);
         const size_t smem = group_smem_bytes(c.B, c.E);
-        if ((rc = allow_smem(route_tail_kernel, smem))) return rc;
-        if ((rc = launch_pdl(route_tail_kernel, 1, kRouteTailThreads, smem, st, cc))) return rc;
+        if (c.B <= kRouteTailMaxB) {
+            if ((rc = launch_router(c, st))) return rc;
+            if ((rc = allow_smem(route_tail_kernel, smem))) return rc;
+            if ((rc = launch_pdl(route_tail_kernel, 1, kRouteTailThreads, smem, st, cc))) return rc;
+        } else {
+            if ((rc = launch_route(c, st))) return rc;
+            if ((rc = allow_smem(group_classify_kernel, smem))) return rc;
+            if ((rc = launch_pdl(group_classify_kernel, 1, kRouteTailThreads, smem, st, cc))) return rc;
+        }
         return launch_experts(c, st, ws, &L, true);
     }
     rc = launch_route(c, st);

@@ -38,6 +38,17 @@ __device__ __forceinline__ float2 bf16x2_to_f2(uint32_t u) {
     return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
 
+// An order-preserving unsigned key of a float (a < b as floats, neither NaN
+// and not both zeros, iff key(a) < key(b)) and its inverse.
+__device__ __forceinline__ unsigned order_key(float f) {
+    const unsigned b = __float_as_uint(f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(unsigned k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
 // SiLU(g) * u with SiLU(z) = z / (1 + e^-z), fp32

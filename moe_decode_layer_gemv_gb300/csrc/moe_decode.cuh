@@ -306,14 +306,7 @@ __device__ __forceinline__ bool dk_poll(const unsigned long long* w, unsigned n,
 // The routing weights follow: the fp32 softmax over all E logits followed by
 // renormalisation over the selection equals the softmax over the selected
 // logits alone (the full denominator cancels), w_j = e^(l_j - l_0) / sum.
-__device__ __forceinline__ unsigned order_key(float f) {
-    const unsigned b = __float_as_uint(f);
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-
-__device__ __forceinline__ float key_value(unsigned k) {
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
+// (order_key / key_value: moe_common.cuh)
 
 // Top-k of token t by one warp from values in registers: lane L holds the
 // logit of expert L + 32 s in v[s] (s < 8; entries for e >= E are ignored)

@@ -134,6 +134,16 @@ __device__ void topk_token(const Ctx& c, int t, int32_t* ids_out, float* w_out) 
         if (e < c.E && !isfinite(v[s])) bad = true;
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(c.status, MOE_DEV_NONFINITE);
+    // each round: the largest logit by a warp max over order-preserving keys,
+    // then the lowest expert id holding it by a warp min -- "logit
+    // descending, ties to the lower id" (zeros made +0 first, so that -0 and
+    // +0 tie as they compare equal; NaN logits, key 0, are never chosen)
+    unsigned key[8];
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+        const float z = v[s] + 0.0f;
+        key[s] = (lane + 32 * s < c.E && !isnan(z)) ? order_key(z) : 0u;
+    }
     unsigned taken = 0;
     float selv[MOE_MAX_TOPK];
     int seli[MOE_MAX_TOPK];
@@ -142,25 +152,17 @@ __device__ void topk_token(const Ctx& c, int t, int32_t* ids_out, float* w_out) 
         selv[j] = -INFINITY;
         seli[j] = 0;
         if (j < c.k) {
-            float bv = -INFINITY;
-            int bi = 0x7fffffff;
+            unsigned kb = 0u;
+            int ib = 0x7fffffff;
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const int e = lane + 32 * s;
-                if (e < c.E && !((taken >> s) & 1u) && (v[s] > bv || (v[s] == bv && e < bi))) {
-                    bv = v[s];
-                    bi = e;
+            for (int s = 0; s < 8; ++s)
+                if (!((taken >> s) & 1u) && key[s] > kb) {
+                    kb = key[s];
+                    ib = lane + 32 * s;
                 }
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                if (ov > bv || (ov == bv && oi < bi)) {
-                    bv = ov;
-                    bi = oi;
-                }
-            }
+            const unsigned km = __reduce_max_sync(0xffffffffu, kb);
+            int bi = (int)__reduce_min_sync(0xffffffffu, (km != 0u && kb == km) ? (unsigned)ib : 0x7fffffffu);
+            const float bv = km != 0u ? key_value(km) : -INFINITY;
             if (bi == 0x7fffffff) bi = 0;  // only with non-finite logits (flagged above)
             if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
             selv[j] = bv;
