@@ -272,13 +272,22 @@ __device__ __forceinline__ long long fix_sum(unsigned long long w, unsigned n) {
     return (long long)(w & (kFixCount - 1ull)) - (long long)n * kFixBias;
 }
 
-// Waits (bounded) until the counted word at w holds n contributions; false
-// when the launch is being aborted (this CTA timed out, or another one did).
-__device__ __forceinline__ bool dk_poll(const unsigned long long* w, unsigned n, unsigned long long& out,
-                                        const DkParams& p, DkMisc* m) {
+// The kDkShadows copies of one counted word (copy sh at w + sh * stride),
+// waited for (bounded) together: each round loads the copies not yet
+// complete at once, so that the wait ends one round trip after the last of
+// them completes.  sum: their exact integer sum; false when aborting.
+__device__ __forceinline__ bool dk_poll_sum(const unsigned long long* w, size_t stride, long long& sum,
+                                            const DkParams& p, DkMisc* m) {
+    unsigned long long v[kDkShadows];
+    unsigned pending = (1u << kDkShadows) - 1u;
     for (unsigned long long it = 0;; ++it) {
-        out = ld_relaxed_gpu_u64(w);
-        if ((unsigned)(out >> 57) >= n) return true;
+#pragma unroll
+        for (int sh = 0; sh < kDkShadows; ++sh)
+            if ((pending >> sh) & 1u) v[sh] = ld_relaxed_gpu_u64(w + (size_t)sh * stride);
+#pragma unroll
+        for (int sh = 0; sh < kDkShadows; ++sh)
+            if ((unsigned)(v[sh] >> 57) >= dk_shadow_ctas(sh)) pending &= ~(1u << sh);
+        if (pending == 0u) break;
         if ((it & 63ull) == 63ull && (ld_relaxed_gpu(p.bar + 1) != 0u || *(volatile int*)&m->abort_flag)) return false;
         if (it > kDkSpinLimit) {
             set_status(p.status, MOE_DEV_TIMEOUT);
@@ -286,6 +295,10 @@ __device__ __forceinline__ bool dk_poll(const unsigned long long* w, unsigned n,
             return false;
         }
     }
+    sum = 0;
+#pragma unroll
+    for (int sh = 0; sh < kDkShadows; ++sh) sum += fix_sum(v[sh], dk_shadow_ctas(sh));
+    return true;
 }
 
 // Top-k of one token (one warp; lane l holds experts l, l+32, ...; E <= 256).
@@ -381,7 +394,7 @@ __device__ __forceinline__ bool dk_tags_are(const Tagged4& t, unsigned tag) {
 }
 
 // Four consecutive tagged elements of x (two 16-byte loads, already issued
-// into t), waited for until each carries tag `tag` (bounded like dk_poll);
+// into t), waited for until each carries tag `tag` (bounded like dk_poll_sum);
 // false when aborting.
 __device__ __forceinline__ bool dk_load_tagged4(const unsigned long long* w, unsigned tag, Tagged4& t, float4& out,
                                                 const DkParams& p, DkMisc* m) {
@@ -1224,23 +1237,13 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_kernel(const DkParams p)
                 float rn = 1.f;
                 if (nacc_now) {  // pre-norm: 1/sqrt(mean(x^2) + eps) of token t's input
                     long long ss = 0;
-#pragma unroll
-                    for (int sh = 0; sh < kDkShadows; ++sh) {
-                        unsigned long long w = 0ull;
-                        polled = polled && dk_poll(nacc_now + (size_t)sh * B + t, dk_shadow_ctas(sh), w, p, m);
-                        ss += fix_sum(w, dk_shadow_ctas(sh));
-                    }
+                    polled = polled && dk_poll_sum(nacc_now + t, (size_t)B, ss, p, m);
                     rn = 1.0f / sqrtf(__ll2float_rn(ss) * (1.0f / kFixScaleSq) / (float)H + p.eps);
                     if (e == 0) m->rn[t] = rn;
                 }
                 if (e < E) {
                     long long sum = 0;  // the shadow copies' integer sums, exact, then one rounding
-#pragma unroll
-                    for (int sh = 0; sh < kDkShadows; ++sh) {
-                        unsigned long long w = 0ull;
-                        polled = polled && dk_poll(acc_now + ((size_t)sh * B + t) * E + e, dk_shadow_ctas(sh), w, p, m);
-                        sum += fix_sum(w, dk_shadow_ctas(sh));
-                    }
+                    polled = polled && dk_poll_sum(acc_now + (size_t)t * E + e, (size_t)B * E, sum, p, m);
                     val = rn * (__ll2float_rn(sum) * (1.0f / kFixScale));
                     if (lw.bias) val += __ldg(lw.bias + e);
                 }
