@@ -74,16 +74,30 @@ __device__ void router_item(const Ctx& c, int item, float* smem) {
         stage_x(c, nullptr, t0, nt, kRouterTB, hc, hn, smem, kRouterHC);
         __syncthreads();
         if (e0 < c.E) {
-            for (int i = lane * 8; i < hn; i += 256) {
+            // this lane's weight vectors of the chunk (kRouterHC / 256 per
+            // expert) are all requested before the first is used: one memory
+            // round trip a chunk instead of one per vector
+            constexpr int kNV = kRouterHC / 256;
+            uint4 wv[EPW][kNV];
+#pragma unroll
+            for (int s = 0; s < kNV; ++s)
+#pragma unroll
+                for (int j = 0; j < EPW; ++j) {
+                    const int i = lane * 8 + 256 * s;
+                    wv[j][s] = (e0 + j < c.E && i < hn) ? ld_weight_v4(c.w.w_router + (size_t)(e0 + j) * c.H + hc + i)
+                                                         : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+            for (int s = 0; s < kNV; ++s) {
+                const int i = lane * 8 + 256 * s;
+                if (i >= hn) break;
                 float2 w[EPW][4];
 #pragma unroll
                 for (int j = 0; j < EPW; ++j) {
-                    const uint4 wv = e0 + j < c.E ? ld_weight_v4(c.w.w_router + (size_t)(e0 + j) * c.H + hc + i)
-                                                  : make_uint4(0u, 0u, 0u, 0u);
-                    w[j][0] = bf16x2_to_f2(wv.x);
-                    w[j][1] = bf16x2_to_f2(wv.y);
-                    w[j][2] = bf16x2_to_f2(wv.z);
-                    w[j][3] = bf16x2_to_f2(wv.w);
+                    w[j][0] = bf16x2_to_f2(wv[j][s].x);
+                    w[j][1] = bf16x2_to_f2(wv[j][s].y);
+                    w[j][2] = bf16x2_to_f2(wv[j][s].z);
+                    w[j][3] = bf16x2_to_f2(wv[j][s].w);
                 }
 #pragma unroll
                 for (int q = 0; q < kRouterTB; ++q) {
