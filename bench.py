@@ -452,7 +452,7 @@ def run_layer_workload(args):
 
 
 def measure_stack(api, accounting, synth, w, dev, steps, warmup, flags=0, seed=0, flush=None, norm=False,
-                  fp8=False, nvfp4=False):
+                  fp8=False, nvfp4=False, layers=None):
     """One token through an L-layer stack per step (L2 flushed before each
     timed step, CUDA events on the launching stream); norm=True makes it a
     pre-norm stack (RMSNorm fused into the router and residual add), fp8=True
@@ -471,7 +471,8 @@ def measure_stack(api, accounting, synth, w, dev, steps, warmup, flags=0, seed=0
         fwd = lambda xb, **kw: api.stack_forward_nvfp4_(xb, sw, w.top_k, **kw)
         lbytes = accounting.layer_bytes_nvfp4
     elif fp8:
-        layers = [synth.make_layer_fp8(w, l, seed=seed, device=dev) for l in range(w.layers)]
+        if layers is None:
+            layers = [synth.make_layer_fp8(w, l, seed=seed, device=dev) for l in range(w.layers)]
         for lw in layers:  # only the codes and scales stay resident
             lw.pop("gate_up", None)
             lw.pop("down", None)
@@ -571,6 +572,15 @@ def config_records(api, accounting, synth, dev, steps, warmup, seed=0):
     # the stack with NVFP4 experts (E2M1 codes, E4M3 scale per 16 weights, fp32 per matrix)
     out["stack_nvfp4"] = measure_stack(api, accounting, synth, synth.STACK, dev, steps, warmup, 0, seed, flush,
                                        nvfp4=True)
+    # one layer of the uniform-routing workload with FP8 experts over the batch
+    # sweep (decode kernel up to B=4, the CUDA-core phase kernels beyond)
+    base = synth.UNIFORM
+    fp8_layer = [synth.make_layer_fp8(base, 0, seed=seed, device=dev)]
+    for B in base.batches:
+        out[f"uniform_B{B}_fp8"] = measure_stack(api, accounting, synth, base.with_batch(B), dev, steps, warmup, 0,
+                                                 seed, flush, fp8=True, layers=fp8_layer)
+    del fp8_layer
+    torch.cuda.empty_cache()
     return out
 
 

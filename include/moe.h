@@ -268,10 +268,12 @@ int moe_stack_forward_norm(int L, const uint16_t* const* w_router, const float* 
  * down_scale [E][ceil(H/128)][ceil(I/128)].  The router stays bf16.  The
  * experts stream half the bytes of bf16 weights; every sum stays fp32.
  * gate_up_q, gate_up_scale, down_q and down_scale are HOST arrays of L
- * device pointers.  Requires H and I multiples of 16 and a batch the
- * persistent decode kernel takes (up to 4 tokens and 32 routes), else
- * MOE_ERR_UNSUPPORTED; flags: MOE_F_NO_DEDUP, MOE_F_NO_PREFETCH.  The other
- * arguments are those of moe_stack_forward.
+ * device pointers.  Requires H and I multiples of 16.  Batches the persistent
+ * decode kernel takes (up to 4 tokens and 32 routes) run in it; larger ones,
+ * and any batch with MOE_F_UNFUSED, run layer by layer on the CUDA-core phase
+ * kernels (the tensor-core GEMMs take bf16 weights only).  flags:
+ * MOE_F_NO_DEDUP, MOE_F_NO_PREFETCH, MOE_F_UNFUSED.  The other arguments are
+ * those of moe_stack_forward.
  */
 int moe_stack_forward_fp8(int L, const uint16_t* const* w_router, const float* const* logit_bias,
                           const uint8_t* const* gate_up_q, const float* const* gate_up_scale,

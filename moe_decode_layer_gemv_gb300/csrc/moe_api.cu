@@ -1043,6 +1043,7 @@ int moe_stack_forward_norm(int Lc, const uint16_t* const* w_router, const float*
     char* ws = static_cast<char*>(workspace);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     LayerWeights lws[MOE_MAX_LAYERS];
+    memset(lws, 0, sizeof lws);  // bf16 experts: no FP8 or NVFP4 scales
     for (int l = 0; l < Lc; ++l) {
         lws[l].w_router = w_router[l];
         lws[l].bias = logit_bias ? logit_bias[l] : nullptr;
@@ -1105,7 +1106,7 @@ int moe_stack_forward_fp8(int Lc, const uint16_t* const* w_router, const float* 
     if (rc) return rc;
     if (Lc < 1 || Lc > MOE_MAX_LAYERS) return MOE_ERR_INVALID_ARG;
     if ((H & 15) || (I & 15)) return MOE_ERR_INVALID_ARG;  // rows of codes in whole 16-byte pieces
-    if (flags & ~(MOE_F_NO_DEDUP | MOE_F_NO_PREFETCH)) return MOE_ERR_INVALID_ARG;
+    if (flags & ~(MOE_F_NO_DEDUP | MOE_F_NO_PREFETCH | MOE_F_UNFUSED)) return MOE_ERR_INVALID_ARG;
     if (B == 0) return MOE_OK;
     if (!w_router || !gate_up_q || !gate_up_scale || !down_q || !down_scale) return MOE_ERR_INVALID_ARG;
     for (int l = 0; l < Lc; ++l) {
@@ -1126,7 +1127,35 @@ int moe_stack_forward_fp8(int Lc, const uint16_t* const* w_router, const float* 
     memset(&dp, 0, sizeof dp);
     size_t dsm = 0;
     const int sms = sm_count();
-    if (!decode_plan(B, H, I, E, top_k, sms, dp, dsm, false, 2)) return MOE_ERR_UNSUPPORTED;
+    if ((flags & MOE_F_UNFUSED) || !decode_plan(B, H, I, E, top_k, sms, dp, dsm, false, 2)) {
+        // Batches beyond the decode kernel: the CUDA-core phase kernels, whose
+        // gate/up and down items read the E4M3 codes with their block scales
+        // (the tensor-core GEMMs take bf16 weights only), layer by layer --
+        // 16-20 % faster than the whole stack in one cooperative launch here.
+        Ctx c = make_ctx(x_inout, MOE_DT_F32, x_inout, x_inout, B, H, I, E, top_k, flags | MOE_F_NO_TC, ws, L,
+                         dev_status);
+        StackArgs sa;
+        memset(&sa, 0, sizeof sa);
+        sa.L = Lc;
+        sa.bar_extra = g_bar_extra;
+        sa.ids_out = expert_ids_out;
+        for (int l = 0; l < Lc; ++l) {
+            sa.layer[l].w_router = w_router[l];
+            sa.layer[l].bias = logit_bias ? logit_bias[l] : nullptr;
+            sa.layer[l].gate_up = reinterpret_cast<const uint16_t*>(gate_up_q[l]);
+            sa.layer[l].down = reinterpret_cast<const uint16_t*>(down_q[l]);
+            sa.layer[l].gate_up_scale = gate_up_scale[l];
+            sa.layer[l].down_scale = down_scale[l];
+        }
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
+        int32_t* ids_ws = c.ids;
+        for (int l = 0; l < Lc; ++l) {
+            c.w = sa.layer[l];
+            c.ids = expert_ids_out ? expert_ids_out + (size_t)l * B * top_k : ids_ws;
+            if ((rc = launch_unfused_layer(c, st, ws, L))) return rc;
+        }
+        return MOE_OK;
+    }
     decode_common(dp, B, H, I, E, top_k, Lc, flags,
                   dev_status ? dev_status : reinterpret_cast<int32_t*>(ws + L.status));
     dp.trace = nullptr;

@@ -7,8 +7,11 @@
 // can see a stale L1 line after a device-wide barrier.
 #pragma once
 
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "moe.h"
 
@@ -47,6 +50,15 @@ __device__ __forceinline__ unsigned order_key(float f) {
 
 __device__ __forceinline__ float key_value(unsigned k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Two E4M3 codes (low byte first) as fp32: the hardware conversion to f16 is
+// exact for every E4M3 value, and so is the widening to f32.
+__device__ __forceinline__ float2 f8x2_to_f2(unsigned v) {
+    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(v & 0xffffu), __NV_E4M3);
+    __half2 h;
+    memcpy(&h, &hr, sizeof h);
+    return __half22float2(h);
 }
 
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }

@@ -665,14 +665,7 @@ __device__ __forceinline__ void dk_down_rows(const unsigned char* st, int nrc, i
 }
 
 // ---------------------------------------------------- block-scaled FP8
-// Two E4M3 codes (low byte first) as fp32: the hardware conversion to f16 is
-// exact for every E4M3 value, and so is the widening to f32.
-__device__ __forceinline__ float2 f8x2_to_f2(unsigned v) {
-    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(v & 0xffffu), __NV_E4M3);
-    __half2 h;
-    memcpy(&h, &hr, sizeof h);
-    return __half22float2(h);
-}
+// (f8x2_to_f2: moe_common.cuh)
 
 // The FP8 form of dk_gate_pair: rows of H E4M3 codes (gate row at grow, up
 // row at urow) with their block scales along the row (gsr, usr: the scale

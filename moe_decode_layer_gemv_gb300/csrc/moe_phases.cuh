@@ -408,7 +408,63 @@ __device__ __forceinline__ void gateup_rowpair(const uint16_t* grow, const uint1
     }
 }
 
+// The block-scaled FP8 form of gateup_rowpair: rows of H one-byte E4M3
+// codes (H % 16 == 0) and their scales along the row (gsr for gate row i, usr
+// for up row I + i: one fp32 per 128 columns).  A lane's 16 consecutive codes
+// lie in one 128-column block, so their products are summed first and
+// scaled once.
+template <int NT>
+__device__ __forceinline__ void gateup_rowpair_f8(const unsigned char* grow, const unsigned char* urow,
+                                                  const float* gsr, const float* usr, int H, const float* xs,
+                                                  int nq, float* hdst, int I) {
+    const int lane = threadIdx.x & 31;
+    float ag[NT], au[NT];
+#pragma unroll
+    for (int q = 0; q < NT; ++q) ag[q] = au[q] = 0.f;
+    for (int base = 0; base < H; base += 512 * kGateUnroll) {  // as many bytes in flight as the bf16 loop
+        uint4 gv[kGateUnroll], uv[kGateUnroll];
+#pragma unroll
+        for (int u = 0; u < kGateUnroll; ++u) {
+            const int idx = base + u * 512 + lane * 16;
+            gv[u] = idx < H ? ld_weight_v4(grow + idx) : make_uint4(0u, 0u, 0u, 0u);
+            uv[u] = idx < H ? ld_weight_v4(urow + idx) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kGateUnroll; ++u) {
+            const int idx = base + u * 512 + lane * 16;
+            if (idx < H) {
+                const float sg = __ldg(gsr + (idx >> 7)), su = __ldg(usr + (idx >> 7));
+                const unsigned gw[4] = {gv[u].x, gv[u].y, gv[u].z, gv[u].w};
+                const unsigned uw[4] = {uv[u].x, uv[u].y, uv[u].z, uv[u].w};
+#pragma unroll
+                for (int q = 0; q < NT; ++q) {
+                    const float4* xp = reinterpret_cast<const float4*>(xs + (size_t)q * H + idx);
+                    float2 pg = make_float2(0.f, 0.f), pu = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {  // codes 4v .. 4v+3 against x[idx + 4v ..]
+                        const float4 xv = xp[v];
+                        pg = ffma2(f8x2_to_f2(gw[v]), make_float2(xv.x, xv.y), pg);
+                        pg = ffma2(f8x2_to_f2(gw[v] >> 16), make_float2(xv.z, xv.w), pg);
+                        pu = ffma2(f8x2_to_f2(uw[v]), make_float2(xv.x, xv.y), pu);
+                        pu = ffma2(f8x2_to_f2(uw[v] >> 16), make_float2(xv.z, xv.w), pu);
+                    }
+                    ag[q] = fmaf(sg, pg.x + pg.y, ag[q]);
+                    au[q] = fmaf(su, pu.x + pu.y, au[q]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < NT; ++q) {
+        const float g = warp_sum(ag[q]);
+        const float u = warp_sum(au[q]);
+        if (lane == q && q < nq) hdst[(size_t)q * I] = silu_mul(g, u);
+    }
+}
+
 // xs: nt_max * H floats of shared memory; tok: nt_max ints of shared memory.
+// Block-scaled FP8 weights when c.w.gate_up_scale is set (gate_up then holds
+// E4M3 codes, one byte each).
 __device__ void gateup_item(const Ctx& c, int item, float* xs, int* tok) {
     const int nib = ceil_div(c.I, kWarps);
     const int sl = item / nib, ib = item - sl * nib;
@@ -427,7 +483,21 @@ __device__ void gateup_item(const Ctx& c, int item, float* xs, int* tok) {
         const int nfill = nq <= 1 ? 1 : nq <= 2 ? 2 : nq <= 4 ? 4 : 8;
         stage_x(c, tok, 0, nq, nfill, 0, c.H, xs, c.H);
         __syncthreads();
-        if (i < c.I) {
+        if (i < c.I && c.w.gate_up_scale) {
+            const unsigned char* G8 = reinterpret_cast<const unsigned char*>(c.w.gate_up) + (size_t)sg.e * 2 * c.I * c.H;
+            const int sld = (c.H + 127) >> 7, se = ((2 * c.I + 127) >> 7) * sld;
+            const float* gsr = c.w.gate_up_scale + (size_t)sg.e * se + (size_t)(i >> 7) * sld;
+            const float* usr = c.w.gate_up_scale + (size_t)sg.e * se + (size_t)((c.I + i) >> 7) * sld;
+            const unsigned char* grow = G8 + (size_t)i * c.H;
+            const unsigned char* urow = G8 + (size_t)(c.I + i) * c.H;
+            float* hdst = c.h + (size_t)g0 * c.I + i;
+            switch (nfill) {
+                case 1: gateup_rowpair_f8<1>(grow, urow, gsr, usr, c.H, xs, nq, hdst, c.I); break;
+                case 2: gateup_rowpair_f8<2>(grow, urow, gsr, usr, c.H, xs, nq, hdst, c.I); break;
+                case 4: gateup_rowpair_f8<4>(grow, urow, gsr, usr, c.H, xs, nq, hdst, c.I); break;
+                default: gateup_rowpair_f8<8>(grow, urow, gsr, usr, c.H, xs, nq, hdst, c.I); break;
+            }
+        } else if (i < c.I) {
             const uint16_t* grow = G + (size_t)i * c.H;
             const uint16_t* urow = G + (size_t)(c.I + i) * c.H;
             float* hdst = c.h + (size_t)g0 * c.I + i;
@@ -505,7 +575,67 @@ __device__ __forceinline__ void down_rows(const uint16_t* D, int row0, int H, in
         }
 }
 
+// The block-scaled FP8 form of down_rows: rows of I E4M3 codes (I % 16 ==
+// 0), the expert's scales dsc [ceil(H/128)][dsc_ld]; a lane's 16 codes lie
+// in one 128-column block and are scaled once.
+template <int NT>
+__device__ __forceinline__ void down_rows_f8(const unsigned char* D, const float* dsc, int dsc_ld, int row0, int H,
+                                             int I, const float* hs, const int* rts, int nq, float* o) {
+    const int lane = threadIdx.x & 31;
+    float acc[kDownRowsPerWarp][NT];
+#pragma unroll
+    for (int rr = 0; rr < kDownRowsPerWarp; ++rr)
+#pragma unroll
+        for (int q = 0; q < NT; ++q) acc[rr][q] = 0.f;
+    for (int base0 = 0; base0 < I; base0 += 512 * kDownUnroll) {  // as many bytes in flight as the bf16 loop
+        uint4 wvu[kDownUnroll][kDownRowsPerWarp];
+        float scu[kDownUnroll][kDownRowsPerWarp];
+#pragma unroll
+        for (int u = 0; u < kDownUnroll; ++u)
+#pragma unroll
+            for (int rr = 0; rr < kDownRowsPerWarp; ++rr) {
+                const int row = row0 + rr, idx = base0 + u * 512 + lane * 16;
+                const bool in = row < H && idx < I;
+                wvu[u][rr] = in ? ld_weight_v4(D + (size_t)row * I + idx) : make_uint4(0u, 0u, 0u, 0u);
+                scu[u][rr] = in ? __ldg(dsc + (size_t)(row >> 7) * dsc_ld + (idx >> 7)) : 0.f;
+            }
+#pragma unroll
+        for (int u = 0; u < kDownUnroll; ++u) {
+        const int idx = base0 + u * 512 + lane * 16;
+        if (idx >= I) continue;
+        const uint4* wv = wvu[u];
+        const float* sc = scu[u];
+#pragma unroll
+        for (int q = 0; q < NT; ++q) {
+            const float4* hp = reinterpret_cast<const float4*>(hs + (size_t)q * I + idx);
+            const float4 h0 = hp[0], h1 = hp[1], h2 = hp[2], h3 = hp[3];
+#pragma unroll
+            for (int rr = 0; rr < kDownRowsPerWarp; ++rr) {
+                float2 a = ffma2(f8x2_to_f2(wv[rr].x), make_float2(h0.x, h0.y), make_float2(0.f, 0.f));
+                a = ffma2(f8x2_to_f2(wv[rr].x >> 16), make_float2(h0.z, h0.w), a);
+                a = ffma2(f8x2_to_f2(wv[rr].y), make_float2(h1.x, h1.y), a);
+                a = ffma2(f8x2_to_f2(wv[rr].y >> 16), make_float2(h1.z, h1.w), a);
+                a = ffma2(f8x2_to_f2(wv[rr].z), make_float2(h2.x, h2.y), a);
+                a = ffma2(f8x2_to_f2(wv[rr].z >> 16), make_float2(h2.z, h2.w), a);
+                a = ffma2(f8x2_to_f2(wv[rr].w), make_float2(h3.x, h3.y), a);
+                a = ffma2(f8x2_to_f2(wv[rr].w >> 16), make_float2(h3.z, h3.w), a);
+                acc[rr][q] = fmaf(sc[rr], a.x + a.y, acc[rr][q]);
+            }
+        }
+        }
+    }
+#pragma unroll
+    for (int rr = 0; rr < kDownRowsPerWarp; ++rr)
+#pragma unroll
+        for (int q = 0; q < NT; ++q) {
+            const float v = warp_sum(acc[rr][q]);
+            const int row = row0 + rr;
+            if (lane == ((rr * NT + q) & 31) && q < nq && row < H) o[(size_t)rts[q] * H + row] = v;
+        }
+}
+
 // hs: nt_max * I floats of shared memory; rts: nt_max ints of shared memory.
+// Block-scaled FP8 weights when c.w.down_scale is set.
 __device__ void down_item(const Ctx& c, int item, float* hs, int* rts) {
     const int nrb = ceil_div(c.H, kDownRows);
     const int sl = item / nrb, rb = item - sl * nrb;
@@ -529,7 +659,17 @@ __device__ void down_item(const Ctx& c, int item, float* hs, int* rts) {
             *reinterpret_cast<float4*>(hs + (size_t)q * c.I + i) = val;
         }
         __syncthreads();
-        if (row0 < c.H) {
+        if (row0 < c.H && c.w.down_scale) {
+            const unsigned char* D8 = reinterpret_cast<const unsigned char*>(c.w.down) + (size_t)sg.e * c.H * c.I;
+            const int sld = (c.I + 127) >> 7;
+            const float* dsc = c.w.down_scale + (size_t)sg.e * ((c.H + 127) >> 7) * sld;
+            switch (nfill) {
+                case 1: down_rows_f8<1>(D8, dsc, sld, row0, c.H, c.I, hs, rts, nq, c.o); break;
+                case 2: down_rows_f8<2>(D8, dsc, sld, row0, c.H, c.I, hs, rts, nq, c.o); break;
+                case 4: down_rows_f8<4>(D8, dsc, sld, row0, c.H, c.I, hs, rts, nq, c.o); break;
+                default: down_rows_f8<8>(D8, dsc, sld, row0, c.H, c.I, hs, rts, nq, c.o); break;
+            }
+        } else if (row0 < c.H) {
             switch (nfill) {
                 case 1: down_rows<1>(D, row0, c.H, c.I, hs, rts, nq, c.o); break;
                 case 2: down_rows<2>(D, row0, c.H, c.I, hs, rts, nq, c.o); break;

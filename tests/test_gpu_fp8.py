@@ -1,6 +1,6 @@
 """Block-scaled FP8 expert weights (E4M3 codes, fp32 scales per 128 x 128
-block) through the persistent decode kernel, against the oracle on the
-dequantised weights."""
+block) through the persistent decode kernel and, for larger batches, the
+CUDA-core phase kernels, against the oracle on the dequantised weights."""
 import numpy as np
 import pytest
 import torch
@@ -82,10 +82,45 @@ def test_fp8_30_layer_stack_at_full_size(cuda_lib):
     torch.cuda.empty_cache()
 
 
-def test_fp8_refuses_batches_beyond_the_decode_kernel(cuda_lib):
-    w = synth.Workload("fp8", B=9, H=256, I=128, E=16, top_k=2, layers=1, sigma_router=256 ** -0.5)
-    sw = cuda_lib.StackWeightsFP8(_fp8_layers(w, 1, seed=1))
-    x = synth.make_x(w, 0, seed=1, device=DEV)
-    with pytest.raises(cuda_lib.MoeError) as e:
-        cuda_lib.stack_forward_fp8_(x, sw, 2)
-    assert e.value.code == cuda_lib.MOE_ERR_UNSUPPORTED
+@pytest.mark.parametrize("B,H,I,E,k,L,flags", [
+    (9, 256, 128, 16, 2, 2, 0),        # beyond the decode kernel: the phase kernels layer by layer
+    (24, 384, 144, 12, 3, 2, 0),       # ragged 128-blocks, several routes per expert
+    (64, 512, 256, 32, 8, 1, 0),       # a uniform-routing batch shape, top-8
+    (40, 256, 128, 8, 2, 2, 2),        # MOE_F_UNFUSED (the same path)
+    (3, 256, 128, 16, 2, 2, 2),        # MOE_F_UNFUSED below the decode kernel's limit
+])
+def test_fp8_phase_kernels_match_oracle_on_dequantised_weights(cuda_lib, B, H, I, E, k, L, flags):
+    """Batches beyond the decode kernel (and MOE_F_UNFUSED) run the CUDA-core
+    phase kernels on the E4M3 codes with their block scales."""
+    w = synth.Workload("fp8", B=B, H=H, I=I, E=E, top_k=k, layers=L, sigma_router=H ** -0.5, sigma_expert=0.05)
+    layers = _fp8_layers(w, L, seed=B + I)
+    sw = cuda_lib.StackWeightsFP8(layers)
+    x0 = synth.make_x(w, 0, seed=B + I, device=DEV)
+    x = x0.clone()
+    ids = torch.empty((L, B, k), dtype=torch.int32, device=DEV)
+    st = cuda_lib.new_status()
+    cuda_lib.stack_forward_fp8_(x, sw, k, flags=flags, ids_out=ids, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    check_y(x, _oracle_walk(x0, layers, k, ids))
+
+
+def test_fp8_uniform_layer_at_full_size(cuda_lib):
+    """One layer of the uniform-routing workload (E=256, top-8, H=2048,
+    I=768) at B=16 with FP8 experts, every row against the oracle."""
+    w = synth.UNIFORM.with_batch(16)
+    layers = _fp8_layers(w, 1, seed=3)
+    for lw in layers:
+        lw.pop("gate_up", None)
+        lw.pop("down", None)
+    sw = cuda_lib.StackWeightsFP8(layers)
+    x0 = synth.make_x(w, 0, seed=3, device=DEV)
+    x = x0.clone()
+    ids = torch.empty((1, w.B, w.top_k), dtype=torch.int32, device=DEV)
+    st = cuda_lib.new_status()
+    cuda_lib.stack_forward_fp8_(x, sw, w.top_k, ids_out=ids, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    check_y(x, _oracle_walk(x0, layers, w.top_k, ids))
+    del layers, sw
+    torch.cuda.empty_cache()
