@@ -461,12 +461,11 @@ def measure_stack(api, accounting, synth, w, dev, steps, warmup, flags=0, seed=0
     import numpy as np
     import torch
     if nvfp4:
-        layers = []
-        for l in range(w.layers):
-            lw = synth.make_layer_nvfp4(w, l, seed=seed, device=dev)
-            lw.pop("gate_up")  # only the codes and scales stay resident
-            lw.pop("down")
-            layers.append(lw)
+        if layers is None:
+            layers = [synth.make_layer_nvfp4(w, l, seed=seed, device=dev) for l in range(w.layers)]
+        for lw in layers:  # only the codes and scales stay resident
+            lw.pop("gate_up", None)
+            lw.pop("down", None)
         sw = api.StackWeightsNVFP4(layers)
         fwd = lambda xb, **kw: api.stack_forward_nvfp4_(xb, sw, w.top_k, **kw)
         lbytes = accounting.layer_bytes_nvfp4
@@ -573,13 +572,21 @@ def config_records(api, accounting, synth, dev, steps, warmup, seed=0):
     out["stack_nvfp4"] = measure_stack(api, accounting, synth, synth.STACK, dev, steps, warmup, 0, seed, flush,
                                        nvfp4=True)
     # one layer of the uniform-routing workload with FP8 experts over the batch
-    # sweep (decode kernel up to B=4, the CUDA-core phase kernels beyond)
+    # sweep (decode kernel up to B=4, the CUDA-core phase kernels beyond), then
+    # the same with NVFP4 experts
     base = synth.UNIFORM
     fp8_layer = [synth.make_layer_fp8(base, 0, seed=seed, device=dev)]
     for B in base.batches:
         out[f"uniform_B{B}_fp8"] = measure_stack(api, accounting, synth, base.with_batch(B), dev, steps, warmup, 0,
                                                  seed, flush, fp8=True, layers=fp8_layer)
     del fp8_layer
+    torch.cuda.empty_cache()
+    # and with NVFP4 experts
+    nvfp4_layer = [synth.make_layer_nvfp4(base, 0, seed=seed, device=dev)]
+    for B in base.batches:
+        out[f"uniform_B{B}_nvfp4"] = measure_stack(api, accounting, synth, base.with_batch(B), dev, steps, warmup, 0,
+                                                   seed, flush, nvfp4=True, layers=nvfp4_layer)
+    del nvfp4_layer
     torch.cuda.empty_cache()
     return out
 

@@ -295,9 +295,11 @@ int moe_stack_forward_fp8(int L, const uint16_t* const* w_router, const float* c
  * fp32.  The router stays bf16; the experts stream a quarter of the bytes of
  * bf16 weights (plus one scale byte per 16 weights); every sum stays fp32.
  * The six weight arguments are HOST arrays of L device pointers.  Requires H
- * and I multiples of 32 and a batch the persistent decode kernel takes (up to
- * 4 tokens and 32 routes), else MOE_ERR_UNSUPPORTED; flags: MOE_F_NO_DEDUP,
- * MOE_F_NO_PREFETCH.  The other arguments are those of moe_stack_forward.
+ * and I multiples of 32.  Batches the persistent decode kernel takes (up to 4
+ * tokens and 32 routes) run in it; larger ones, and any batch with
+ * MOE_F_UNFUSED, run layer by layer on the CUDA-core phase kernels.  flags:
+ * MOE_F_NO_DEDUP, MOE_F_NO_PREFETCH, MOE_F_UNFUSED.  The other arguments are
+ * those of moe_stack_forward.
  */
 int moe_stack_forward_nvfp4(int L, const uint16_t* const* w_router, const float* const* logit_bias,
                             const uint8_t* const* gate_up_q, const uint8_t* const* gate_up_bs,

@@ -1187,7 +1187,7 @@ int moe_stack_forward_nvfp4(int Lc, const uint16_t* const* w_router, const float
     if (rc) return rc;
     if (Lc < 1 || Lc > MOE_MAX_LAYERS) return MOE_ERR_INVALID_ARG;
     if ((H & 31) || (I & 31)) return MOE_ERR_INVALID_ARG;  // rows of codes in whole 16-byte pieces
-    if (flags & ~(MOE_F_NO_DEDUP | MOE_F_NO_PREFETCH)) return MOE_ERR_INVALID_ARG;
+    if (flags & ~(MOE_F_NO_DEDUP | MOE_F_NO_PREFETCH | MOE_F_UNFUSED)) return MOE_ERR_INVALID_ARG;
     if (B == 0) return MOE_OK;
     if (!w_router || !gate_up_q || !gate_up_bs || !gate_up_gs || !down_q || !down_bs || !down_gs)
         return MOE_ERR_INVALID_ARG;
@@ -1209,7 +1209,28 @@ int moe_stack_forward_nvfp4(int Lc, const uint16_t* const* w_router, const float
     memset(&dp, 0, sizeof dp);
     size_t dsm = 0;
     const int sms = sm_count();
-    if (!decode_plan(B, H, I, E, top_k, sms, dp, dsm, false, 1)) return MOE_ERR_UNSUPPORTED;
+    if ((flags & MOE_F_UNFUSED) || !decode_plan(B, H, I, E, top_k, sms, dp, dsm, false, 1)) {
+        // beyond the decode kernel: the CUDA-core phase kernels layer by
+        // layer, their items reading the E2M1 codes with both scales
+        Ctx c = make_ctx(x_inout, MOE_DT_F32, x_inout, x_inout, B, H, I, E, top_k, flags | MOE_F_NO_TC, ws, L,
+                         dev_status);
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
+        int32_t* ids_ws = c.ids;
+        for (int l = 0; l < Lc; ++l) {
+            memset(&c.w, 0, sizeof c.w);
+            c.w.w_router = w_router[l];
+            c.w.bias = logit_bias ? logit_bias[l] : nullptr;
+            c.w.gate_up = reinterpret_cast<const uint16_t*>(gate_up_q[l]);
+            c.w.down = reinterpret_cast<const uint16_t*>(down_q[l]);
+            c.w.gate_up_bs = gate_up_bs[l];
+            c.w.down_bs = down_bs[l];
+            c.w.gate_up_gs = gate_up_gs[l];
+            c.w.down_gs = down_gs[l];
+            c.ids = expert_ids_out ? expert_ids_out + (size_t)l * B * top_k : ids_ws;
+            if ((rc = launch_unfused_layer(c, st, ws, L))) return rc;
+        }
+        return MOE_OK;
+    }
     decode_common(dp, B, H, I, E, top_k, Lc, flags,
                   dev_status ? dev_status : reinterpret_cast<int32_t*>(ws + L.status));
     dp.trace = nullptr;

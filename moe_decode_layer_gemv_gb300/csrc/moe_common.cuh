@@ -8,6 +8,7 @@
 #pragma once
 
 #include <cuda_fp16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -59,6 +60,23 @@ __device__ __forceinline__ float2 f8x2_to_f2(unsigned v) {
     __half2 h;
     memcpy(&h, &hr, sizeof h);
     return __half22float2(h);
+}
+
+// Two E2M1 codes (one byte, low nibble first) as fp32, and one E4M3 code as
+// fp32: the hardware conversions to f16 are exact for every code, and so is
+// the widening to f32.
+__device__ __forceinline__ float2 f4x2_to_f2(unsigned v) {
+    const __half2_raw hr = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)(v & 0xffu), __NV_E2M1);
+    __half2 h;
+    memcpy(&h, &hr, sizeof h);
+    return __half22float2(h);
+}
+
+__device__ __forceinline__ float f8_to_f(unsigned v) {
+    const __half_raw hr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)(v & 0xffu), __NV_E4M3);
+    __half h;
+    memcpy(&h, &hr, sizeof h);
+    return __half2float(h);
 }
 
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }

@@ -772,22 +772,7 @@ __device__ __forceinline__ void dk_down_rows_f8(const unsigned char* st, int nrc
 }
 
 // ---------------------------------------------------------------- NVFP4
-// Two E2M1 codes (low nibble first) as fp32, and one E4M3 code as fp32: the
-// hardware conversions to f16 are exact for every code, and so is the
-// widening to f32.
-__device__ __forceinline__ float2 f4x2_to_f2(unsigned v) {
-    const __half2_raw hr = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)(v & 0xffu), __NV_E2M1);
-    __half2 h;
-    memcpy(&h, &hr, sizeof h);
-    return __half22float2(h);
-}
-
-__device__ __forceinline__ float f8_to_f(unsigned v) {
-    const __half_raw hr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)(v & 0xffu), __NV_E4M3);
-    __half h;
-    memcpy(&h, &hr, sizeof h);
-    return __half2float(h);
-}
+// (f4x2_to_f2, f8_to_f: moe_common.cuh)
 
 // The NVFP4 form of dk_gate_pair: rows of H E2M1 codes two to a byte (gate
 // row at grow, up row at urow), the rows' E4M3 block scales (gbs, ubs: one

@@ -462,9 +462,68 @@ __device__ __forceinline__ void gateup_rowpair_f8(const unsigned char* grow, con
     }
 }
 
+// The NVFP4 form of gateup_rowpair: rows of H E2M1 codes two to a byte (H %
+// 32 == 0), the rows' E4M3 scales of 16-element blocks (gbs, ubs) and the
+// matrix scale gs.  A lane takes 16 codes (8 bytes), one scale block: their
+// products are summed first and scaled once.
+template <int NT>
+__device__ __forceinline__ void gateup_rowpair_f4(const unsigned char* grow, const unsigned char* urow,
+                                                  const unsigned char* gbs, const unsigned char* ubs, float gs, int H,
+                                                  const float* xs, int nq, float* hdst, int I) {
+    const int lane = threadIdx.x & 31;
+    float ag[NT], au[NT];
+#pragma unroll
+    for (int q = 0; q < NT; ++q) ag[q] = au[q] = 0.f;
+    for (int base = 0; base < H; base += 512 * kGateUnroll) {
+        uint2 gv[kGateUnroll], uv[kGateUnroll];
+        unsigned gb[kGateUnroll], ub[kGateUnroll];
+#pragma unroll
+        for (int u = 0; u < kGateUnroll; ++u) {
+            const int idx = base + u * 512 + lane * 16;
+            const bool in = idx < H;
+            gv[u] = in ? __ldg(reinterpret_cast<const uint2*>(grow + (idx >> 1))) : make_uint2(0u, 0u);
+            uv[u] = in ? __ldg(reinterpret_cast<const uint2*>(urow + (idx >> 1))) : make_uint2(0u, 0u);
+            gb[u] = in ? __ldg(gbs + (idx >> 4)) : 0u;
+            ub[u] = in ? __ldg(ubs + (idx >> 4)) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kGateUnroll; ++u) {
+            const int idx = base + u * 512 + lane * 16;
+            if (idx < H) {
+                const float sg = f8_to_f(gb[u]) * gs, su = f8_to_f(ub[u]) * gs;
+                const unsigned gw[2] = {gv[u].x, gv[u].y};
+                const unsigned uw[2] = {uv[u].x, uv[u].y};
+#pragma unroll
+                for (int q = 0; q < NT; ++q) {
+                    const float4* xp = reinterpret_cast<const float4*>(xs + (size_t)q * H + idx);
+                    float2 pg = make_float2(0.f, 0.f), pu = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {  // codes 4v .. 4v+3 (two bytes) against x[idx + 4v ..]
+                        const float4 xv = xp[v];
+                        const unsigned gbyte = gw[v >> 1] >> (16 * (v & 1)), ubyte = uw[v >> 1] >> (16 * (v & 1));
+                        pg = ffma2(f4x2_to_f2(gbyte), make_float2(xv.x, xv.y), pg);
+                        pg = ffma2(f4x2_to_f2(gbyte >> 8), make_float2(xv.z, xv.w), pg);
+                        pu = ffma2(f4x2_to_f2(ubyte), make_float2(xv.x, xv.y), pu);
+                        pu = ffma2(f4x2_to_f2(ubyte >> 8), make_float2(xv.z, xv.w), pu);
+                    }
+                    ag[q] = fmaf(sg, pg.x + pg.y, ag[q]);
+                    au[q] = fmaf(su, pu.x + pu.y, au[q]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < NT; ++q) {
+        const float g = warp_sum(ag[q]);
+        const float u = warp_sum(au[q]);
+        if (lane == q && q < nq) hdst[(size_t)q * I] = silu_mul(g, u);
+    }
+}
+
 // xs: nt_max * H floats of shared memory; tok: nt_max ints of shared memory.
 // Block-scaled FP8 weights when c.w.gate_up_scale is set (gate_up then holds
-// E4M3 codes, one byte each).
+// E4M3 codes, one byte each), NVFP4 ones when c.w.gate_up_bs is set (E2M1
+// codes two to a byte).
 __device__ void gateup_item(const Ctx& c, int item, float* xs, int* tok) {
     const int nib = ceil_div(c.I, kWarps);
     const int sl = item / nib, ib = item - sl * nib;
@@ -483,7 +542,23 @@ __device__ void gateup_item(const Ctx& c, int item, float* xs, int* tok) {
         const int nfill = nq <= 1 ? 1 : nq <= 2 ? 2 : nq <= 4 ? 4 : 8;
         stage_x(c, tok, 0, nq, nfill, 0, c.H, xs, c.H);
         __syncthreads();
-        if (i < c.I && c.w.gate_up_scale) {
+        if (i < c.I && c.w.gate_up_bs) {
+            const size_t rb = (size_t)c.H >> 1, sb = (size_t)c.H >> 4;  // bytes of a row of codes, of scales
+            const unsigned char* G4 = reinterpret_cast<const unsigned char*>(c.w.gate_up) + (size_t)sg.e * 2 * c.I * rb;
+            const unsigned char* S4 = c.w.gate_up_bs + (size_t)sg.e * 2 * c.I * sb;
+            const float gs = __ldg(c.w.gate_up_gs + sg.e);
+            const unsigned char* grow = G4 + (size_t)i * rb;
+            const unsigned char* urow = G4 + (size_t)(c.I + i) * rb;
+            const unsigned char* gbs = S4 + (size_t)i * sb;
+            const unsigned char* ubs = S4 + (size_t)(c.I + i) * sb;
+            float* hdst = c.h + (size_t)g0 * c.I + i;
+            switch (nfill) {
+                case 1: gateup_rowpair_f4<1>(grow, urow, gbs, ubs, gs, c.H, xs, nq, hdst, c.I); break;
+                case 2: gateup_rowpair_f4<2>(grow, urow, gbs, ubs, gs, c.H, xs, nq, hdst, c.I); break;
+                case 4: gateup_rowpair_f4<4>(grow, urow, gbs, ubs, gs, c.H, xs, nq, hdst, c.I); break;
+                default: gateup_rowpair_f4<8>(grow, urow, gbs, ubs, gs, c.H, xs, nq, hdst, c.I); break;
+            }
+        } else if (i < c.I && c.w.gate_up_scale) {
             const unsigned char* G8 = reinterpret_cast<const unsigned char*>(c.w.gate_up) + (size_t)sg.e * 2 * c.I * c.H;
             const int sld = (c.H + 127) >> 7, se = ((2 * c.I + 127) >> 7) * sld;
             const float* gsr = c.w.gate_up_scale + (size_t)sg.e * se + (size_t)(i >> 7) * sld;
@@ -634,8 +709,68 @@ __device__ __forceinline__ void down_rows_f8(const unsigned char* D, const float
         }
 }
 
+// The NVFP4 form of down_rows: rows of I E2M1 codes two to a byte (I % 32 ==
+// 0), row r's E4M3 block scales at dbs + r * I/16, matrix scale gs.
+template <int NT>
+__device__ __forceinline__ void down_rows_f4(const unsigned char* D, const unsigned char* dbs, float gs, int row0,
+                                             int H, int I, const float* hs, const int* rts, int nq, float* o) {
+    const int lane = threadIdx.x & 31;
+    const size_t rb = (size_t)I >> 1, sb = (size_t)I >> 4;
+    float acc[kDownRowsPerWarp][NT];
+#pragma unroll
+    for (int rr = 0; rr < kDownRowsPerWarp; ++rr)
+#pragma unroll
+        for (int q = 0; q < NT; ++q) acc[rr][q] = 0.f;
+    for (int base0 = 0; base0 < I; base0 += 512 * kDownUnroll) {
+        uint2 wvu[kDownUnroll][kDownRowsPerWarp];
+        float scu[kDownUnroll][kDownRowsPerWarp];
+#pragma unroll
+        for (int u = 0; u < kDownUnroll; ++u)
+#pragma unroll
+            for (int rr = 0; rr < kDownRowsPerWarp; ++rr) {
+                const int row = row0 + rr, idx = base0 + u * 512 + lane * 16;
+                const bool in = row < H && idx < I;
+                wvu[u][rr] = in ? __ldg(reinterpret_cast<const uint2*>(D + (size_t)row * rb + (idx >> 1)))
+                                : make_uint2(0u, 0u);
+                scu[u][rr] = in ? f8_to_f(__ldg(dbs + (size_t)row * sb + (idx >> 4))) * gs : 0.f;
+            }
+#pragma unroll
+        for (int u = 0; u < kDownUnroll; ++u) {
+            const int idx = base0 + u * 512 + lane * 16;
+            if (idx >= I) continue;
+#pragma unroll
+            for (int q = 0; q < NT; ++q) {
+                const float4* hp = reinterpret_cast<const float4*>(hs + (size_t)q * I + idx);
+                const float4 h0 = hp[0], h1 = hp[1], h2 = hp[2], h3 = hp[3];
+                const float4 hv[4] = {h0, h1, h2, h3};
+#pragma unroll
+                for (int rr = 0; rr < kDownRowsPerWarp; ++rr) {
+                    const unsigned w[2] = {wvu[u][rr].x, wvu[u][rr].y};
+                    float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const unsigned byte2 = w[v >> 1] >> (16 * (v & 1));
+                        a = ffma2(f4x2_to_f2(byte2), make_float2(hv[v].x, hv[v].y), a);
+                        a = ffma2(f4x2_to_f2(byte2 >> 8), make_float2(hv[v].z, hv[v].w), a);
+                    }
+                    acc[rr][q] = fmaf(scu[u][rr], a.x + a.y, acc[rr][q]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int rr = 0; rr < kDownRowsPerWarp; ++rr)
+#pragma unroll
+        for (int q = 0; q < NT; ++q) {
+            const float v = warp_sum(acc[rr][q]);
+            const int row = row0 + rr;
+            if (lane == ((rr * NT + q) & 31) && q < nq && row < H) o[(size_t)rts[q] * H + row] = v;
+        }
+}
+
 // hs: nt_max * I floats of shared memory; rts: nt_max ints of shared memory.
-// Block-scaled FP8 weights when c.w.down_scale is set.
+// Block-scaled FP8 weights when c.w.down_scale is set, NVFP4 ones when
+// c.w.down_bs is.
 __device__ void down_item(const Ctx& c, int item, float* hs, int* rts) {
     const int nrb = ceil_div(c.H, kDownRows);
     const int sl = item / nrb, rb = item - sl * nrb;
@@ -659,7 +794,17 @@ __device__ void down_item(const Ctx& c, int item, float* hs, int* rts) {
             *reinterpret_cast<float4*>(hs + (size_t)q * c.I + i) = val;
         }
         __syncthreads();
-        if (row0 < c.H && c.w.down_scale) {
+        if (row0 < c.H && c.w.down_bs) {
+            const unsigned char* D4 = reinterpret_cast<const unsigned char*>(c.w.down) + (size_t)sg.e * c.H * (c.I >> 1);
+            const unsigned char* S4 = c.w.down_bs + (size_t)sg.e * c.H * (c.I >> 4);
+            const float gs = __ldg(c.w.down_gs + sg.e);
+            switch (nfill) {
+                case 1: down_rows_f4<1>(D4, S4, gs, row0, c.H, c.I, hs, rts, nq, c.o); break;
+                case 2: down_rows_f4<2>(D4, S4, gs, row0, c.H, c.I, hs, rts, nq, c.o); break;
+                case 4: down_rows_f4<4>(D4, S4, gs, row0, c.H, c.I, hs, rts, nq, c.o); break;
+                default: down_rows_f4<8>(D4, S4, gs, row0, c.H, c.I, hs, rts, nq, c.o); break;
+            }
+        } else if (row0 < c.H && c.w.down_scale) {
             const unsigned char* D8 = reinterpret_cast<const unsigned char*>(c.w.down) + (size_t)sg.e * c.H * c.I;
             const int sld = (c.I + 127) >> 7;
             const float* dsc = c.w.down_scale + (size_t)sg.e * ((c.H + 127) >> 7) * sld;

@@ -1,6 +1,7 @@
 """NVFP4 expert weights (E2M1 codes two a byte, an E4M3 scale per 16
-elements, an fp32 scale per matrix) through the persistent decode kernel,
-against the oracle on the dequantised weights."""
+elements, an fp32 scale per matrix) through the persistent decode kernel
+and, for larger batches, the CUDA-core phase kernels, against the oracle on
+the dequantised weights."""
 import numpy as np
 import pytest
 import torch
@@ -88,10 +89,24 @@ def test_nvfp4_30_layer_stack_at_full_size(cuda_lib):
     torch.cuda.empty_cache()
 
 
-def test_nvfp4_refuses_batches_beyond_the_decode_kernel(cuda_lib):
-    w = synth.Workload("nvfp4", B=9, H=256, I=128, E=16, top_k=2, layers=1, sigma_router=256 ** -0.5)
-    sw = cuda_lib.StackWeightsNVFP4(_nvfp4_layers(w, 1, seed=1))
-    x = synth.make_x(w, 0, seed=1, device=DEV)
-    with pytest.raises(cuda_lib.MoeError) as e:
-        cuda_lib.stack_forward_nvfp4_(x, sw, 2)
-    assert e.value.code == cuda_lib.MOE_ERR_UNSUPPORTED
+@pytest.mark.parametrize("B,H,I,E,k,L,flags", [
+    (9, 256, 128, 16, 2, 2, 0),        # beyond the decode kernel: the phase kernels layer by layer
+    (24, 384, 160, 12, 3, 2, 0),       # 16-element blocks across 128-column boundaries
+    (64, 512, 256, 32, 8, 1, 0),       # a uniform-routing batch shape, top-8
+    (3, 256, 128, 16, 2, 2, 2),        # MOE_F_UNFUSED below the decode kernel's limit
+])
+def test_nvfp4_phase_kernels_match_oracle_on_dequantised_weights(cuda_lib, B, H, I, E, k, L, flags):
+    """Batches beyond the decode kernel (and MOE_F_UNFUSED) run the CUDA-core
+    phase kernels on the E2M1 codes with their block and matrix scales."""
+    w = synth.Workload("nvfp4", B=B, H=H, I=I, E=E, top_k=k, layers=L, sigma_router=H ** -0.5,
+                       sigma_expert=0.05)
+    layers = _nvfp4_layers(w, L, seed=B + I)
+    sw = cuda_lib.StackWeightsNVFP4(layers)
+    x0 = synth.make_x(w, 0, seed=B + I, device=DEV)
+    x = x0.clone()
+    ids = torch.empty((L, B, k), dtype=torch.int32, device=DEV)
+    st = cuda_lib.new_status()
+    cuda_lib.stack_forward_nvfp4_(x, sw, k, flags=flags, ids_out=ids, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    check_y(x, _oracle_walk(x0, layers, k, ids))
