@@ -285,6 +285,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
             const bool v = get_seg(c, ld_act_i(c.seg_list + maxseg + i), sg);
             segtab[i] = make_int4(sg.e, sg.p0, sg.p1, v ? 1 : 0);
         }
+    // Items of unequal cost (a launch whose largest segment has more than 32
+    // tokens) and few items a CTA: the segments are ordered by token count,
+    // largest first (stable), and the items are dealt in a snake, so that the
+    // CTAs drawing the costliest items in the first round draw the cheapest
+    // (or none) in the second.  The order decides only which CTA computes an
+    // item, never a value.
+    const int G = (int)gridDim.x;
+    const bool snake = cached && nmax > kTcBoxN && n_items <= 4 * G && nts <= kTcThreads;
+    if (snake) {
+        __syncthreads();
+        const int i = threadIdx.x;
+        int4 mine = make_int4(0, 0, 0, 0);
+        int rank = 0;
+        if (i < nts) {
+            mine = segtab[i];
+            const int ni = mine.w ? mine.z - mine.y : 0;
+            for (int j = 0; j < nts; ++j) {
+                const int4 o = segtab[j];
+                const int nj = o.w ? o.z - o.y : 0;
+                rank += (nj > ni || (nj == ni && j < i)) ? 1 : 0;
+            }
+        }
+        __syncthreads();
+        if (i < nts) segtab[rank] = mine;
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -293,7 +318,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     uint32_t g = 0;         // stages through the ring so far (same in every role)
     uint32_t g_armed = 0;   // stages whose copies the producer armed (producer lane only)
     int d = 0;              // items processed (same in every role)
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    // slot = round * G + blockIdx.x; a snake's odd rounds run backwards, so
+    // its last round may hold items for CTAs whose slot is past n_items
+    const int slot_end = n_items + (snake ? (int)blockIdx.x : 0);
+    for (int slot = blockIdx.x; slot < slot_end; slot += G) {
+        int item = slot;
+        if (snake && ((slot / G) & 1)) item = (slot / G + 1) * G - 1 - (int)blockIdx.x;
+        if (item >= n_items) continue;  // uniform
         // the token chunk varies slowest: items of later chunks (which exist
         // only for segments with more than 128 routes) come after every
         // first chunk, so no CTA draws only empty items
