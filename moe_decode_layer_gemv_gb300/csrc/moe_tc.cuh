@@ -49,6 +49,12 @@ constexpr uint32_t kTcWaitLimit = 1u << 24;
 constexpr uint32_t kTcTmemCols = 256;    // two accumulators of 128 columns
 static_assert(128 * kTcEpiLd * 4 <= kTcEpiBytes, "epilogue tile");
 
+// Selects one of the two compiled copies of the GEMM's item loop.
+template <bool B>
+struct TcVar {
+    static constexpr bool value = B;
+};
+
 // Barriers and flags at the start of the kernel's shared memory.
 struct TcBars {
     uint64_t full[kTcMaxStages];   // a stage's tiles landed (TMA transaction count)
@@ -257,9 +263,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     int ksub = 1;
     while (ksub < 4 && stage_of(ksub) < 32768u && ring_bytes / stage_of(2 * ksub) >= 3u) ksub *= 2;
     const uint32_t stage_bytes = stage_of(ksub);
-    const uint32_t b_off = (uint32_t)ksub * kTcATile;   // activation tiles after the ksub weight tiles
     const int S = min(kTcMaxStages, (int)(ring_bytes / stage_bytes));
-    const int nst = (nk + ksub - 1) / ksub;             // stages per item
+    // In a launch of unequal items (below), an item with fewer tokens than the
+    // launch's largest packs more k-steps into a stage, up to stage_bytes: a
+    // copy stream passes about one stage per round trip whatever it carries,
+    // so a cheap item then takes fewer ring phases.  Every role derives the
+    // same value from the item's n.
+    auto ksub_of = [&](int n_pad) {
+        const uint32_t per = kTcATile + nb * (uint32_t)n_pad * 128u;
+        int ks = ksub;
+        while (ks < 4 && (uint32_t)(2 * ks) * per <= stage_bytes) ks *= 2;
+        return ks;
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTcMaxStages; ++s) {
@@ -318,168 +333,185 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     uint32_t g = 0;         // stages through the ring so far (same in every role)
     uint32_t g_armed = 0;   // stages whose copies the producer armed (producer lane only)
     int d = 0;              // items processed (same in every role)
-    // slot = round * G + blockIdx.x; a snake's odd rounds run backwards, so
-    // its last round may hold items for CTAs whose slot is past n_items
-    const int slot_end = n_items + (snake ? (int)blockIdx.x : 0);
-    for (int slot = blockIdx.x; slot < slot_end; slot += G) {
-        int item = slot;
-        if (snake && ((slot / G) & 1)) item = (slot / G + 1) * G - 1 - (int)blockIdx.x;
-        if (item >= n_items) continue;  // uniform
-        // the token chunk varies slowest: items of later chunks (which exist
-        // only for segments with more than 128 routes) come after every
-        // first chunk, so no CTA draws only empty items
-        const int per_chunk = n_items / nchunk;
-        const int nc = item / per_chunk;
-        const int rem = item - nc * per_chunk;
-        const int sl = rem / mtiles, mt = rem - sl * mtiles;
-        Seg sg;
-        if (cached) {
-            const int4 t = segtab[sl];
-            if (!t.w) continue;  // uniform
-            sg.e = t.x;
-            sg.p0 = t.y;
-            sg.p1 = t.z;
-        } else if (!get_seg(c, ld_act_i(c.seg_list + maxseg + sl), sg)) {
-            continue;  // uniform
-        }
-        const int q0 = sg.p0 + nc * kTcMaxN;
-        if (q0 >= sg.p1) continue;
-        const int n = min(kTcMaxN, sg.p1 - q0);
-        const int n_pad = (n + kTcBoxN - 1) / kTcBoxN * kTcBoxN;
-        const int buf = d & 1, use = d >> 1;
+    // The item loop is compiled twice.  Launches of equal items take the
+    // static strided order and the launch's stage layout; launches of unequal
+    // items (the snake) also give each item its own stage layout.  One copy
+    // serving both measured slower on the launches of equal items.
+    auto item_loop = [&](auto var) {
+        constexpr bool kVar = decltype(var)::value;
+        // slot = round * G + blockIdx.x; a snake's odd rounds run backwards, so
+        // its last round may hold items for CTAs whose slot is past n_items
+        const int slot_end = n_items + (kVar ? (int)blockIdx.x : 0);
+        for (int slot = blockIdx.x; slot < slot_end; slot += G) {
+            int item = slot;
+            if (kVar && ((slot / G) & 1)) item = (slot / G + 1) * G - 1 - (int)blockIdx.x;
+            if (kVar && item >= n_items) continue;  // uniform
+            // the token chunk varies slowest: items of later chunks (which exist
+            // only for segments with more than 128 routes) come after every
+            // first chunk, so no CTA draws only empty items
+            const int per_chunk = n_items / nchunk;
+            const int nc = item / per_chunk;
+            const int rem = item - nc * per_chunk;
+            const int sl = rem / mtiles, mt = rem - sl * mtiles;
+            Seg sg;
+            if (cached) {
+                const int4 t = segtab[sl];
+                if (!t.w) continue;  // uniform
+                sg.e = t.x;
+                sg.p0 = t.y;
+                sg.p1 = t.z;
+            } else if (!get_seg(c, ld_act_i(c.seg_list + maxseg + sl), sg)) {
+                continue;  // uniform
+            }
+            const int q0 = sg.p0 + nc * kTcMaxN;
+            if (q0 >= sg.p1) continue;
+            const int n = min(kTcMaxN, sg.p1 - q0);
+            const int n_pad = (n + kTcBoxN - 1) / kTcBoxN * kTcBoxN;
+            const int buf = d & 1, use = d >> 1;
+            // stage layout of this item: ks weight tiles, then ks activation
+            // tiles (hi), then ks (lo)
+            const int ks = kVar ? ksub_of(n_pad) : ksub;
+            const int nst = (nk + ks - 1) / ks;  // stages of this item
+            const uint32_t bb = kVar ? (uint32_t)n_pad * 128u : bbytes;  // one activation operand
+            const uint32_t b_off = (uint32_t)ks * kTcATile;
 
-        if (warp == 4) {
-            if (lane == 0) {
-                // ---------------- TMA producer
-                // MOE_F_HOT_L2: the experts with at least MOE_TC_MIN_ROUTES
-                // routes are the step's most chosen ones; their weights are
-                // loaded with evict_last so that they stay in L2 for the next
-                // steps, those of the others with evict_first
-                const bool hot = (c.flags & MOE_F_HOT_L2) != 0;
-                const uint64_t pol = !hot                                   ? 0ull
-                                     : sg.p1 - sg.p0 >= MOE_TC_MIN_ROUTES ? l2_policy_evict_last()
-                                                                           : l2_policy_evict_first();
-                const uint32_t bytes = kTcATile + (uint32_t)n_pad * 128u * (p.with_lo ? 2u : 1u);
-                int arow0, arow1 = 0;
-                if (p.gate) {
-                    arow0 = sg.e * 2 * c.I + mt * 64;
-                    arow1 = arow0 + c.I;
-                } else {
-                    arow0 = sg.e * c.H + mt * 128;
-                }
-                for (int j = 0; j < nst; ++j) {
-                    const uint32_t gs = g + (uint32_t)j;
-                    const int s = (int)(gs % (uint32_t)S);
-                    const uint32_t ph = (gs / (uint32_t)S) & 1u;
-                    if (gs >= (uint32_t)S && !tc_wait_ab(&b->empty[s], ph ^ 1u, b)) break;
-                    unsigned char* st = ring + (size_t)s * stage_bytes;
-                    const int k0 = j * ksub, ke = min(ksub, nk - k0);  // k-steps k0 .. k0+ke-1
-                    mbar_arrive_expect_tx(&b->full[s], (uint32_t)ke * bytes);
-                    g_armed = gs + 1u;
-                    for (int u = 0; u < ke; ++u) {
-                        const int kx = (k0 + u) * kTcBK;
-                        unsigned char* sa = st + (size_t)u * kTcATile;
-                        unsigned char* sb = st + b_off + (size_t)u * bbytes;
-                        if (hot) {
-                            tma_load_2d_hint(sa, &p.ta, kx, arow0, &b->full[s], pol);
-                            if (p.gate) tma_load_2d_hint(sa + 8192, &p.ta, kx, arow1, &b->full[s], pol);
-                        } else {
-                            tma_load_2d(sa, &p.ta, kx, arow0, &b->full[s]);
-                            if (p.gate) tma_load_2d(sa + 8192, &p.ta, kx, arow1, &b->full[s]);
-                        }
-                        for (int r = 0; r < n_pad; r += kTcBoxN) {
-                            tma_load_2d(sb + r * 128, &p.tb_hi, kx, q0 + r, &b->full[s]);
-                            if (p.with_lo)
-                                tma_load_2d(sb + (size_t)ksub * bbytes + r * 128, &p.tb_lo, kx, q0 + r, &b->full[s]);
+            if (warp == 4) {
+                if (lane == 0) {
+                    // ---------------- TMA producer
+                    // MOE_F_HOT_L2: the experts with at least MOE_TC_MIN_ROUTES
+                    // routes are the step's most chosen ones; their weights are
+                    // loaded with evict_last so that they stay in L2 for the next
+                    // steps, those of the others with evict_first
+                    const bool hot = (c.flags & MOE_F_HOT_L2) != 0;
+                    const uint64_t pol = !hot                                   ? 0ull
+                                         : sg.p1 - sg.p0 >= MOE_TC_MIN_ROUTES ? l2_policy_evict_last()
+                                                                               : l2_policy_evict_first();
+                    const uint32_t bytes = kTcATile + (uint32_t)n_pad * 128u * (p.with_lo ? 2u : 1u);
+                    int arow0, arow1 = 0;
+                    if (p.gate) {
+                        arow0 = sg.e * 2 * c.I + mt * 64;
+                        arow1 = arow0 + c.I;
+                    } else {
+                        arow0 = sg.e * c.H + mt * 128;
+                    }
+                    for (int j = 0; j < nst; ++j) {
+                        const uint32_t gs = g + (uint32_t)j;
+                        const int s = (int)(gs % (uint32_t)S);
+                        const uint32_t ph = (gs / (uint32_t)S) & 1u;
+                        if (gs >= (uint32_t)S && !tc_wait_ab(&b->empty[s], ph ^ 1u, b)) break;
+                        unsigned char* st = ring + (size_t)s * stage_bytes;
+                        const int k0 = j * ks, ke = min(ks, nk - k0);  // k-steps k0 .. k0+ke-1
+                        mbar_arrive_expect_tx(&b->full[s], (uint32_t)ke * bytes);
+                        g_armed = gs + 1u;
+                        for (int u = 0; u < ke; ++u) {
+                            const int kx = (k0 + u) * kTcBK;
+                            unsigned char* sa = st + (size_t)u * kTcATile;
+                            unsigned char* sb = st + b_off + (size_t)u * bb;
+                            if (hot) {
+                                tma_load_2d_hint(sa, &p.ta, kx, arow0, &b->full[s], pol);
+                                if (p.gate) tma_load_2d_hint(sa + 8192, &p.ta, kx, arow1, &b->full[s], pol);
+                            } else {
+                                tma_load_2d(sa, &p.ta, kx, arow0, &b->full[s]);
+                                if (p.gate) tma_load_2d(sa + 8192, &p.ta, kx, arow1, &b->full[s]);
+                            }
+                            for (int r = 0; r < n_pad; r += kTcBoxN) {
+                                tma_load_2d(sb + r * 128, &p.tb_hi, kx, q0 + r, &b->full[s]);
+                                if (p.with_lo)
+                                    tma_load_2d(sb + (size_t)ks * bb + r * 128, &p.tb_lo, kx, q0 + r, &b->full[s]);
+                            }
                         }
                     }
                 }
-            }
-            __syncwarp();
-        } else if (warp == 5) {
-            if (lane == 0) {
-                // ---------------- MMA issuer (one thread)
-                bool ok = use == 0 || tc_wait_ab(&b->acc_empty[buf], (uint32_t)((use - 1) & 1), b);
-                tc_fence_after();
-                const uint32_t tacc = tmem + (uint32_t)(buf * 128);
-                const uint32_t idesc = umma_idesc_bf16(128, n_pad);
-                for (int j = 0; ok && j < nst; ++j) {
-                    const uint32_t gs = g + (uint32_t)j;
-                    const int s = (int)(gs % (uint32_t)S);
-                    const uint32_t ph = (gs / (uint32_t)S) & 1u;
-                    if (!tc_wait_ab(&b->full[s], ph, b)) {
-                        ok = false;
-                        break;
-                    }
+                __syncwarp();
+            } else if (warp == 5) {
+                if (lane == 0) {
+                    // ---------------- MMA issuer (one thread)
+                    bool ok = use == 0 || tc_wait_ab(&b->acc_empty[buf], (uint32_t)((use - 1) & 1), b);
                     tc_fence_after();
-                    const int ke = min(ksub, nk - j * ksub);
-                    const uint32_t st_addr = smem_u32(ring + (size_t)s * stage_bytes);
-                    for (int u = 0; u < ke; ++u) {
-                        const uint32_t a_addr = st_addr + (uint32_t)u * kTcATile;
-                        const uint32_t bh_addr = st_addr + b_off + (uint32_t)u * bbytes;
-                        const uint32_t bl_addr = bh_addr + (uint32_t)ksub * bbytes;
-#pragma unroll
-                        for (int kk = 0; kk < kTcBK / 16; ++kk) {
-                            const uint64_t ad = umma_sdesc(a_addr + kk * 32);
-                            umma_bf16(tacc, ad, umma_sdesc(bh_addr + kk * 32), idesc, (j > 0 || u > 0 || kk > 0) ? 1u : 0u);
-                            if (p.with_lo) umma_bf16(tacc, ad, umma_sdesc(bl_addr + kk * 32), idesc, 1u);
+                    const uint32_t tacc = tmem + (uint32_t)(buf * 128);
+                    const uint32_t idesc = umma_idesc_bf16(128, n_pad);
+                    for (int j = 0; ok && j < nst; ++j) {
+                        const uint32_t gs = g + (uint32_t)j;
+                        const int s = (int)(gs % (uint32_t)S);
+                        const uint32_t ph = (gs / (uint32_t)S) & 1u;
+                        if (!tc_wait_ab(&b->full[s], ph, b)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const int ke = min(ks, nk - j * ks);
+                        const uint32_t st_addr = smem_u32(ring + (size_t)s * stage_bytes);
+                        for (int u = 0; u < ke; ++u) {
+                            const uint32_t a_addr = st_addr + (uint32_t)u * kTcATile;
+                            const uint32_t bh_addr = st_addr + b_off + (uint32_t)u * bb;
+                            const uint32_t bl_addr = bh_addr + (uint32_t)ks * bb;
+    #pragma unroll
+                            for (int kk = 0; kk < kTcBK / 16; ++kk) {
+                                const uint64_t ad = umma_sdesc(a_addr + kk * 32);
+                                umma_bf16(tacc, ad, umma_sdesc(bh_addr + kk * 32), idesc, (j > 0 || u > 0 || kk > 0) ? 1u : 0u);
+                                if (p.with_lo) umma_bf16(tacc, ad, umma_sdesc(bl_addr + kk * 32), idesc, 1u);
+                            }
+                        }
+                        umma_commit(&b->empty[s]);  // the stage is free once these MMAs have read it
+                    }
+                    if (ok) umma_commit(&b->acc_full[buf]);  // arrives when every MMA of the item is complete
+                }
+                __syncwarp();
+            } else {
+                // ---------------- epilogue (warps 0-3: accumulator lanes 32w..32w+31)
+                // (one decision for all 128 threads: they meet at named barriers)
+                // the down pass writes o by flat route: the item's route indices
+                // once into shared memory (ordered before their use by the first
+                // barrier below), not a dependent global load per column
+                if (!p.gate && (int)threadIdx.x < n) rr[threadIdx.x] = route_at(c, q0 + (int)threadIdx.x);
+                const bool ok = !named_sync_or(1, 128, !tc_wait_ab(&b->acc_full[buf], (uint32_t)(use & 1), b));
+                tc_fence_after();
+                const uint32_t row_addr = tmem + (uint32_t)(buf * 128) + ((uint32_t)(warp * 32) << 16);
+                for (int col0 = 0; ok && col0 < n_pad; col0 += kTcEpiCols) {
+                    float v[kTcEpiCols];
+                    tmem_ld16(row_addr + col0, *reinterpret_cast<float(*)[16]>(v));
+                    tmem_ld16(row_addr + col0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+                    if (col0 + kTcEpiCols >= n_pad) {  // the accumulator is read: the MMA warp may reuse it
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&b->acc_empty[buf]);
+                    }
+    #pragma unroll
+                    for (int j = 0; j < kTcEpiCols; ++j) epi[threadIdx.x * kTcEpiLd + j] = v[j];
+                    named_sync(1, 128);
+                    const int ncol = min(kTcEpiCols, n - col0);
+                    if (p.gate) {
+                        const int i0 = mt * 64;
+                        for (int t = threadIdx.x; t < 64 * ncol; t += 128) {
+                            const int i = t & 63, jj = t >> 6;
+                            const float hv = silu_mul(epi[i * kTcEpiLd + jj], epi[(64 + i) * kTcEpiLd + jj]);
+                            const uint16_t hi = f2bf_bits(hv);
+                            const size_t at = (size_t)(q0 + col0 + jj) * c.I + i0 + i;
+                            p.h_hi[at] = hi;
+                            p.h_lo[at] = f2bf_bits(hv - bf_bits2f(hi));
+                        }
+                    } else {
+                        const int r0 = mt * 128;
+                        for (int t = threadIdx.x; t < 128 * ncol; t += 128) {
+                            const int row = t & 127, jj = t >> 7;
+                            c.o[(size_t)rr[col0 + jj] * c.H + r0 + row] = epi[row * kTcEpiLd + jj];
                         }
                     }
-                    umma_commit(&b->empty[s]);  // the stage is free once these MMAs have read it
+                    named_sync(1, 128);
                 }
-                if (ok) umma_commit(&b->acc_full[buf]);  // arrives when every MMA of the item is complete
             }
-            __syncwarp();
-        } else {
-            // ---------------- epilogue (warps 0-3: accumulator lanes 32w..32w+31)
-            // (one decision for all 128 threads: they meet at named barriers)
-            // the down pass writes o by flat route: the item's route indices
-            // once into shared memory (ordered before their use by the first
-            // barrier below), not a dependent global load per column
-            if (!p.gate && (int)threadIdx.x < n) rr[threadIdx.x] = route_at(c, q0 + (int)threadIdx.x);
-            const bool ok = !named_sync_or(1, 128, !tc_wait_ab(&b->acc_full[buf], (uint32_t)(use & 1), b));
-            tc_fence_after();
-            const uint32_t row_addr = tmem + (uint32_t)(buf * 128) + ((uint32_t)(warp * 32) << 16);
-            for (int col0 = 0; ok && col0 < n_pad; col0 += kTcEpiCols) {
-                float v[kTcEpiCols];
-                tmem_ld16(row_addr + col0, *reinterpret_cast<float(*)[16]>(v));
-                tmem_ld16(row_addr + col0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
-                if (col0 + kTcEpiCols >= n_pad) {  // the accumulator is read: the MMA warp may reuse it
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&b->acc_empty[buf]);
-                }
-#pragma unroll
-                for (int j = 0; j < kTcEpiCols; ++j) epi[threadIdx.x * kTcEpiLd + j] = v[j];
-                named_sync(1, 128);
-                const int ncol = min(kTcEpiCols, n - col0);
-                if (p.gate) {
-                    const int i0 = mt * 64;
-                    for (int t = threadIdx.x; t < 64 * ncol; t += 128) {
-                        const int i = t & 63, jj = t >> 6;
-                        const float hv = silu_mul(epi[i * kTcEpiLd + jj], epi[(64 + i) * kTcEpiLd + jj]);
-                        const uint16_t hi = f2bf_bits(hv);
-                        const size_t at = (size_t)(q0 + col0 + jj) * c.I + i0 + i;
-                        p.h_hi[at] = hi;
-                        p.h_lo[at] = f2bf_bits(hv - bf_bits2f(hi));
-                    }
-                } else {
-                    const int r0 = mt * 128;
-                    for (int t = threadIdx.x; t < 128 * ncol; t += 128) {
-                        const int row = t & 127, jj = t >> 7;
-                        c.o[(size_t)rr[col0 + jj] * c.H + r0 + row] = epi[row * kTcEpiLd + jj];
-                    }
-                }
-                named_sync(1, 128);
-            }
+            g += (uint32_t)nst;
+            ++d;
+            // stop on abort, with one decision per barrier group (the epilogue
+            // warps meet at named barriers, a warp's lanes at __syncwarp)
+            const bool stop = *(volatile int*)&b->abort != 0;
+            if (warp < 4 ? named_sync_or(1, 128, stop) : __any_sync(0xffffffffu, stop)) break;
         }
-        g += (uint32_t)nst;
-        ++d;
-        // stop on abort, with one decision per barrier group (the epilogue
-        // warps meet at named barriers, a warp's lanes at __syncwarp)
-        const bool stop = *(volatile int*)&b->abort != 0;
-        if (warp < 4 ? named_sync_or(1, 128, stop) : __any_sync(0xffffffffu, stop)) break;
-    }
+    };
+    if (snake)
+        item_loop(TcVar<true>{});
+    else
+        item_loop(TcVar<false>{});
     // teardown: no MMA and no copy may still be in flight when the tensor
     // memory is freed and the CTA exits
     if (warp == 5 && lane == 0) {
