@@ -68,25 +68,30 @@ __device__ void router_item(const Ctx& c, int item, float* smem) {
     for (int j = 0; j < EPW; ++j)
 #pragma unroll
         for (int q = 0; q < kRouterTB; ++q) acc[j][q] = make_float2(0.f, 0.f);
+    // this lane's weight vectors of a chunk (kRouterHC / 256 per expert), all
+    // requested together: the first chunk's before x is staged, each next
+    // chunk's as soon as the current one is computed, so that the weights'
+    // memory round trip overlaps the staging of x instead of following it
+    constexpr int kNV = kRouterHC / 256;
+    uint4 wv[EPW][kNV];
+    auto load_w = [&](int hc) {
+        const int hn = min(kRouterHC, c.H - hc);
+#pragma unroll
+        for (int s = 0; s < kNV; ++s)
+#pragma unroll
+            for (int j = 0; j < EPW; ++j) {
+                const int i = lane * 8 + 256 * s;
+                wv[j][s] = (e0 + j < c.E && i < hn) ? ld_weight_v4(c.w.w_router + (size_t)(e0 + j) * c.H + hc + i)
+                                                     : make_uint4(0u, 0u, 0u, 0u);
+            }
+    };
+    if (e0 < c.E) load_w(0);
     for (int hc = 0; hc < c.H; hc += kRouterHC) {
         const int hn = min(kRouterHC, c.H - hc);
         __syncthreads();
         stage_x(c, nullptr, t0, nt, kRouterTB, hc, hn, smem, kRouterHC);
         __syncthreads();
         if (e0 < c.E) {
-            // this lane's weight vectors of the chunk (kRouterHC / 256 per
-            // expert) are all requested before the first is used: one memory
-            // round trip a chunk instead of one per vector
-            constexpr int kNV = kRouterHC / 256;
-            uint4 wv[EPW][kNV];
-#pragma unroll
-            for (int s = 0; s < kNV; ++s)
-#pragma unroll
-                for (int j = 0; j < EPW; ++j) {
-                    const int i = lane * 8 + 256 * s;
-                    wv[j][s] = (e0 + j < c.E && i < hn) ? ld_weight_v4(c.w.w_router + (size_t)(e0 + j) * c.H + hc + i)
-                                                         : make_uint4(0u, 0u, 0u, 0u);
-                }
 #pragma unroll
             for (int s = 0; s < kNV; ++s) {
                 const int i = lane * 8 + 256 * s;
@@ -112,6 +117,7 @@ __device__ void router_item(const Ctx& c, int item, float* smem) {
                     }
                 }
             }
+            if (hc + kRouterHC < c.H) load_w(hc + kRouterHC);
         }
     }
 #pragma unroll
