@@ -105,3 +105,25 @@ def test_hot_expert_l2_policy_leaves_results_unchanged(cuda_lib, split):
     assert torch.equal(i0, i1) and torch.equal(y0, y1)
     y_o, _, _ = oracle_layer_following(x, layer_weights_np(lw), k, i1)
     check_y(y1, y_o)
+
+
+@pytest.mark.parametrize("x_bf16", [False, True])
+def test_unequal_items_snake_order_and_per_item_stages(cuda_lib, x_bf16):
+    """A launch whose segments differ widely in size (one expert with more
+    than 96 of the 128 tokens beside experts with at most 32): the GEMM
+    ranks its segments by size, deals the items in a snake, and (fp32
+    activations) packs two k-steps into a stage for the small experts'
+    items.  The layer still matches the oracle and the CUDA-core path."""
+    B, H, I, E, k = 128, 1024, 256, 64, 4
+    lw, x = _case(B, H, I, E, k, seed=11, x_bf16=x_bf16, skew=True)
+    y, ids, _ = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k, bias=lw["bias"])
+    yg, idsg, _ = cuda_lib.layer_forward(x, lw["w_router"], lw["gate_up"], lw["down"], k, bias=lw["bias"],
+                                         flags=cuda_lib.MOE_F_NO_TC)
+    torch.cuda.synchronize()
+    counts = np.bincount(ids.cpu().numpy().ravel(), minlength=E)
+    assert counts.max() > 96 and ((counts > 0) & (counts <= 32)).any()
+    assert torch.equal(ids, idsg)
+    assert float((y - yg).abs().max()) <= 1e-4 * float(yg.abs().max())
+    y_o, _, _ = oracle_layer_following(x, layer_weights_np(lw), k, ids)
+    rel = check_y(y, y_o)
+    assert rel < 1e-4
